@@ -1,0 +1,300 @@
+"""ctypes binding of libssmstate's C ABI (include/ssm_state.h).
+
+Argument marshalling only: every function below has the name of its C
+entry point, checks the tensors it is given (device, dtype, contiguity,
+size) and passes raw pointers; all work runs in the library's CUDA kernels.
+There is no fallback: if the library is missing the import fails.
+
+Tensors: device tensors are ``torch.Tensor`` on the pool's CUDA device; bf16
+inputs are ``torch.bfloat16``, fp32 are ``torch.float32``; slot lists,
+cu_seqlens and chunk sequence numbers are host sequences (lists, numpy
+arrays or CPU tensors) as the C ABI takes them.  ``stream`` defaults to
+torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libssmstate.so")
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_INVALID_CHUNK, SSM_ERR_INVALID_STATE = 0, 1, 2, 3
+SSM_ERR_SEQUENCE, SSM_ERR_DUPLICATE, SSM_ERR_SCHEMA, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_NO_MEMORY = 4, 5, 6, 7, 8, 9
+SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 2
+SSM_MODE_COPY, SSM_MODE_REPLAY = 0, 1
+SSM_FLAG_NONFINITE_INPUT, SSM_FLAG_POISONED_SLOT, SSM_FLAG_BAD_ACCEPT = 1, 2, 4
+SSM_FLAG_LOG_NOT_EMPTY, SSM_FLAG_TIMEOUT = 8, 16
+
+# every entry point the header declares (the CPU test checks the library exports them)
+EXPORTS = (
+    "ssm_state_init", "ssm_state_destroy", "ssm_state_reset", "ssm_state_release", "ssm_state_checkpoint",
+    "ssm_state_restore", "ssm_slot_info", "ssm_state_gather", "ssm_scan_chunk", "ssm_decode_step",
+    "ssm_verify_copy", "ssm_verify_replay", "ssm_state_commit", "ssm_pool_status", "ssm_last_path",
+    "ssm_status_string", "ssm_pool_bytes",
+)
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class ssm_config(ctypes.Structure):
+    _fields_ = [("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32), ("dstate", ctypes.c_int32),
+                ("ngroups", ctypes.c_int32), ("input_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("window", ctypes.c_int32), ("max_tokens", ctypes.c_int32)]
+
+
+class ssm_slot_meta(ctypes.Structure):
+    _fields_ = [("position", ctypes.c_int64), ("next_chunk", ctypes.c_int64), ("epoch", ctypes.c_int64),
+                ("log_len", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libssmstate is not built ({LIB_PATH} missing); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    V, I32, I64, U32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+    P_I32 = ctypes.POINTER(I32)
+    P_I64 = ctypes.POINTER(I64)
+    sig = {
+        "ssm_state_init": [ctypes.POINTER(ssm_config), I32, V, V, ctypes.POINTER(V)],
+        "ssm_state_destroy": [V],
+        "ssm_state_reset": [V, P_I32, I32, V],
+        "ssm_state_release": [V, P_I32, I32],
+        "ssm_state_checkpoint": [V, I32, V, V, ctypes.c_size_t, ctypes.POINTER(ssm_slot_meta), V],
+        "ssm_state_restore": [V, I32, V, ctypes.c_size_t, ctypes.POINTER(ssm_slot_meta), V],
+        "ssm_slot_info": [V, I32, ctypes.POINTER(ssm_slot_meta), V],
+        "ssm_state_gather": [V, I32, P_I32, V, V],
+        "ssm_scan_chunk": [V, I32, P_I32, P_I32, P_I64, V, V, V, V, V, V, V, V],
+        "ssm_decode_step": [V, I32, P_I32, V, V, V, V, V, V, V, V],
+        "ssm_verify_copy": [V, I32, I32, P_I32, V, V, V, V, V, V, V, V],
+        "ssm_verify_replay": [V, I32, I32, P_I32, V, V, V, V, V, V, V, V],
+        "ssm_state_commit": [V, I32, P_I32, V, I32, V, V],
+        "ssm_pool_status": [V, ctypes.POINTER(U32), I32, V],
+        "ssm_last_path": [V],
+        "ssm_status_string": [ctypes.c_int],
+        "ssm_pool_bytes": [V],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.ssm_last_path.restype = ctypes.c_char_p
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_pool_bytes.restype = ctypes.c_size_t
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.ssm_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != SSM_OK:
+        raise SSMError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _host_i32(v):
+    a = np.ascontiguousarray(np.asarray(v.cpu() if hasattr(v, "cpu") else v), dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _host_i64(v):
+    a = np.ascontiguousarray(np.asarray(v.cpu() if hasattr(v, "cpu") else v), dtype=np.int64)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def _dev(t, name, dtype=None, numel=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@dataclass
+class Pool:
+    """Handle returned by ssm_state_init, with the config it was made with."""
+    handle: ctypes.c_void_p
+    cfg: ssm_config
+    n_slots: int
+
+    @property
+    def H(self):
+        return self.cfg.nheads
+
+    @property
+    def P(self):
+        return self.cfg.headdim
+
+    @property
+    def N(self):
+        return self.cfg.dstate
+
+    @property
+    def G(self):
+        return self.cfg.ngroups
+
+    def torch_dtype(self, code=None):
+        import torch
+        code = self.cfg.input_dtype if code is None else code
+        return torch.bfloat16 if code == SSM_DTYPE_BF16 else torch.float32
+
+
+def make_config(nheads, headdim, dstate, ngroups, input_dtype=SSM_DTYPE_F32, dt_dtype=SSM_DTYPE_F32,
+                mode=SSM_MODE_COPY, window=16, max_tokens=9) -> ssm_config:
+    return ssm_config(nheads, headdim, dstate, ngroups, input_dtype, dt_dtype, mode, window, max_tokens)
+
+
+# ---------------------------------------------------------------- lifecycle
+
+def ssm_state_init(cfg: ssm_config, n_slots: int, init_state=None, stream=None) -> Pool:
+    import torch
+    hpn = cfg.nheads * cfg.headdim * cfg.dstate
+    ptr = _dev(init_state, "init_state", torch.float32, n_slots * hpn) if init_state is not None else None
+    out = ctypes.c_void_p()
+    _check(_lib.ssm_state_init(ctypes.byref(cfg), int(n_slots), ptr, _stream(stream), ctypes.byref(out)),
+           "ssm_state_init")
+    return Pool(out, cfg, int(n_slots))
+
+
+def ssm_state_destroy(pool: Pool) -> None:
+    if pool.handle:
+        _check(_lib.ssm_state_destroy(pool.handle), "ssm_state_destroy")
+        pool.handle = ctypes.c_void_p()
+
+
+def ssm_state_reset(pool: Pool, slots, stream=None) -> int:
+    a, p = _host_i32(slots)
+    return _lib.ssm_state_reset(pool.handle, p, len(a), _stream(stream))
+
+
+def ssm_state_release(pool: Pool, slots) -> int:
+    a, p = _host_i32(slots)
+    return _lib.ssm_state_release(pool.handle, p, len(a))
+
+
+def ssm_state_checkpoint(pool: Pool, slot: int, A=None, stream=None):
+    """Returns (status, state ndarray float32 [H][P][N], ssm_slot_meta)."""
+    import torch
+    host = np.empty((pool.H, pool.P, pool.N), np.float32)
+    meta = ssm_slot_meta()
+    st = _lib.ssm_state_checkpoint(pool.handle, int(slot), _dev(A, "A", torch.float32, pool.H),
+                                   host.ctypes.data_as(ctypes.c_void_p), host.nbytes, ctypes.byref(meta),
+                                   _stream(stream))
+    return st, host, meta
+
+
+def ssm_state_restore(pool: Pool, slot: int, host_state: np.ndarray, meta: ssm_slot_meta, stream=None) -> int:
+    h = np.ascontiguousarray(host_state, dtype=np.float32)
+    return _lib.ssm_state_restore(pool.handle, int(slot), h.ctypes.data_as(ctypes.c_void_p), h.nbytes,
+                                  ctypes.byref(meta), _stream(stream))
+
+
+def ssm_slot_info(pool: Pool, slot: int, stream=None):
+    meta = ssm_slot_meta()
+    st = _lib.ssm_slot_info(pool.handle, int(slot), ctypes.byref(meta), _stream(stream))
+    return st, meta
+
+
+def ssm_state_gather(pool: Pool, slots, dst, stream=None) -> int:
+    import torch
+    a, p = _host_i32(slots)
+    ptr = _dev(dst, "dst", torch.float32, len(a) * pool.H * pool.P * pool.N)
+    return _lib.ssm_state_gather(pool.handle, len(a), p, ptr, _stream(stream))
+
+
+# ---------------------------------------------------------------- hot path
+
+def _inputs(pool: Pool, n_tok_total: int, x, dt, B, C, A, D, y):
+    import torch
+    td, tdt = pool.torch_dtype(), pool.torch_dtype(pool.cfg.dt_dtype)
+    H, P, N, G = pool.H, pool.P, pool.N, pool.G
+    return (_dev(x, "x", td, n_tok_total * H * P), _dev(dt, "dt", tdt, n_tok_total * H),
+            _dev(B, "B", td, n_tok_total * G * N), _dev(C, "C", td, n_tok_total * G * N),
+            _dev(A, "A", torch.float32, H), _dev(D, "D", torch.float32, H),
+            _dev(y, "y", td, n_tok_total * H * P))
+
+
+def ssm_scan_chunk(pool: Pool, cu_seqlens, slots, chunk_seq, x, dt, B, C, A, D, y, stream=None) -> int:
+    cu, pcu = _host_i32(cu_seqlens)
+    sl, psl = _host_i32(slots)
+    cs, pcs = _host_i64(chunk_seq)
+    if len(cu) != len(sl) + 1 or len(cs) != len(sl):
+        raise ValueError("cu_seqlens must have n_seq + 1 entries and chunk_seq n_seq")
+    total = int(cu[-1])
+    if total == 0:
+        ptrs = (None,) * 7
+    else:
+        ptrs = _inputs(pool, total, x, dt, B, C, A, D, y)
+    return _lib.ssm_scan_chunk(pool.handle, len(sl), pcu, psl, pcs, *ptrs, _stream(stream))
+
+
+def ssm_decode_step(pool: Pool, slots, x, dt, B, C, A, D, y, stream=None) -> int:
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_decode_step(pool.handle, len(sl), psl, *_inputs(pool, len(sl), x, dt, B, C, A, D, y),
+                                _stream(stream))
+
+
+def ssm_verify_copy(pool: Pool, slots, n_tok: int, x, dt, B, C, A, D, y, stream=None) -> int:
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_verify_copy(pool.handle, len(sl), int(n_tok), psl,
+                                *_inputs(pool, len(sl) * n_tok, x, dt, B, C, A, D, y), _stream(stream))
+
+
+def ssm_verify_replay(pool: Pool, slots, n_tok: int, x, dt, B, C, A, D, y, stream=None) -> int:
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_verify_replay(pool.handle, len(sl), int(n_tok), psl,
+                                  *_inputs(pool, len(sl) * n_tok, x, dt, B, C, A, D, y), _stream(stream))
+
+
+def ssm_state_commit(pool: Pool, slots, accept, force_fold: bool = False, A=None, stream=None) -> int:
+    import torch
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_state_commit(pool.handle, len(sl), psl, _dev(accept, "accept", torch.int32, len(sl)),
+                                 1 if force_fold else 0, _dev(A, "A", torch.float32, pool.H), _stream(stream))
+
+
+# ---------------------------------------------------------------- diagnostics
+
+def ssm_pool_status(pool: Pool, clear: bool = False, stream=None):
+    f = ctypes.c_uint32()
+    st = _lib.ssm_pool_status(pool.handle, ctypes.byref(f), 1 if clear else 0, _stream(stream))
+    return st, int(f.value)
+
+
+def ssm_last_path(pool: Pool) -> str:
+    return _lib.ssm_last_path(pool.handle).decode()
+
+
+def ssm_pool_bytes(pool: Pool) -> int:
+    return int(_lib.ssm_pool_bytes(pool.handle))

@@ -1,0 +1,218 @@
+// Internal declarations of libssmstate (not part of the C ABI).
+//
+// Thread layout shared by the state-streaming kernels (decode, copy verify,
+// replay verify, fold, sequential scan): one CTA per (request or sequence,
+// head).  A head's state is P rows of N fp32 values, N contiguous.  Each row
+// is covered by LPR = N / 16 lanes; a lane owns 16 values of the row as four
+// float4 at float4 indices sub, sub + LPR, sub + 2 LPR, sub + 3 LPR, so each
+// 128-bit load or store instruction of a warp touches 32 / LPR rows in
+// contiguous 16 * LPR-byte runs (fully used 128-byte lines for N >= 128).
+// A thread owns kRowsPerThread rows; a warp covers RPW * kRowsPerThread rows,
+// RPW = 32 / LPR, and the CTA has ceil(P / (RPW * kRowsPerThread)) warps.
+// C . h over a row is a partial dot over the lane's 16 values followed by an
+// xor-shuffle reduction over the LPR lanes of the row.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <vector>
+
+#include "ssm_state.h"
+
+namespace ssm {
+
+constexpr int kMaxSlotsPerLaunch = 1024;  // slot lists travel in kernel parameters
+constexpr int kMaxSeqPerLaunch = 1024;
+constexpr int kRowsPerThread = 2;
+constexpr int kMaxThreads = 512;  // per CTA of the state-streaming kernels
+constexpr uint32_t kSlotPoisoned = 1u;
+
+// ---------------------------------------------------------------- pool
+
+struct Pool {
+    ssm_config cfg;
+    int n_slots = 0;
+    int device = 0;
+    int H = 0, P = 0, N = 0, G = 0, hpg = 0;
+    size_t pn = 0;    // P * N floats per head
+    size_t hpn = 0;   // H * P * N floats per slot
+    int t1max = 0;    // max tokens per verify step
+    int wcap = 0;     // replay log capacity: W - 1 + t1max
+    size_t in_bytes = 0;  // bytes per x / B / C element
+
+    float *state = nullptr;      // [n_slots][H][P][N]
+    float *snap = nullptr;       // copy mode: [2][t1max][n_slots][H][P][N]
+    void *log_x = nullptr;       // replay: [n_slots][wcap][H][P]   input dtype
+    float *log_dt = nullptr;     // replay: [n_slots][wcap][H]
+    void *log_B = nullptr;       // replay: [n_slots][wcap][G][N]   input dtype
+    int64_t *d_position = nullptr;
+    int32_t *d_log_len = nullptr;
+    int32_t *d_cur = nullptr;          // copy mode: -1 = base state, else half * t1max + j
+    uint32_t *d_slot_flags = nullptr;  // kSlotPoisoned
+    uint32_t *d_flags = nullptr;       // sticky SSM_FLAG_* bits
+    float *d_stage = nullptr;          // one slot's state, for checkpoint / restore
+    size_t bytes = 0;
+
+    // host mirror
+    std::vector<int64_t> next_chunk, epoch;
+    std::vector<uint8_t> released;
+    std::vector<int32_t> pending_ntok;  // n_tok of the last uncommitted verify, 0 = none
+    const char *last_path = "none";
+};
+
+// ---------------------------------------------------------------- kernel args
+
+struct StepArgs {  // decode, copy verify, replay verify
+    const void *x, *dt, *B, *C;
+    const float *A, *D;
+    void *y;
+    float *state;
+    float *snap;
+    void *log_x;
+    float *log_dt;
+    void *log_B;
+    int64_t *position;
+    int32_t *log_len;
+    int32_t *cur;
+    uint32_t *slot_flags;
+    uint32_t *flags;
+    int H, P, N, G, hpg;
+    int n_slots, t1max, wcap;
+    int n_tok;        // tokens per request in this call (1 for decode)
+    int dt_bf16;      // dt dtype is bf16
+    int check_log;    // replay pool: in-place updates need an empty log
+    int batch;
+    int32_t slots[kMaxSlotsPerLaunch];
+};
+
+struct CommitArgs {
+    const int32_t *accept;
+    const float *A;
+    float *state;
+    void *log_x;
+    float *log_dt;
+    void *log_B;
+    int64_t *position;
+    int32_t *log_len;
+    int32_t *cur;
+    uint32_t *slot_flags;
+    uint32_t *flags;
+    int H, P, N, G, hpg;
+    int n_slots, t1max, wcap, W;
+    int force_fold;
+    int flush;        // fold the log only (checkpoint); accept is ignored
+    int batch;
+    int32_t slots[kMaxSlotsPerLaunch];
+    int32_t ntok[kMaxSlotsPerLaunch];
+};
+
+struct ScanArgs {
+    const void *x, *dt, *B, *C;
+    const float *A, *D;
+    void *y;
+    float *state;
+    float *snap;
+    int32_t *cur;
+    int n_slots;
+    int64_t *position;
+    int32_t *log_len;
+    uint32_t *slot_flags;
+    uint32_t *flags;
+    int H, P, N, G, hpg;
+    int dt_bf16;
+    int check_log;
+    int n_seq;
+    int32_t cu[kMaxSeqPerLaunch + 1];
+    int32_t slots[kMaxSeqPerLaunch];
+};
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaGetLastError() of its launch(es).
+
+cudaError_t launch_decode(const Pool &pool, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_verify_copy(const Pool &pool, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s);
+cudaError_t launch_scan_seq(const Pool &pool, const ScanArgs &a, cudaStream_t s);
+cudaError_t launch_reset(const Pool &pool, const int32_t *slots, int n, cudaStream_t s);
+cudaError_t launch_gather(const Pool &pool, const int32_t *slots, int n, float *dst, cudaStream_t s);
+
+size_t replay_smem_bytes(const Pool &pool, int n_tok);
+size_t fold_smem_bytes(const Pool &pool);
+
+// Instantiate BODY (which names the dstate as NN) for each supported dstate.
+#define SSM_DISPATCH_N(N_, ...)                               \
+    switch (N_) {                                             \
+    case 16: { constexpr int NN = 16; __VA_ARGS__; } break;   \
+    case 32: { constexpr int NN = 32; __VA_ARGS__; } break;   \
+    case 64: { constexpr int NN = 64; __VA_ARGS__; } break;   \
+    case 128: { constexpr int NN = 128; __VA_ARGS__; } break; \
+    case 256: { constexpr int NN = 256; __VA_ARGS__; } break; \
+    default: return cudaErrorInvalidValue;                    \
+    }
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float load_dt(const void *dt, size_t idx, int is_bf16) {
+    return is_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(dt)[idx])
+                   : reinterpret_cast<const float *>(dt)[idx];
+}
+
+// Four consecutive input values starting at element e (e multiple of 4).
+__device__ __forceinline__ float4 load4(const float *p, size_t e) {
+    return *reinterpret_cast<const float4 *>(p + e);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p, size_t e) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p + e);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+    const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ bool finite4(float4 v) {
+    return isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w);
+}
+
+// The lane's 16 values of a length-N vector (see the layout note above).
+template <int N, typename T>
+__device__ __forceinline__ void load_lane16(const T *v, int sub, float (&out)[16]) {
+    constexpr int LPR = N / 16;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 f = load4(v, (size_t)4 * (sub + LPR * q));
+        out[4 * q + 0] = f.x; out[4 * q + 1] = f.y; out[4 * q + 2] = f.z; out[4 * q + 3] = f.w;
+    }
+}
+
+template <int LPR>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Current state of (slot, head h).  Copy pools keep a slot's current state
+// either in the base array (cur = -1) or in snapshot cur after a commit.
+__device__ __forceinline__ float *current_state(float *state, float *snap, const int32_t *cur, int n_slots,
+                                                size_t hpn, size_t pn, int slot, int h) {
+    const size_t off = (size_t)slot * hpn + (size_t)h * pn;
+    if (snap != nullptr) {
+        const int c = cur[slot];
+        if (c >= 0) return snap + (size_t)c * n_slots * hpn + off;
+    }
+    return state + off;
+}
+
+__device__ __forceinline__ float4 ld_stream(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
+__device__ __forceinline__ void st_stream(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
+
+}  // namespace ssm

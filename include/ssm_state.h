@@ -1,0 +1,274 @@
+/*
+ * ssm_state.h -- C ABI of libssmstate, the GB300 (sm_103a) library for the
+ * Mamba-2 selective-state recurrence in its three serving forms.
+ *
+ * The recurrence (Mamba-2 structured state space duality: Mamba Streaming
+ * State That Survives Chunking, section Separate Mamba-2 algebra from kernel
+ * behavior; Why Speculative Decoding Slows Hybrid Mamba Models at Large Batch
+ * Sizes, section The Fix: each token first decays the previous state and then
+ * adds its own rank-one contribution), per request r, head h, row
+ * p < headdim, column n < dstate:
+ *
+ *     dA_t      = exp(dt_t * A_h)
+ *     h_t[p,n]  = dA_t * h_{t-1}[p,n] + dt_t * x_t[p] * B_t[g(h),n]
+ *     y_t[p]    = sum_n C_t[g(h),n] * h_t[p,n] + D_h * x_t[p]
+ *
+ * with groups of contiguous heads, g(h) = h / (nheads / ngroups).  dt arrives
+ * already positive (no softplus or bias is applied here); y reads the state
+ * after the token.  The state is always fp32.
+ *
+ * Layouts (row-major, innermost last; every pointer below is a DEVICE pointer
+ * unless it says host):
+ *   state of a slot   float [nheads][headdim][dstate]
+ *   x, y              [tokens][nheads][headdim]        input dtype
+ *   dt                [tokens][nheads]                  dt dtype
+ *   B, C              [tokens][ngroups][dstate]         input dtype
+ *   A, D              float [nheads]
+ * For a decode step "tokens" is the batch; for a verify step it is
+ * [batch][n_tok]; for a scan it is the packed tokens of all sequences.
+ *
+ * Ownership.  The pool owns all state, snapshot, log and metadata memory
+ * (allocated once by ssm_state_init, freed by ssm_state_destroy).  The caller
+ * owns every input and output buffer and the stream.  All calls are
+ * asynchronous on the given stream unless marked "synchronous".
+ *
+ * Errors.  Host-side checks (null pointers, shapes, slot range, duplicate or
+ * released slots, chunk order) return an error before any work is queued:
+ * nothing advances.  Errors found on the device (non-finite input, a
+ * poisoned slot, an accept count out of range, a non-empty replay log where
+ * none is allowed) do not stop the stream: the kernel skips the affected
+ * (request, head) work, sets a sticky bit in the pool's device flag word,
+ * and marks the slot poisoned; poisoned slots are skipped by every later
+ * call until ssm_state_reset or ssm_state_restore.  ssm_pool_status reads
+ * the flag word.  A pool is not thread safe.
+ */
+#ifndef SSM_STATE_H
+#define SSM_STATE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (0 = the legacy default stream). */
+typedef struct CUstream_st *ssm_stream_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,   /* bad pointer, size, shape, dtype, slot index */
+    SSM_ERR_INVALID_CHUNK = 2, /* malformed chunk (Mamba Streaming State, runnable artifact: invalid_chunk) */
+    SSM_ERR_INVALID_STATE = 3, /* slot released, or commit without a verify (same artifact: invalid_state) */
+    SSM_ERR_SEQUENCE = 4,      /* chunk sequence number out of order (Let the full scan define legal chunking) */
+    SSM_ERR_DUPLICATE = 5,     /* chunk sequence number already applied (same section: a chunk applied twice) */
+    SSM_ERR_SCHEMA = 6,        /* restore of a state whose layout does not match the pool */
+    SSM_ERR_CUDA = 7,          /* a CUDA runtime call failed */
+    SSM_ERR_TIMEOUT = 8,       /* a bounded device wait gave up */
+    SSM_ERR_NO_MEMORY = 9      /* device or host allocation failed */
+} ssm_status;
+
+/* dtype codes (those of the SSM.PREFIX state blob: 0 = fp32, 2 = bf16) */
+enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 2 };
+
+/* speculative verify flavour of a pool */
+enum {
+    SSM_MODE_COPY = 0,   /* verify keeps a full state after every step token */
+    SSM_MODE_REPLAY = 1  /* verify reads checkpoint + input log; commit appends or folds */
+};
+
+/* sticky device flag bits (ssm_pool_status) */
+enum {
+    SSM_FLAG_NONFINITE_INPUT = 1u << 0, /* a NaN or Inf in x, dt, B or C */
+    SSM_FLAG_POISONED_SLOT = 1u << 1,   /* work on a poisoned slot was skipped */
+    SSM_FLAG_BAD_ACCEPT = 1u << 2,      /* accept count outside [0, n_tok - 1] */
+    SSM_FLAG_LOG_NOT_EMPTY = 1u << 3,   /* in-place update on a replay slot whose log is not empty */
+    SSM_FLAG_TIMEOUT = 1u << 4          /* a bounded device wait gave up */
+};
+
+typedef struct {
+    int32_t nheads;      /* H */
+    int32_t headdim;     /* P, 1..256 */
+    int32_t dstate;      /* N, one of 16, 32, 64, 128, 256 */
+    int32_t ngroups;     /* G, divides H */
+    int32_t input_dtype; /* x, B, C and y: SSM_DTYPE_F32 or SSM_DTYPE_BF16 */
+    int32_t dt_dtype;    /* dt: SSM_DTYPE_F32 or SSM_DTYPE_BF16 */
+    int32_t mode;        /* SSM_MODE_COPY or SSM_MODE_REPLAY */
+    int32_t window;      /* replay window W >= 1 (replay mode; ignored otherwise) */
+    int32_t max_tokens;  /* largest n_tok (= T + 1) of one verify step, 1..64 */
+} ssm_config;
+
+/* per-slot metadata (Make reset, checkpoint, and cancellation observable:
+ * the absolute position and the chunk sequence travel with the state) */
+typedef struct {
+    int64_t position;   /* tokens applied since the last reset */
+    int64_t next_chunk; /* chunk sequence number ssm_scan_chunk expects next */
+    int64_t epoch;      /* number of resets of this slot */
+    int32_t log_len;    /* replay mode: tokens in the input log (0..W-1) */
+    uint32_t flags;     /* bit 0: poisoned; bit 1: released */
+} ssm_slot_meta;
+
+typedef struct ssm_pool_s *ssm_pool;
+
+/* ---------------------------------------------------------------- lifecycle */
+
+/*
+ * Create a pool of n_slots fixed-size fp32 states on the current device,
+ * each at position zero with a zero or caller-given initial state (Make
+ * reset, checkpoint, and cancellation observable: initialization).
+ * init_state: device float [n_slots][H][P][N] copied in, or NULL for zeros.
+ * Copy mode also allocates 2 x max_tokens snapshot states per slot; replay
+ * mode allocates a log of W - 1 + max_tokens entries per slot.
+ * Synchronous.  *out is set only on SSM_OK.
+ */
+ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *init_state,
+                          ssm_stream_t stream, ssm_pool *out);
+
+/* Free every allocation of the pool (synchronous; the pool must be idle). */
+ssm_status ssm_state_destroy(ssm_pool pool);
+
+/*
+ * Reset slots (host int32[n]): new sequence boundary, state := 0,
+ * position := 0, next chunk := 0, log emptied, poison cleared, epoch += 1;
+ * also re-opens a released slot (Make reset, checkpoint, and cancellation
+ * observable: a reset cuts every tie to the previous stream).
+ */
+ssm_status ssm_state_reset(ssm_pool pool, const int32_t *slots, int32_t n, ssm_stream_t stream);
+
+/*
+ * Cancellation (host int32[n] slots): the slot stops advancing; every later
+ * call naming it fails with SSM_ERR_INVALID_STATE until it is reset (Make
+ * reset, checkpoint, and cancellation observable: cancellation ends
+ * ownership and further advancement).
+ */
+ssm_status ssm_state_release(ssm_pool pool, const int32_t *slots, int32_t n);
+
+/*
+ * Checkpoint one slot: in replay mode first fold the input log into the
+ * state (A: device float [H], the layer's A; may be NULL in copy mode), then
+ * copy the state (float [H][P][N], H*P*N*4 bytes) into the host buffer and
+ * its metadata into *meta (Make reset, checkpoint, and cancellation
+ * observable: a checkpoint holds what resuming the same stream needs).
+ * Synchronous.
+ * SSM_ERR_INVALID_ARG if cap_bytes is too small.
+ */
+ssm_status ssm_state_checkpoint(ssm_pool pool, int32_t slot, const float *A, float *host_state,
+                                size_t cap_bytes, ssm_slot_meta *meta, ssm_stream_t stream);
+
+/*
+ * Restore one slot from a checkpoint: host float [H][P][N] of exactly
+ * H*P*N*4 bytes and the metadata it was saved with (position, next_chunk,
+ * epoch).  The log is emptied and the poison cleared.  SSM_ERR_SCHEMA if
+ * bytes does not match the pool's state size: an incompatible resume is
+ * refused, never padded or truncated (Make reset, checkpoint, and
+ * cancellation observable: checkpoint receipt).  Synchronous.
+ */
+ssm_status ssm_state_restore(ssm_pool pool, int32_t slot, const float *host_state, size_t bytes,
+                             const ssm_slot_meta *meta, ssm_stream_t stream);
+
+/* Read one slot's metadata (synchronous; no fold). */
+ssm_status ssm_slot_info(ssm_pool pool, int32_t slot, ssm_slot_meta *meta, ssm_stream_t stream);
+
+/*
+ * Copy the current states of n slots (host int32[n]) into dst, device
+ * float [n][H][P][N].  Copy mode resolves which snapshot is current; replay
+ * mode copies the checkpoint as stored (logged tokens not folded in).
+ */
+ssm_status ssm_state_gather(ssm_pool pool, int32_t n, const int32_t *slots, float *dst,
+                            ssm_stream_t stream);
+
+/* ---------------------------------------------------------------- hot path */
+
+/*
+ * Chunked scan of n_seq packed sequences with state handoff ("Let the full
+ * scan define legal chunking": scanning A + B equals scanning A, handing its
+ * final state to B).  Sequence i owns tokens [cu_seqlens[i], cu_seqlens[i+1])
+ * of x / dt / B / C / y and continues from slot slots[i]; its final state is
+ * written back to that slot.  Lengths may be zero (an empty chunk consumes a
+ * sequence number and changes nothing).
+ *   cu_seqlens  host int32[n_seq + 1], non-decreasing, cu_seqlens[0] = 0
+ *   slots       host int32[n_seq], distinct
+ *   chunk_seq   host int64[n_seq]: must equal each slot's next chunk number;
+ *               a smaller value is SSM_ERR_DUPLICATE, a larger one
+ *               SSM_ERR_SEQUENCE (declared mismatch, nothing advances).
+ * Replay pools require an empty log on each slot (device check).
+ */
+ssm_status ssm_scan_chunk(ssm_pool pool, int32_t n_seq, const int32_t *cu_seqlens, const int32_t *slots,
+                          const int64_t *chunk_seq, const void *x, const void *dt, const void *B,
+                          const void *C, const float *A, const float *D, void *y, ssm_stream_t stream);
+
+/*
+ * One decode token for each of `batch` requests, state updated in place
+ * (batched single-token incremental update).  slots: host int32[batch],
+ * distinct.  x [batch][H][P], dt [batch][H], B, C [batch][G][N],
+ * y [batch][H][P].  position += 1.  Replay pools require an empty log.
+ */
+ssm_status ssm_decode_step(ssm_pool pool, int32_t batch, const int32_t *slots, const void *x,
+                           const void *dt, const void *B, const void *C, const float *A,
+                           const float *D, void *y, ssm_stream_t stream);
+
+/*
+ * Speculative verify, copy flavour (copy pools only): each request walks its
+ * n_tok = T + 1 tokens (the pending real token, then T drafts) from its
+ * current state and keeps a full state copy after every token (Why
+ * Speculative Decoding Slows Hybrid Mamba Models, The Problem: undo of a
+ * rejected draft needs a saved state per draft).
+ * x [batch][n_tok][H][P], dt [batch][n_tok][H], B, C [batch][n_tok][G][N],
+ * y [batch][n_tok][H][P].  The current state is not modified.
+ */
+ssm_status ssm_verify_copy(ssm_pool pool, int32_t batch, int32_t n_tok, const int32_t *slots,
+                           const void *x, const void *dt, const void *B, const void *C,
+                           const float *A, const float *D, void *y, ssm_stream_t stream);
+
+/*
+ * Speculative verify, ReplaySSM flavour (replay pools only): outputs come
+ * from the checkpoint and the input log; no state is written in between
+ * (The Fix: the unrolled update gives each output from the checkpoint and
+ * the logged inputs):
+ *   y_j[p] = exp(A * sum of all applied dt) * (C_j . h_ckpt[p,:])
+ *          + sum_s exp(A * sum of dt applied after s) * dt_s * (C_j . B_s) * x_s[p]
+ *          + D * x_j[p]
+ * over the logged tokens and step tokens 0..j.  The step's x, dt and B are
+ * staged after the log for the commit.  Arguments as ssm_verify_copy.
+ */
+ssm_status ssm_verify_replay(ssm_pool pool, int32_t batch, int32_t n_tok, const int32_t *slots,
+                             const void *x, const void *dt, const void *B, const void *C,
+                             const float *A, const float *D, void *y, ssm_stream_t stream);
+
+/*
+ * Commit the last verify of each slot: c = 1 + accept[i] tokens (the real
+ * token plus the drafts kept before the first miss).  accept: device
+ * int32[batch] in [0, n_tok - 1] (outside: SSM_FLAG_BAD_ACCEPT, slot
+ * skipped).  position += c.
+ *   copy mode:   the state after token c - 1 becomes current (a pointer
+ *                move into the snapshots; no state bytes are copied).
+ *   replay mode: if log_len + c < W and !force_fold the c tokens are
+ *                appended to the log; otherwise the log and the c tokens are
+ *                folded into the checkpoint and the log empties (The Fix:
+ *                the full state is written only when the window is full).
+ *                Rejected drafts never enter the log.
+ * Every slot must have had a verify since its last commit or reset
+ * (SSM_ERR_INVALID_STATE otherwise).  A is the same float [H] as the verify's.
+ */
+ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, const int32_t *accept,
+                            int32_t force_fold, const float *A, ssm_stream_t stream);
+
+/* ------------------------------------------------------------- diagnostics */
+
+/* Read (and if clear != 0, clear) the pool's sticky device flags.  Synchronous. */
+ssm_status ssm_pool_status(ssm_pool pool, uint32_t *flags_out, int32_t clear, ssm_stream_t stream);
+
+/* Name of the kernel path the last hot-path call used (static string). */
+const char *ssm_last_path(ssm_pool pool);
+
+/* Static text of a status code. */
+const char *ssm_status_string(ssm_status s);
+
+/* Bytes of device memory the pool holds. */
+size_t ssm_pool_bytes(ssm_pool pool);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_STATE_H */

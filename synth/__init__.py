@@ -12,9 +12,10 @@ Distributions (the synthetic workloads of the Mamba-2 recurrence):
   D_h         ~ N(0, 1)                          (one scalar per head)
   init state  ~ N(0, 0.1)  (standard deviation 0.1)
   accept      = leading successes of T Bernoulli(p) draft checks, i.e. the
-                drafts kept before the first rejected one ("the real token,
-                plus drafts until the first miss", Why Speculative Decoding
-                Slows Hybrid Mamba Models, Implementing It / Role 1).
+                drafts kept before the first rejected one (Why Speculative
+                Decoding Slows Hybrid Mamba Models, Implementing It / Role 1:
+                a step keeps its real token and the drafts up to the first
+                rejection).
 
 bf16 values are produced by round-to-nearest-even from fp32 samples and are
 carried as uint16 bit patterns; ``bf16_to_f32`` widens them exactly.
@@ -43,8 +44,9 @@ def rng(*key: int) -> np.random.Generator:
 def f32_to_bf16(a: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (nearest, ties to even). Returns uint16 bit patterns."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    bias = ((u >> 16) & 1) + 0x7FFF
+    u = a.view(np.uint32)
+    # finite values stay below 2**32 after adding the bias; NaN is set below
+    bias = ((u >> 16) & np.uint32(1)) + np.uint32(0x7FFF)
     out = ((u + bias) >> 16).astype(np.uint16)
     nan = np.isnan(a)
     if nan.any():

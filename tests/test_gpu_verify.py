@@ -1,0 +1,225 @@
+"""GPU parity of speculative verify (state copies and ReplaySSM replay) and of
+the commit (pointer move, log append, fold) against the CPU oracle.  Index
+state (positions, log lengths, fold decisions) must match bit for bit."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests._helpers import check_close, empty_like_out, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+SEED = synth.BASE_SEED + 3000
+
+
+def _mod():
+    import hybrid_serving_mamba_gb300 as m
+    return m
+
+
+def _dev_inputs(x, dt, B, C, dt_in, dt_dt):
+    return to_device(x, dt_in), to_device(dt, dt_dt), to_device(B, dt_in), to_device(C, dt_in)
+
+
+def _wide(x, dt, B, C, dt_in, dt_dt):
+    return synth.widen(x, dt_in), synth.widen(dt, dt_dt), synth.widen(B, dt_in), synth.widen(C, dt_in)
+
+
+def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_tok_pattern=None, force_last=True):
+    import torch
+    m = _mod()
+    n_slots, slots = 8, [6, 1, 3, 0, 7]
+    R = len(slots)
+    T1 = T + 1
+    A, D = synth.head_params(SEED, H)
+    init = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(n_slots)])
+    cfg = m.make_config(H, P, N, G, dt_in, synth.F32, mode, W, T1)
+    pool = m.ssm_state_init(cfg, n_slots, torch.from_numpy(init).cuda())
+    opool = oracle.OraclePool(H, P, N, G, n_slots, A, D, mode=mode, W=W, max_tokens=T1,
+                              init_state=init.astype(np.float64))
+    Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+    acc_all = synth.accept_counts(SEED, steps, R, T, p)
+    verify = m.ssm_verify_copy if mode == m.SSM_MODE_COPY else m.ssm_verify_replay
+    ys = []
+    try:
+        for s in range(steps):
+            nt = T1 if n_tok_pattern is None else n_tok_pattern[s % len(n_tok_pattern)]
+            acc = np.minimum(acc_all[s], nt - 1).astype(np.int32)
+            x, dt, B, C = synth.batch_tokens(SEED, s, R, nt, H, P, G, N, dt_in, synth.F32)
+            y = empty_like_out((R, nt, H, P), dt_in)
+            assert verify(pool, slots, nt, *_dev_inputs(x, dt, B, C, dt_in, synth.F32), Ad, Dd, y) == m.SSM_OK
+            _, yo = opool.verify(slots, *_wide(x, dt, B, C, dt_in, synth.F32))
+            check_close(to_host(y), yo, dt_in, f"y step {s}", positions_axis=1)
+            ys.append(to_host(y))
+            force = force_last and s == steps - 1
+            assert m.ssm_state_commit(pool, slots, torch.from_numpy(acc).cuda(), force, Ad) == m.SSM_OK
+            _, folded = opool.commit(slots, acc, force_fold=force)
+            for sl in range(n_slots):
+                st, meta = m.ssm_slot_info(pool, sl)
+                assert st == m.SSM_OK
+                assert meta.position == opool.position[sl], (s, sl)
+                assert meta.log_len == opool.log_len[sl], (s, sl)
+                assert meta.flags == 0
+        got = torch.empty((n_slots, H, P, N), dtype=torch.float32, device="cuda")
+        assert m.ssm_state_gather(pool, list(range(n_slots)), got) == m.SSM_OK
+        check_close(to_host(got), opool.state, dt_in, "state")
+        st, flags = m.ssm_pool_status(pool)
+        assert st == m.SSM_OK and flags == 0
+        return pool, opool, ys, (A, D)
+    except BaseException:
+        m.ssm_state_destroy(pool)
+        raise
+
+
+@pytest.mark.parametrize("T,p", [(4, 0.6), (3, 0.9)])
+def test_copy_verify_matches_oracle(T, p):
+    m = _mod()
+    pool, _, _, _ = _run_small(m.SSM_MODE_COPY, 16, T, p, steps=7)
+    m.ssm_state_destroy(pool)
+
+
+@pytest.mark.parametrize("W,T,p", [(3, 4, 0.6), (8, 4, 0.8), (16, 2, 0.5), (1, 3, 0.7)])
+def test_replay_verify_matches_oracle(W, T, p):
+    m = _mod()
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, W, T, p, steps=9)
+    m.ssm_state_destroy(pool)
+
+
+def test_replay_mixed_token_counts_and_checkpoint_fold():
+    import torch
+    m = _mod()
+    pool, opool, _, (A, D) = _run_small(m.SSM_MODE_REPLAY, 8, 4, 0.7, steps=6, n_tok_pattern=[5, 2, 3, 1],
+                                        force_last=False)
+    try:
+        Ad = torch.from_numpy(A).cuda()
+        for sl in (6, 1):
+            st, host, meta = m.ssm_state_checkpoint(pool, sl, Ad)
+            assert st == m.SSM_OK and meta.log_len == 0
+            opool.flush([sl])
+            check_close(host.astype(np.float64), opool.state[sl], synth.F32, f"checkpoint {sl}")
+            assert meta.position == opool.position[sl]
+    finally:
+        m.ssm_state_destroy(pool)
+
+
+def test_copy_and_replay_agree_on_gpu():
+    """Same inputs and accept counts through both flavours: outputs agree and,
+    after a final forced fold, so do the states (The Fix: the same math)."""
+    import torch
+    m = _mod()
+    pc, _, yc, _ = _run_small(m.SSM_MODE_COPY, 16, 4, 0.7, steps=8)
+    pr, _, yr, _ = _run_small(m.SSM_MODE_REPLAY, 4, 4, 0.7, steps=8)
+    try:
+        for a, b in zip(yc, yr):
+            check_close(b, a, synth.F32, "replay vs copy y")
+        sc = torch.empty((8, 4, 16, 32), dtype=torch.float32, device="cuda")
+        sr = torch.empty_like(sc)
+        m.ssm_state_gather(pc, list(range(8)), sc)
+        m.ssm_state_gather(pr, list(range(8)), sr)
+        check_close(to_host(sr), to_host(sc), synth.F32, "replay vs copy state")
+    finally:
+        m.ssm_state_destroy(pc)
+        m.ssm_state_destroy(pr)
+
+
+def test_verify_host_side_errors():
+    import torch
+    m = _mod()
+    H, P, N, G = 2, 16, 16, 1
+    cfg = m.make_config(H, P, N, G, 0, 0, m.SSM_MODE_COPY, 4, 3)
+    pool = m.ssm_state_init(cfg, 4)
+    try:
+        A = torch.full((H,), -1.0, device="cuda")
+        acc = torch.zeros(2, dtype=torch.int32, device="cuda")
+        # commit with no verify since the last reset
+        assert m.ssm_state_commit(pool, [0, 1], acc, False, A) == m.SSM_ERR_INVALID_STATE
+        x = torch.zeros((2, 3, H, P), device="cuda")
+        dt = torch.zeros((2, 3, H), device="cuda")
+        B = torch.zeros((2, 3, G, N), device="cuda")
+        y = torch.empty_like(x)
+        # duplicate slot, slot out of range, too many tokens, wrong flavour
+        assert m.ssm_verify_copy(pool, [1, 1], 3, x, dt, B, B, A, A, y) == m.SSM_ERR_INVALID_ARG
+        assert m.ssm_verify_copy(pool, [1, 4], 3, x, dt, B, B, A, A, y) == m.SSM_ERR_INVALID_ARG
+        x4 = torch.zeros((2, 4, H, P), device="cuda")
+        sl_arr, sl_ptr = m._binding._host_i32([0, 1])
+        assert m._binding._lib.ssm_verify_copy(pool.handle, 2, 4, sl_ptr,
+                                               x4.data_ptr(), dt.data_ptr(), B.data_ptr(), B.data_ptr(),
+                                               A.data_ptr(), A.data_ptr(), x4.data_ptr(), None) == m.SSM_ERR_INVALID_ARG
+        del sl_arr
+        assert m.ssm_verify_replay(pool, [0, 1], 3, x, dt, B, B, A, A, y) == m.SSM_ERR_INVALID_ARG
+        # a released slot refuses work until reset
+        assert m.ssm_state_release(pool, [1]) == m.SSM_OK
+        assert m.ssm_verify_copy(pool, [0, 1], 3, x, dt, B, B, A, A, y) == m.SSM_ERR_INVALID_STATE
+        assert m.ssm_state_reset(pool, [1]) == m.SSM_OK
+        assert m.ssm_verify_copy(pool, [0, 1], 3, x, dt, B, B, A, A, y) == m.SSM_OK
+        # accept outside [0, n_tok - 1] is flagged on the device and the slot skipped
+        bad = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
+        assert m.ssm_state_commit(pool, [0, 1], bad, False, A) == m.SSM_OK
+        st, flags = m.ssm_pool_status(pool, clear=True)
+        assert flags & m.SSM_FLAG_BAD_ACCEPT
+        assert m.ssm_slot_info(pool, 0)[1].position == 2 and m.ssm_slot_info(pool, 0)[1].flags == 0
+        assert m.ssm_slot_info(pool, 1)[1].position == 0 and m.ssm_slot_info(pool, 1)[1].flags & 1
+    finally:
+        m.ssm_state_destroy(pool)
+
+
+@pytest.mark.parametrize("T,p,W", [(8, 0.8, 16), (4, 0.6, 8)])
+def test_config3_full_batch_sampled(T, p, W):
+    """Speculative verify at batch 512 with Nemotron-shaped heads, bf16 token
+    inputs, fp32 state: copy and replay flavours on the same inputs and
+    accept counts; three requests followed by the oracle; every slot's
+    position and log length checked against the oracle's commit rule."""
+    import torch
+    m = _mod()
+    H, P, N, G, R, steps = 128, 64, 128, 8, 512, 6
+    T1 = T + 1
+    A, D = synth.head_params(SEED, H)
+    init = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(R)])
+    init_t = torch.from_numpy(init).cuda()
+    sample = [0, 211, 511]
+    osample = {md: oracle.OraclePool(H, P, N, G, len(sample), A, D, mode=md, W=W, max_tokens=T1,
+                                     init_state=init[sample].astype(np.float64)) for md in (0, 1)}
+    del init
+    # the commit rule on every slot, tracked by the oracle pool at unit size
+    meta_rule = oracle.OraclePool(1, 1, 16, 1, R, np.zeros(1), np.zeros(1), mode=1, W=W, max_tokens=T1)
+    pools = {md: m.ssm_state_init(m.make_config(H, P, N, G, synth.BF16, synth.F32, md, W, T1), R, init_t)
+             for md in (0, 1)}
+    del init_t
+    Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+    acc_all = synth.accept_counts(SEED, steps, R, T, p)
+    slots = list(range(R))
+    try:
+        for s in range(steps):
+            x, dt, B, C = synth.batch_tokens(SEED, s, R, T1, H, P, G, N, synth.BF16, synth.F32)
+            dev = _dev_inputs(x, dt, B, C, synth.BF16, synth.F32)
+            acc = torch.from_numpy(acc_all[s]).cuda()
+            ys = {}
+            for md, fn in ((0, m.ssm_verify_copy), (1, m.ssm_verify_replay)):
+                y = empty_like_out((R, T1, H, P), synth.BF16)
+                assert fn(pools[md], slots, T1, *dev, Ad, Dd, y) == m.SSM_OK
+                assert m.ssm_state_commit(pools[md], slots, acc, False, Ad) == m.SSM_OK
+                ys[md] = y
+                _, yo = osample[md].verify(list(range(len(sample))),
+                                           *_wide(x[sample], dt[sample], B[sample], C[sample], synth.BF16, synth.F32))
+                osample[md].commit(list(range(len(sample))), acc_all[s][sample])
+                check_close(to_host(y[sample]), yo, synth.BF16, f"mode {md} y step {s}", positions_axis=1)
+            check_close(to_host(ys[1]), to_host(ys[0]), synth.BF16, f"replay vs copy step {s}")
+            z = np.zeros((R, T1, 1, 1))
+            meta_rule.verify(slots, z, np.zeros((R, T1, 1)), np.zeros((R, T1, 1, 16)), np.zeros((R, T1, 1, 16)))
+            meta_rule.commit(slots, acc_all[s])
+        torch.cuda.synchronize()
+        for md in (0, 1):
+            st, flags = m.ssm_pool_status(pools[md])
+            assert st == m.SSM_OK and flags == 0
+            for sl in slots[::37] + [R - 1]:
+                _, meta = m.ssm_slot_info(pools[md], sl)
+                assert meta.position == meta_rule.position[sl]
+                if md == 1:
+                    assert meta.log_len == meta_rule.log_len[sl]
+            got = torch.empty((len(sample), H, P, N), dtype=torch.float32, device="cuda")
+            m.ssm_state_gather(pools[md], sample, got)
+            check_close(to_host(got), osample[md].state, synth.BF16, f"mode {md} state")
+    finally:
+        for pl in pools.values():
+            m.ssm_state_destroy(pl)
