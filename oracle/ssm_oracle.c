@@ -10,8 +10,8 @@
  * Independent (request, head) pairs are spread over threads with OpenMP;
  * that changes no arithmetic, since each pair's loop is sequential.
  *
- * The recurrence (Mamba-2 selective state space, "structured state space
- * duality", as used by all three pages: Mamba Streaming State That Survives
+ * The recurrence (Mamba-2 selective state space, as used by all three
+ * pages: Mamba Streaming State That Survives
  * Chunking / Separate Mamba-2 algebra from kernel behavior; Why Speculative
  * Decoding Slows Hybrid Mamba Models / The Fix):
  *
@@ -19,8 +19,8 @@
  *   h_t[p,n]  = dA_t * h_{t-1}[p,n] + dt_t * x_t[p] * B_t[g(h),n]
  *   y_t[p]    = sum_n C_t[g(h),n] * h_t[p,n] + D_h * x_t[p]
  *
- * "decay the old state, then add the new token's contribution" (The Fix);
- * the output reads the state after the token is applied.  Heads map to
+ * Each token decays the previous state and then adds its own contribution
+ * (The Fix); the output reads the state after the token is applied.  Heads map to
  * groups in contiguous blocks, g(h) = h / (H / G).
  *
  * Functions:
@@ -109,8 +109,8 @@ void oracle_decode_step(int R, int H, int P, int N, int G, double *state,
 
 /*
  * Speculative verify with per-draft state copies (Why Speculative Decoding
- * Slows Hybrid Mamba Models / The Problem: "saves a full copy of the state
- * after every draft token").  Request r walks its T1 = T+1 tokens from its
+ * Slows Hybrid Mamba Models / The Problem: one full state copy is kept per
+ * draft so that a rejected draft can be undone).  Request r walks its T1 = T+1 tokens from its
  * current state; after token j the full state is saved as snapshot j.
  *   state [R][H][P][N]         read only
  *   x [R][T1][H][P], dt [R][T1][H], B, C [R][T1][G][N]
@@ -144,8 +144,9 @@ void oracle_verify_copy(int R, int T1, int H, int P, int N, int G,
 
 /*
  * ReplaySSM output for one (request, head), closed form (Why Speculative
- * Decoding Slows Hybrid Mamba Models / The Fix: "the checkpoint, decayed,
- * plus each logged token's contribution, decayed by how long ago it came").
+ * Decoding Slows Hybrid Mamba Models / The Fix: the unrolled update is the
+ * decayed checkpoint plus every logged token's term, each decayed by the
+ * time elapsed since that token).
  *
  * u_0 .. u_{k+n_tok-1} are the k logged tokens followed by the n_tok step
  * tokens.  For step token j, the tokens applied so far are u_0 .. u_{m-1}
@@ -245,8 +246,8 @@ void oracle_verify_replay(int R, int T1, int H, int P, int N, int G, int Wc,
 
 /*
  * Fold: write the checkpoint forward through the logged tokens and then the
- * first c[r] step tokens, sequentially ("the full state is written ... when
- * the log fills", The Fix).  Requests with fold[r] == 0 are untouched.
+ * first c[r] step tokens, sequentially (The Fix: the full state is written
+ * only when the log window is full).  Requests with fold[r] == 0 are untouched.
  *   ckpt [R][H][P][N] in/out; log arrays as in oracle_verify_replay;
  *   step tokens x [R][T1][H][P], dt [R][T1][H], B [R][T1][G][N]
  *   (C is not needed: no output is produced).
