@@ -61,6 +61,9 @@ void free_all(Pool &p) {
     cudaFree(p.d_slot_flags);
     cudaFree(p.d_flags);
     cudaFree(p.d_stage);
+    cudaFree(p.d_cb);
+    cudaFree(p.d_fold_items);
+    cudaFree(p.d_fold_count);
 }
 
 int warps_needed(int N, int P) {
@@ -94,6 +97,7 @@ void fill_step(const Pool &p, ssm::StepArgs &a, const void *x, const void *dt, c
     a.x = x; a.dt = dt; a.B = B; a.C = C; a.A = A; a.D = D; a.y = y;
     a.state = p.state; a.snap = p.snap;
     a.log_x = p.log_x; a.log_dt = p.log_dt; a.log_B = p.log_B;
+    a.cb = p.d_cb;
     a.position = p.d_position; a.log_len = p.d_log_len; a.cur = p.d_cur;
     a.slot_flags = p.d_slot_flags; a.flags = p.d_flags;
     a.H = p.H; a.P = p.P; a.N = p.N; a.G = p.G; a.hpg = p.hpg;
@@ -177,11 +181,15 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     p.wcap = c.mode == SSM_MODE_REPLAY ? c.window - 1 + c.max_tokens : 0;
     p.in_bytes = in_elem(c.input_dtype);
     if (cudaGetDevice(&p.device) != cudaSuccess) { delete pool; return SSM_ERR_CUDA; }
+    if (cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess || p.sm_count < 1)
+        p.sm_count = 1;
+    p.cb_rows = std::min(n_slots, ssm::kMaxSlotsPerLaunch);
 
     if (c.mode == SSM_MODE_REPLAY) {
         int max_smem = 0;
         cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device);
         if (ssm::replay_smem_bytes(p, c.max_tokens) > (size_t)max_smem ||
+            ssm::replay_prep_smem_bytes(p, c.max_tokens) > (size_t)max_smem ||
             ssm::fold_smem_bytes(p) > (size_t)max_smem) {
             delete pool;
             return SSM_ERR_INVALID_ARG;
@@ -200,6 +208,9 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         if (e == cudaSuccess) e = alloc(&p.log_dt, ns * p.wcap * p.H, b);
         if (e == cudaSuccess) e = alloc(&lB, ns * p.wcap * p.G * p.N * p.in_bytes, b);
         p.log_B = lB;
+        if (e == cudaSuccess) e = alloc(&p.d_cb, (size_t)p.cb_rows * p.G * p.t1max * p.wcap, b);
+        if (e == cudaSuccess) e = alloc(&p.d_fold_items, (size_t)ssm::kMaxSlotsPerLaunch, b);
+        if (e == cudaSuccess) e = alloc(&p.d_fold_count, 1, b);
     }
     if (e == cudaSuccess) e = alloc(&p.d_position, ns, b);
     if (e == cudaSuccess) e = alloc(&p.d_log_len, ns, b);
@@ -317,6 +328,7 @@ ssm_status ssm_state_checkpoint(ssm_pool pool, int32_t slot, const float *A, flo
         c.slot_flags = p.d_slot_flags; c.flags = p.d_flags;
         c.H = p.H; c.P = p.P; c.N = p.N; c.G = p.G; c.hpg = p.hpg;
         c.n_slots = p.n_slots; c.t1max = p.t1max; c.wcap = p.wcap; c.W = p.cfg.window;
+        c.fold_items = p.d_fold_items; c.fold_count = p.d_fold_count; c.fold_grid = p.H;
         c.flush = 1; c.batch = 1;
         c.slots[0] = slot;
         c.ntok[0] = 1;
@@ -480,11 +492,13 @@ ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, 
     c.slot_flags = p.d_slot_flags; c.flags = p.d_flags;
     c.H = p.H; c.P = p.P; c.N = p.N; c.G = p.G; c.hpg = p.hpg;
     c.n_slots = p.n_slots; c.t1max = p.t1max; c.wcap = p.wcap; c.W = p.cfg.window;
+    c.fold_items = p.d_fold_items; c.fold_count = p.d_fold_count;
     c.force_fold = force_fold ? 1 : 0;
     for (int base = 0; base < batch; base += ssm::kMaxSlotsPerLaunch) {
         const int m = std::min(batch - base, ssm::kMaxSlotsPerLaunch);
         c.accept = accept + base;
         c.batch = m;
+        c.fold_grid = std::min(m * p.H, 2 * p.sm_count);
         for (int i = 0; i < m; ++i) {
             c.slots[i] = slots[base + i];
             c.ntok[i] = p.pending_ntok[slots[base + i]];

@@ -5,18 +5,24 @@
 // u_k .. u_{k+n_tok-1} forming one token sequence u, the output of step
 // token j (m = k + j + 1 tokens applied) is
 //
-//   y_j[p] = exp(A a_j) (C_j . h_c[p,:]) + sum_{s<m} W[j][s] x_s[p] + D x_j[p]
-//   W[j][s] = exp(A a_{j,s}) dt_s (C_j . B_s)
+//   y_j[p] = exp(A a_j) (C_j . h_c[p,:]) + sum_{s<m} W[j][s] x_s[p]
+//   W[j][s] = exp(A a_{j,s}) dt_s (C_j . B_s)  (+ D for s = m - 1, the skip term)
 //
 // where a_j is the sum of all m applied dt and a_{j,s} the sum of the dt
-// applied after token s.  The checkpoint is read once; each state element
-// costs n_tok FMAs (the C_j . h_c products); the small W matrix and the
-// log term W X are computed from shared memory.  No state is written.
+// applied after token s.  Two kernels:
+//   replay_prep   one CTA per (request, group): C_j . B_s for the pairs
+//                 s <= k + j, into pool scratch (shared by the group's heads);
+//                 also appends the step's B after the log;
+//   verify_replay one CTA per (request, head): reads the checkpoint once,
+//                 n_tok FMAs per state element for C_j . h_c, then the small
+//                 W X product from shared memory.  No state is written.
 //
-// The commit (same page, The Fix, and The Problem for the copy flavour):
-// copy pools move the slot's current-state index onto the snapshot of the
-// last kept token; replay pools either append the kept tokens to the log or,
-// when the window would fill, fold log + kept tokens into the checkpoint in
+// The commit (same page, The Fix; The Problem for the copy flavour): a
+// one-thread-per-request kernel makes the index decisions (bit exact): copy
+// pools move the slot's current-state index onto the snapshot of the last
+// kept token; replay pools append the kept tokens (already staged after the
+// log) or, when the window would fill, list the request for a fold.  A
+// persistent kernel then folds only the listed (request, head) pairs in
 // closed form, h <- exp(A a) h + sum_s (exp(A a_s) dt_s x_s) (x) B_s.
 #include "ssm_internal.cuh"
 
@@ -36,22 +42,81 @@ __device__ __forceinline__ void raise_flag(uint32_t *flags, uint32_t *slot_flags
     if (bit != SSM_FLAG_POISONED_SLOT) atomicOr(slot_flags + slot, kSlotPoisoned);
 }
 
+__device__ __forceinline__ size_t cb_index(const StepArgs &a, int i, int g, int j, int s) {
+    return (((size_t)i * a.G + g) * a.t1max + j) * a.wcap + s;
+}
+
+// ------------------------------------------------------------------ prep: C_j . B_s per group
+
+template <int N, typename TI>
+__global__ void __launch_bounds__(256) replay_prep_kernel(const __grid_constant__ StepArgs a) {
+    extern __shared__ float4 smem4[];
+    const int g = blockIdx.x, i = blockIdx.y;
+    const int slot = a.slots[i];
+    const int T1 = a.n_tok;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int wmax = a.wcap - a.t1max;
+    const int k = a.log_len[slot];
+    if ((a.slot_flags[slot] & kSlotPoisoned) || k < 0 || k > wmax) return;  // the main kernel reports it
+    const int m = k + T1;
+    float *sC = reinterpret_cast<float *>(smem4);  // [T1][N]
+    float *sB = sC + (size_t)T1 * N;               // [m][N]
+    const TI *lB = reinterpret_cast<const TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
+    TI *wB = reinterpret_cast<TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
+    const TI *stepB = reinterpret_cast<const TI *>(a.B);
+    const TI *stepC = reinterpret_cast<const TI *>(a.C);
+    bool bad = false;
+    for (int e = threadIdx.x; e < T1 * N; e += blockDim.x) {
+        const int j = e / N, n = e - j * N;
+        const float c = to_f(stepC[(((size_t)i * T1 + j) * a.G + g) * N + n]);
+        bad |= !isfinite(c);
+        sC[e] = c;
+    }
+    for (int e = threadIdx.x; e < m * N; e += blockDim.x) {
+        const int s = e / N, n = e - s * N;
+        float b;
+        if (s < k) {
+            b = to_f(lB[((size_t)s * a.G + g) * N + n]);
+        } else {
+            const TI raw = stepB[(((size_t)i * T1 + (s - k)) * a.G + g) * N + n];
+            b = to_f(raw);
+            bad |= !isfinite(b);
+            wB[((size_t)s * a.G + g) * N + n] = raw;  // staged after the log for the commit
+        }
+        sB[e] = b;
+    }
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_NONFINITE_INPUT);
+        return;
+    }
+    // one warp per (j, s) pair with s <= k + j, lanes over n
+    for (int pr = warp; pr < T1 * m; pr += nwarps) {
+        const int j = pr / m, s = pr - j * m;
+        if (s > k + j) continue;
+        float dot = 0.f;
+#pragma unroll
+        for (int n = lane; n < N; n += 32) dot = fmaf(sC[(size_t)j * N + n], sB[(size_t)s * N + n], dot);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) a.cb[cb_index(a, i, g, j, s)] = dot;
+    }
+}
+
+// ------------------------------------------------------------------ verify
+
 struct ReplaySmem {
-    float *B, *x, *C, *dt, *W, *decay, *d;
+    float *C, *x, *dt, *W, *decay, *d;
 };
 
-// Shared-memory carve-up for m token rows and n_tok step tokens.
-// C and B first: N is a multiple of 16, so both stay 16-byte aligned for
-// float4 reads whatever P is.
+// C first: N is a multiple of 16, so C stays 16-byte aligned for float4 reads.
 __host__ __device__ inline size_t replay_floats(int m, int n_tok, int N, int P) {
-    return (size_t)n_tok * N + (size_t)m * N + (size_t)m * P + m + (size_t)n_tok * m + n_tok + (size_t)n_tok * P;
+    return (size_t)n_tok * N + (size_t)m * P + m + (size_t)n_tok * m + n_tok + (size_t)n_tok * P;
 }
 
 __device__ inline ReplaySmem carve(float *base, int m, int n_tok, int N, int P) {
     ReplaySmem s;
     s.C = base;
-    s.B = s.C + (size_t)n_tok * N;
-    s.x = s.B + (size_t)m * N;
+    s.x = s.C + (size_t)n_tok * N;
     s.dt = s.x + (size_t)m * P;
     s.W = s.dt + m;
     s.decay = s.W + (size_t)n_tok * m;
@@ -69,7 +134,7 @@ __global__ void __launch_bounds__(kMaxThreads) verify_replay_kernel(const __grid
     const int slot = a.slots[i];
     const int g = h / a.hpg;
     const int P = a.P, T1 = a.n_tok;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane % LPR, rw = lane / LPR;
     const int wmax = a.wcap - a.t1max;  // W - 1, the largest legal log length
 
@@ -103,31 +168,16 @@ __global__ void __launch_bounds__(kMaxThreads) verify_replay_kernel(const __grid
     const float A = a.A[h], D = a.D[h];
 
     const TI *lx = reinterpret_cast<const TI *>(a.log_x) + (size_t)slot * a.wcap * a.H * P;
-    const TI *lB = reinterpret_cast<const TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
     const float *ldt = a.log_dt + (size_t)slot * a.wcap * a.H;
-    const TI *sx = reinterpret_cast<const TI *>(a.x);
-    const TI *sB = reinterpret_cast<const TI *>(a.B);
-    const TI *sC = reinterpret_cast<const TI *>(a.C);
     TI *wx = reinterpret_cast<TI *>(a.log_x) + (size_t)slot * a.wcap * a.H * P;
-    TI *wB = reinterpret_cast<TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
     float *wdt = a.log_dt + (size_t)slot * a.wcap * a.H;
+    const TI *sx = reinterpret_cast<const TI *>(a.x);
+    const TI *sC = reinterpret_cast<const TI *>(a.C);
 
-    // token sequence u = log[0..k) ++ step tokens, staged in shared memory;
-    // the step tokens are also written after the log for the commit
+    // x and dt of the token sequence u = log[0..k) ++ step tokens; the step's
+    // x and dt are staged after the log for the commit.  C was checked by
+    // the prep kernel (which poisons the slot before this kernel runs).
     bool bad = false;
-    for (int e = threadIdx.x; e < m * N; e += blockDim.x) {
-        const int s = e / N, n = e - s * N;
-        float b;
-        if (s < k) {
-            b = to_f(lB[((size_t)s * a.G + g) * N + n]);
-        } else {
-            const TI raw = sB[(((size_t)i * T1 + (s - k)) * a.G + g) * N + n];
-            b = to_f(raw);
-            bad |= !isfinite(b);
-            if (h == g * a.hpg) wB[((size_t)s * a.G + g) * N + n] = raw;
-        }
-        sm.B[e] = b;
-    }
     for (int e = threadIdx.x; e < m * P; e += blockDim.x) {
         const int s = e / P, p = e - s * P;
         float xv;
@@ -141,12 +191,6 @@ __global__ void __launch_bounds__(kMaxThreads) verify_replay_kernel(const __grid
         }
         sm.x[e] = xv;
     }
-    for (int e = threadIdx.x; e < T1 * N; e += blockDim.x) {
-        const int j = e / N, n = e - j * N;
-        const float c = to_f(sC[(((size_t)i * T1 + j) * a.G + g) * N + n]);
-        bad |= !isfinite(c);
-        sm.C[e] = c;
-    }
     for (int s = threadIdx.x; s < m; s += blockDim.x) {
         float d;
         if (s < k) {
@@ -158,32 +202,32 @@ __global__ void __launch_bounds__(kMaxThreads) verify_replay_kernel(const __grid
         }
         sm.dt[s] = d;
     }
+    for (int e = threadIdx.x; e < T1 * N; e += blockDim.x) {
+        const int j = e / N, n = e - j * N;
+        sm.C[e] = to_f(sC[(((size_t)i * T1 + j) * a.G + g) * N + n]);
+    }
     if (__syncthreads_or(bad)) {
         if (threadIdx.x == 0) raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_NONFINITE_INPUT);
         return;
     }
 
-    // decay weights: thread j accumulates the dt applied after each token,
-    // from the newest token backwards (the time elapsed since token s)
-    for (int j = threadIdx.x; j < T1; j += blockDim.x) {
-        float after = 0.f;
-        for (int s = k + j; s >= 0; --s) {
-            sm.W[(size_t)j * m + s] = expf(A * after) * sm.dt[s];
-            after += sm.dt[s];
+    // W[j][s]: one thread per pair; the dt applied after token s are summed
+    // newest first (the time elapsed since token s)
+    for (int t = threadIdx.x; t < T1 * m; t += blockDim.x) {
+        const int j = t / m, s = t - j * m;
+        float w = 0.f;
+        if (s <= k + j) {
+            float after = 0.f;
+            for (int r = k + j; r > s; --r) after += sm.dt[r];
+            w = expf(A * after) * sm.dt[s] * a.cb[cb_index(a, i, g, j, s)];
+            if (s == k + j) w += D;  // skip connection D x_j
         }
-        for (int s = k + j + 1; s < m; ++s) sm.W[(size_t)j * m + s] = 0.f;
-        sm.decay[j] = expf(A * after);
+        sm.W[t] = w;
     }
-    __syncthreads();
-    // W[j][s] *= C_j . B_s for s <= k + j: one warp per pair, lanes over n
-    for (int pr = warp; pr < T1 * m; pr += nwarps) {
-        const int j = pr / m, s = pr - j * m;
-        if (s > k + j) continue;
-        float dot = 0.f;
-        for (int n = lane; n < N; n += 32) dot = fmaf(sm.C[(size_t)j * N + n], sm.B[(size_t)s * N + n], dot);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (lane == 0) sm.W[(size_t)j * m + s] *= dot;
+    for (int j = threadIdx.x; j < T1; j += blockDim.x) {
+        float total = 0.f;
+        for (int r = k + j; r >= 0; --r) total += sm.dt[r];
+        sm.decay[j] = expf(A * total);
     }
 
     // C_j . h_c[p,:] for every step token and row
@@ -209,22 +253,21 @@ __global__ void __launch_bounds__(kMaxThreads) verify_replay_kernel(const __grid
     }
     __syncthreads();
 
-    // y_j[p] = decay_j d_j[p] + sum_s W[j][s] x_s[p] + D x_j[p]
+    // y_j[p] = decay_j d_j[p] + sum_{s <= k+j} W[j][s] x_s[p]
     TI *y = reinterpret_cast<TI *>(a.y);
     for (int e = threadIdx.x; e < T1 * P; e += blockDim.x) {
         const int j = e / P, p = e - j * P;
         float acc = sm.decay[j] * sm.d[e];
         const float *wj = sm.W + (size_t)j * m;
         for (int s = 0; s <= k + j; ++s) acc = fmaf(wj[s], sm.x[(size_t)s * P + p], acc);
-        acc = fmaf(D, sm.x[(size_t)(k + j) * P + p], acc);
         y[(((size_t)i * T1 + j) * a.H + h) * P + p] = from_f<TI>(acc);
     }
 }
 
 // ------------------------------------------------------------------ commit
 
-// Decision shared by the fold and metadata kernels: tokens committed (c)
-// and whether the log is folded.  Returns false when the slot is skipped.
+// Decision of one request: tokens committed (c) and whether the log is
+// folded.  Returns false when the request is skipped (err says why).
 __device__ __forceinline__ bool commit_decision(const CommitArgs &a, int i, int slot, int k, int &c, bool &fold,
                                                 uint32_t &err) {
     err = 0;
@@ -241,109 +284,6 @@ __device__ __forceinline__ bool commit_decision(const CommitArgs &a, int i, int 
     return true;
 }
 
-template <int N, typename TI>
-__global__ void __launch_bounds__(kMaxThreads) fold_kernel(const __grid_constant__ CommitArgs a) {
-    constexpr int LPR = N / 16, RPW = 32 / LPR;
-    extern __shared__ float4 smem4[];
-    __shared__ int s_go, s_m;
-    const int h = blockIdx.x, i = blockIdx.y;
-    const int slot = a.slots[i];
-    const int g = h / a.hpg;
-    const int P = a.P;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = lane % LPR, rw = lane / LPR;
-
-    if (threadIdx.x == 0) {
-        const int k = a.log_len[slot];
-        int c = 0;
-        bool fold = false;
-        uint32_t err;
-        const bool ok = commit_decision(a, i, slot, k, c, fold, err);
-        s_go = ok && fold && k >= 0 && k + c <= a.wcap;
-        s_m = k + c;
-    }
-    __syncthreads();
-    if (!s_go) return;
-    const int m = s_m;
-    float *sB = reinterpret_cast<float *>(smem4);   // [m][N]
-    float *sxw = sB + (size_t)m * N;                 // [m][P]  w_s x_s[p]
-    float *sdt = sxw + (size_t)m * P;                // [m]
-    float *sw = sdt + m;                             // [m]
-    __shared__ float s_decay;
-
-    float *st = a.state + ((size_t)slot * a.H + h) * (size_t)P * N;
-    float4 v[RPT][4];
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        const int p = (warp * RPT + r) * RPW + rw;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            v[r][q] = p < P ? ld_stream(st + (size_t)p * N + 4 * (sub + LPR * q)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const float A = a.A[h];
-    const TI *lx = reinterpret_cast<const TI *>(a.log_x) + (size_t)slot * a.wcap * a.H * P;
-    const TI *lB = reinterpret_cast<const TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
-    const float *ldt = a.log_dt + (size_t)slot * a.wcap * a.H;
-    for (int s = threadIdx.x; s < m; s += blockDim.x) sdt[s] = ldt[(size_t)s * a.H + h];
-    for (int e = threadIdx.x; e < m * N; e += blockDim.x) {
-        const int s = e / N, n = e - s * N;
-        sB[e] = to_f(lB[((size_t)s * a.G + g) * N + n]);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {  // time elapsed after each token, newest first
-        float after = 0.f;
-        for (int s = m - 1; s >= 0; --s) {
-            sw[s] = expf(A * after) * sdt[s];
-            after += sdt[s];
-        }
-        s_decay = expf(A * after);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < m * P; e += blockDim.x) {
-        const int s = e / P, p = e - s * P;
-        sxw[e] = sw[s] * to_f(lx[((size_t)s * a.H + h) * P + p]);
-    }
-    __syncthreads();
-
-    const float decay = s_decay;
-#pragma unroll
-    for (int r = 0; r < RPT; ++r)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[r][q].x *= decay; v[r][q].y *= decay; v[r][q].z *= decay; v[r][q].w *= decay;
-        }
-    const float4 *B4 = reinterpret_cast<const float4 *>(sB);
-    int prow[RPT];
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        const int p = (warp * RPT + r) * RPW + rw;
-        prow[r] = p < P ? p : 0;
-    }
-    for (int s = 0; s < m; ++s) {
-        float4 b[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) b[q] = B4[(size_t)s * (N / 4) + sub + LPR * q];
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            const float u = sxw[(size_t)s * P + prow[r]];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                v[r][q].x = fmaf(u, b[q].x, v[r][q].x);
-                v[r][q].y = fmaf(u, b[q].y, v[r][q].y);
-                v[r][q].z = fmaf(u, b[q].z, v[r][q].z);
-                v[r][q].w = fmaf(u, b[q].w, v[r][q].w);
-            }
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        const int p = (warp * RPT + r) * RPW + rw;
-        if (p < P)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) st_stream(st + (size_t)p * N + 4 * (sub + LPR * q), v[r][q]);
-    }
-}
-
 // One thread per request: the index side of the commit (bit exact).
 __global__ void commit_meta_kernel(const __grid_constant__ CommitArgs a, int replay) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -358,6 +298,11 @@ __global__ void commit_meta_kernel(const __grid_constant__ CommitArgs a, int rep
         return;
     }
     if (replay) {
+        if (k < 0 || k + c > a.wcap) {  // corrupted log length
+            raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_BAD_ACCEPT);
+            return;
+        }
+        if (fold) a.fold_items[atomicAdd(a.fold_count, 1)] = make_int2(i, k + c);
         a.log_len[slot] = fold ? 0 : k + c;
     } else {
         const int cur = a.cur[slot];
@@ -367,11 +312,116 @@ __global__ void commit_meta_kernel(const __grid_constant__ CommitArgs a, int rep
     a.position[slot] += c;
 }
 
+// Persistent: CTAs walk the listed (request, head) pairs.
+template <int N, typename TI>
+__global__ void __launch_bounds__(kMaxThreads) fold_kernel(const __grid_constant__ CommitArgs a) {
+    constexpr int LPR = N / 16, RPW = 32 / LPR;
+    extern __shared__ float4 smem4[];
+    __shared__ float s_decay;
+    const int P = a.P;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane % LPR, rw = lane / LPR;
+    const int total = *a.fold_count * a.H;
+    float *sB = reinterpret_cast<float *>(smem4);   // [m][N]
+
+    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        const int2 item = a.fold_items[w / a.H];
+        const int h = w - (w / a.H) * a.H;
+        const int i = item.x, m = item.y;
+        const int slot = a.slots[i];
+        const int g = h / a.hpg;
+        float *sxw = sB + (size_t)m * N;             // [m][P]  w_s x_s[p]
+        float *sdt = sxw + (size_t)m * P;            // [m]
+        float *sw = sdt + m;                         // [m]
+
+        float *st = a.state + ((size_t)slot * a.H + h) * (size_t)P * N;
+        float4 v[RPT][4];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int p = (warp * RPT + r) * RPW + rw;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                v[r][q] = p < P ? ld_stream(st + (size_t)p * N + 4 * (sub + LPR * q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float A = a.A[h];
+        const TI *lx = reinterpret_cast<const TI *>(a.log_x) + (size_t)slot * a.wcap * a.H * P;
+        const TI *lB = reinterpret_cast<const TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
+        const float *ldt = a.log_dt + (size_t)slot * a.wcap * a.H;
+        for (int s = threadIdx.x; s < m; s += blockDim.x) sdt[s] = ldt[(size_t)s * a.H + h];
+        for (int e = threadIdx.x; e < m * N; e += blockDim.x) {
+            const int s = e / N, n = e - s * N;
+            sB[e] = to_f(lB[((size_t)s * a.G + g) * N + n]);
+        }
+        __syncthreads();
+        // decay weight of token s: exp(A * dt applied after it), newest first
+        for (int s = threadIdx.x; s < m; s += blockDim.x) {
+            float after = 0.f;
+            for (int r = m - 1; r > s; --r) after += sdt[r];
+            sw[s] = expf(A * after) * sdt[s];
+        }
+        if (threadIdx.x == 0) {
+            float all = 0.f;
+            for (int r = m - 1; r >= 0; --r) all += sdt[r];
+            s_decay = expf(A * all);
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < m * P; e += blockDim.x) {
+            const int s = e / P, p = e - s * P;
+            sxw[e] = sw[s] * to_f(lx[((size_t)s * a.H + h) * P + p]);
+        }
+        __syncthreads();
+
+        const float decay = s_decay;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                v[r][q].x *= decay; v[r][q].y *= decay; v[r][q].z *= decay; v[r][q].w *= decay;
+            }
+        const float4 *B4 = reinterpret_cast<const float4 *>(sB);
+        int prow[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int p = (warp * RPT + r) * RPW + rw;
+            prow[r] = p < P ? p : 0;
+        }
+        for (int s = 0; s < m; ++s) {
+            float4 b[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) b[q] = B4[(size_t)s * (N / 4) + sub + LPR * q];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const float u = sxw[(size_t)s * P + prow[r]];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    v[r][q].x = fmaf(u, b[q].x, v[r][q].x);
+                    v[r][q].y = fmaf(u, b[q].y, v[r][q].y);
+                    v[r][q].z = fmaf(u, b[q].z, v[r][q].z);
+                    v[r][q].w = fmaf(u, b[q].w, v[r][q].w);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int p = (warp * RPT + r) * RPW + rw;
+            if (p < P)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st_stream(st + (size_t)p * N + 4 * (sub + LPR * q), v[r][q]);
+        }
+        __syncthreads();  // shared memory is reused by the next item
+    }
+}
+
 }  // namespace
 
 size_t replay_smem_bytes(const Pool &pool, int n_tok) {
     const int m = pool.wcap - pool.t1max + n_tok;  // W - 1 + n_tok
     return replay_floats(m, n_tok, pool.N, pool.P) * sizeof(float);
+}
+
+size_t replay_prep_smem_bytes(const Pool &pool, int n_tok) {
+    const int m = pool.wcap - pool.t1max + n_tok;
+    return ((size_t)n_tok * pool.N + (size_t)m * pool.N) * sizeof(float);
 }
 
 size_t fold_smem_bytes(const Pool &pool) {
@@ -385,21 +435,27 @@ static cudaError_t set_smem(K kernel, size_t bytes) {
 }
 
 cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s) {
-    const dim3 grid(a.H, a.batch);
     const size_t smem = replay_smem_bytes(pool, a.n_tok);
+    const size_t psmem = replay_prep_smem_bytes(pool, a.n_tok);
     const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
     SSM_DISPATCH_N(a.N, {
         const dim3 block(32 * warps_for<NN>(a.P));
         if (bf) {
+            auto kp = replay_prep_kernel<NN, __nv_bfloat16>;
             auto k = verify_replay_kernel<NN, __nv_bfloat16>;
-            cudaError_t e = set_smem(k, smem);
+            cudaError_t e = set_smem(kp, psmem);
+            if (e == cudaSuccess) e = set_smem(k, smem);
             if (e != cudaSuccess) return e;
-            k<<<grid, block, smem, s>>>(a);
+            kp<<<dim3(a.G, a.batch), 256, psmem, s>>>(a);
+            k<<<dim3(a.H, a.batch), block, smem, s>>>(a);
         } else {
+            auto kp = replay_prep_kernel<NN, float>;
             auto k = verify_replay_kernel<NN, float>;
-            cudaError_t e = set_smem(k, smem);
+            cudaError_t e = set_smem(kp, psmem);
+            if (e == cudaSuccess) e = set_smem(k, smem);
             if (e != cudaSuccess) return e;
-            k<<<grid, block, smem, s>>>(a);
+            kp<<<dim3(a.G, a.batch), 256, psmem, s>>>(a);
+            k<<<dim3(a.H, a.batch), block, smem, s>>>(a);
         }
     });
     return cudaGetLastError();
@@ -408,7 +464,11 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
 cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s) {
     const bool replay = pool.cfg.mode == SSM_MODE_REPLAY;
     if (replay) {
-        const dim3 grid(a.H, a.batch);
+        const cudaError_t e = cudaMemsetAsync(a.fold_count, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return e;
+    }
+    commit_meta_kernel<<<(a.batch + 127) / 128, 128, 0, s>>>(a, replay ? 1 : 0);
+    if (replay) {
         const size_t smem = fold_smem_bytes(pool);
         const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
         SSM_DISPATCH_N(a.N, {
@@ -417,18 +477,15 @@ cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s)
                 auto k = fold_kernel<NN, __nv_bfloat16>;
                 cudaError_t e = set_smem(k, smem);
                 if (e != cudaSuccess) return e;
-                k<<<grid, block, smem, s>>>(a);
+                k<<<a.fold_grid, block, smem, s>>>(a);
             } else {
                 auto k = fold_kernel<NN, float>;
                 cudaError_t e = set_smem(k, smem);
                 if (e != cudaSuccess) return e;
-                k<<<grid, block, smem, s>>>(a);
+                k<<<a.fold_grid, block, smem, s>>>(a);
             }
         });
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
     }
-    commit_meta_kernel<<<(a.batch + 127) / 128, 128, 0, s>>>(a, replay ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -52,6 +52,12 @@ struct Pool {
     uint32_t *d_slot_flags = nullptr;  // kSlotPoisoned
     uint32_t *d_flags = nullptr;       // sticky SSM_FLAG_* bits
     float *d_stage = nullptr;          // one slot's state, for checkpoint / restore
+    // replay scratch: C_j . B_s of one launch's requests, [cb_rows][G][t1max][wcap]
+    float *d_cb = nullptr;
+    int cb_rows = 0;
+    int2 *d_fold_items = nullptr;      // (request index, tokens to fold) of one commit launch
+    int32_t *d_fold_count = nullptr;
+    int sm_count = 1;
     size_t bytes = 0;
 
     // host mirror
@@ -72,6 +78,7 @@ struct StepArgs {  // decode, copy verify, replay verify
     void *log_x;
     float *log_dt;
     void *log_B;
+    float *cb;        // replay scratch (see Pool::d_cb)
     int64_t *position;
     int32_t *log_len;
     int32_t *cur;
@@ -98,8 +105,11 @@ struct CommitArgs {
     int32_t *cur;
     uint32_t *slot_flags;
     uint32_t *flags;
+    int2 *fold_items;
+    int32_t *fold_count;
     int H, P, N, G, hpg;
     int n_slots, t1max, wcap, W;
+    int fold_grid;    // CTAs of the persistent fold kernel
     int force_fold;
     int flush;        // fold the log only (checkpoint); accept is ignored
     int batch;
@@ -139,6 +149,7 @@ cudaError_t launch_reset(const Pool &pool, const int32_t *slots, int n, cudaStre
 cudaError_t launch_gather(const Pool &pool, const int32_t *slots, int n, float *dst, cudaStream_t s);
 
 size_t replay_smem_bytes(const Pool &pool, int n_tok);
+size_t replay_prep_smem_bytes(const Pool &pool, int n_tok);
 size_t fold_smem_bytes(const Pool &pool);
 
 // Instantiate BODY (which names the dstate as NN) for each supported dstate.
