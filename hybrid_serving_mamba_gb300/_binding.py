@@ -34,7 +34,7 @@ EXPORTS = (
     "ssm_state_init", "ssm_state_destroy", "ssm_state_reset", "ssm_state_release", "ssm_state_checkpoint",
     "ssm_state_restore", "ssm_slot_info", "ssm_state_gather", "ssm_scan_chunk", "ssm_decode_step",
     "ssm_verify_copy", "ssm_verify_replay", "ssm_state_commit", "ssm_pool_status", "ssm_last_path",
-    "ssm_status_string", "ssm_pool_bytes",
+    "ssm_status_string", "ssm_pool_bytes", "ssm_verify_replay_static",
 )
 
 
@@ -81,6 +81,8 @@ def _load():
         "ssm_last_path": [V],
         "ssm_status_string": [ctypes.c_int],
         "ssm_pool_bytes": [V],
+        "ssm_verify_replay_static": [I32, I32, I32, I32, I32, I32, I32, I32, I32, V, V, V, V, V,
+                                     V, V, V, V, V, V, V, V, V],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -298,3 +300,28 @@ def ssm_last_path(pool: Pool) -> str:
 
 def ssm_pool_bytes(pool: Pool) -> int:
     return int(_lib.ssm_pool_bytes(pool.handle))
+
+
+# ---------------------------------------------------------------- no-allocation variant
+
+SSM_STATIC_SCRATCH_FLOATS = 1047552
+
+
+def ssm_verify_replay_static(batch, n_tok, nheads, headdim, dstate, ngroups, window, input_dtype, dt_dtype,
+                             ckpt, log_x, log_dt, log_B, log_len, x, dt, B, C, A, D, y, flags, stream=None) -> int:
+    """Replay verify on caller-owned buffers with the library's built-in
+    scratch (no pool, no allocation); see ssm_verify_replay_static in
+    include/ssm_state.h for the buffer shapes."""
+    import torch
+    wc = window - 1 + n_tok
+    tin = torch.bfloat16 if input_dtype == SSM_DTYPE_BF16 else torch.float32
+    tdt = torch.bfloat16 if dt_dtype == SSM_DTYPE_BF16 else torch.float32
+    H, P, N, G = nheads, headdim, dstate, ngroups
+    return _lib.ssm_verify_replay_static(
+        int(batch), int(n_tok), H, P, N, G, int(window), int(input_dtype), int(dt_dtype),
+        _dev(ckpt, "ckpt", torch.float32, batch * H * P * N), _dev(log_x, "log_x", tin, batch * wc * H * P),
+        _dev(log_dt, "log_dt", torch.float32, batch * wc * H), _dev(log_B, "log_B", tin, batch * wc * G * N),
+        _dev(log_len, "log_len", torch.int32, batch), _dev(x, "x", tin, batch * n_tok * H * P),
+        _dev(dt, "dt", tdt, batch * n_tok * H), _dev(B, "B", tin, batch * n_tok * G * N),
+        _dev(C, "C", tin, batch * n_tok * G * N), _dev(A, "A", torch.float32, H), _dev(D, "D", torch.float32, H),
+        _dev(y, "y", tin, batch * n_tok * H * P), _dev(flags, "flags", torch.int32, 1), _stream(stream))

@@ -24,6 +24,9 @@
 // log) or, when the window would fill, list the request for a fold.  A
 // persistent kernel then folds only the listed (request, head) pairs in
 // closed form, h <- exp(A a) h + sum_s (exp(A a_s) dt_s x_s) (x) B_s.
+#include <cstring>
+#include <mutex>
+
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -490,3 +493,115 @@ cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s)
 }
 
 }  // namespace ssm
+
+// ---------------------------------------------------------------------------
+// Replay verify for callers that cannot allocate device memory.
+//
+// Code that cannot call cudaMalloc -- a serving engine whose caching
+// allocator owns all device memory, or a plugin that is handed only the
+// buffers its host runtime manages -- cannot create a pool.  ssm_verify_replay_static runs the same two kernels as
+// ssm_verify_replay on buffers the caller owns and takes its scratch (the
+// C_j . B_s pair matrix and one status word per request) from the
+// file-scope array below, which is part of the library image: every GPU
+// that loads the library holds its 4 MiB until the process exits, and no
+// call allocates anything.  Every call shares the array, so calls that
+// overlap on the GPU (two streams, or two threads) race on it.
+namespace ssm {
+namespace {
+
+constexpr size_t kStaticScratchFloats = size_t(1) << 20;  // 4 MiB
+constexpr size_t kStaticFlagWords = kMaxSlotsPerLaunch;    // per-request status words, at the end
+static_assert(kStaticFlagWords < kStaticScratchFloats, "scratch layout");
+constexpr size_t kStaticCbFloats = kStaticScratchFloats - kStaticFlagWords;
+static_assert(kStaticCbFloats == SSM_STATIC_SCRATCH_FLOATS, "header and library disagree");
+
+static __device__ __align__(256) float g_noalloc_scratch[kStaticScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a stand-in for the symbol, so the address is
+// looked up once per device, with that device current.
+cudaError_t noalloc_scratch(float **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace ssm
+
+extern "C" ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int32_t nheads, int32_t headdim,
+                                               int32_t dstate, int32_t ngroups, int32_t window, int32_t input_dtype,
+                                               int32_t dt_dtype, const float *ckpt, void *log_x, float *log_dt,
+                                               void *log_B, const int32_t *log_len, const void *x, const void *dt,
+                                               const void *B, const void *C, const float *A, const float *D, void *y,
+                                               uint32_t *flags, ssm_stream_t stream) {
+    using namespace ssm;
+    const bool n_ok = dstate == 16 || dstate == 32 || dstate == 64 || dstate == 128 || dstate == 256;
+    if (batch < 1 || batch > kMaxSlotsPerLaunch || n_tok < 1 || n_tok > 64 || nheads < 1 || headdim < 1 ||
+        headdim > 256 || !n_ok || ngroups < 1 || nheads % ngroups || window < 1 || window > 1024)
+        return SSM_ERR_INVALID_ARG;
+    if ((input_dtype != SSM_DTYPE_F32 && input_dtype != SSM_DTYPE_BF16) ||
+        (dt_dtype != SSM_DTYPE_F32 && dt_dtype != SSM_DTYPE_BF16))
+        return SSM_ERR_INVALID_ARG;
+    if (!ckpt || !log_x || !log_dt || !log_B || !log_len || !x || !dt || !B || !C || !A || !D || !y || !flags)
+        return SSM_ERR_INVALID_ARG;
+    const int wcap = window - 1 + n_tok;
+    if ((size_t)batch * ngroups * n_tok * wcap > kStaticCbFloats) return SSM_ERR_INVALID_ARG;  // scratch too small
+    const int rows_per_warp = (32 / (dstate / 16)) * kRowsPerThread;
+    if (32 * ((headdim + rows_per_warp - 1) / rows_per_warp) > kMaxThreads) return SSM_ERR_INVALID_ARG;
+
+    // launch geometry only: a Pool describing the caller's buffers (no allocation)
+    Pool view;
+    view.cfg.nheads = nheads; view.cfg.headdim = headdim; view.cfg.dstate = dstate; view.cfg.ngroups = ngroups;
+    view.cfg.input_dtype = input_dtype; view.cfg.dt_dtype = dt_dtype; view.cfg.mode = SSM_MODE_REPLAY;
+    view.cfg.window = window; view.cfg.max_tokens = n_tok;
+    view.H = nheads; view.P = headdim; view.N = dstate; view.G = ngroups; view.hpg = nheads / ngroups;
+    view.t1max = n_tok; view.wcap = wcap; view.n_slots = batch;
+    int dev = 0, max_smem = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (replay_smem_bytes(view, n_tok) > (size_t)max_smem || replay_prep_smem_bytes(view, n_tok) > (size_t)max_smem)
+        return SSM_ERR_INVALID_ARG;
+
+    float *scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return SSM_ERR_CUDA;
+    uint32_t *req_flags = reinterpret_cast<uint32_t *>(scratch + kStaticCbFloats);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // per-request status words start clear on every call (the pair matrix
+    // is fully rewritten for every pair the verify reads)
+    if (cudaMemsetAsync(req_flags, 0, (size_t)batch * sizeof(uint32_t), s) != cudaSuccess) return SSM_ERR_CUDA;
+
+    StepArgs a;
+    std::memset(&a, 0, offsetof(StepArgs, slots));
+    a.x = x; a.dt = dt; a.B = B; a.C = C; a.A = A; a.D = D; a.y = y;
+    a.state = const_cast<float *>(ckpt);  // read only: the replay kernels never write the checkpoint
+    a.log_x = log_x; a.log_dt = log_dt; a.log_B = log_B;
+    a.cb = scratch;
+    a.log_len = const_cast<int32_t *>(log_len);  // read only
+    a.slot_flags = req_flags;
+    a.flags = flags;
+    a.H = nheads; a.P = headdim; a.N = dstate; a.G = ngroups; a.hpg = nheads / ngroups;
+    a.n_slots = batch; a.t1max = n_tok; a.wcap = wcap;
+    a.n_tok = n_tok;
+    a.dt_bf16 = dt_dtype == SSM_DTYPE_BF16;
+    a.check_log = 1;
+    a.batch = batch;
+    for (int i = 0; i < batch; ++i) a.slots[i] = i;  // request i owns row i of every caller buffer
+    const cudaError_t e = launch_verify_replay(view, a, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}

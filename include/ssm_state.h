@@ -253,6 +253,41 @@ ssm_status ssm_verify_replay(ssm_pool pool, int32_t batch, int32_t n_tok, const 
 ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, const int32_t *accept,
                             int32_t force_fold, const float *A, ssm_stream_t stream);
 
+/*
+ * ssm_verify_replay without a pool and without any allocation.  The pages
+ * have no counterpart to this entry point: it is for callers that cannot
+ * call cudaMalloc -- a serving engine whose caching allocator owns all
+ * device memory, or a plugin that is handed only the buffers its host
+ * runtime manages -- and so cannot create a pool.  It runs the same kernels
+ * as ssm_verify_replay.
+ * The caller owns every buffer; request i uses row i of each (Wc = window - 1 + n_tok):
+ *   ckpt     device float [batch][H][P][N], the checkpoints (read only)
+ *   log_x    device [batch][Wc][H][P] (input dtype)
+ *   log_dt   device float [batch][Wc][H]
+ *   log_B    device [batch][Wc][G][N] (input dtype)
+ *   log_len  device int32 [batch], logged tokens per request, each in [0, window - 1]
+ *   x, dt, B, C, A, D, y   as ssm_verify_replay, [batch][n_tok][...]
+ *   flags    device uint32: SSM_FLAG_* bits are ORed in, never cleared
+ * Like ssm_verify_replay it writes the step's x, dt and B after each log
+ * (entries log_len .. log_len + n_tok - 1), so appending c accepted tokens
+ * is log_len += c; folding into ckpt is the caller's business.
+ * Its scratch is a 4 MiB array inside the library, held by every GPU that
+ * loads it until the process exits: batch <= 1024 and
+ * batch * G * n_tok * Wc <= SSM_STATIC_SCRATCH_FLOATS, else
+ * SSM_ERR_INVALID_ARG.  The first call on a device looks up the array's
+ * device address (once per device, with that device current); make that
+ * first call before any stream capture.  All calls share the array, which
+ * keeps the last call's contents: calls that overlap on the GPU race.
+ * Asynchronous on stream.
+ */
+#define SSM_STATIC_SCRATCH_FLOATS 1047552
+ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int32_t nheads, int32_t headdim, int32_t dstate,
+                                    int32_t ngroups, int32_t window, int32_t input_dtype, int32_t dt_dtype,
+                                    const float *ckpt, void *log_x, float *log_dt, void *log_B,
+                                    const int32_t *log_len, const void *x, const void *dt, const void *B,
+                                    const void *C, const float *A, const float *D, void *y, uint32_t *flags,
+                                    ssm_stream_t stream);
+
 /* ------------------------------------------------------------- diagnostics */
 
 /* Read (and if clear != 0, clear) the pool's sticky device flags.  Synchronous. */
