@@ -98,6 +98,7 @@ void fill_step(const Pool &p, ssm::StepArgs &a, const void *x, const void *dt, c
     a.state = p.state; a.snap = p.snap;
     a.log_x = p.log_x; a.log_dt = p.log_dt; a.log_B = p.log_B;
     a.cb = p.d_cb;
+    a.cb_w = p.cb_w;
     a.position = p.d_position; a.log_len = p.d_log_len; a.cur = p.d_cur;
     a.slot_flags = p.d_slot_flags; a.flags = p.d_flags;
     a.H = p.H; a.P = p.P; a.N = p.N; a.G = p.G; a.hpg = p.hpg;
@@ -179,6 +180,7 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     p.hpn = (size_t)p.H * p.pn;
     p.t1max = c.max_tokens;
     p.wcap = c.mode == SSM_MODE_REPLAY ? c.window - 1 + c.max_tokens : 0;
+    p.cb_w = (p.wcap + 3) / 4 * 4;
     p.in_bytes = in_elem(c.input_dtype);
     if (cudaGetDevice(&p.device) != cudaSuccess) { delete pool; return SSM_ERR_CUDA; }
     if (cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess || p.sm_count < 1)
@@ -208,7 +210,7 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         if (e == cudaSuccess) e = alloc(&p.log_dt, ns * p.wcap * p.H, b);
         if (e == cudaSuccess) e = alloc(&lB, ns * p.wcap * p.G * p.N * p.in_bytes, b);
         p.log_B = lB;
-        if (e == cudaSuccess) e = alloc(&p.d_cb, (size_t)p.cb_rows * p.G * p.t1max * p.wcap, b);
+        if (e == cudaSuccess) e = alloc(&p.d_cb, (size_t)p.cb_rows * p.G * p.t1max * p.cb_w, b);
         if (e == cudaSuccess) e = alloc(&p.d_fold_items, (size_t)ssm::kMaxSlotsPerLaunch, b);
         if (e == cudaSuccess) e = alloc(&p.d_fold_count, 1, b);
     }
@@ -453,11 +455,17 @@ static ssm_status verify_common(ssm_pool pool, int32_t batch, int32_t n_tok, con
     DeviceGuard g(p.device);
     ssm::StepArgs a;
     fill_step(p, a, x, dt, B, C, A, D, y, n_tok);
-    st = run_step(p, a, slots, batch, n_tok, mode == SSM_MODE_COPY ? ssm::launch_verify_copy : ssm::launch_verify_replay,
-                  reinterpret_cast<cudaStream_t>(stream));
+    const char *path = mode == SSM_MODE_COPY ? "verify_copy" : "verify_replay";
+    auto replay = [&path](const Pool &pl, const ssm::StepArgs &sa, cudaStream_t s) {
+        return ssm::launch_verify_replay(pl, sa, s, &path);
+    };
+    if (mode == SSM_MODE_COPY)
+        st = run_step(p, a, slots, batch, n_tok, ssm::launch_verify_copy, reinterpret_cast<cudaStream_t>(stream));
+    else
+        st = run_step(p, a, slots, batch, n_tok, replay, reinterpret_cast<cudaStream_t>(stream));
     if (st != SSM_OK) return st;
     for (int i = 0; i < batch; ++i) p.pending_ntok[slots[i]] = n_tok;
-    p.last_path = mode == SSM_MODE_COPY ? "verify_copy" : "verify_replay";
+    p.last_path = path;
     return SSM_OK;
 }
 

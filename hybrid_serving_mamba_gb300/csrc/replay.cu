@@ -46,7 +46,7 @@ __device__ __forceinline__ void raise_flag(uint32_t *flags, uint32_t *slot_flags
 }
 
 __device__ __forceinline__ size_t cb_index(const StepArgs &a, int i, int g, int j, int s) {
-    return (((size_t)i * a.G + g) * a.t1max + j) * a.wcap + s;
+    return (((size_t)i * a.G + g) * a.t1max + j) * a.cb_w + s;
 }
 
 // ------------------------------------------------------------------ prep: C_j . B_s per group
@@ -437,7 +437,7 @@ static cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s) {
+cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path) {
     const size_t smem = replay_smem_bytes(pool, a.n_tok);
     const size_t psmem = replay_prep_smem_bytes(pool, a.n_tok);
     const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
@@ -445,19 +445,32 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
         const dim3 block(32 * warps_for<NN>(a.P));
         if (bf) {
             auto kp = replay_prep_kernel<NN, __nv_bfloat16>;
-            auto k = verify_replay_kernel<NN, __nv_bfloat16>;
             cudaError_t e = set_smem(kp, psmem);
-            if (e == cudaSuccess) e = set_smem(k, smem);
             if (e != cudaSuccess) return e;
             kp<<<dim3(a.G, a.batch), 256, psmem, s>>>(a);
-            k<<<dim3(a.H, a.batch), block, smem, s>>>(a);
         } else {
             auto kp = replay_prep_kernel<NN, float>;
-            auto k = verify_replay_kernel<NN, float>;
             cudaError_t e = set_smem(kp, psmem);
-            if (e == cudaSuccess) e = set_smem(k, smem);
             if (e != cudaSuccess) return e;
             kp<<<dim3(a.G, a.batch), 256, psmem, s>>>(a);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = launch_verify_replay_pipe(pool, a, s);
+        if (e != cudaErrorNotSupported) {
+            if (path) *path = "verify_replay_pipe";
+            return e;
+        }
+        if (path) *path = "verify_replay";
+        if (bf) {
+            auto k = verify_replay_kernel<NN, __nv_bfloat16>;
+            e = set_smem(k, smem);
+            if (e != cudaSuccess) return e;
+            k<<<dim3(a.H, a.batch), block, smem, s>>>(a);
+        } else {
+            auto k = verify_replay_kernel<NN, float>;
+            e = set_smem(k, smem);
+            if (e != cudaSuccess) return e;
             k<<<dim3(a.H, a.batch), block, smem, s>>>(a);
         }
     });
@@ -560,7 +573,8 @@ extern "C" ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int
     if (!ckpt || !log_x || !log_dt || !log_B || !log_len || !x || !dt || !B || !C || !A || !D || !y || !flags)
         return SSM_ERR_INVALID_ARG;
     const int wcap = window - 1 + n_tok;
-    if ((size_t)batch * ngroups * n_tok * wcap > kStaticCbFloats) return SSM_ERR_INVALID_ARG;  // scratch too small
+    const int cb_w = (wcap + 3) / 4 * 4;
+    if ((size_t)batch * ngroups * n_tok * cb_w > kStaticCbFloats) return SSM_ERR_INVALID_ARG;  // scratch too small
     const int rows_per_warp = (32 / (dstate / 16)) * kRowsPerThread;
     if (32 * ((headdim + rows_per_warp - 1) / rows_per_warp) > kMaxThreads) return SSM_ERR_INVALID_ARG;
 
@@ -570,7 +584,7 @@ extern "C" ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int
     view.cfg.input_dtype = input_dtype; view.cfg.dt_dtype = dt_dtype; view.cfg.mode = SSM_MODE_REPLAY;
     view.cfg.window = window; view.cfg.max_tokens = n_tok;
     view.H = nheads; view.P = headdim; view.N = dstate; view.G = ngroups; view.hpg = nheads / ngroups;
-    view.t1max = n_tok; view.wcap = wcap; view.n_slots = batch;
+    view.t1max = n_tok; view.wcap = wcap; view.n_slots = batch; view.cb_w = cb_w;
     int dev = 0, max_smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
@@ -592,6 +606,7 @@ extern "C" ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int
     a.state = const_cast<float *>(ckpt);  // read only: the replay kernels never write the checkpoint
     a.log_x = log_x; a.log_dt = log_dt; a.log_B = log_B;
     a.cb = scratch;
+    a.cb_w = cb_w;
     a.log_len = const_cast<int32_t *>(log_len);  // read only
     a.slot_flags = req_flags;
     a.flags = flags;

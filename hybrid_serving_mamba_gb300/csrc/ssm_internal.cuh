@@ -55,6 +55,7 @@ struct Pool {
     // replay scratch: C_j . B_s of one launch's requests, [cb_rows][G][t1max][wcap]
     float *d_cb = nullptr;
     int cb_rows = 0;
+    int cb_w = 0;                      // row stride of d_cb: wcap rounded up to 4 floats
     int2 *d_fold_items = nullptr;      // (request index, tokens to fold) of one commit launch
     int32_t *d_fold_count = nullptr;
     int sm_count = 1;
@@ -79,6 +80,7 @@ struct StepArgs {  // decode, copy verify, replay verify
     float *log_dt;
     void *log_B;
     float *cb;        // replay scratch (see Pool::d_cb)
+    int cb_w;         // its row stride in floats (a multiple of 4)
     int64_t *position;
     int32_t *log_len;
     int32_t *cur;
@@ -142,7 +144,13 @@ struct ScanArgs {
 
 cudaError_t launch_decode(const Pool &pool, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_verify_copy(const Pool &pool, const StepArgs &a, cudaStream_t s);
-cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s);
+// Replay verify: the C.B prep kernel, then the pipelined kernel where the
+// shapes and pointers allow bulk copies, else the one-CTA-per-head kernel.
+// *path (if given) names the verify kernel used.
+cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path = nullptr);
+// Pipelined replay verify (persistent CTAs, bulk-copy ring); returns
+// cudaErrorNotSupported when the shapes or pointers do not allow it.
+cudaError_t launch_verify_replay_pipe(const Pool &pool, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s);
 cudaError_t launch_scan_seq(const Pool &pool, const ScanArgs &a, cudaStream_t s);
 cudaError_t launch_reset(const Pool &pool, const int32_t *slots, int n, cudaStream_t s);

@@ -273,7 +273,8 @@ ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, 
  * is log_len += c; folding into ckpt is the caller's business.
  * Its scratch is a 4 MiB array inside the library, held by every GPU that
  * loads it until the process exits: batch <= 1024 and
- * batch * G * n_tok * Wc <= SSM_STATIC_SCRATCH_FLOATS, else
+ * batch * G * n_tok * Wc4 <= SSM_STATIC_SCRATCH_FLOATS, with Wc4 = Wc rounded
+ * up to a multiple of 4, else
  * SSM_ERR_INVALID_ARG.  The first call on a device looks up the array's
  * device address (once per device, with that device current); make that
  * first call before any stream capture.  All calls share the array, which

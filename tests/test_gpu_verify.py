@@ -26,7 +26,8 @@ def _wide(x, dt, B, C, dt_in, dt_dt):
     return synth.widen(x, dt_in), synth.widen(dt, dt_dt), synth.widen(B, dt_in), synth.widen(C, dt_in)
 
 
-def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_tok_pattern=None, force_last=True):
+def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_tok_pattern=None, force_last=True,
+               expect_path=None):
     import torch
     m = _mod()
     n_slots, slots = 8, [6, 1, 3, 0, 7]
@@ -49,6 +50,8 @@ def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_to
             x, dt, B, C = synth.batch_tokens(SEED, s, R, nt, H, P, G, N, dt_in, synth.F32)
             y = empty_like_out((R, nt, H, P), dt_in)
             assert verify(pool, slots, nt, *_dev_inputs(x, dt, B, C, dt_in, synth.F32), Ad, Dd, y) == m.SSM_OK
+            if expect_path is not None:
+                assert m.ssm_last_path(pool) == expect_path
             _, yo = opool.verify(slots, *_wide(x, dt, B, C, dt_in, synth.F32))
             check_close(to_host(y), yo, dt_in, f"y step {s}", positions_axis=1)
             ys.append(to_host(y))
@@ -83,6 +86,18 @@ def test_copy_verify_matches_oracle(T, p):
 def test_replay_verify_matches_oracle(W, T, p):
     m = _mod()
     pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, W, T, p, steps=9)
+    m.ssm_state_destroy(pool)
+
+
+def test_replay_kernel_choice():
+    """Rows whose bytes are a multiple of 16 go through the pipelined kernel
+    (bulk copies); bf16 rows of 20 elements (40 bytes) through the
+    one-CTA-per-head kernel.  Both match the oracle."""
+    m = _mod()
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, 4, 3, 0.7, steps=6, expect_path="verify_replay_pipe")
+    m.ssm_state_destroy(pool)
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, 4, 3, 0.7, steps=6, P=20, dt_in=synth.BF16,
+                               expect_path="verify_replay")
     m.ssm_state_destroy(pool)
 
 
@@ -198,6 +213,7 @@ def test_config3_full_batch_sampled(T, p, W):
             for md, fn in ((0, m.ssm_verify_copy), (1, m.ssm_verify_replay)):
                 y = empty_like_out((R, T1, H, P), synth.BF16)
                 assert fn(pools[md], slots, T1, *dev, Ad, Dd, y) == m.SSM_OK
+                assert m.ssm_last_path(pools[md]) == ("verify_copy" if md == 0 else "verify_replay_pipe")
                 assert m.ssm_state_commit(pools[md], slots, acc, False, Ad) == m.SSM_OK
                 ys[md] = y
                 _, yo = osample[md].verify(list(range(len(sample))),
