@@ -414,10 +414,11 @@ ssm_status ssm_scan_chunk(ssm_pool pool, int32_t n_seq, const int32_t *cu_seqlen
             a.n_seq = m;
             for (int i = 0; i <= m; ++i) a.cu[i] = cu_seqlens[base + i];
             for (int i = 0; i < m; ++i) a.slots[i] = slots[base + i];
-            const cudaError_t e = ssm::launch_scan_seq(p, a, s);
+            const bool ssd = ssm::scan_ssd_supported(p);
+            const cudaError_t e = ssd ? ssm::launch_scan_ssd(p, a, s) : ssm::launch_scan_seq(p, a, s);
             if (e != cudaSuccess) return cuda_status(e);
+            p.last_path = ssd ? "scan_ssd" : "scan_seq";
         }
-        p.last_path = "scan_seq";
     }
     for (int i = 0; i < n_seq; ++i) {
         p.next_chunk[slots[i]] += 1;

@@ -153,6 +153,9 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
 cudaError_t launch_verify_replay_pipe(const Pool &pool, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s);
 cudaError_t launch_scan_seq(const Pool &pool, const ScanArgs &a, cudaStream_t s);
+// Tensor-core chunked scan (bf16 x / B / C, headdim 64, dstate 128).
+bool scan_ssd_supported(const Pool &pool);
+cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s);
 cudaError_t launch_reset(const Pool &pool, const int32_t *slots, int n, cudaStream_t s);
 cudaError_t launch_gather(const Pool &pool, const int32_t *slots, int n, float *dst, cudaStream_t s);
 

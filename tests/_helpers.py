@@ -5,6 +5,8 @@ Comparison rule for floating point, per element:
 where rms is taken over the compared tensor, so that an element that is
 small only because of cancellation is judged against the tensor's scale.
 fp32 inputs: rel 1e-5, abs 1e-6.  bf16 inputs: rel 2e-2, abs 0.
+Two GPU results compared with each other (each carrying its own rounding
+against the exact value) use twice the bound (``pair=True``).
 """
 import numpy as np
 
@@ -17,10 +19,12 @@ def tol(dtype_code):
     return TOL[dtype_code]
 
 
-def check_close(gpu, ref, dtype_code, what="", positions_axis=None):
+def check_close(gpu, ref, dtype_code, what="", positions_axis=None, pair=False):
     """Assert the comparison rule; on failure report the worst elements and
     the maximum error per position along ``positions_axis``."""
     rel, abs_ = tol(dtype_code)
+    if pair:
+        rel, abs_ = 2 * rel, 2 * abs_
     g = np.asarray(gpu, np.float64)
     o = np.asarray(ref, np.float64)
     assert g.shape == o.shape, (what, g.shape, o.shape)

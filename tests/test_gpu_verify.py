@@ -127,12 +127,12 @@ def test_copy_and_replay_agree_on_gpu():
     pr, _, yr, _ = _run_small(m.SSM_MODE_REPLAY, 4, 4, 0.7, steps=8)
     try:
         for a, b in zip(yc, yr):
-            check_close(b, a, synth.F32, "replay vs copy y")
+            check_close(b, a, synth.F32, "replay vs copy y", pair=True)
         sc = torch.empty((8, 4, 16, 32), dtype=torch.float32, device="cuda")
         sr = torch.empty_like(sc)
         m.ssm_state_gather(pc, list(range(8)), sc)
         m.ssm_state_gather(pr, list(range(8)), sr)
-        check_close(to_host(sr), to_host(sc), synth.F32, "replay vs copy state")
+        check_close(to_host(sr), to_host(sc), synth.F32, "replay vs copy state", pair=True)
     finally:
         m.ssm_state_destroy(pc)
         m.ssm_state_destroy(pr)
@@ -220,7 +220,7 @@ def test_config3_full_batch_sampled(T, p, W):
                                            *_wide(x[sample], dt[sample], B[sample], C[sample], synth.BF16, synth.F32))
                 osample[md].commit(list(range(len(sample))), acc_all[s][sample])
                 check_close(to_host(y[sample]), yo, synth.BF16, f"mode {md} y step {s}", positions_axis=1)
-            check_close(to_host(ys[1]), to_host(ys[0]), synth.BF16, f"replay vs copy step {s}")
+            check_close(to_host(ys[1]), to_host(ys[0]), synth.BF16, f"replay vs copy step {s}", pair=True)
             z = np.zeros((R, T1, 1, 1))
             meta_rule.verify(slots, z, np.zeros((R, T1, 1)), np.zeros((R, T1, 1, 16)), np.zeros((R, T1, 1, 16)))
             meta_rule.commit(slots, acc_all[s])
