@@ -485,6 +485,10 @@ cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s)
     }
     commit_meta_kernel<<<(a.batch + 127) / 128, 128, 0, s>>>(a, replay ? 1 : 0);
     if (replay) {
+        cudaError_t ep = cudaGetLastError();
+        if (ep != cudaSuccess) return ep;
+        ep = launch_fold_pipe(pool, a, s);
+        if (ep != cudaErrorNotSupported) return ep;
         const size_t smem = fold_smem_bytes(pool);
         const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
         SSM_DISPATCH_N(a.N, {

@@ -62,6 +62,20 @@ __device__ __forceinline__ void raise_flag(uint32_t *flags, uint32_t *slot_flags
     if (bit != SSM_FLAG_POISONED_SLOT) atomicOr(slot_flags + slot, kSlotPoisoned);
 }
 
+// Two consecutive inputs as floats, and two outputs from floats.
+__device__ __forceinline__ float2 load2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+__device__ __forceinline__ float2 load2(const __nv_bfloat16 *p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+}
+__device__ __forceinline__ void store2(float *p, float a, float b) { *reinterpret_cast<float2 *>(p) = make_float2(a, b); }
+__device__ __forceinline__ void store2(__nv_bfloat16 *p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
+__device__ __forceinline__ void copy2(float *d, const float *s) { *reinterpret_cast<float2 *>(d) = *reinterpret_cast<const float2 *>(s); }
+__device__ __forceinline__ void copy2(__nv_bfloat16 *d, const __nv_bfloat16 *s) {
+    *reinterpret_cast<uint32_t *>(d) = *reinterpret_cast<const uint32_t *>(s);
+}
+
 // Barrier over the consumer threads that also ORs a predicate across them.
 __device__ __forceinline__ bool consumers_or(int nthreads, bool pred) {
     uint32_t r;
@@ -184,7 +198,7 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
     float *dsm = reinterpret_cast<float *>(smem + L.d);
     float *Cf = reinterpret_cast<float *>(smem + L.Cf);
     double *cum = reinterpret_cast<double *>(smem + L.cum);
-    const float rcpP = 1.0f / (float)P;
+    const float rcpP2 = 2.0f / (float)P;
     TI *yout = reinterpret_cast<TI *>(a.y);
     TI *wx = reinterpret_cast<TI *>(a.log_x);
     int n = 0;
@@ -228,12 +242,8 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
                 carry += __shfl_sync(0xffffffffu, v, 31);
             }
         }
-        bool bad = false;
+        bool bad = false;  // step x is checked in phase C, where it is read anyway
         for (int e = threadIdx.x; e < T1 * N; e += nct) Cf[e] = to_f(Cs[e]);
-        for (int e = threadIdx.x; e < T1 * P; e += nct) {
-            const int j = (int)(((float)e + 0.5f) * rcpP), p = e - j * P;
-            bad |= !isfinite(to_f(xs[(size_t)(k + j) * P + p]));
-        }
         for (int j = threadIdx.x; j < T1; j += nct) bad |= !isfinite(dts[k + j]);
         bar_sync_named(1, nct);  // cum visible
         const float rcpm = 1.0f / (float)m;
@@ -272,31 +282,237 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
             for (int q = 0; q < 4; ++q) c[q] = C4[(size_t)j * (N / 4) + sub + LPR * q];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
-                float acc = 0.f;
+                float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    acc = fmaf(c[q].x, v[r][q].x, acc);
-                    acc = fmaf(c[q].y, v[r][q].y, acc);
-                    acc = fmaf(c[q].z, v[r][q].z, acc);
-                    acc = fmaf(c[q].w, v[r][q].w, acc);
+                    acc2 = ffma2(make_float2(c[q].x, c[q].y), make_float2(v[r][q].x, v[r][q].y), acc2);
+                    acc2 = ffma2(make_float2(c[q].z, c[q].w), make_float2(v[r][q].z, v[r][q].w), acc2);
                 }
-                acc = row_sum<LPR>(acc);
+                const float acc = row_sum<LPR>(acc2.x + acc2.y);
                 const int p = (warp * RPT + r) * RPW + rw;
                 if (sub == 0 && p < P) dsm[(size_t)j * P + p] = acc;
             }
         }
         bar_sync_named(1, nct);
 
-        // phase C: outputs, and the step's x and dt after the log
-        for (int e = threadIdx.x; e < T1 * P; e += nct) {
-            const int j = (int)(((float)e + 0.5f) * rcpP), p = e - j * P;
-            float acc = decay[j] * dsm[e];
+        // phase C: outputs (two rows p per thread), the step's x and dt
+        // staged after the log, and the non-finite check of the step's x
+        const int P2 = P >> 1;
+        for (int e = threadIdx.x; e < T1 * P2; e += nct) {
+            const int j = (int)(((float)e + 0.5f) * rcpP2), pp = e - j * P2;
+            const float dec = decay[j];
+            float2 acc = make_float2(dec * dsm[(size_t)j * P + 2 * pp], dec * dsm[(size_t)j * P + 2 * pp + 1]);
             const float *wj = W + (size_t)j * m;
-            for (int s = 0; s <= k + j; ++s) acc = fmaf(wj[s], to_f(xs[(size_t)s * P + p]), acc);
-            yout[(((size_t)i * T1 + j) * H + h) * P + p] = from_f<TI>(acc);
-            wx[(((size_t)slot * a.wcap + k + j) * H + h) * P + p] = xs[(size_t)(k + j) * P + p];
+            const int last = k + j;
+            for (int s = 0; s <= last; ++s) {
+                const float w = wj[s];
+                acc = ffma2(make_float2(w, w), load2(xs + (size_t)s * P + 2 * pp), acc);
+            }
+            const float acc0 = acc.x, acc1 = acc.y;
+            const float2 xl = load2(xs + (size_t)last * P + 2 * pp);
+            bad |= !isfinite(xl.x) || !isfinite(xl.y);
+            store2(yout + (((size_t)i * T1 + j) * H + h) * P + 2 * pp, acc0, acc1);
+            copy2(wx + (((size_t)slot * a.wcap + last) * H + h) * P + 2 * pp, xs + (size_t)last * P + 2 * pp);
         }
         for (int j = threadIdx.x; j < T1; j += nct) a.log_dt[((size_t)slot * a.wcap + k + j) * H + h] = dts[k + j];
+        if (consumers_or(nct, bad) && threadIdx.x == 0)  // also: the stage and work area are free again
+            raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_NONFINITE_INPUT);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fold, pipelined: the (request, head) pairs listed by the commit walk the
+// same kind of ring.  Per item the producer brings the checkpoint and the m
+// logged rows of x and B; the consumers form w_s = exp(A sum_{r>s} dt_r) dt_s
+// from fp64 prefix sums of dt, then h <- exp(A sum dt) h + sum_s (w_s x_s) (x) B_s
+// with m FMAs per element, and store the checkpoint back from registers.
+
+struct FoldLayout {
+    uint32_t st, xs, bs, dt, hdr, stage;
+    uint32_t xw, bf, cum, sw, A, bars, total;
+};
+
+__host__ __device__ inline FoldLayout fold_layout(int P, int N, int in_b, int mmax, int H) {
+    FoldLayout L;
+    uint32_t o = 0;
+    L.st = o;  o = up16(o + (uint32_t)P * N * 4);
+    L.xs = o;  o = up16(o + (uint32_t)mmax * P * in_b);
+    L.bs = o;  o = up16(o + (uint32_t)mmax * N * in_b);
+    L.dt = o;  o = up16(o + (uint32_t)mmax * 4);
+    L.hdr = o; o = up16(o + 16);
+    L.stage = (o + 127u) & ~127u;
+    o = kStages * L.stage;
+    L.xw = o;  o = up16(o + (uint32_t)mmax * P * 4);
+    L.bf = o;  o = up16(o + (uint32_t)mmax * N * 4);
+    L.cum = o; o = up16(o + (uint32_t)mmax * 8);
+    L.sw = o;  o = up16(o + (uint32_t)mmax * 4 + 4);  // + the total decay
+    L.A = o;   o = up16(o + (uint32_t)H * 4);
+    L.bars = o; o += 2 * kStages * 8;
+    L.total = o;
+    return L;
+}
+
+template <int N, typename TI>
+__global__ void __launch_bounds__(kPipeMaxThreads) fold_pipe_kernel(const __grid_constant__ CommitArgs a, int ncw) {
+    constexpr int LPR = N / 16, RPW = 32 / LPR;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int P = a.P, H = a.H;
+    const int mmax = a.wcap;
+    const FoldLayout L = fold_layout(P, N, (int)sizeof(TI), mmax, H);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + kStages;
+    float *sA = reinterpret_cast<float *>(smem + L.A);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nct = ncw * 32;
+    const int n_items = *a.fold_count * H;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], ncw);
+        }
+        mbar_fence_init();
+    }
+    for (int h = threadIdx.x; h < H; h += blockDim.x) sA[h] = a.A[h];
+    __syncthreads();
+
+    if (warp == ncw) {
+        // ------------------------------------------------------------ producer
+        const size_t in_b = sizeof(TI);
+        const TI *lx = reinterpret_cast<const TI *>(a.log_x);
+        const TI *lB = reinterpret_cast<const TI *>(a.log_B);
+        int n = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+            const int st = n % kStages;
+            if (n >= kStages && !mbar_wait(&empty[st], (uint32_t)((n / kStages) - 1) & 1u)) {
+                if (lane == 0) atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+                return;
+            }
+            const int f = item / H, h = item - f * H;
+            const int2 it = a.fold_items[f];
+            const int m = it.y;
+            const int slot = a.slots[it.x];
+            const int g = h / a.hpg;
+            unsigned char *S = smem + (size_t)st * L.stage;
+            const uint32_t bytes = (uint32_t)((size_t)P * N * 4 + (size_t)m * (P + N) * in_b);
+            for (int c = lane; c < 1 + 2 * m; c += 32) {
+                if (c == 0) {
+                    bulk_g2s(S + L.st, a.state + ((size_t)slot * H + h) * (size_t)P * N, (uint32_t)P * N * 4, &full[st]);
+                } else if (c <= m) {
+                    const int s = c - 1;
+                    bulk_g2s(S + L.xs + (size_t)s * P * in_b, lx + (((size_t)slot * a.wcap + s) * H + h) * P,
+                             (uint32_t)(P * in_b), &full[st]);
+                } else {
+                    const int s = c - 1 - m;
+                    bulk_g2s(S + L.bs + (size_t)s * N * in_b, lB + (((size_t)slot * a.wcap + s) * a.G + g) * N,
+                             (uint32_t)(N * in_b), &full[st]);
+                }
+            }
+            float *dts = reinterpret_cast<float *>(S + L.dt);
+            for (int s = lane; s < m; s += 32) dts[s] = a.log_dt[((size_t)slot * a.wcap + s) * H + h];
+            if (lane == 0) {
+                int *hdr = reinterpret_cast<int *>(S + L.hdr);
+                hdr[0] = m;
+                hdr[1] = slot;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int sub = lane % LPR, rw = lane / LPR;
+    float *xw = reinterpret_cast<float *>(smem + L.xw);
+    float *bf = reinterpret_cast<float *>(smem + L.bf);
+    double *cum = reinterpret_cast<double *>(smem + L.cum);
+    float *sw = reinterpret_cast<float *>(smem + L.sw);
+    const float rcpP = 1.0f / (float)P;
+    int n = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+        const int st = n % kStages;
+        if (!mbar_wait(&full[st], (uint32_t)(n / kStages) & 1u)) {
+            if (threadIdx.x == 0) atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+            return;
+        }
+        const unsigned char *S = smem + (size_t)st * L.stage;
+        const int *hdr = reinterpret_cast<const int *>(S + L.hdr);
+        const int m = hdr[0], slot = hdr[1];
+        const int h = item - (item / H) * H;
+        const float A = sA[h];
+        const TI *xs = reinterpret_cast<const TI *>(S + L.xs);
+        const TI *bs = reinterpret_cast<const TI *>(S + L.bs);
+        const float *dts = reinterpret_cast<const float *>(S + L.dt);
+
+        if (warp == 0) {  // prefix sums of dt (fp64: their differences lose nothing)
+            double carry = 0.0;
+            for (int base = 0; base < m; base += 32) {
+                const int s = base + lane;
+                double v = s < m ? (double)dts[s] : 0.0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += u;
+                }
+                if (s < m) cum[s] = carry + v;
+                carry += __shfl_sync(0xffffffffu, v, 31);
+            }
+        }
+        for (int e = threadIdx.x; e < m * N; e += nct) bf[e] = to_f(bs[e]);
+        bar_sync_named(1, nct);
+        for (int s = threadIdx.x; s < m; s += nct)  // exp(A * dt applied after token s) dt_s
+            sw[s] = expf(A * (float)(cum[m - 1] - cum[s])) * dts[s];
+        if (threadIdx.x == 0) sw[mmax] = expf(A * (float)cum[m - 1]);
+        bar_sync_named(1, nct);
+        for (int e = threadIdx.x; e < m * P; e += nct) {
+            const int s = (int)(((float)e + 0.5f) * rcpP);
+            xw[e] = sw[s] * to_f(xs[e]);
+        }
+        bar_sync_named(1, nct);
+
+        const float decay = sw[mmax];
+        const float4 *st4 = reinterpret_cast<const float4 *>(S + L.st);
+        const float4 *B4 = reinterpret_cast<const float4 *>(bf);
+        float *gst = a.state + ((size_t)slot * H + h) * (size_t)P * N;
+        int prow[RPT];
+        float2 v[RPT][8];  // the thread's 16 values of each of its rows, as pairs
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int p = (warp * RPT + r) * RPW + rw;
+            prow[r] = p < P ? p : 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 f = st4[((size_t)prow[r] * N) / 4 + sub + LPR * q];
+                v[r][2 * q] = make_float2(f.x * decay, f.y * decay);
+                v[r][2 * q + 1] = make_float2(f.z * decay, f.w * decay);
+            }
+        }
+        for (int s = 0; s < m; ++s) {
+            float4 b[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) b[q] = B4[(size_t)s * (N / 4) + sub + LPR * q];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const float u = xw[(size_t)s * P + prow[r]];
+                const float2 uu = make_float2(u, u);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    v[r][2 * q] = ffma2(uu, make_float2(b[q].x, b[q].y), v[r][2 * q]);
+                    v[r][2 * q + 1] = ffma2(uu, make_float2(b[q].z, b[q].w), v[r][2 * q + 1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int p = (warp * RPT + r) * RPW + rw;
+            if (p < P)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st_stream(gst + (size_t)p * N + 4 * (sub + LPR * q),
+                              make_float4(v[r][2 * q].x, v[r][2 * q].y, v[r][2 * q + 1].x, v[r][2 * q + 1].y));
+        }
         bar_sync_named(1, nct);  // the stage and the work area are free again
         if (lane == 0) mbar_arrive(&empty[st]);
     }
@@ -334,6 +550,44 @@ cudaError_t launch_verify_replay_pipe(const Pool &pool, const StepArgs &a, cudaS
             k<<<grid, block, L.total, s>>>(a, ncw);
         } else {
             auto k = verify_replay_pipe_kernel<NN, float>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+            if (e != cudaSuccess) return e;
+            k<<<grid, block, L.total, s>>>(a, ncw);
+        }
+    });
+    return cudaGetLastError();
+}
+
+}  // namespace ssm
+
+namespace ssm {
+
+cudaError_t launch_fold_pipe(const Pool &pool, const CommitArgs &a, cudaStream_t s) {
+    const int in_b = pool.cfg.input_dtype == SSM_DTYPE_BF16 ? 2 : 4;
+    if ((a.P * in_b) % 16 || (a.N * in_b) % 16) return cudaErrorNotSupported;
+    if (reinterpret_cast<uintptr_t>(a.log_x) % 16 || reinterpret_cast<uintptr_t>(a.log_B) % 16 ||
+        reinterpret_cast<uintptr_t>(a.state) % 16)
+        return cudaErrorNotSupported;
+    const int rows = (32 / (a.N / 16)) * RPT;
+    const int ncw = (a.P + rows - 1) / rows;
+    if (32 * ncw > kMaxThreads) return cudaErrorNotSupported;
+    const FoldLayout L = fold_layout(a.P, a.N, in_b, a.wcap, a.H);
+    int dev = 0, max_smem = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (L.total > (uint32_t)max_smem) return cudaErrorNotSupported;
+    const int per_sm = (int)(2 * L.total) <= max_smem ? 2 : 1;
+    const int grid = per_sm * pool.sm_count;
+    const bool bf = in_b == 2;
+    SSM_DISPATCH_N(a.N, {
+        const dim3 block(32 * (ncw + 1));
+        if (bf) {
+            auto k = fold_pipe_kernel<NN, __nv_bfloat16>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+            if (e != cudaSuccess) return e;
+            k<<<grid, block, L.total, s>>>(a, ncw);
+        } else {
+            auto k = fold_pipe_kernel<NN, float>;
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
             if (e != cudaSuccess) return e;
             k<<<grid, block, L.total, s>>>(a, ncw);

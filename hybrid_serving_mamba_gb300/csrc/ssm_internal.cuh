@@ -152,6 +152,9 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
 // cudaErrorNotSupported when the shapes or pointers do not allow it.
 cudaError_t launch_verify_replay_pipe(const Pool &pool, const StepArgs &a, cudaStream_t s);
 cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s);
+// Pipelined fold of the requests the commit listed; cudaErrorNotSupported
+// when the shapes or pointers do not allow bulk copies.
+cudaError_t launch_fold_pipe(const Pool &pool, const CommitArgs &a, cudaStream_t s);
 cudaError_t launch_scan_seq(const Pool &pool, const ScanArgs &a, cudaStream_t s);
 // Tensor-core chunked scan (bf16 x / B / C, headdim 64, dstate 128).
 bool scan_ssd_supported(const Pool &pool);
@@ -232,6 +235,16 @@ __device__ __forceinline__ float *current_state(float *state, float *snap, const
         if (c >= 0) return snap + (size_t)c * n_slots * hpn + off;
     }
     return state + off;
+}
+
+// Packed two-wide fp32 FMA (one instruction, each lane rounded like fmaf).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(*reinterpret_cast<unsigned long long *>(&d))
+        : "l"(*reinterpret_cast<const unsigned long long *>(&a)), "l"(*reinterpret_cast<const unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<const unsigned long long *>(&c)));
+    return d;
 }
 
 __device__ __forceinline__ float4 ld_stream(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
