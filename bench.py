@@ -331,6 +331,38 @@ def bench_verify(torch, m, args):
             torch.cuda.synchronize()
             out["plain_decode_us"] = 1000.0 * e0.elapsed_time(e1) / S
         m.ssm_state_destroy(pool)
+    # algorithmic bytes per step.  Copy: read the state, write T+1 states,
+    # token inputs and outputs.  Replay: read the checkpoint and the k logged
+    # entries, token inputs and outputs, stage the step's entries after the
+    # log; a fold reads the checkpoint and its m entries and writes the
+    # checkpoint.  Log lengths and folds follow the commit rule on the same
+    # accept counts (integer bookkeeping only).
+    state = H * P * N * 4
+    tok_in = H * P * 2 + H * 4 + 2 * G * N * 2
+    entry = H * P * 2 + H * 4 + G * N * 2
+    y_b = H * P * 2
+    copy_b = R * (state * (T1 + 1) + T1 * (tok_in + y_b))
+    accs = acc.cpu().numpy()
+    total = 0
+    k = [0] * R
+    for n_run, counted in ((3, False), (S, True)):  # the warm-up run, then the timed one
+        for step in range(n_run):
+            for r in range(R):
+                kept = int(accs[step % S][r]) + 1
+                b = state + k[r] * entry + T1 * (tok_in + y_b + entry)
+                if k[r] + kept >= W:
+                    b += 2 * state + (k[r] + kept) * entry
+                    k[r] = 0
+                else:
+                    k[r] += kept
+                if counted:
+                    total += b
+    replay_b = total / S
+    peak, _, kind = measured_peaks()
+    for name, b in (("copy", copy_b), ("replay", replay_b)):
+        gbs = b / (out[name]["us_per_step"] * 1e-6) / 1e9
+        out[name].update(algorithmic_bytes=b, achieved_gbs=gbs, frac_of_hbm=gbs / peak)
+    out["hbm_peak_source"] = kind
     out["copy_over_plain"] = out["copy"]["us_per_step"] / out["plain_decode_us"]
     out["replay_over_plain"] = out["replay"]["us_per_step"] / out["plain_decode_us"]
     out["config"] = dict(batch=R, T=T, p=c["p"], W=W, steps=S, heads=H, headdim=P, dstate=N, groups=G)
@@ -377,6 +409,114 @@ def bench_prefill(torch, m, args):
     return dict(us_per_scan=1000 * ms, tokens_per_s=R * L / (ms / 1000), path=path,
                 achieved_gbs=alg / (ms / 1000) / 1e9, algorithmic_bytes=alg,
                 config=dict(seqs=R, seqlen=L, heads=H, headdim=P, dstate=N, groups=G, includes="reset + scan"))
+
+
+def bench_prefill_varlen(torch, m, args):
+    """2.7B-shaped layer (80 heads of 64, dstate 128, one group): 64 packed
+    sequences with lengths U(512, 8192), fed as user chunks of 1024 tokens
+    (each call packs the next chunk of every live sequence).  Time per wave
+    of all 64 sequences, from reset."""
+    import synth
+    H, P, N, G, S, chunk = 80, 64, 128, 1, 64, 1024
+    lens = synth.varlen_lengths(SEED + 4000, S, 512, 8192)
+    total = int(lens.sum())
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(SEED + 77 + 17 * args.rank)
+    A, D = head_params(torch, gen, H)
+    x = _gen(torch, (total, H, P), gen, torch.bfloat16, "normal")
+    dt = _gen(torch, (total, H), gen, torch.bfloat16, "dt")
+    B = _gen(torch, (total, G, N), gen, torch.bfloat16, "normal")
+    C = _gen(torch, (total, G, N), gen, torch.bfloat16, "normal")
+    starts = [0]
+    for L in lens[:-1]:
+        starts.append(starts[-1] + int(L))
+    # pack each call's chunks contiguously (the layout a serving engine hands over)
+    calls = []
+    for a0 in range(0, int(lens.max()), chunk):
+        live = [i for i in range(S) if lens[i] > a0]
+        idx = torch.cat([torch.arange(starts[i] + a0, starts[i] + min(a0 + chunk, int(lens[i])), device="cuda")
+                         for i in live])
+        cu = [0]
+        for i in live:
+            cu.append(cu[-1] + min(a0 + chunk, int(lens[i])) - a0)
+        calls.append((live, cu, x[idx].contiguous(), dt[idx].contiguous(), B[idx].contiguous(), C[idx].contiguous(),
+                      torch.empty((len(idx), H, P), dtype=torch.bfloat16, device="cuda")))
+    del x, dt, B, C
+    pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_BF16, m.SSM_MODE_COPY, 16, 1), S)
+    stream = torch.cuda.current_stream()
+
+    def wave():
+        m.ssm_state_reset(pool, list(range(S)), stream=stream)
+        for q, (live, cu, xc, dc, bc, cc, yc) in enumerate(calls):
+            st = m.ssm_scan_chunk(pool, cu, live, [q] * len(live), xc, dc, bc, cc, A, D, yc, stream=stream)
+            if st != m.SSM_OK:
+                raise m.SSMError(st, "ssm_scan_chunk")
+
+    wave()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 3
+    e0.record(stream)
+    for _ in range(n):
+        wave()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    path = m.ssm_last_path(pool)
+    st, flags = m.ssm_pool_status(pool)
+    assert st == m.SSM_OK and flags == 0, f"varlen prefill raised device flags {flags}"
+    m.ssm_state_destroy(pool)
+    alg = 2 * total * H * P * 2 + total * (H * 2 + 2 * G * N * 2) + S * H * P * N * 4
+    return dict(ms_per_wave=ms, tokens=total, tokens_per_s=total / (ms / 1000), path=path,
+                achieved_gbs=alg / (ms / 1000) / 1e9, algorithmic_bytes=alg, calls_per_wave=len(calls),
+                config=dict(seqs=S, lengths="U(512, 8192)", user_chunk=chunk, heads=H, headdim=P, dstate=N,
+                            groups=G, includes="reset + every chunk call"))
+
+
+def bench_replay_plain_decode(torch, m, args):
+    """ReplaySSM used for plain decode (one token per step, no drafts): the
+    batch-256 decode workload through verify_replay (n_tok = 1) + commit,
+    window 16, against the in-place decode step."""
+    c = DEC
+    H, P, N, G, R, T = c["H"], c["P"], c["N"], c["G"], c["R"], c["tokens"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(SEED + 131 + 17 * args.rank)
+    A, D = head_params(torch, gen, H)
+    x, dt, B, C = step_inputs(torch, gen, T * R, H, P, G, N)
+    x, dt, B, C = (t.view(T, R, *t.shape[1:]) for t in (x, dt, B, C))
+    zeros = torch.zeros(R, dtype=torch.int32, device="cuda")
+    y = torch.empty((R, H, P), dtype=torch.bfloat16, device="cuda")
+    slots = list(range(R))
+    stream = torch.cuda.current_stream()
+    out = {}
+    for name, mode in (("decode", m.SSM_MODE_COPY), ("replay", m.SSM_MODE_REPLAY)):
+        init = (torch.randn((R, H, P, N), generator=gen, device="cuda") * 0.1).contiguous()
+        pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, mode, 16, 1), R, init)
+        del init
+
+        def run(n):
+            for t in range(n):
+                k = t % T
+                if mode == m.SSM_MODE_COPY:
+                    m.ssm_decode_step(pool, slots, x[k], dt[k], B[k], C[k], A, D, y, stream=stream)
+                else:
+                    m.ssm_verify_replay(pool, slots, 1, x[k], dt[k], B[k], C[k], A, D, y, stream=stream)
+                    m.ssm_state_commit(pool, slots, zeros, False, A, stream=stream)
+
+        run(16)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(T)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[name + "_us_per_step"] = 1000.0 * e0.elapsed_time(e1) / T
+        st, flags = m.ssm_pool_status(pool)
+        assert st == m.SSM_OK and flags == 0, f"{name} raised device flags {flags}"
+        m.ssm_state_destroy(pool)
+    out["replay_speedup_over_decode"] = out["decode_us_per_step"] / out["replay_us_per_step"]
+    out["config"] = dict(batch=R, W=16, tokens=T, heads=H, headdim=P, dstate=N, groups=G)
+    return out
 
 
 def cpu_baseline(budget_s=12.0):
@@ -485,6 +625,8 @@ def main():
     if not args.no_extras:
         extras["verify_b512"] = bench_verify(torch, m, args)
         extras["prefill"] = bench_prefill(torch, m, args)
+        extras["prefill_varlen"] = bench_prefill_varlen(torch, m, args)
+        extras["replay_plain_decode_b256"] = bench_replay_plain_decode(torch, m, args)
         e2e = bench_decode_e2e(torch, m, args)
     else:
         e2e = None
