@@ -2,10 +2,10 @@
 // duality") form (Mamba Streaming State That Survives Chunking, Separate
 // Mamba-2 algebra from kernel behavior: the dual view lets prefill use the
 // parallel structure inside a chunk while the recurrent state crosses
-// chunks).  One CTA of 128 threads walks one (sequence, head) chain in
-// kernel chunks of Q = 128 tokens, with the head's fp32 state in registers
-// (thread n holds column n of the 64 x 128 state).  Per chunk, with
-// cum_i = A * (dt_0 + ... + dt_i) over the chunk:
+// chunks).  One CTA of 256 threads walks one (sequence, head) chain in
+// kernel chunks of Q = 128 tokens; the head's fp32 state stays in registers
+// (thread (n, half) holds S[p][n] for the 32 rows p of its half).  Per chunk,
+// with cum_i = A * (dt_0 + ... + dt_i) over the chunk:
 //
 //   CB      = C B^T                                    (128 x 128, K = 128)
 //   M[i][j] = CB[i][j] exp(cum_i - cum_j) dt_j, j <= i  (CUDA cores, to bf16)
@@ -15,11 +15,19 @@
 //   y_i     = Y_i + exp(cum_i) Z_i + D x_i
 //   S      <- exp(cum_last) S + dS
 //
-// All four products are tcgen05.mma kind::f16 (bf16 operands from shared
-// memory in the 128-byte-swizzled K-major layout, fp32 accumulators in
-// TMEM, M = 128).  x, B and C are bf16 inputs, so C B^T and the X operands
-// are exact; M, w o X and the state copy are rounded to bf16, the state
-// itself stays fp32.  Tokens past the end of a sequence are zero rows.
+// All four products are tcgen05.mma kind::f16 with bf16 operands in
+// 128-byte-swizzled shared-memory tiles and fp32 accumulators in TMEM
+// (M = 128).  Operands are stored the way their producers write them -- one
+// row per token (C, B, X, w o X) or per state column (S) -- and read K-major
+// or MN-major as each product needs, so no transposes are made.  x, B and C
+// are bf16 inputs, so C B^T and X are exact; M, w o X and the state copy
+// are rounded to bf16, the state itself stays fp32.
+//
+// exp(cum_i - cum_j) is factored per 32-row block r of the chunk as
+// exp(cum_i - cum_r) * exp(cum_r - cum_j): both factors are at most 1 for
+// j before the block, and inside the block the second factor is bounded by
+// the block's own dt range, which is checked; a block whose range could
+// overflow fp32 computes its diagonal terms one exp at a time.
 #include "ssm_internal.cuh"
 #include "tc.cuh"
 #include "tma.cuh"
@@ -28,27 +36,20 @@ namespace ssm {
 namespace {
 
 constexpr int Q = 128, SP = 64, SN = 128;
-constexpr uint32_t kTile128 = 128 * 128;  // bytes of one K-tile (64 bf16) of a 128-row operand
-constexpr uint32_t kTile64 = 64 * 128;    // ... of a 64-row operand
-constexpr uint32_t OFF_C = 0;                         // C   [i][n]   rows i, K = n   (2 K-tiles)
-constexpr uint32_t OFF_B = OFF_C + 2 * kTile128;      // B   [j][n]   rows j, K = n
-constexpr uint32_t OFF_BT = OFF_B + 2 * kTile128;     // B^T [n][j]   rows n, K = j
-constexpr uint32_t OFF_M = OFF_BT + 2 * kTile128;     // M   [i][j]   rows i, K = j
-constexpr uint32_t OFF_XT = OFF_M + 2 * kTile128;     // X^T [p][j]   rows p, K = j
-constexpr uint32_t OFF_XW = OFF_XT + 2 * kTile64;     // (w o X)^T [p][j]
-constexpr uint32_t OFF_S = OFF_XW + 2 * kTile64;      // S   [p][n]   rows p, K = n
-constexpr uint32_t OFF_MISC = OFF_S + 2 * kTile64;    // cum[128], dt[128], warp sums, mbarrier, tmem base
-constexpr uint32_t kSsdSmem = OFF_MISC + 2048 + 1024; // + slack to align the base to 1024
+constexpr int kThreads = 256;
+constexpr uint32_t kTile128 = 128 * 128;  // one 64-wide (128-byte) column block of a 128-row tile
+constexpr uint32_t OFF_C = 0;                      // C  [i][n]  two n blocks: A of C B^T and of Z (K-major)
+constexpr uint32_t OFF_B = OFF_C + 2 * kTile128;   // B  [j][n]  B of C B^T (K-major); A of dS^T (MN-major)
+constexpr uint32_t OFF_M = OFF_B + 2 * kTile128;   // M  [i][j]  two j blocks: A of Y (K-major)
+constexpr uint32_t OFF_X = OFF_M + 2 * kTile128;   // X  [j][p]  B of Y (MN-major)
+constexpr uint32_t OFF_XW = OFF_X + kTile128;      // (w o X) [j][p]  B of dS^T (MN-major)
+constexpr uint32_t OFF_S = OFF_XW + kTile128;      // S  [n][p]  B of Z (MN-major)
+constexpr uint32_t OFF_MISC = OFF_S + kTile128;
+// misc: cum[128], dt[128], colf[4][128], wsum[4], safe[4], mbarrier, tmem base, gate
+constexpr uint32_t M_CUM = 0, M_DT = 512, M_COLF = 1024, M_WSUM = 3072, M_SAFE = 3088, M_BAR = 3104,
+                   M_TMEM = 3112, M_GATE = 3116;
+constexpr uint32_t kSsdSmem = OFF_MISC + 3200 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 256;  // [0,128) C B^T, then Z in [0,64) and dS^T in [64,128); Y in [128,192)
-
-// Byte offset of element (r, k) of an operand whose K spans two 64-wide tiles.
-__device__ __forceinline__ uint32_t opnd_off(uint32_t tile_bytes, uint32_t r, uint32_t k) {
-    return (k >> 6) * tile_bytes + tc::sw128_offset(r, k & 63u);
-}
-
-__device__ __forceinline__ void st_bf16(unsigned char *base, uint32_t off, float v) {
-    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(v);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -60,31 +61,45 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     return __bfloat1622float2(h);
 }
 
-// K = 128 product of two swizzled operands into TMEM (8 MMAs of K = 16).
-__device__ __forceinline__ void mma_k128(uint32_t d_tmem, uint32_t a_base, uint32_t a_tile, uint32_t b_base,
-                                         uint32_t b_tile, uint32_t idesc) {
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (uint32_t)(ks & 3) * 32u;  // 16 bf16 along K inside the 128-byte row
-        const uint64_t a = tc::smem_desc_sw128(a_base + (uint32_t)(ks >> 2) * a_tile + koff, 1024);
-        const uint64_t b = tc::smem_desc_sw128(b_base + (uint32_t)(ks >> 2) * b_tile + koff, 1024);
-        tc::mma_bf16(d_tmem, a, b, idesc, ks > 0);
-    }
+// A NaN or Inf in either bf16 half of w (all exponent bits set).
+__device__ __forceinline__ bool nonfinite_bf16x2(uint32_t w) {
+    return __vcmpeq2(w & 0x7F807F80u, 0x7F807F80u) != 0u;
+}
+
+__device__ __forceinline__ bool nonfinite_bf16x8(uint4 v) {
+    return nonfinite_bf16x2(v.x) | nonfinite_bf16x2(v.y) | nonfinite_bf16x2(v.z) | nonfinite_bf16x2(v.w);
+}
+
+// 16-byte chunk c (of 8 bf16) of row r in a 128-byte-row swizzled block.
+__device__ __forceinline__ uint32_t chunk_off(uint32_t r, uint32_t c) { return r * 128u + (((c ^ r) & 7u) << 4); }
+
+// K = 128 product into TMEM: 8 MMAs of K = 16.  K-major operands step 32
+// bytes along their 128-byte row and 16 KiB to the next 64-wide K block;
+// MN-major operands step 16 rows (2 KiB).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int ks) {
+    return tc::smem_desc_sw128(base + (uint32_t)(ks >> 2) * kTile128 + (uint32_t)(ks & 3) * 32u, 1024);
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int ks) {
+    // leading offset: stride between 64-wide MN blocks; stride offset: 8-row K groups
+    return tc::smem_desc_sw128_lbo(base + (uint32_t)ks * 2048u, kTile128, 1024);
 }
 
 template <typename TI>
-__global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant__ ScanArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_constant__ ScanArgs a) {
     static_assert(sizeof(TI) == 2, "tensor-core scan takes bf16 x, B and C");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     unsigned char *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_addr(smem);
-    float *s_cum = reinterpret_cast<float *>(smem + OFF_MISC);         // [128]
-    float *s_dt = s_cum + Q;                                           // [128]
-    float *s_wsum = s_dt + Q;                                          // [4]
-    uint64_t *s_bar = reinterpret_cast<uint64_t *>(smem + OFF_MISC + 1056);
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 1072);
-    uint32_t *s_gate = s_tmem + 1;
+    unsigned char *misc = smem + OFF_MISC;
+    float *s_cum = reinterpret_cast<float *>(misc + M_CUM);
+    float *s_dt = reinterpret_cast<float *>(misc + M_DT);
+    float *s_colf = reinterpret_cast<float *>(misc + M_COLF);  // [4][128]
+    float *s_wsum = reinterpret_cast<float *>(misc + M_WSUM);
+    int *s_safe = reinterpret_cast<int *>(misc + M_SAFE);
+    uint64_t *s_bar = reinterpret_cast<uint64_t *>(misc + M_BAR);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc + M_TMEM);
+    uint32_t *s_gate = reinterpret_cast<uint32_t *>(misc + M_GATE);
 
     const int h = blockIdx.x, i_seq = blockIdx.y;
     const int t0 = a.cu[i_seq], t1 = a.cu[i_seq + 1];
@@ -92,6 +107,9 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
     const int slot = a.slots[i_seq];
     const int H = a.H, G = a.G, g = h / a.hpg;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = tid & 127;      // token row (P1, P3, P5) or state column n
+    const int half = tid >> 7;      // which half of the columns this thread takes
+    const int rb = (tid >> 5) & 3;  // 32-row block of `row` = this warp's TMEM lane quadrant
 
     if (tid == 0) {
         uint32_t gate = 0;
@@ -115,7 +133,7 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *s_tmem;
-    const uint32_t lane_addr = (uint32_t)(32 * warp) << 16;  // this warp's TMEM lane quadrant
+    const uint32_t lane_addr = (uint32_t)(32 * rb) << 16;  // TMEM lane quadrant of this warp
 
     const float A = a.A[h], D = a.D[h];
     const TI *xg = reinterpret_cast<const TI *>(a.x);
@@ -124,96 +142,91 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
     TI *yg = reinterpret_cast<TI *>(a.y);
     float *st = current_state(a.state, a.snap, a.cur, a.n_slots, (size_t)H * SP * SN, (size_t)SP * SN, slot, h);
 
-    // state: thread n holds S[p][n] for all p, and writes the bf16 copy
-    float S[SP];
+    // state: thread (n, half) holds S[p][n] for p in [32 half, 32 half + 32)
+    const int n_col = row, p0 = 32 * half;
+    float S[32];
 #pragma unroll
-    for (int p = 0; p < SP; ++p) S[p] = st[(size_t)p * SN + tid];
+    for (int p = 0; p < 32; ++p) S[p] = st[(size_t)(p0 + p) * SN + n_col];
+    auto write_state_copy = [&]() {  // bf16 copy, row n of the [n][p] tile, this half's 4 chunks
 #pragma unroll
-    for (int p = 0; p < SP; ++p) st_bf16(smem, OFF_S + opnd_off(kTile64, p, tid), S[p]);
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4 *>(smem + OFF_S + chunk_off(n_col, 4 * half + c)) =
+                make_uint4(pack_bf16(S[8 * c + 0], S[8 * c + 1]), pack_bf16(S[8 * c + 2], S[8 * c + 3]),
+                           pack_bf16(S[8 * c + 4], S[8 * c + 5]), pack_bf16(S[8 * c + 6], S[8 * c + 7]));
+    };
+    write_state_copy();
 
-    constexpr uint32_t kIdN128 = tc::idesc_bf16_f32(128, 128);
-    constexpr uint32_t kIdN64 = tc::idesc_bf16_f32(128, 64);
+    constexpr uint32_t kIdCB = tc::idesc_bf16_f32(128, 128);                 // K-major x K-major
+    constexpr uint32_t kIdY = tc::idesc_bf16_f32(128, 64) | (1u << 16);      // B MN-major
+    constexpr uint32_t kIdZ = tc::idesc_bf16_f32(128, 64) | (1u << 16);      // B MN-major
+    constexpr uint32_t kIdDS = tc::idesc_bf16_f32(128, 64) | (1u << 15) | (1u << 16);  // both MN-major
     uint32_t phase = 0;
     bool bad = false, timeout = false;
     const int L = t1 - t0;
-    for (int c0 = 0; c0 < L && !timeout; c0 += Q) {
+    for (int c0 = 0; c0 < L; c0 += Q) {
         const int len = L - c0 < Q ? L - c0 : Q;
-        const int t = tid;
-        const bool valid = t < len;
-        const size_t tok = (size_t)(t0 + c0 + t);
+        const bool valid = row < len;
+        const size_t tok = (size_t)(t0 + c0 + row);
 
-        // ---- P1: inputs of row t; dt prefix sums
+        // ---- P1: rows of C and B (half 0) or of x and dt (half 1); dt prefix sums
         uint4 xr[8];
         float dtv = 0.f;
-        if (valid) {
-            const uint4 *xs = reinterpret_cast<const uint4 *>(xg + (tok * H + h) * SP);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) xr[c] = xs[c];
-            dtv = load_dt(a.dt, tok * H + h, a.dt_bf16);
+        if (half == 0) {
             const uint4 *cs = reinterpret_cast<const uint4 *>(Cg + (tok * G + g) * SN);
             const uint4 *bs = reinterpret_cast<const uint4 *>(Bg + (tok * G + g) * SN);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const uint4 cv = cs[c], bv = bs[c];
-                const uint32_t off = (uint32_t)(c >> 3) * kTile128 + (uint32_t)t * 128u +
-                                     ((((uint32_t)c & 7u) ^ ((uint32_t)t & 7u)) << 4);
+                const uint4 cv = valid ? cs[c] : make_uint4(0, 0, 0, 0);
+                const uint4 bv = valid ? bs[c] : make_uint4(0, 0, 0, 0);
+                bad |= nonfinite_bf16x8(cv) | nonfinite_bf16x8(bv);
+                const uint32_t off = (uint32_t)(c >> 3) * kTile128 + chunk_off((uint32_t)row, (uint32_t)c);
                 *reinterpret_cast<uint4 *>(smem + OFF_C + off) = cv;
                 *reinterpret_cast<uint4 *>(smem + OFF_B + off) = bv;
-                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-                const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 bf = unpack_bf16(bw[e]), cf = unpack_bf16(cw[e]);
-                    bad |= !isfinite(bf.x) || !isfinite(bf.y) || !isfinite(cf.x) || !isfinite(cf.y);
-                    const uint32_t n = (uint32_t)c * 8u + 2u * e;
-                    // B^T: row n, column (K) t
-                    *reinterpret_cast<uint16_t *>(smem + OFF_BT + opnd_off(kTile128, n, t)) = (uint16_t)(bw[e] & 0xFFFFu);
-                    *reinterpret_cast<uint16_t *>(smem + OFF_BT + opnd_off(kTile128, n + 1, t)) = (uint16_t)(bw[e] >> 16);
-                }
             }
-            bad |= !isfinite(dtv);
         } else {
+            const uint4 *xs = reinterpret_cast<const uint4 *>(xg + (tok * H + h) * SP);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) xr[c] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint32_t off = (uint32_t)(c >> 3) * kTile128 + (uint32_t)t * 128u +
-                                     ((((uint32_t)c & 7u) ^ ((uint32_t)t & 7u)) << 4);
-                *reinterpret_cast<uint4 *>(smem + OFF_C + off) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(smem + OFF_B + off) = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < 8; ++c) {
+                xr[c] = valid ? xs[c] : make_uint4(0, 0, 0, 0);
+                bad |= nonfinite_bf16x8(xr[c]);
+                *reinterpret_cast<uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c)) = xr[c];
             }
-#pragma unroll 8
-            for (int n = 0; n < SN; ++n) *reinterpret_cast<uint16_t *>(smem + OFF_BT + opnd_off(kTile128, n, t)) = 0;
-        }
-        // inclusive prefix sum of dt over the chunk's 128 rows
-        float v = dtv;
+            dtv = valid ? load_dt(a.dt, tok * H + h, a.dt_bf16) : 0.f;
+            bad |= !isfinite(dtv);
+            // inclusive prefix sum over the 128 rows (warps 4..7)
+            float v = dtv;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (lane == 31) s_wsum[rb] = v;
+            s_dt[row] = dtv;
+            bar_sync_named(1, 128);
+            for (int w = 0; w < rb; ++w) v += s_wsum[w];
+            s_cum[row] = A * v;
         }
-        if (lane == 31) s_wsum[warp] = v;
-        s_dt[t] = dtv;
-        __syncthreads();
-        for (int w = 0; w < warp; ++w) v += s_wsum[w];
-        const float cum = A * v;
-        s_cum[t] = cum;
         __syncthreads();
         const float cum_last = s_cum[Q - 1];
-        const float wt = expf(cum_last - cum) * dtv;  // weight of token t in the state update
-        // X^T and (w o X)^T: column t
+        const float cum = s_cum[row];
+        // column factors colf[r][j] = exp(cum_{32r} - cum_j) dt_j for j < 32 r + 32,
+        // and whether block r's own range keeps them finite
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint32_t xw[4] = {xr[c].x, xr[c].y, xr[c].z, xr[c].w};
+        for (int q = 0; q < 2; ++q) {
+            const int r = 2 * half + q;
+            const float ref = s_cum[32 * r];
+            s_colf[r * Q + row] = row < 32 * r + 32 ? expf(ref - cum) * s_dt[row] : 0.f;
+        }
+        if (tid < 4) s_safe[tid] = (s_cum[32 * tid] - s_cum[32 * tid + 31]) < 80.f;
+        if (half == 1) {  // w o X, row j = row: weight of token j in the state update
+            const float wt = expf(cum_last - cum) * dtv;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 xf = unpack_bf16(xw[e]);
-                bad |= !isfinite(xf.x) || !isfinite(xf.y);
-                const uint32_t p = (uint32_t)c * 8u + 2u * e;
-                *reinterpret_cast<uint16_t *>(smem + OFF_XT + opnd_off(kTile64, p, t)) = (uint16_t)(xw[e] & 0xFFFFu);
-                *reinterpret_cast<uint16_t *>(smem + OFF_XT + opnd_off(kTile64, p + 1, t)) = (uint16_t)(xw[e] >> 16);
-                st_bf16(smem, OFF_XW + opnd_off(kTile64, p, t), xf.x * wt);
-                st_bf16(smem, OFF_XW + opnd_off(kTile64, p + 1, t), xf.y * wt);
+            for (int c = 0; c < 8; ++c) {
+                const float2 f0 = unpack_bf16(xr[c].x), f1 = unpack_bf16(xr[c].y);
+                const float2 f2 = unpack_bf16(xr[c].z), f3 = unpack_bf16(xr[c].w);
+                *reinterpret_cast<uint4 *>(smem + OFF_XW + chunk_off((uint32_t)row, (uint32_t)c)) =
+                    make_uint4(pack_bf16(f0.x * wt, f0.y * wt), pack_bf16(f1.x * wt, f1.y * wt),
+                               pack_bf16(f2.x * wt, f2.y * wt), pack_bf16(f3.x * wt, f3.y * wt));
             }
         }
         tc::fence_proxy_async_smem();
@@ -222,7 +235,9 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
         // ---- P2: C B^T
         if (tid == 0) {
             tc::fence_after_sync();
-            mma_k128(tmem, sbase + OFF_C, kTile128, sbase + OFF_B, kTile128, kIdN128);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem, kmajor_desc(sbase + OFF_C, ks), kmajor_desc(sbase + OFF_B, ks), kIdCB, ks > 0);
             tc::mma_commit(s_bar);
         }
         if (__syncthreads_or(!mbar_wait(s_bar, phase & 1u))) {  // uniform across the CTA
@@ -232,26 +247,37 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
         ++phase;
         tc::fence_after_sync();
 
-        // ---- P3: M = C B^T o decay o dt, masked to j <= i (row i = tid)
+        // ---- P3: M = C B^T o decay o dt, masked to j <= i (row i = row, columns of this half)
+        {
+            const int i = row;
+            const float erow = expf(cum - s_cum[32 * rb]);  // <= 1
+            const bool safe = s_safe[rb] != 0;
+            const float *colf = s_colf + rb * Q;
 #pragma unroll 1
-        for (int jb = 0; jb < Q; jb += 32) {
-            float cb[32];
-            tc::tmem_ld32(tmem + lane_addr + (uint32_t)jb, cb);
+            for (int jb = 64 * half; jb < 64 * half + 64; jb += 32) {
+                float cb[32];
+                tc::tmem_ld32(tmem + lane_addr + (uint32_t)jb, cb);
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-                uint32_t pk[4];
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    uint32_t pk[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float mv[2];
+                    for (int e = 0; e < 4; ++e) {
+                        float mv[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int j = jb + q8 * 8 + 2 * e + u;
-                        mv[u] = j <= t ? cb[q8 * 8 + 2 * e + u] * expf(cum - s_cum[j]) * s_dt[j] : 0.f;
+                        for (int u = 0; u < 2; ++u) {
+                            const int j = jb + q8 * 8 + 2 * e + u;
+                            float f;
+                            if (j > i) f = 0.f;
+                            else if (j < 32 * rb || safe) f = erow * colf[j];
+                            else f = expf(cum - s_cum[j]) * s_dt[j];
+                            mv[u] = cb[q8 * 8 + 2 * e + u] * f;
+                        }
+                        pk[e] = pack_bf16(mv[0], mv[1]);
                     }
-                    pk[e] = pack_bf16(mv[0], mv[1]);
+                    const uint32_t j0 = (uint32_t)(jb + q8 * 8);
+                    *reinterpret_cast<uint4 *>(smem + OFF_M + (j0 >> 6) * kTile128 + chunk_off((uint32_t)i, (j0 >> 3) & 7u)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                const uint32_t j0 = (uint32_t)(jb + q8 * 8);
-                *reinterpret_cast<uint4 *>(smem + OFF_M + opnd_off(kTile128, t, j0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
         }
         tc::fence_before_sync();
@@ -261,9 +287,12 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
         // ---- P4: Y = M X, Z = C S^T, dS^T = B^T (w o X)
         if (tid == 0) {
             tc::fence_after_sync();
-            mma_k128(tmem + 128, sbase + OFF_M, kTile128, sbase + OFF_XT, kTile64, kIdN64);
-            mma_k128(tmem + 0, sbase + OFF_C, kTile128, sbase + OFF_S, kTile64, kIdN64);
-            mma_k128(tmem + 64, sbase + OFF_BT, kTile128, sbase + OFF_XW, kTile64, kIdN64);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                tc::mma_bf16(tmem + 128, kmajor_desc(sbase + OFF_M, ks), mnmajor_desc(sbase + OFF_X, ks), kIdY, ks > 0);
+                tc::mma_bf16(tmem + 0, kmajor_desc(sbase + OFF_C, ks), mnmajor_desc(sbase + OFF_S, ks), kIdZ, ks > 0);
+                tc::mma_bf16(tmem + 64, mnmajor_desc(sbase + OFF_B, ks), mnmajor_desc(sbase + OFF_XW, ks), kIdDS, ks > 0);
+            }
             tc::mma_commit(s_bar);
         }
         if (__syncthreads_or(!mbar_wait(s_bar, phase & 1u))) {
@@ -273,35 +302,37 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
         ++phase;
         tc::fence_after_sync();
 
-        // ---- P5: outputs of row t, and the state update of column n = t
-        const float ecum = expf(cum);
-        const float dA = expf(cum_last);
-#pragma unroll
-        for (int pb = 0; pb < SP; pb += 32) {
+        // ---- P5: outputs of row i (this half's 32 columns p), state update of column n = row
+        {
+            const float ecum = expf(cum);
+            const float dA = expf(cum_last);
             float yv[32], zv[32], ds[32];
-            tc::tmem_ld32(tmem + lane_addr + 128u + (uint32_t)pb, yv);
-            tc::tmem_ld32(tmem + lane_addr + 0u + (uint32_t)pb, zv);
-            tc::tmem_ld32(tmem + lane_addr + 64u + (uint32_t)pb, ds);
-            uint32_t out[16];
+            tc::tmem_ld32(tmem + lane_addr + 128u + (uint32_t)p0, yv);
+            tc::tmem_ld32(tmem + lane_addr + 0u + (uint32_t)p0, zv);
+            tc::tmem_ld32(tmem + lane_addr + 64u + (uint32_t)p0, ds);
+            uint4 outc[4];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int c = (pb + 2 * e) >> 3, w4 = ((pb + 2 * e) & 7) >> 1;
-                const uint32_t xwv = w4 == 0 ? xr[c].x : w4 == 1 ? xr[c].y : w4 == 2 ? xr[c].z : xr[c].w;
-                const float2 xf = unpack_bf16(xwv);
-                const float y0 = fmaf(ecum, zv[2 * e], yv[2 * e]) + D * xf.x;
-                const float y1 = fmaf(ecum, zv[2 * e + 1], yv[2 * e + 1]) + D * xf.y;
-                out[e] = pack_bf16(y0, y1);
+            for (int c = 0; c < 4; ++c) {
+                const uint4 xc = *reinterpret_cast<const uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)(4 * half + c)));
+                const uint32_t xw4[4] = {xc.x, xc.y, xc.z, xc.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 xf = unpack_bf16(xw4[e]);
+                    const int q = 8 * c + 2 * e;
+                    o[e] = pack_bf16(fmaf(ecum, zv[q], yv[q]) + D * xf.x, fmaf(ecum, zv[q + 1], yv[q + 1]) + D * xf.y);
+                }
+                outc[c] = make_uint4(o[0], o[1], o[2], o[3]);
             }
             if (valid) {
-                uint4 *yo = reinterpret_cast<uint4 *>(yg + (tok * H + h) * SP + pb);
+                uint4 *yo = reinterpret_cast<uint4 *>(yg + (tok * H + h) * SP + p0);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) yo[c] = make_uint4(out[4 * c], out[4 * c + 1], out[4 * c + 2], out[4 * c + 3]);
+                for (int c = 0; c < 4; ++c) yo[c] = outc[c];
             }
 #pragma unroll
-            for (int p = 0; p < 32; ++p) S[pb + p] = fmaf(dA, S[pb + p], ds[p]);
+            for (int p = 0; p < 32; ++p) S[p] = fmaf(dA, S[p], ds[p]);
         }
-#pragma unroll
-        for (int p = 0; p < SP; ++p) st_bf16(smem, OFF_S + opnd_off(kTile64, p, tid), S[p]);
+        write_state_copy();
         tc::fence_before_sync();
         tc::fence_proxy_async_smem();
         __syncthreads();
@@ -310,7 +341,7 @@ __global__ void __launch_bounds__(128, 1) scan_ssd_kernel(const __grid_constant_
     const bool any_bad = __syncthreads_or(bad);
     if (!any_bad && !timeout) {
 #pragma unroll
-        for (int p = 0; p < SP; ++p) st[(size_t)p * SN + tid] = S[p];
+        for (int p = 0; p < 32; ++p) st[(size_t)(p0 + p) * SN + n_col] = S[p];
         if (h == 0 && tid == 0) a.position[slot] += L;
     } else if (tid == 0) {
         atomicOr(a.flags, timeout ? SSM_FLAG_TIMEOUT : SSM_FLAG_NONFINITE_INPUT);
@@ -332,7 +363,7 @@ cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s)
     auto k = scan_ssd_kernel<__nv_bfloat16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSsdSmem);
     if (e != cudaSuccess) return e;
-    k<<<dim3(a.H, a.n_seq), 128, kSsdSmem, s>>>(a);
+    k<<<dim3(a.H, a.n_seq), kThreads, kSsdSmem, s>>>(a);
     return cudaGetLastError();
 }
 

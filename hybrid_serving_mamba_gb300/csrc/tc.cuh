@@ -33,8 +33,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_byte_addr, uin
     return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and
-// an fp32 accumulator: D format bits 4..5 = 1 (f32), A format bits 7..9 =
+// The same with an explicit leading byte offset, for MN-major operands:
+// there the leading offset is the stride between 64-element MN blocks and
+// the stride offset the stride between 8-row groups along K.
+__device__ __forceinline__ uint64_t smem_desc_sw128_lbo(uint32_t smem_byte_addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_byte_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes & 0x3FFFFu) >> 4) << 16;
+    d |= (uint64_t)((sbo_bytes & 0x3FFFFu) >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (both K-major; bit
+// 15 / bit 16 select MN-major A / B) and an fp32 accumulator: D format bits 4..5 = 1 (f32), A format bits 7..9 =
 // 1 (bf16), B format bits 10..12 = 1 (bf16), N >> 3 in bits 17..22, M >> 4
 // in bits 24..28.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
