@@ -553,6 +553,32 @@ def cpu_baseline(budget_s=12.0):
 
 # ---------------------------------------------------------------------------
 
+def run_case(args):
+    """One workload alone, small enough for a profiler capture: a few
+    iterations, one short text line (no benchmark JSON)."""
+    import torch
+
+    import hybrid_serving_mamba_gb300 as m
+    torch.cuda.set_device(0)
+    args.rank = 0
+    if args.case == "verify":
+        VER["R"] = args.batch or VER["R"]
+        VER["steps"] = 4
+        out = bench_verify(torch, m, args)
+        print(json.dumps({"case": "verify", "batch": VER["R"], "copy_us": out["copy"]["us_per_step"],
+                          "replay_us": out["replay"]["us_per_step"]}))
+    elif args.case == "prefill":
+        PRE["R"] = args.batch or PRE["R"]
+        out = bench_prefill(torch, m, args)
+        print(json.dumps({"case": "prefill", "seqs": PRE["R"], "us": out["us_per_scan"], "path": out["path"]}))
+    elif args.case == "prefill_varlen":
+        out = bench_prefill_varlen(torch, m, args)
+        print(json.dumps({"case": "prefill_varlen", "ms": out["ms_per_wave"], "path": out["path"]}))
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    return 0
+
+
 def run_reference(args):
     """The oracle as the reference arm: rank 0 times it on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -589,9 +615,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extras", action="store_true", help="decode only (no verify / prefill / e2e / cpu)")
+    ap.add_argument("--case", choices=("verify", "prefill", "prefill_varlen"),
+                    help="run one workload alone (for profiler captures)")
+    ap.add_argument("--batch", type=int, default=0, help="batch / sequence count of --case")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.case:
+        return run_case(args)
     if args.warmup < 3:
         args.warmup = 3
 
