@@ -38,8 +38,10 @@ __device__ __forceinline__ void raise_flag(uint32_t *flags, uint32_t *slot_flags
 
 // ------------------------------------------------------------------ decode
 
-template <int N, typename TI>
-__global__ void __launch_bounds__(kMaxThreads) decode_kernel(const __grid_constant__ StepArgs a) {
+// MAXT / MINB: launch bounds.  CTAs of up to 256 threads are compiled for
+// three per SM (at most 85 registers a thread): more state loads in flight.
+template <int N, typename TI, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) decode_kernel(const __grid_constant__ StepArgs a) {
     constexpr int LPR = N / 16, RPW = 32 / LPR;
     __shared__ uint32_t s_gate;
     const int h = blockIdx.x, i = blockIdx.y;
@@ -117,8 +119,8 @@ __global__ void __launch_bounds__(kMaxThreads) decode_kernel(const __grid_consta
 
 // ------------------------------------------------------------------ copy verify
 
-template <int N, typename TI>
-__global__ void __launch_bounds__(kMaxThreads) verify_copy_kernel(const __grid_constant__ StepArgs a) {
+template <int N, typename TI, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) verify_copy_kernel(const __grid_constant__ StepArgs a) {
     constexpr int LPR = N / 16, RPW = 32 / LPR;
     __shared__ uint32_t s_gate;
     const int h = blockIdx.x, i = blockIdx.y;
@@ -234,13 +236,20 @@ __global__ void reset_kernel(float *state, size_t hpn, int64_t *position, int32_
 
 // ------------------------------------------------------------------ launchers
 
+// Launch K<N, TI, 256, 3> for CTAs of at most 256 threads, else K<N, TI, kMaxThreads, 1>.
+#define SSM_LAUNCH_BOUNDED(K, NN, TI, grid, block, s, a)                       \
+    do {                                                                        \
+        if ((block).x <= 256) K<NN, TI, 256, 3><<<grid, block, 0, s>>>(a);      \
+        else K<NN, TI, kMaxThreads, 1><<<grid, block, 0, s>>>(a);               \
+    } while (0)
+
 cudaError_t launch_decode(const Pool &pool, const StepArgs &a, cudaStream_t s) {
     const dim3 grid(a.H, a.batch);
     const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
     SSM_DISPATCH_N(a.N, {
         const dim3 block(32 * warps_for<NN>(a.P));
-        if (bf) decode_kernel<NN, __nv_bfloat16><<<grid, block, 0, s>>>(a);
-        else decode_kernel<NN, float><<<grid, block, 0, s>>>(a);
+        if (bf) SSM_LAUNCH_BOUNDED(decode_kernel, NN, __nv_bfloat16, grid, block, s, a);
+        else SSM_LAUNCH_BOUNDED(decode_kernel, NN, float, grid, block, s, a);
     });
     return cudaGetLastError();
 }
@@ -250,8 +259,8 @@ cudaError_t launch_verify_copy(const Pool &pool, const StepArgs &a, cudaStream_t
     const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
     SSM_DISPATCH_N(a.N, {
         const dim3 block(32 * warps_for<NN>(a.P));
-        if (bf) verify_copy_kernel<NN, __nv_bfloat16><<<grid, block, 0, s>>>(a);
-        else verify_copy_kernel<NN, float><<<grid, block, 0, s>>>(a);
+        if (bf) SSM_LAUNCH_BOUNDED(verify_copy_kernel, NN, __nv_bfloat16, grid, block, s, a);
+        else SSM_LAUNCH_BOUNDED(verify_copy_kernel, NN, float, grid, block, s, a);
     });
     return cudaGetLastError();
 }
