@@ -62,6 +62,9 @@ void free_all(Pool &p) {
     cudaFree(p.d_flags);
     cudaFree(p.d_stage);
     cudaFree(p.d_cb);
+    cudaFree(p.d_wsc);
+    cudaFree(p.d_dec);
+    cudaFree(p.d_cf);
     cudaFree(p.d_fold_items);
     cudaFree(p.d_fold_count);
 }
@@ -99,6 +102,10 @@ void fill_step(const Pool &p, ssm::StepArgs &a, const void *x, const void *dt, c
     a.log_x = p.log_x; a.log_dt = p.log_dt; a.log_B = p.log_B;
     a.cb = p.d_cb;
     a.cb_w = p.cb_w;
+    a.wsc = p.d_wsc;
+    a.dec = p.d_dec;
+    a.cf = p.d_cf;
+    a.t1pad = p.t1pad;
     a.position = p.d_position; a.log_len = p.d_log_len; a.cur = p.d_cur;
     a.slot_flags = p.d_slot_flags; a.flags = p.d_flags;
     a.H = p.H; a.P = p.P; a.N = p.N; a.G = p.G; a.hpg = p.hpg;
@@ -181,6 +188,7 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     p.t1max = c.max_tokens;
     p.wcap = c.mode == SSM_MODE_REPLAY ? c.window - 1 + c.max_tokens : 0;
     p.cb_w = (p.wcap + 3) / 4 * 4;
+    p.t1pad = (p.t1max + 3) / 4 * 4;
     p.in_bytes = in_elem(c.input_dtype);
     if (cudaGetDevice(&p.device) != cudaSuccess) { delete pool; return SSM_ERR_CUDA; }
     if (cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess || p.sm_count < 1)
@@ -211,6 +219,9 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         if (e == cudaSuccess) e = alloc(&lB, ns * p.wcap * p.G * p.N * p.in_bytes, b);
         p.log_B = lB;
         if (e == cudaSuccess) e = alloc(&p.d_cb, (size_t)p.cb_rows * p.G * p.t1max * p.cb_w, b);
+        if (e == cudaSuccess) e = alloc(&p.d_wsc, (size_t)p.cb_rows * p.H * p.t1max * p.cb_w, b);
+        if (e == cudaSuccess) e = alloc(&p.d_dec, (size_t)p.cb_rows * p.H * p.t1pad, b);
+        if (e == cudaSuccess) e = alloc(&p.d_cf, (size_t)p.cb_rows * p.G * p.t1max * p.N, b);
         if (e == cudaSuccess) e = alloc(&p.d_fold_items, (size_t)ssm::kMaxSlotsPerLaunch, b);
         if (e == cudaSuccess) e = alloc(&p.d_fold_count, 1, b);
     }
@@ -236,6 +247,7 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         delete pool;
         return cuda_status(e);
     }
+    if (c.mode == SSM_MODE_REPLAY) ssm::replay_tma_encode(p);  // else the bulk-copy / plain kernels serve
     p.next_chunk.assign(ns, 0);
     p.epoch.assign(ns, 0);
     p.released.assign(ns, 0);

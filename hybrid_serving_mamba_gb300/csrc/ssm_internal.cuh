@@ -13,6 +13,7 @@
 // xor-shuffle reduction over the LPR lanes of the row.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the encoder is looked up at run time)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -56,6 +57,13 @@ struct Pool {
     float *d_cb = nullptr;
     int cb_rows = 0;
     int cb_w = 0;                      // row stride of d_cb: wcap rounded up to 4 floats
+    float *d_wsc = nullptr;            // replay: W[j][s] per head, [cb_rows][H][t1max][cb_w]
+    float *d_dec = nullptr;            // replay: decay_j per head, [cb_rows][H][t1pad]
+    float *d_cf = nullptr;             // replay: C_j in fp32 per group, [cb_rows][G][t1max][N]
+    int t1pad = 0;                     // t1max rounded up to 4
+    CUtensorMap tm_state;              // replay: checkpoint rows, 32-column boxes, 128-byte swizzle
+    CUtensorMap tm_logx;               // replay: one head's log of x rows per box
+    bool tm_ok = false;                // both maps encoded
     int2 *d_fold_items = nullptr;      // (request index, tokens to fold) of one commit launch
     int32_t *d_fold_count = nullptr;
     int sm_count = 1;
@@ -81,6 +89,10 @@ struct StepArgs {  // decode, copy verify, replay verify
     void *log_B;
     float *cb;        // replay scratch (see Pool::d_cb)
     int cb_w;         // its row stride in floats (a multiple of 4)
+    float *wsc;       // replay scratch (see Pool::d_wsc); null: no tensor-map verify
+    float *dec;
+    float *cf;
+    int t1pad;
     int64_t *position;
     int32_t *log_len;
     int32_t *cur;
@@ -148,6 +160,14 @@ cudaError_t launch_verify_copy(const Pool &pool, const StepArgs &a, cudaStream_t
 // shapes and pointers allow bulk copies, else the one-CTA-per-head kernel.
 // *path (if given) names the verify kernel used.
 cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path = nullptr);
+// Replay verify with the checkpoint streamed by tensor-map copies
+// (per-group coefficient kernel + persistent streaming kernel; needs the
+// wsc / dec / cf scratch and the pool's tensor maps); cudaErrorNotSupported
+// when it cannot run.  replay_tma_encode fills Pool::tm_* (false: shape not
+// covered or no encoder in the driver).
+cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s);
+size_t replay_coef_smem_bytes(const Pool &pool, int n_tok);
+bool replay_tma_encode(Pool &p);
 // Pipelined replay verify (persistent CTAs, bulk-copy ring); returns
 // cudaErrorNotSupported when the shapes or pointers do not allow it.
 cudaError_t launch_verify_replay_pipe(const Pool &pool, const StepArgs &a, cudaStream_t s);

@@ -90,14 +90,15 @@ def test_replay_verify_matches_oracle(W, T, p):
 
 
 def test_replay_kernel_choice():
-    """Rows whose bytes are a multiple of 16 go through the pipelined kernel
-    (bulk copies); bf16 rows of 20 elements (40 bytes) through the
-    one-CTA-per-head kernel.  Both match the oracle."""
+    """Pools take the tensor-map verify (group coefficient + streaming
+    kernels); an odd headdim (21, which neither the tensor-map nor the
+    bulk-copy kernel takes) runs the one-CTA-per-head kernel and the
+    unpipelined fold.  The bulk-copy kernel serves ssm_verify_replay_static
+    (test_zz_no_alloc).  All match the oracle."""
     m = _mod()
-    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, 4, 3, 0.7, steps=6, expect_path="verify_replay_pipe")
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, 4, 3, 0.7, steps=6, expect_path="verify_replay_tma")
     m.ssm_state_destroy(pool)
-    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, 4, 3, 0.7, steps=6, P=20, dt_in=synth.BF16,
-                               expect_path="verify_replay")
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, 4, 3, 0.7, steps=6, P=21, expect_path="verify_replay")
     m.ssm_state_destroy(pool)
 
 
@@ -213,7 +214,7 @@ def test_config3_full_batch_sampled(T, p, W):
             for md, fn in ((0, m.ssm_verify_copy), (1, m.ssm_verify_replay)):
                 y = empty_like_out((R, T1, H, P), synth.BF16)
                 assert fn(pools[md], slots, T1, *dev, Ad, Dd, y) == m.SSM_OK
-                assert m.ssm_last_path(pools[md]) == ("verify_copy" if md == 0 else "verify_replay_pipe")
+                assert m.ssm_last_path(pools[md]) == ("verify_copy" if md == 0 else "verify_replay_tma")
                 assert m.ssm_state_commit(pools[md], slots, acc, False, Ad) == m.SSM_OK
                 ys[md] = y
                 _, yo = osample[md].verify(list(range(len(sample))),
