@@ -106,6 +106,7 @@ void fill_step(const Pool &p, ssm::StepArgs &a, const void *x, const void *dt, c
     a.dec = p.d_dec;
     a.cf = p.d_cf;
     a.t1pad = p.t1pad;
+    a.cf_rows = p.cf_rows;
     a.position = p.d_position; a.log_len = p.d_log_len; a.cur = p.d_cur;
     a.slot_flags = p.d_slot_flags; a.flags = p.d_flags;
     a.H = p.H; a.P = p.P; a.N = p.N; a.G = p.G; a.hpg = p.hpg;
@@ -188,7 +189,9 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     p.t1max = c.max_tokens;
     p.wcap = c.mode == SSM_MODE_REPLAY ? c.window - 1 + c.max_tokens : 0;
     p.cb_w = (p.wcap + 3) / 4 * 4;
+    if (c.mode == SSM_MODE_REPLAY && p.wcap <= 32) p.cb_w = 32;  // whole-row float4 reads of the W rows
     p.t1pad = (p.t1max + 3) / 4 * 4;
+    p.cf_rows = (p.t1max + 15) / 16 * 16;
     p.in_bytes = in_elem(c.input_dtype);
     if (cudaGetDevice(&p.device) != cudaSuccess) { delete pool; return SSM_ERR_CUDA; }
     if (cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, p.device) != cudaSuccess || p.sm_count < 1)
@@ -221,7 +224,7 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         if (e == cudaSuccess) e = alloc(&p.d_cb, (size_t)p.cb_rows * p.G * p.t1max * p.cb_w, b);
         if (e == cudaSuccess) e = alloc(&p.d_wsc, (size_t)p.cb_rows * p.H * p.t1max * p.cb_w, b);
         if (e == cudaSuccess) e = alloc(&p.d_dec, (size_t)p.cb_rows * p.H * p.t1pad, b);
-        if (e == cudaSuccess) e = alloc(&p.d_cf, (size_t)p.cb_rows * p.G * p.t1max * p.N, b);
+        if (e == cudaSuccess) e = alloc(&p.d_cf, (size_t)p.cb_rows * p.G * p.cf_rows * p.N, b);
         if (e == cudaSuccess) e = alloc(&p.d_fold_items, (size_t)ssm::kMaxSlotsPerLaunch, b);
         if (e == cudaSuccess) e = alloc(&p.d_fold_count, 1, b);
     }
@@ -241,6 +244,11 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     if (e == cudaSuccess) e = cudaMemsetAsync(p.d_cur, 0xff, ns * sizeof(int32_t), s);  // -1: base state
     if (e == cudaSuccess) e = cudaMemsetAsync(p.d_slot_flags, 0, ns * sizeof(uint32_t), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(p.d_flags, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess && c.mode == SSM_MODE_REPLAY) {  // padding rows of the scratch read as zeros
+        e = cudaMemsetAsync(p.d_cf, 0, (size_t)p.cb_rows * p.G * p.cf_rows * p.N * sizeof(float), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(p.d_wsc, 0, (size_t)p.cb_rows * p.H * p.t1max * p.cb_w * sizeof(float), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(p.d_dec, 0, (size_t)p.cb_rows * p.H * p.t1pad * sizeof(float), s);
+    }
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) {
         free_all(p);

@@ -439,11 +439,8 @@ static cudaError_t set_smem(K kernel, size_t bytes) {
 
 cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path) {
     {  // the tensor-map path brings its own C . B and staging
-        const cudaError_t e = launch_verify_replay_tma(pool, a, s);
-        if (e != cudaErrorNotSupported) {
-            if (path) *path = "verify_replay_tma";
-            return e;
-        }
+        const cudaError_t e = launch_verify_replay_tma(pool, a, s, path);
+        if (e != cudaErrorNotSupported) return e;
     }
     const size_t smem = replay_smem_bytes(pool, a.n_tok);
     const size_t psmem = replay_prep_smem_bytes(pool, a.n_tok);

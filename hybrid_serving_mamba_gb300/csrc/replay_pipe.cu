@@ -12,7 +12,7 @@
 // come from L2 after the first head.
 //
 // Consumer phases per item:
-//   A  inclusive prefix sums of dt in fp64 (one warp), then W, decay_j,
+//   A  inclusive prefix sums of dt as fp32 pairs (one warp), then W, decay_j,
 //      C in fp32, and the non-finite check of the step inputs;
 //   B  the checkpoint rows from shared memory into registers, n_tok FMAs per
 //      element for C_j . h_c, xor-shuffle reduction over a row's lanes;
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
     float *decay = reinterpret_cast<float *>(smem + L.decay);
     float *dsm = reinterpret_cast<float *>(smem + L.d);
     float *Cf = reinterpret_cast<float *>(smem + L.Cf);
-    double *cum = reinterpret_cast<double *>(smem + L.cum);
+    Sum2 *cum = reinterpret_cast<Sum2 *>(smem + L.cum);
     const float rcpP2 = 2.0f / (float)P;
     TI *yout = reinterpret_cast<TI *>(a.y);
     TI *wx = reinterpret_cast<TI *>(a.log_x);
@@ -226,22 +226,9 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
         const float *cbs = reinterpret_cast<const float *>(S + L.cb);
         const float *dts = reinterpret_cast<const float *>(S + L.dt);
 
-        // phase A: prefix sums of dt (fp64, so that differences of them lose
-        // nothing), W, decay, C in fp32, and the step inputs' finiteness
-        if (warp == 0) {
-            double carry = 0.0;
-            for (int base = 0; base < m; base += 32) {
-                const int s = base + lane;
-                double v = s < m ? (double)dts[s] : 0.0;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const double u = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += u;
-                }
-                if (s < m) cum[s] = carry + v;
-                carry += __shfl_sync(0xffffffffu, v, 31);
-            }
-        }
+        // phase A: prefix sums of dt (fp32 pairs, so that differences of them
+        // are exact to fp32), W, decay, C in fp32, and the step inputs' finiteness
+        if (warp == 0) warp_prefix_sum2(dts, cum, m, lane);
         bool bad = false;  // step x is checked in phase C, where it is read anyway
         for (int e = threadIdx.x; e < T1 * N; e += nct) Cf[e] = to_f(Cs[e]);
         for (int j = threadIdx.x; j < T1; j += nct) bad |= !isfinite(dts[k + j]);
@@ -251,13 +238,13 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
             const int j = (int)(((float)t + 0.5f) * rcpm), s = t - j * m;
             float w = 0.f;
             if (s <= k + j) {
-                const float after = (float)(cum[k + j] - cum[s]);
+                const float after = sum2_diff(cum[k + j], cum[s]);
                 w = expf(A * after) * dts[s] * cbs[(size_t)j * a.cb_w + s];
                 if (s == k + j) w += D;  // skip connection D x_j
             }
             W[t] = w;
         }
-        for (int j = threadIdx.x; j < T1; j += nct) decay[j] = expf(A * (float)cum[k + j]);
+        for (int j = threadIdx.x; j < T1; j += nct) decay[j] = expf(A * (cum[k + j].hi + cum[k + j].lo));
         if (consumers_or(nct, bad)) {
             if (threadIdx.x == 0) raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_NONFINITE_INPUT);
             __syncwarp();
@@ -326,7 +313,7 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
 // Fold, pipelined: the (request, head) pairs listed by the commit walk the
 // same kind of ring.  Per item the producer brings the checkpoint and the m
 // logged rows of x and B; the consumers form w_s = exp(A sum_{r>s} dt_r) dt_s
-// from fp64 prefix sums of dt, then h <- exp(A sum dt) h + sum_s (w_s x_s) (x) B_s
+// from prefix sums of dt kept as fp32 pairs, then h <- exp(A sum dt) h + sum_s (w_s x_s) (x) B_s
 // with m FMAs per element, and store the checkpoint back from registers.
 
 struct FoldLayout {
@@ -427,7 +414,7 @@ __global__ void __launch_bounds__(kPipeMaxThreads) fold_pipe_kernel(const __grid
     const int sub = lane % LPR, rw = lane / LPR;
     float *xw = reinterpret_cast<float *>(smem + L.xw);
     float *bf = reinterpret_cast<float *>(smem + L.bf);
-    double *cum = reinterpret_cast<double *>(smem + L.cum);
+    Sum2 *cum = reinterpret_cast<Sum2 *>(smem + L.cum);
     float *sw = reinterpret_cast<float *>(smem + L.sw);
     const float rcpP = 1.0f / (float)P;
     int n = 0;
@@ -446,25 +433,12 @@ __global__ void __launch_bounds__(kPipeMaxThreads) fold_pipe_kernel(const __grid
         const TI *bs = reinterpret_cast<const TI *>(S + L.bs);
         const float *dts = reinterpret_cast<const float *>(S + L.dt);
 
-        if (warp == 0) {  // prefix sums of dt (fp64: their differences lose nothing)
-            double carry = 0.0;
-            for (int base = 0; base < m; base += 32) {
-                const int s = base + lane;
-                double v = s < m ? (double)dts[s] : 0.0;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const double u = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += u;
-                }
-                if (s < m) cum[s] = carry + v;
-                carry += __shfl_sync(0xffffffffu, v, 31);
-            }
-        }
+        if (warp == 0) warp_prefix_sum2(dts, cum, m, lane);  // differences exact to fp32
         for (int e = threadIdx.x; e < m * N; e += nct) bf[e] = to_f(bs[e]);
         bar_sync_named(1, nct);
         for (int s = threadIdx.x; s < m; s += nct)  // exp(A * dt applied after token s) dt_s
-            sw[s] = expf(A * (float)(cum[m - 1] - cum[s])) * dts[s];
-        if (threadIdx.x == 0) sw[mmax] = expf(A * (float)cum[m - 1]);
+            sw[s] = expf(A * sum2_diff(cum[m - 1], cum[s])) * dts[s];
+        if (threadIdx.x == 0) sw[mmax] = expf(A * (cum[m - 1].hi + cum[m - 1].lo));
         bar_sync_named(1, nct);
         for (int e = threadIdx.x; e < m * P; e += nct) {
             const int s = (int)(((float)e + 0.5f) * rcpP);

@@ -10,7 +10,7 @@
 // replay_group_coef_kernel  one CTA per (request, group): C_j . B_s once
 //     for the group's heads, the step's B, x and dt staged after the log (the
 //     commit folds them from there), the non-finite check of the step inputs,
-//     then per head (one warp) fp64 prefix sums of dt, W and decay_j into pool
+//     then per head (one warp) prefix sums of dt as fp32 pairs, W and decay_j into pool
 //     scratch, and C in fp32.  No state traffic.
 //
 // verify_replay_tma_kernel  persistent, one CTA per SM.  A producer warp
@@ -35,6 +35,7 @@
 #include <algorithm>
 
 #include "ssm_internal.cuh"
+#include "tc.cuh"
 #include "tma.cuh"
 
 namespace ssm {
@@ -85,7 +86,7 @@ template <> struct Vec16<float> {
     }
 };
 
-// smem: C [T1][N] | B [mmax][N] | C.B [T1][mmax] | dt per warp [nw][mmax] | prefix sums per warp [nw][mmax] f64
+// smem: C [T1][N] | B [mmax][N] | C.B [T1][mmax] | dt per warp [nw][mmax] | prefix sums per warp [nw][mmax] (pairs)
 __host__ __device__ inline size_t gcoef_smem_bytes(int T1, int mmax, int N, int nwarps) {
     size_t f = (size_t)T1 * N + (size_t)mmax * N + (size_t)T1 * mmax + (size_t)nwarps * mmax;
     f = (f + 1) & ~(size_t)1;
@@ -114,14 +115,21 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
     float *sDt = sCB + (size_t)T1 * mmax;
     size_t off = (size_t)T1 * N + (size_t)mmax * N + (size_t)T1 * mmax + (size_t)nwarps * mmax;
     off = (off + 1) & ~(size_t)1;
-    double *sCum = reinterpret_cast<double *>(reinterpret_cast<float *>(smem4) + off);
+    Sum2 *sCum = reinterpret_cast<Sum2 *>(reinterpret_cast<float *>(smem4) + off);
 
     const TI *stepC = reinterpret_cast<const TI *>(a.C);
     const TI *stepB = reinterpret_cast<const TI *>(a.B);
     const TI *lB = reinterpret_cast<const TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
     TI *wB = reinterpret_cast<TI *>(a.log_B) + (size_t)slot * a.wcap * a.G * N;
     bool bad = false;
-    float *cf = a.cf + ((size_t)i * a.G + g) * a.t1max * N;
+    float *cf = a.cf + ((size_t)i * a.G + g) * a.cf_rows * N;
+    const int nm = a.cf_nm;
+    // fp32 C for the streaming kernels: 4 values (a 16-byte chunk) of row j, columns n .. n + 3
+    auto cf_chunk = [&](int j, int n) -> float * {
+        if (!nm) return cf + (size_t)j * N + n;
+        const int kb = n >> 5, c = (n & 31) >> 2;
+        return cf + ((size_t)kb * nm + j) * 32 + ((c ^ (j & 7)) << 2);
+    };
     for (int e = threadIdx.x; e < T1 * NV; e += blockDim.x) {  // C rows, also kept in fp32
         const int j = e / NV, q = e - j * NV;
         const uint4 v = *reinterpret_cast<const uint4 *>(stepC + (((size_t)i * T1 + j) * a.G + g) * N + q * EV);
@@ -130,7 +138,11 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
         V::widen(v, o);
 #pragma unroll
         for (int u = 0; u < EV; u += 4)
-            *reinterpret_cast<float4 *>(cf + (size_t)j * N + q * EV + u) = *reinterpret_cast<const float4 *>(o + u);
+            *reinterpret_cast<float4 *>(cf_chunk(j, q * EV + u)) = *reinterpret_cast<const float4 *>(o + u);
+    }
+    for (int e = threadIdx.x; e < (nm - T1) * (N / 4); e += blockDim.x) {  // padding rows of the MMA operand
+        const int j = T1 + e / (N / 4), n = (e % (N / 4)) * 4;
+        *reinterpret_cast<float4 *>(cf_chunk(j, n)) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     for (int e = threadIdx.x; e < m * NV; e += blockDim.x) {  // B rows: the log, then the step
         const int s = e / NV, q = e - s * NV;
@@ -185,42 +197,29 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
     }
     __syncthreads();
     float *dts = sDt + (size_t)warp * mmax;
-    double *cum = sCum + (size_t)warp * mmax;
+    Sum2 *cum = sCum + (size_t)warp * mmax;
     for (int hh = warp; hh < hpg; hh += nwarps) {
         const int h = g * hpg + hh;
         const float A = a.A[h], D = a.D[h];
-        double carry = 0.0;  // inclusive prefix sums of dt in fp64: their differences lose nothing
-        for (int base = 0; base < m; base += 32) {
-            const int s = base + lane;
-            const float d = s < m ? a.log_dt[((size_t)slot * a.wcap + s) * H + h] : 0.f;
-            double v = (double)d;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
-            }
-            if (s < m) {
-                dts[s] = d;
-                cum[s] = carry + v;
-            }
-            carry += __shfl_sync(0xffffffffu, v, 31);
-        }
+        for (int s = lane; s < m; s += 32) dts[s] = a.log_dt[((size_t)slot * a.wcap + s) * H + h];
+        __syncwarp();
+        warp_prefix_sum2(dts, cum, m, lane);  // differences of these are exact to fp32
         __syncwarp();
         // W rows over the whole stride: zero past k + j, so readers need no bound
         float *wrow = a.wsc + ((size_t)i * H + h) * a.t1max * a.cb_w;
         for (int s = lane; s < a.cb_w; s += 32) {
-            const double cs = s < m ? cum[s] : 0.0;
+            const Sum2 cs = s < m ? cum[s] : Sum2{0.f, 0.f};
             const float ds = s < m ? dts[s] : 0.f;
             for (int j = 0; j < T1; ++j) {
                 float w = 0.f;
                 if (s <= k + j) {
-                    w = expf(A * (float)(cum[k + j] - cs)) * ds * sCB[(size_t)j * mmax + s];
+                    w = expf(A * sum2_diff(cum[k + j], cs)) * ds * sCB[(size_t)j * mmax + s];
                     if (s == k + j) w += D;  // skip connection D x_j
                 }
                 wrow[(size_t)j * a.cb_w + s] = w;
             }
         }
-        for (int j = lane; j < T1; j += 32) a.dec[((size_t)i * H + h) * a.t1pad + j] = expf(A * (float)cum[k + j]);
+        for (int j = lane; j < T1; j += 32) a.dec[((size_t)i * H + h) * a.t1pad + j] = expf(A * (cum[k + j].hi + cum[k + j].lo));
         __syncwarp();
     }
 }
@@ -325,46 +324,65 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint32_t bytes = (uint32_t)P * N * 4 + (uint32_t)a.wcap * P * sizeof(TI) + (uint32_t)T1 * N * 4 +
-                                   (uint32_t)T1 * a.cb_w * 4 + (uint32_t)up4(T1) * 4;
-            int last[kMaxStages];
-            for (int s = 0; s < kMaxStages; ++s) last[s] = -1;
-            for (int u = 0;; ++u) {
-                const int item = blockIdx.x + u * gridDim.x;
-                if (item >= n_items) break;
-                const int st = u % nstage;
-                if (u >= nstage && !wait_or_abort(&empty[st], (uint32_t)((u / nstage) - 1) & 1u, &s_abort, a.flags))
-                    break;
+        // The whole warp walks the items; lanes prefetch the gate inputs (log
+        // length, slot flags) of the next 32 items, lane 0 issues the copies.
+        const uint32_t bytes = (uint32_t)P * N * 4 + (uint32_t)a.wcap * P * sizeof(TI) + (uint32_t)T1 * N * 4 +
+                               (uint32_t)T1 * a.cb_w * 4 + (uint32_t)up4(T1) * 4;
+        int last[kMaxStages];
+        for (int s = 0; s < kMaxStages; ++s) last[s] = -1;
+        int my_k = 0;
+        uint32_t my_gate = 0;
+        for (int u = 0;; ++u) {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) break;
+            if ((u & 31) == 0) {
+                const int it2 = item + lane * gridDim.x;
+                my_k = 0;
+                my_gate = 0;
+                if (it2 < n_items) {
+                    const int sl = a.slots[it2 / H];
+                    my_k = a.log_len[sl];
+                    if (a.slot_flags[sl] & kSlotPoisoned) my_gate = SSM_FLAG_POISONED_SLOT;
+                    else if (my_k < 0 || my_k > wmax) my_gate = SSM_FLAG_BAD_ACCEPT;
+                }
+            }
+            const int k = __shfl_sync(0xffffffffu, my_k, u & 31);
+            const uint32_t gate = __shfl_sync(0xffffffffu, my_gate, u & 31);
+            const int st = u % nstage;
+            int ok = 1;
+            if (u >= nstage && lane == 0)
+                ok = wait_or_abort(&empty[st], (uint32_t)((u / nstage) - 1) & 1u, &s_abort, a.flags);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            if (lane == 0) {
                 const int i = item / H, h = item - i * H;
                 const int slot = a.slots[i];
                 const int g = h / a.hpg;
-                const int k = a.log_len[slot];
-                uint32_t gate = 0;
-                if (a.slot_flags[slot] & kSlotPoisoned) gate = SSM_FLAG_POISONED_SLOT;
-                else if (k < 0 || k > wmax) gate = SSM_FLAG_BAD_ACCEPT;
                 unsigned char *S = smem + (size_t)st * L.stage;
                 int *hdr = reinterpret_cast<int *>(S + L.hdr);
                 hdr[0] = (int)gate;
                 hdr[1] = k;
                 if (gate) {
                     mbar_arrive(&full[st]);
-                    continue;
+                } else {
+                    mbar_arrive_expect_tx(&full[st], bytes);
+                    const int row0 = (slot * H + h) * P;
+                    for (int kb = 0; kb < nkb; ++kb)
+                        tma_load_2d(S + L.st + (size_t)kb * P * 128, &tm_state, kb * 32, row0, &full[st]);
+                    tma_load_3d(S + L.xs, &tm_x, 0, h, slot * a.wcap, &full[st]);
+                    bulk_g2s(S + L.cf, a.cf + ((size_t)i * a.G + g) * a.cf_rows * N, (uint32_t)T1 * N * 4, &full[st]);
+                    bulk_g2s(S + L.w, a.wsc + ((size_t)i * H + h) * a.t1max * a.cb_w, (uint32_t)T1 * a.cb_w * 4,
+                             &full[st]);
+                    bulk_g2s(S + L.dec, a.dec + ((size_t)i * H + h) * a.t1pad, (uint32_t)up4(T1) * 4, &full[st]);
+                    last[st] = u;
                 }
-                mbar_arrive_expect_tx(&full[st], bytes);
-                const int row0 = (slot * H + h) * P;
-                for (int kb = 0; kb < nkb; ++kb) tma_load_2d(S + L.st + (size_t)kb * P * 128, &tm_state, kb * 32, row0, &full[st]);
-                tma_load_3d(S + L.xs, &tm_x, 0, h, slot * a.wcap, &full[st]);
-                bulk_g2s(S + L.cf, a.cf + ((size_t)i * a.G + g) * a.t1max * N, (uint32_t)T1 * N * 4, &full[st]);
-                bulk_g2s(S + L.w, a.wsc + ((size_t)i * H + h) * a.t1max * a.cb_w, (uint32_t)T1 * a.cb_w * 4, &full[st]);
-                bulk_g2s(S + L.dec, a.dec + ((size_t)i * H + h) * a.t1pad, (uint32_t)up4(T1) * 4, &full[st]);
-                last[st] = u;
             }
-            // no copy may still be landing when the CTA exits
+            __syncwarp();
+        }
+        // no copy may still be landing when the CTA exits
+        if (lane == 0)
             for (int s = 0; s < nstage; ++s)
                 if (last[s] >= 0 && !mbar_wait(&full[s], (uint32_t)(last[s] / nstage) & 1u))
                     atomicOr(a.flags, SSM_FLAG_TIMEOUT);
-        }
     } else {
         // ------------------------------------------------------------ consumers
         const int grp = warp / kGroupWarps, w = warp % kGroupWarps, gt = w * 32 + lane;
@@ -470,6 +488,396 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     __syncthreads();
 }
 
+// ------------------------------------------------------------------ tensor-core streaming kernel
+//
+// verify_replay_tc_kernel: the same outputs with C_j . h_c on the 5th-generation
+// tensor cores.  An item is the pair of heads (h, h + 1) of one request (same
+// group, so the same C): their checkpoints stacked are the M = 128 rows of A
+// (P = 64 each), K = N, and the step tokens are the N = NM columns (16 or 32,
+// padded).  A kind::tf32 MMA reads an fp32 operand through its tf32 part: the
+// sign, the exponent and the top 10 mantissa bits (the 13 low bits are
+// dropped).  With hi = v with those 13 bits cleared and lo = v - hi (exact in
+// fp32, at most 2^-10 |v|, and itself cut to tf32 with a relative error of
+// 2^-11 more), C . h = C . h_hi + C . h_lo, and for fp32 inputs also
+// + C_lo . h_hi; bf16 C is a tf32 value already.  The dropped C_lo . h_lo and
+// the cut of lo leave about 2^-20 of each product, below the fp32 rounding of
+// the sum.
+//
+// Data flow per item: the producer streams the checkpoint in 32-column blocks
+// (16 KiB: 128 rows x 128 bytes, 128-byte swizzle) into a ring of slots, and C
+// (fp32, K-major swizzled), the x rows, W and decay_j of the two heads into a
+// small per-item ring.  Each split warp reads its 32 rows of a block (thread =
+// row, so the swizzle spreads the eight rows of a bank group), writes hi and
+// lo into a 64-column TMEM operand slot and frees the ring slot at once; the
+// warps work independently (no barrier between them per block).  The MMA
+// issuer takes A (hi, then lo) from TMEM and B (C) from shared memory, one
+// accumulator per item, and commits once per item (a commit costs about as
+// much as four MMAs) to that item's `done` barrier, which frees its operand
+// slots and stage and hands D to the epilogue.
+//
+// Warps:  0-3 epilogue (TMEM lane quarters 0-3: row = 32 w + lane), the log
+//         term from the staged x and W rows, y = decay_j D[row][j] + log term;
+//         4-7 and 8-11 split, two groups (each over the four lane quarters)
+//           taking even and odd blocks: a block takes a group about half a
+//           microsecond end to end, so one group alone could not keep up with
+//           the stream; group 0 also makes C_lo for fp32 inputs;
+//         12 producer (per-item data and the checkpoint blocks; gate inputs
+//           prefetched a warp at a time);
+//         13 MMA issuer (lane 0) and TMEM owner.
+// TMEM: D buffer b (two) at columns NM b; operand slots of 64 columns (hi at
+// +0, lo at +32) from column 2 NM.
+constexpr int kTcEpiWarps = 4;
+constexpr int kTcSplitGroups = 2;  // split groups take alternate checkpoint blocks
+constexpr int kTcProd = 4 + 4 * kTcSplitGroups;
+constexpr int kTcMma = kTcProd + 1;
+constexpr int kTcThreads = (kTcMma + 1) * 32;
+constexpr int kTcMaxRing = 12;  // checkpoint blocks in flight
+constexpr int kTcMaxAux = 3;    // per-item stages
+constexpr int kTcASlots = 6;    // TMEM operand slots (hi + lo of one 32-column block each)
+constexpr int kTcDone = 4;      // per-item MMA completion barriers (waiters lag by < 4 items)
+constexpr uint32_t kTcCols = 512;
+constexpr uint32_t kTf32Keep = 0xFFFFE000u;  // sign, exponent and the 10 tf32 mantissa bits
+constexpr int kTcBarEpi = 0, kTcBarSplit = 1;  // group_or groups: named barriers 1 and 2
+
+struct TcLayout {
+    uint32_t Bt, Blo, xs, w, dec, hdr, aux;  // inside one per-item stage
+    uint32_t ring_bytes, aux_base, bars;     // after alignment of the base to 1024
+};
+
+__host__ __device__ inline TcLayout tc_layout(int N, int NM, int P, int in_b, int wcap, int t1max, int cb_w,
+                                             int t1pad, bool split_c, int nring, int naux) {
+    TcLayout L;
+    const uint32_t nkb = (uint32_t)N / 32;
+    uint32_t o = 0;
+    L.Bt = 0;   o = nkb * (uint32_t)NM * 128u;            // NM rows x 128 bytes per column block
+    L.Blo = o;  if (split_c) o += nkb * (uint32_t)NM * 128u;
+    L.xs = o;   o = up16(o + 2u * wcap * P * in_b);       // [s][2 heads][P]
+    L.w = o;    o = up16(o + 2u * t1max * cb_w * 4);      // [2 heads][t1max][cb_w]
+    L.dec = o;  o = up16(o + 2u * t1pad * 4);             // [2 heads][t1pad]
+    L.hdr = o;  o += 16;
+    L.aux = (o + 1023u) & ~1023u;
+    L.ring_bytes = (uint32_t)nring * 16384u;
+    L.aux_base = L.ring_bytes;
+    L.bars = L.aux_base + (uint32_t)naux * L.aux;
+    return L;
+}
+
+__host__ __device__ inline size_t tc_smem_bytes(const TcLayout &L) {
+    return (size_t)L.bars + (2 * kTcMaxRing + 2 * kTcMaxAux + kTcASlots + kTcDone + 2) * 8 + 1024;
+}
+
+template <typename TI, int NM>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    verify_replay_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap tm_state2,
+                            const __grid_constant__ CUtensorMap tm_x2, int nring, int naux) {
+    constexpr bool kSplitC = sizeof(TI) == 4;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ uint32_t s_abort, s_tmem;
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int P = a.P, N = a.N, T1 = a.n_tok, H = a.H;
+    const int nkb = N / 32, hp = H / 2;
+    const int wmax = a.wcap - a.t1max;
+    const int n_items = a.batch * hp;
+    const TcLayout L = tc_layout(N, NM, P, (int)sizeof(TI), a.wcap, a.t1max, a.cb_w, a.t1pad, kSplitC, nring, naux);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *rfull = bars, *rempty = rfull + kTcMaxRing;                // checkpoint ring
+    uint64_t *xfull = rempty + kTcMaxRing, *xempty = xfull + kTcMaxAux;  // per-item ring
+    uint64_t *afull = xempty + kTcMaxAux;                                // TMEM operand slots
+    uint64_t *done = afull + kTcASlots;                                  // MMAs of an item finished
+    uint64_t *dempty = done + kTcDone;                                   // TMEM D buffers
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nring; ++s) {
+            mbar_init(&rfull[s], 1);
+            mbar_init(&rempty[s], 4);
+        }
+        for (int s = 0; s < naux; ++s) {
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], kTcEpiWarps);
+        }
+        for (int s = 0; s < kTcASlots; ++s) mbar_init(&afull[s], 4);
+        for (int s = 0; s < kTcDone; ++s) mbar_init(&done[s], 1);
+        for (int s = 0; s < 2; ++s) mbar_init(&dempty[s], kTcEpiWarps);
+        mbar_fence_init();
+        s_abort = 0u;
+    }
+    if (warp == kTcMma) tc::tmem_alloc(&s_tmem, kTcCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == kTcProd) {
+        // ------------------------------------------------------------ producer
+        const uint32_t cbytes = (uint32_t)nkb * NM * 128u;  // C, already in the operand layout
+        const uint32_t xbytes = cbytes + 2u * a.wcap * P * sizeof(TI) + 2u * a.t1max * a.cb_w * 4u + 2u * a.t1pad * 4u;
+        int xlast[kTcMaxAux], rlast[kTcMaxRing];
+        for (int s = 0; s < kTcMaxAux; ++s) xlast[s] = -1;
+        for (int s = 0; s < kTcMaxRing; ++s) rlast[s] = -1;
+        int my_k = 0, nblk = 0;
+        uint32_t my_gate = 0;
+        bool alive = true;
+        for (int u = 0; alive; ++u) {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) break;
+            if ((u & 31) == 0) {
+                const int it2 = item + lane * gridDim.x;
+                my_k = 0;
+                my_gate = 0;
+                if (it2 < n_items) {
+                    const int sl = a.slots[it2 / hp];
+                    my_k = a.log_len[sl];
+                    if (a.slot_flags[sl] & kSlotPoisoned) my_gate = SSM_FLAG_POISONED_SLOT;
+                    else if (my_k < 0 || my_k > wmax) my_gate = SSM_FLAG_BAD_ACCEPT;
+                }
+            }
+            const int k = __shfl_sync(0xffffffffu, my_k, u & 31);
+            const uint32_t gate = __shfl_sync(0xffffffffu, my_gate, u & 31);
+            if (lane == 0) {
+                const int xs_ = u % naux;
+                const int i = item / hp, h0 = 2 * (item - i * hp);
+                const int slot = a.slots[i];
+                const int g = h0 / a.hpg;
+                if (u >= naux && !wait_or_abort(&xempty[xs_], (uint32_t)((u / naux) - 1) & 1u, &s_abort, a.flags)) {
+                    alive = false;
+                } else {
+                    unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
+                    int *hdr = reinterpret_cast<int *>(X + L.hdr);
+                    hdr[0] = (int)gate;
+                    hdr[1] = k;
+                    if (gate) {
+                        mbar_arrive(&xfull[xs_]);
+                    } else {
+                        mbar_arrive_expect_tx(&xfull[xs_], xbytes);
+                        bulk_g2s(X + L.Bt, a.cf + ((size_t)i * a.G + g) * a.cf_rows * N, cbytes, &xfull[xs_]);
+                        tma_load_3d(X + L.xs, &tm_x2, 0, h0, slot * a.wcap, &xfull[xs_]);
+                        bulk_g2s(X + L.w, a.wsc + ((size_t)i * H + h0) * a.t1max * a.cb_w,
+                                 2u * a.t1max * a.cb_w * 4u, &xfull[xs_]);
+                        bulk_g2s(X + L.dec, a.dec + ((size_t)i * H + h0) * a.t1pad, 2u * a.t1pad * 4u, &xfull[xs_]);
+                        xlast[xs_] = u;
+                        const int row0 = (slot * H + h0) * P;
+                        for (int kb = 0; kb < nkb; ++kb, ++nblk) {
+                            const int rs = nblk % nring;
+                            if (nblk >= nring &&
+                                !wait_or_abort(&rempty[rs], (uint32_t)((nblk / nring) - 1) & 1u, &s_abort, a.flags)) {
+                                alive = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(&rfull[rs], 16384u);
+                            tma_load_2d(smem + (size_t)rs * 16384, &tm_state2, kb * 32, row0, &rfull[rs]);
+                            rlast[rs] = nblk;
+                        }
+                    }
+                }
+            }
+            alive = __shfl_sync(0xffffffffu, (int)alive, 0) != 0;
+        }
+        if (lane == 0) {  // no copy may still be landing when the CTA exits
+            for (int s = 0; s < naux; ++s)
+                if (xlast[s] >= 0 && !mbar_wait(&xfull[s], (uint32_t)(xlast[s] / naux) & 1u))
+                    atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+            for (int s = 0; s < nring; ++s)
+                if (rlast[s] >= 0 && !mbar_wait(&rfull[s], (uint32_t)(rlast[s] / nring) & 1u))
+                    atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else if (warp == kTcMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_tf32_f32(128, NM);
+            int nproc = 0;
+            bool alive = true;
+            for (int u = 0; alive; ++u) {
+                const int item = blockIdx.x + u * gridDim.x;
+                if (item >= n_items) break;
+                const int xs_ = u % naux;
+                if (!wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags)) break;
+                const unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
+                if (reinterpret_cast<const int *>(X + L.hdr)[0]) continue;
+                const int db = nproc & 1;
+                if (nproc >= 2 && !wait_or_abort(&dempty[db], (uint32_t)((nproc >> 1) - 1) & 1u, &s_abort, a.flags))
+                    break;
+                tc::fence_after_sync();
+                const uint32_t d_tm = tmem + (uint32_t)db * NM;
+                const uint32_t b_hi = smem_addr(X + L.Bt), b_lo = smem_addr(X + L.Blo);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const int c = nproc * nkb + kb, as = c % kTcASlots;
+                    if (!wait_or_abort(&afull[as], (uint32_t)(c / kTcASlots) & 1u, &s_abort, a.flags)) {
+                        if (kb > 0) {  // MMAs of this item are in flight: let them finish first
+                            tc::mma_commit(&done[nproc % kTcDone]);
+                            mbar_wait(&done[nproc % kTcDone], (uint32_t)(nproc / kTcDone) & 1u);
+                        }
+                        alive = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t a_hi = tmem + 2u * NM + (uint32_t)as * 64u, a_lo = a_hi + 32u;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {  // K = 8 tf32 per MMA
+                        const uint32_t boff = (uint32_t)kb * NM * 128 + 32 * kk;
+                        const uint64_t dbh = tc::smem_desc_sw128(b_hi + boff, 1024);
+                        tc::mma_tf32_ta(d_tm, a_hi + 8 * kk, dbh, idesc, (kb | kk) != 0);
+                        tc::mma_tf32_ta(d_tm, a_lo + 8 * kk, dbh, idesc, true);
+                        if (kSplitC) tc::mma_tf32_ta(d_tm, a_hi + 8 * kk, tc::smem_desc_sw128(b_lo + boff, 1024), idesc, true);
+                    }
+                }
+                if (!alive) break;
+                tc::mma_commit(&done[nproc % kTcDone]);
+                ++nproc;
+            }
+            // every MMA issued has completed before TMEM is released
+            if (alive && nproc > 0 && !mbar_wait(&done[(nproc - 1) % kTcDone], (uint32_t)((nproc - 1) / kTcDone) & 1u))
+                atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else if (warp >= kTcEpiWarps && warp < kTcProd) {
+        // ------------------------------------------------------------ split
+        const int q = warp & 3;                       // TMEM lane quarter
+        const int sg = (warp - kTcEpiWarps) >> 2;     // split group: blocks c with c % 2 == sg
+        const int row = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        int nproc = 0;
+        bool alive = true;
+        for (int u = 0; alive; ++u) {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) break;
+            const int xs_ = u % naux;
+            if (!wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags)) break;
+            unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
+            if (reinterpret_cast<const int *>(X + L.hdr)[0]) continue;
+            if (kSplitC && sg == 0) {  // C_lo = C - C_hi beside C (this warp's share), before block 0 is signalled
+                const uint4 *b4 = reinterpret_cast<const uint4 *>(X + L.Bt);
+                uint4 *bl4 = reinterpret_cast<uint4 *>(X + L.Blo);
+                for (int e = row; e < nkb * NM * 8; e += 128) {
+                    const uint4 v = b4[e];
+                    bl4[e] = make_uint4(__float_as_uint(__uint_as_float(v.x) - __uint_as_float(v.x & kTf32Keep)),
+                                        __float_as_uint(__uint_as_float(v.y) - __uint_as_float(v.y & kTf32Keep)),
+                                        __float_as_uint(__uint_as_float(v.z) - __uint_as_float(v.z & kTf32Keep)),
+                                        __float_as_uint(__uint_as_float(v.w) - __uint_as_float(v.w & kTf32Keep)));
+                }
+                tc::fence_proxy_async_smem();
+            }
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int c = nproc * nkb + kb, rs = c % nring, as = c % kTcASlots;
+                if ((c & 1) != sg) continue;
+                bool ok = wait_or_abort(&rfull[rs], (uint32_t)(c / nring) & 1u, &s_abort, a.flags);
+                if (ok && c >= kTcASlots) {  // the slot's previous block belongs to item (c - slots) / nkb
+                    const int pj = (c - kTcASlots) / nkb;
+                    ok = wait_or_abort(&done[pj % kTcDone], (uint32_t)(pj / kTcDone) & 1u, &s_abort, a.flags);
+                }
+                if (!ok) {
+                    alive = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                // this thread's row of the block: 8 chunks of 16 bytes, chunk c at c ^ (row % 8)
+                const unsigned char *blk = smem + (size_t)rs * 16384 + (size_t)row * 128;
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(blk + ((ch ^ (row & 7)) << 4));
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hi[4 * ch + e] = w[e] & kTf32Keep;
+                        lo[4 * ch + e] = __float_as_uint(__uint_as_float(w[e]) - __uint_as_float(hi[4 * ch + e]));
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rempty[rs]);  // the rows are in registers: free the ring slot
+                const uint32_t a_hi = tmem + lane_off + 2u * NM + (uint32_t)as * 64u;
+                tc::tmem_st32(a_hi, hi);
+                tc::tmem_st32(a_hi + 32u, lo);
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[as]);
+            }
+            ++nproc;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int r = warp * 32 + lane, hd = r / 64, p = r - hd * 64;
+        TI *y = reinterpret_cast<TI *>(a.y);
+        int nproc = 0;
+        for (int u = 0;; ++u) {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) break;
+            const int xs_ = u % naux;
+            const bool ok = wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags);
+            if (group_or(kTcBarEpi, !ok)) break;
+            const unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
+            const int gate = reinterpret_cast<const int *>(X + L.hdr)[0];
+            const int k = reinterpret_cast<const int *>(X + L.hdr)[1];
+            const int i = item / hp, h0 = 2 * (item - i * hp);
+            if (gate) {
+                if (r == 0) raise_flag(a.flags, a.slot_flags, a.slots[i], (uint32_t)gate);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xempty[xs_]);
+                continue;
+            }
+            const int m = k + T1;
+            // log term: x of this row's head as pairs (zero past the sequence), W rows as float4
+            const TI *xs = reinterpret_cast<const TI *>(X + L.xs);
+            float2 xr[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int s = 2 * q;
+                xr[q].x = s < m ? to_f(xs[((size_t)s * 2 + hd) * P + p]) : 0.f;
+                xr[q].y = s + 1 < m ? to_f(xs[((size_t)(s + 1) * 2 + hd) * P + p]) : 0.f;
+            }
+            const float *Wh = reinterpret_cast<const float *>(X + L.w) + (size_t)hd * a.t1max * a.cb_w;
+            const float *dh = reinterpret_cast<const float *>(X + L.dec) + (size_t)hd * a.t1pad;
+            float lt[NM], dj[NM];
+#pragma unroll
+            for (int j = 0; j < NM; ++j) {
+                lt[j] = 0.f;
+                dj[j] = 0.f;
+                if (j < T1) {
+                    const float4 *w4 = reinterpret_cast<const float4 *>(Wh + (size_t)j * a.cb_w);
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 wv = w4[q];
+                        acc = ffma2(make_float2(wv.x, wv.y), xr[2 * q], acc);
+                        acc = ffma2(make_float2(wv.z, wv.w), xr[2 * q + 1], acc);
+                    }
+                    lt[j] = acc.x + acc.y;
+                    dj[j] = dh[j];
+                }
+            }
+            const int db = nproc & 1;
+            const bool okd = wait_or_abort(&done[nproc % kTcDone], (uint32_t)(nproc / kTcDone) & 1u, &s_abort, a.flags);
+            if (group_or(kTcBarEpi, !okd)) break;
+            tc::fence_after_sync();
+            float d[NM];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)db * NM;
+#pragma unroll
+            for (int c = 0; c < NM; c += 16) {
+                float part[16];
+                tc::tmem_ld16(taddr + c, part);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) d[c + q] = part[q];
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[db]);
+            TI *yrow = y + ((size_t)i * T1 * H + h0 + hd) * P + p;
+#pragma unroll
+            for (int j = 0; j < NM; ++j)
+                if (j < T1) yrow[(size_t)j * H * P] = from_f<TI>(fmaf(dj[j], d[j], lt[j]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xempty[xs_]);
+            ++nproc;
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kTcMma) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTcCols);
+    }
+}
+
 template <typename Kernel>
 cudaError_t set_smem(Kernel k, size_t bytes) {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -512,6 +920,17 @@ bool replay_tma_encode(Pool &p) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     p.tm_ok = true;
+    // tensor-core kernel: pairs of heads of P = 64 rows, 32-column boxes of both heads' rows
+    if (p.P == 64 && p.H % 2 == 0 && p.hpg % 2 == 0 && p.cb_w == 32) {
+        const cuuint32_t sb2[2] = {32u, 128u};
+        const cuuint32_t xb2[3] = {(cuuint32_t)p.P, 2u, (cuuint32_t)p.wcap};
+        p.tm_tc_ok = enc(&p.tm_state2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.state, sd, ss, sb2, se,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+                     enc(&p.tm_logx2, xt, 3, p.log_x, xd, xst, xb2, xe, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     return true;
 }
 
@@ -519,7 +938,7 @@ size_t replay_coef_smem_bytes(const Pool &pool, int n_tok) {
     return gcoef_smem_bytes(n_tok, pool.wcap - pool.t1max + n_tok, pool.N, kCoefThreads / 32);
 }
 
-cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s) {
+cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path) {
     if (!pool.tm_ok || !a.wsc || !a.cf || !a.dec) return cudaErrorNotSupported;
     const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
     const int in_b = bf ? 2 : 4;
@@ -529,14 +948,37 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         reinterpret_cast<uintptr_t>(a.C) % 16)
         return cudaErrorNotSupported;
     const int T1 = a.n_tok;
-    const TmaLayout L = tma_layout(a.P, a.N, in_b, T1, a.wcap, a.cb_w);
     const size_t csmem = replay_coef_smem_bytes(pool, T1);
     int dev = 0, max_smem = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (csmem > (size_t)max_smem) return cudaErrorNotSupported;
+
+    // the streaming kernel first, since it fixes the layout the coefficient kernel writes C in:
+    // tensor cores take pairs of heads, at most 32 step tokens, whole W rows of 32
+    int NM = 0, nring = 0, naux = 0;
+    size_t tsmem = 0;
+    if (pool.tm_tc_ok && T1 <= 32 && T1 <= pool.cf_rows && a.P == 64 && a.cb_w == 32 && a.N <= 128) {
+        NM = T1 <= 16 ? 16 : 32;
+        if (NM > pool.cf_rows) NM = 0;
+        for (int na = kTcMaxAux; NM && na >= 2 && !nring; --na)
+            for (int nr = kTcMaxRing; nr >= 4; --nr) {
+                const size_t b =
+                    tc_smem_bytes(tc_layout(a.N, NM, a.P, in_b, a.wcap, a.t1max, a.cb_w, a.t1pad, !bf, nr, na));
+                if (b <= (size_t)max_smem) {
+                    nring = nr;
+                    naux = na;
+                    tsmem = b;
+                    break;
+                }
+            }
+    }
+    const TmaLayout L = tma_layout(a.P, a.N, in_b, T1, a.wcap, a.cb_w);
     const int nstage = std::min(kMaxStages, (int)(((long)max_smem - (long)L.fixed) / (long)L.stage));
-    if (nstage < 2 || csmem > (size_t)max_smem) return cudaErrorNotSupported;
+    if (!nring && nstage < 2) return cudaErrorNotSupported;
     const size_t smem = (size_t)nstage * L.stage + L.fixed;
+    StepArgs ac = a;
+    ac.cf_nm = nring ? NM : 0;
 
     cudaError_t e = cudaSuccess;
     SSM_DISPATCH_N(a.N, {
@@ -544,16 +986,37 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
             auto k = replay_group_coef_kernel<NN, __nv_bfloat16>;
             e = set_smem(k, csmem);
             if (e != cudaSuccess) return e;
-            k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(a);
+            k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(ac);
         } else {
             auto k = replay_group_coef_kernel<NN, float>;
             e = set_smem(k, csmem);
             if (e != cudaSuccess) return e;
-            k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(a);
+            k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(ac);
         }
     });
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+
+    if (nring) {
+        const int tgrid = std::min(a.batch * (a.H / 2), pool.sm_count);
+#define SSM_TC(TI, NMV)                                                                                \
+    do {                                                                                               \
+        auto k = verify_replay_tc_kernel<TI, NMV>;                                                     \
+        e = set_smem(k, tsmem);                                                                        \
+        if (e != cudaSuccess) return e;                                                                \
+        k<<<tgrid, kTcThreads, tsmem, s>>>(ac, pool.tm_state2, pool.tm_logx2, nring, naux);           \
+    } while (0)
+        if (bf) {
+            if (NM == 16) SSM_TC(__nv_bfloat16, 16);
+            else SSM_TC(__nv_bfloat16, 32);
+        } else {
+            if (NM == 16) SSM_TC(float, 16);
+            else SSM_TC(float, 32);
+        }
+#undef SSM_TC
+        if (path) *path = "verify_replay_tc";
+        return cudaGetLastError();
+    }
 
     const int n_items = a.batch * a.H;
     const int grid = std::min(n_items, pool.sm_count);
@@ -562,7 +1025,7 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         auto k = verify_replay_tma_kernel<TI, RP>;                                                     \
         e = set_smem(k, smem);                                                                         \
         if (e != cudaSuccess) return e;                                                                \
-        k<<<grid, kTmaThreads, smem, s>>>(a, pool.tm_state, pool.tm_logx, nstage);                     \
+        k<<<grid, kTmaThreads, smem, s>>>(ac, pool.tm_state, pool.tm_logx, nstage);                    \
     } while (0)
     if (bf) {
         if (a.P <= 32) SSM_TMA(__nv_bfloat16, 1);
@@ -572,6 +1035,7 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         else SSM_TMA(float, 2);
     }
 #undef SSM_TMA
+    if (path) *path = "verify_replay_tma";
     return cudaGetLastError();
 }
 

@@ -59,11 +59,15 @@ struct Pool {
     int cb_w = 0;                      // row stride of d_cb: wcap rounded up to 4 floats
     float *d_wsc = nullptr;            // replay: W[j][s] per head, [cb_rows][H][t1max][cb_w]
     float *d_dec = nullptr;            // replay: decay_j per head, [cb_rows][H][t1pad]
-    float *d_cf = nullptr;             // replay: C_j in fp32 per group, [cb_rows][G][t1max][N]
+    float *d_cf = nullptr;             // replay: C_j in fp32 per group, [cb_rows][G][cf_rows][N]
+    int cf_rows = 0;                   // t1max rounded up to 16
     int t1pad = 0;                     // t1max rounded up to 4
     CUtensorMap tm_state;              // replay: checkpoint rows, 32-column boxes, 128-byte swizzle
     CUtensorMap tm_logx;               // replay: one head's log of x rows per box
     bool tm_ok = false;                // both maps encoded
+    CUtensorMap tm_state2;             // replay, tensor cores: 32 columns x 128 rows (two heads) per box
+    CUtensorMap tm_logx2;              // replay, tensor cores: two heads' logs of x rows per box
+    bool tm_tc_ok = false;             // the two maps above encoded
     int2 *d_fold_items = nullptr;      // (request index, tokens to fold) of one commit launch
     int32_t *d_fold_count = nullptr;
     int sm_count = 1;
@@ -93,6 +97,9 @@ struct StepArgs {  // decode, copy verify, replay verify
     float *dec;
     float *cf;
     int t1pad;
+    int cf_rows;      // row stride of a (request, group) block of cf, in rows of N
+    int cf_nm;        // 0: cf rows plain; else NM rows (T1 padded with zero rows) as the MMA's K-major
+                      // swizzled operand: [column block][row][32], 16-byte chunk c of row j at c ^ (j % 8)
     int64_t *position;
     int32_t *log_len;
     int32_t *cur;
@@ -165,7 +172,7 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
 // wsc / dec / cf scratch and the pool's tensor maps); cudaErrorNotSupported
 // when it cannot run.  replay_tma_encode fills Pool::tm_* (false: shape not
 // covered or no encoder in the driver).
-cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s);
+cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path);
 size_t replay_coef_smem_bytes(const Pool &pool, int n_tok);
 bool replay_tma_encode(Pool &p);
 // Pipelined replay verify (persistent CTAs, bulk-copy ring); returns
@@ -198,6 +205,42 @@ size_t fold_smem_bytes(const Pool &pool);
     }
 
 // ---------------------------------------------------------------- device helpers
+
+// Prefix sums of dt kept as unevaluated pairs hi + lo of fp32 values: each
+// addition also carries its rounding error (Knuth's two-sum), so the
+// difference of two prefix sums is as accurate as its fp32 result can hold
+// (a sum of the dt between two tokens, the exponent of a decay factor)
+// without fp64 arithmetic, whose throughput on this GPU is a small fraction
+// of fp32's.  No multiplies are involved, so FMA contraction cannot change it.
+struct Sum2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ Sum2 sum2_add(Sum2 a, Sum2 b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    const float e = ((a.hi - (s - bb)) + (b.hi - bb)) + (a.lo + b.lo);
+    const float hi = s + e;
+    return Sum2{hi, e - (hi - s)};
+}
+
+__device__ __forceinline__ float sum2_diff(Sum2 a, Sum2 b) { return (a.hi - b.hi) + (a.lo - b.lo); }
+
+// Inclusive prefix sums of dt[0 .. m) into cum[0 .. m) by one warp.
+__device__ __forceinline__ void warp_prefix_sum2(const float *dt, Sum2 *cum, int m, int lane) {
+    Sum2 carry{0.f, 0.f};
+    for (int base = 0; base < m; base += 32) {
+        const int s = base + lane;
+        Sum2 v{s < m ? dt[s] : 0.f, 0.f};
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const Sum2 u{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+            if (lane >= o) v = sum2_add(u, v);
+        }
+        if (s < m) cum[s] = sum2_add(carry, v);
+        carry = sum2_add(carry, Sum2{__shfl_sync(0xffffffffu, v.hi, 31), __shfl_sync(0xffffffffu, v.lo, 31)});
+    }
+}
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }

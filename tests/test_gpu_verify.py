@@ -102,6 +102,29 @@ def test_replay_kernel_choice():
     m.ssm_state_destroy(pool)
 
 
+@pytest.mark.parametrize("dt_in,T,W,path", [
+    (synth.F32, 8, 16, "verify_replay_tc"),   # fp32 inputs: C split too (three MMAs per K step)
+    (synth.BF16, 8, 16, "verify_replay_tc"),
+    (synth.BF16, 19, 8, "verify_replay_tc"),  # 20 step tokens: 32 MMA columns
+    (synth.F32, 19, 8, "verify_replay_tc"),
+])
+def test_replay_tensor_core_verify(dt_in, T, W, path):
+    """Heads of 64 rows in pairs run C_j . h_c on the tensor cores with hi / lo
+    tf32 splits; at fp32 inputs the oracle's 1e-5 tolerance checks that the
+    splits keep fp32 accuracy."""
+    m = _mod()
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, W, T, 0.7, steps=6, H=4, P=64, N=128, G=2, dt_in=dt_in,
+                               expect_path=path)
+    m.ssm_state_destroy(pool)
+
+
+def test_replay_tensor_core_mixed_token_counts():
+    m = _mod()
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, 8, 8, 0.6, steps=8, H=8, P=64, N=128, G=2, dt_in=synth.BF16,
+                               n_tok_pattern=[9, 3, 1, 7], expect_path="verify_replay_tc")
+    m.ssm_state_destroy(pool)
+
+
 def test_replay_mixed_token_counts_and_checkpoint_fold():
     import torch
     m = _mod()
@@ -214,7 +237,7 @@ def test_config3_full_batch_sampled(T, p, W):
             for md, fn in ((0, m.ssm_verify_copy), (1, m.ssm_verify_replay)):
                 y = empty_like_out((R, T1, H, P), synth.BF16)
                 assert fn(pools[md], slots, T1, *dev, Ad, Dd, y) == m.SSM_OK
-                assert m.ssm_last_path(pools[md]) == ("verify_copy" if md == 0 else "verify_replay_tma")
+                assert m.ssm_last_path(pools[md]) == ("verify_copy" if md == 0 else "verify_replay_tc")
                 assert m.ssm_state_commit(pools[md], slots, acc, False, Ad) == m.SSM_OK
                 ys[md] = y
                 _, yo = osample[md].verify(list(range(len(sample))),
