@@ -561,7 +561,14 @@ def run_case(args):
     import hybrid_serving_mamba_gb300 as m
     torch.cuda.set_device(0)
     args.rank = 0
-    if args.case == "verify":
+    if args.case == "decode":
+        DEC["R"] = args.batch or DEC["R"]
+        DEC["tokens"] = 4
+        args.steps, args.warmup = 1, 1
+        out = bench_decode(torch, m, None, args, ClockSampler(0))
+        print(json.dumps({"case": "decode", "batch": DEC["R"], "launch_us": 1000 * out["launch_ms"],
+                          "bytes_per_launch": out["bytes_per_launch"]}))
+    elif args.case == "verify":
         VER["R"] = args.batch or VER["R"]
         VER["steps"] = 4
         out = bench_verify(torch, m, args)
@@ -615,7 +622,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extras", action="store_true", help="decode only (no verify / prefill / e2e / cpu)")
-    ap.add_argument("--case", choices=("verify", "prefill", "prefill_varlen"),
+    ap.add_argument("--case", choices=("decode", "verify", "prefill", "prefill_varlen"),
                     help="run one workload alone (for profiler captures)")
     ap.add_argument("--batch", type=int, default=0, help="batch / sequence count of --case")
     args = ap.parse_args()
