@@ -615,6 +615,18 @@ def run_reference(args):
     return 0
 
 
+def job_rate(local_ms, local_units, dist=None, device="cpu"):
+    """Whole-job rate of N replicas: the units all ranks processed divided by
+    the slowest rank's time (max over ranks); returns (rate per second, ms)."""
+    ms, world = float(local_ms), 1
+    if dist is not None:
+        import torch
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, world = float(t.item()), dist.get_world_size()
+    return local_units * world / (ms / 1000.0), ms
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,13 +659,7 @@ def main():
 
     clocks = ClockSampler(local)
     dec = bench_decode(torch, m, dist, args, clocks)
-    ms = dec["ms"]
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens_all = dec["tokens"] * world
-    value = tokens_all / (ms / 1000.0)
+    value, ms = job_rate(dec["ms"], dec["tokens"], dist, "cuda")
     hbm_peak, _, peak_kind = measured_peaks()
     achieved = dec["bytes_per_launch"] / (dec["launch_ms"] / 1000.0) / 1e9
     traffic = profiled_traffic("decode_kernel_nemotron_b256.md", "hybrid_serving_mamba_gb300/csrc/step_kernels.cu",
