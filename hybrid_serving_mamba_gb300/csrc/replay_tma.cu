@@ -503,41 +503,56 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // the cut of lo leave about 2^-20 of each product, below the fp32 rounding of
 // the sum.
 //
-// Data flow per item: the producer streams the checkpoint in 32-column blocks
-// (16 KiB: 128 rows x 128 bytes, 128-byte swizzle) into a ring of slots, and C
-// (fp32, K-major swizzled), the x rows, W and decay_j of the two heads into a
-// small per-item ring.  Each split warp reads its 32 rows of a block (thread =
+// Data flow per item: one producer streams the checkpoint in 32-column blocks
+// (16 KiB: 128 rows x 128 bytes, 128-byte swizzle) into a ring of slots, as far
+// ahead as the ring allows; another loads C (fp32, K-major swizzled), the x
+// rows, W and decay_j of the two heads into a small per-item ring.  Only those
+// two rings pace the loads: the checkpoint of an item is in flight while earlier
+// items are still in the MMA and the epilogue.  Each split warp reads its 32 rows of a block (thread =
 // row, so the swizzle spreads the eight rows of a bank group), writes hi and
 // lo into a 64-column TMEM operand slot and frees the ring slot at once; the
 // warps work independently (no barrier between them per block).  The MMA
 // issuer takes A (hi, then lo) from TMEM and B (C) from shared memory, one
 // accumulator per item, and commits once per item (a commit costs about as
 // much as four MMAs) to that item's `done` barrier, which frees its operand
-// slots and stage and hands D to the epilogue.
+// slots and stage and hands D to the epilogue.  Split and MMA treat every item
+// alike; an item whose request is gated (poisoned slot, bad accept count) gets
+// no per-item loads and the epilogue drops its D.
 //
-// Warps:  0-3 epilogue (TMEM lane quarters 0-3: row = 32 w + lane), the log
-//         term from the staged x and W rows, y = decay_j D[row][j] + log term;
+// Warps:  0-3 epilogue (TMEM lane quarters 0-3: row = 32 q + lane, q = w % 4),
+//         the log term from the staged x and W rows, y = decay_j D[row][j] +
+//         log term; with 16 step columns a second epilogue group (warps 15-18)
+//         takes the odd items, since one group's time per item (log term,
+//         D read, stores) is longer than the checkpoint stream's;
 //         4-7 and 8-11 split, two groups (each over the four lane quarters)
 //           taking even and odd blocks: a block takes a group about half a
 //           microsecond end to end, so one group alone could not keep up with
 //           the stream; group 0 also makes C_lo for fp32 inputs;
-//         12 producer (per-item data and the checkpoint blocks; gate inputs
-//           prefetched a warp at a time);
-//         13 MMA issuer (lane 0) and TMEM owner.
-// TMEM: D buffer b (two) at columns NM b; operand slots of 64 columns (hi at
-// +0, lo at +32) from column 2 NM.
+//         12 per-item producer (gate inputs prefetched a warp at a time);
+//         13 checkpoint producer;
+//         14 MMA issuer (lane 0) and TMEM owner.
+// TMEM: D buffer b (four) at columns NM b; operand slots of 64 columns (hi at
+// +0, lo at +32) from column 4 NM.
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcSplitGroups = 2;  // split groups take alternate checkpoint blocks
 constexpr int kTcProd = 4 + 4 * kTcSplitGroups;
-constexpr int kTcMma = kTcProd + 1;
-constexpr int kTcThreads = (kTcMma + 1) * 32;
+constexpr int kTcRing = kTcProd + 1;
+constexpr int kTcMma = kTcRing + 1;
 constexpr int kTcMaxRing = 12;  // checkpoint blocks in flight
 constexpr int kTcMaxAux = 3;    // per-item stages
 constexpr int kTcASlots = 6;    // TMEM operand slots (hi + lo of one 32-column block each)
 constexpr int kTcDone = 4;      // per-item MMA completion barriers (waiters lag by < 4 items)
+constexpr int kTcDbuf = 4;      // TMEM accumulators: the MMA runs at most 4 items ahead of the epilogue
 constexpr uint32_t kTcCols = 512;
 constexpr uint32_t kTf32Keep = 0xFFFFE000u;  // sign, exponent and the 10 tf32 mantissa bits
-constexpr int kTcBarEpi = 0, kTcBarSplit = 1;  // group_or groups: named barriers 1 and 2
+static_assert(kTcDbuf <= kTcDone, "a done barrier must not complete twice ahead of its waiter");
+
+// One epilogue group per item, alternating when there are two (group_or groups 0 and 1).
+template <int NM>
+struct TcShape {
+    static constexpr int kEpiGroups = NM == 16 ? 2 : 1;
+    static constexpr int kThreads = (kTcMma + 1 + 4 * (kEpiGroups - 1)) * 32;
+};
 
 struct TcLayout {
     uint32_t Bt, Blo, xs, w, dec, hdr, aux;  // inside one per-item stage
@@ -563,11 +578,11 @@ __host__ __device__ inline TcLayout tc_layout(int N, int NM, int P, int in_b, in
 }
 
 __host__ __device__ inline size_t tc_smem_bytes(const TcLayout &L) {
-    return (size_t)L.bars + (2 * kTcMaxRing + 2 * kTcMaxAux + kTcASlots + kTcDone + 2) * 8 + 1024;
+    return (size_t)L.bars + (2 * kTcMaxRing + 2 * kTcMaxAux + kTcASlots + kTcDone + kTcDbuf) * 8 + 1024;
 }
 
 template <typename TI, int NM>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
     verify_replay_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap tm_state2,
                             const __grid_constant__ CUtensorMap tm_x2, int nring, int naux) {
     constexpr bool kSplitC = sizeof(TI) == 4;
@@ -598,7 +613,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int s = 0; s < kTcASlots; ++s) mbar_init(&afull[s], 4);
         for (int s = 0; s < kTcDone; ++s) mbar_init(&done[s], 1);
-        for (int s = 0; s < 2; ++s) mbar_init(&dempty[s], kTcEpiWarps);
+        for (int s = 0; s < kTcDbuf; ++s) mbar_init(&dempty[s], kTcEpiWarps);
         mbar_fence_init();
         s_abort = 0u;
     }
@@ -612,10 +627,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ producer
         const uint32_t cbytes = (uint32_t)nkb * NM * 128u;  // C, already in the operand layout
         const uint32_t xbytes = cbytes + 2u * a.wcap * P * sizeof(TI) + 2u * a.t1max * a.cb_w * 4u + 2u * a.t1pad * 4u;
-        int xlast[kTcMaxAux], rlast[kTcMaxRing];
+        int xlast[kTcMaxAux];
         for (int s = 0; s < kTcMaxAux; ++s) xlast[s] = -1;
-        for (int s = 0; s < kTcMaxRing; ++s) rlast[s] = -1;
-        int my_k = 0, nblk = 0;
+        int my_k = 0;
         uint32_t my_gate = 0;
         bool alive = true;
         for (int u = 0; alive; ++u) {
@@ -656,18 +670,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                  2u * a.t1max * a.cb_w * 4u, &xfull[xs_]);
                         bulk_g2s(X + L.dec, a.dec + ((size_t)i * H + h0) * a.t1pad, 2u * a.t1pad * 4u, &xfull[xs_]);
                         xlast[xs_] = u;
-                        const int row0 = (slot * H + h0) * P;
-                        for (int kb = 0; kb < nkb; ++kb, ++nblk) {
-                            const int rs = nblk % nring;
-                            if (nblk >= nring &&
-                                !wait_or_abort(&rempty[rs], (uint32_t)((nblk / nring) - 1) & 1u, &s_abort, a.flags)) {
-                                alive = false;
-                                break;
-                            }
-                            mbar_arrive_expect_tx(&rfull[rs], 16384u);
-                            tma_load_2d(smem + (size_t)rs * 16384, &tm_state2, kb * 32, row0, &rfull[rs]);
-                            rlast[rs] = nblk;
-                        }
                     }
                 }
             }
@@ -677,6 +679,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int s = 0; s < naux; ++s)
                 if (xlast[s] >= 0 && !mbar_wait(&xfull[s], (uint32_t)(xlast[s] / naux) & 1u))
                     atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else if (warp == kTcRing) {
+        // ------------------------------------------------------------ checkpoint producer
+        if (lane == 0) {
+            int rlast[kTcMaxRing];
+            for (int s = 0; s < kTcMaxRing; ++s) rlast[s] = -1;
+            int nblk = 0;
+            bool alive = true;
+            for (int u = 0; alive; ++u) {
+                const int item = blockIdx.x + u * gridDim.x;
+                if (item >= n_items) break;
+                const int i = item / hp, h0 = 2 * (item - i * hp);
+                const int row0 = (a.slots[i] * H + h0) * P;
+                for (int kb = 0; kb < nkb; ++kb, ++nblk) {
+                    const int rs = nblk % nring;
+                    if (nblk >= nring &&
+                        !wait_or_abort(&rempty[rs], (uint32_t)((nblk / nring) - 1) & 1u, &s_abort, a.flags)) {
+                        alive = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&rfull[rs], 16384u);
+                    tma_load_2d(smem + (size_t)rs * 16384, &tm_state2, kb * 32, row0, &rfull[rs]);
+                    rlast[rs] = nblk;
+                }
+            }
+            // no copy may still be landing when the CTA exits
             for (int s = 0; s < nring; ++s)
                 if (rlast[s] >= 0 && !mbar_wait(&rfull[s], (uint32_t)(rlast[s] / nring) & 1u))
                     atomicOr(a.flags, SSM_FLAG_TIMEOUT);
@@ -693,9 +721,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int xs_ = u % naux;
                 if (!wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags)) break;
                 const unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
-                if (reinterpret_cast<const int *>(X + L.hdr)[0]) continue;
-                const int db = nproc & 1;
-                if (nproc >= 2 && !wait_or_abort(&dempty[db], (uint32_t)((nproc >> 1) - 1) & 1u, &s_abort, a.flags))
+                const int db = nproc % kTcDbuf;
+                if (nproc >= kTcDbuf &&
+                    !wait_or_abort(&dempty[db], (uint32_t)((nproc / kTcDbuf) - 1) & 1u, &s_abort, a.flags))
                     break;
                 tc::fence_after_sync();
                 const uint32_t d_tm = tmem + (uint32_t)db * NM;
@@ -711,7 +739,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t a_hi = tmem + 2u * NM + (uint32_t)as * 64u, a_lo = a_hi + 32u;
+                    const uint32_t a_hi = tmem + (uint32_t)kTcDbuf * NM + (uint32_t)as * 64u, a_lo = a_hi + 32u;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {  // K = 8 tf32 per MMA
                         const uint32_t boff = (uint32_t)kb * NM * 128 + 32 * kk;
@@ -740,11 +768,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int u = 0; alive; ++u) {
             const int item = blockIdx.x + u * gridDim.x;
             if (item >= n_items) break;
-            const int xs_ = u % naux;
-            if (!wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags)) break;
-            unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
-            if (reinterpret_cast<const int *>(X + L.hdr)[0]) continue;
             if (kSplitC && sg == 0) {  // C_lo = C - C_hi beside C (this warp's share), before block 0 is signalled
+                const int xs_ = u % naux;
+                if (!wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags)) break;
+                unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
                 const uint4 *b4 = reinterpret_cast<const uint4 *>(X + L.Bt);
                 uint4 *bl4 = reinterpret_cast<uint4 *>(X + L.Blo);
                 for (int e = row; e < nkb * NM * 8; e += 128) {
@@ -784,7 +811,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&rempty[rs]);  // the rows are in registers: free the ring slot
-                const uint32_t a_hi = tmem + lane_off + 2u * NM + (uint32_t)as * 64u;
+                const uint32_t a_hi = tmem + lane_off + (uint32_t)kTcDbuf * NM + (uint32_t)as * 64u;
                 tc::tmem_st32(a_hi, hi);
                 tc::tmem_st32(a_hi + 32u, lo);
                 tc::tmem_wait_st();
@@ -795,62 +822,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ++nproc;
         }
     } else {
-        // ------------------------------------------------------------ epilogue
-        const int r = warp * 32 + lane, hd = r / 64, p = r - hd * 64;
+        // ------------------------------------------------------------ epilogue (warps 0-3, 15-18)
+        constexpr int EG = TcShape<NM>::kEpiGroups;
+        const int eg = warp < kTcEpiWarps ? 0 : 1;
+        const int q = warp & 3, r = q * 32 + lane, hd = r / 64, p = r - hd * 64;
         TI *y = reinterpret_cast<TI *>(a.y);
-        int nproc = 0;
-        for (int u = 0;; ++u) {
+        for (int u = eg;; u += EG) {  // every item goes through the MMA, so item u has D buffer u % kTcDbuf
             const int item = blockIdx.x + u * gridDim.x;
             if (item >= n_items) break;
             const int xs_ = u % naux;
             const bool ok = wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags);
-            if (group_or(kTcBarEpi, !ok)) break;
+            if (group_or(eg, !ok)) break;
             const unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
             const int gate = reinterpret_cast<const int *>(X + L.hdr)[0];
             const int k = reinterpret_cast<const int *>(X + L.hdr)[1];
             const int i = item / hp, h0 = 2 * (item - i * hp);
-            if (gate) {
-                if (r == 0) raise_flag(a.flags, a.slot_flags, a.slots[i], (uint32_t)gate);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&xempty[xs_]);
-                continue;
-            }
-            const int m = k + T1;
-            // log term: x of this row's head as pairs (zero past the sequence), W rows as float4
-            const TI *xs = reinterpret_cast<const TI *>(X + L.xs);
-            float2 xr[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const int s = 2 * q;
-                xr[q].x = s < m ? to_f(xs[((size_t)s * 2 + hd) * P + p]) : 0.f;
-                xr[q].y = s + 1 < m ? to_f(xs[((size_t)(s + 1) * 2 + hd) * P + p]) : 0.f;
-            }
+            if (gate && r == 0) raise_flag(a.flags, a.slot_flags, a.slots[i], (uint32_t)gate);
+            const int m = gate ? 0 : k + T1;
+            // log term sum_s W[j][s] x_s[p], s in quads (the W rows, zero past s = k + j, as float4),
+            // every j per quad so that the loads of a quad are independent; cut at the length m
+            const int nq = (m + 3) >> 2;
+            const TI *xrow = reinterpret_cast<const TI *>(X + L.xs) + (size_t)hd * P + p;  // x_s at s * 2P
             const float *Wh = reinterpret_cast<const float *>(X + L.w) + (size_t)hd * a.t1max * a.cb_w;
             const float *dh = reinterpret_cast<const float *>(X + L.dec) + (size_t)hd * a.t1pad;
+            float2 acc[NM];
+#pragma unroll
+            for (int j = 0; j < NM; ++j) acc[j] = make_float2(0.f, 0.f);
+#pragma unroll 1
+            for (int qq = 0; qq < nq; ++qq) {
+                const int s = 4 * qq;
+                const float2 x01 = make_float2(s < m ? to_f(xrow[(size_t)s * 2 * P]) : 0.f,
+                                               s + 1 < m ? to_f(xrow[(size_t)(s + 1) * 2 * P]) : 0.f);
+                const float2 x23 = make_float2(s + 2 < m ? to_f(xrow[(size_t)(s + 2) * 2 * P]) : 0.f,
+                                               s + 3 < m ? to_f(xrow[(size_t)(s + 3) * 2 * P]) : 0.f);
+                const float4 *w4 = reinterpret_cast<const float4 *>(Wh) + qq;
+#pragma unroll
+                for (int j = 0; j < NM; ++j) {
+                    if (j < T1) {
+                        const float4 wv = w4[(size_t)j * (a.cb_w / 4)];
+                        acc[j] = ffma2(make_float2(wv.x, wv.y), x01, acc[j]);
+                        acc[j] = ffma2(make_float2(wv.z, wv.w), x23, acc[j]);
+                    }
+                }
+            }
             float lt[NM], dj[NM];
 #pragma unroll
             for (int j = 0; j < NM; ++j) {
-                lt[j] = 0.f;
-                dj[j] = 0.f;
-                if (j < T1) {
-                    const float4 *w4 = reinterpret_cast<const float4 *>(Wh + (size_t)j * a.cb_w);
-                    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 wv = w4[q];
-                        acc = ffma2(make_float2(wv.x, wv.y), xr[2 * q], acc);
-                        acc = ffma2(make_float2(wv.z, wv.w), xr[2 * q + 1], acc);
-                    }
-                    lt[j] = acc.x + acc.y;
-                    dj[j] = dh[j];
-                }
+                lt[j] = acc[j].x + acc[j].y;
+                dj[j] = (j < T1 && !gate) ? dh[j] : 0.f;
             }
-            const int db = nproc & 1;
-            const bool okd = wait_or_abort(&done[nproc % kTcDone], (uint32_t)(nproc / kTcDone) & 1u, &s_abort, a.flags);
-            if (group_or(kTcBarEpi, !okd)) break;
+            const int db = u % kTcDbuf;
+            const bool okd = wait_or_abort(&done[u % kTcDone], (uint32_t)(u / kTcDone) & 1u, &s_abort, a.flags);
+            if (group_or(eg, !okd)) break;
+            __syncwarp();  // the item's MMAs are done with C and the stage is read: hand it back
+            if (lane == 0) mbar_arrive(&xempty[xs_]);
             tc::fence_after_sync();
             float d[NM];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)db * NM;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)db * NM;
 #pragma unroll
             for (int c = 0; c < NM; c += 16) {
                 float part[16];
@@ -862,12 +890,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&dempty[db]);
             TI *yrow = y + ((size_t)i * T1 * H + h0 + hd) * P + p;
+            if (!gate) {
 #pragma unroll
-            for (int j = 0; j < NM; ++j)
-                if (j < T1) yrow[(size_t)j * H * P] = from_f<TI>(fmaf(dj[j], d[j], lt[j]));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xempty[xs_]);
-            ++nproc;
+                for (int j = 0; j < NM; ++j)
+                    if (j < T1) yrow[(size_t)j * H * P] = from_f<TI>(fmaf(dj[j], d[j], lt[j]));
+            }
         }
     }
     tc::fence_before_sync();
@@ -1004,7 +1031,7 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         auto k = verify_replay_tc_kernel<TI, NMV>;                                                     \
         e = set_smem(k, tsmem);                                                                        \
         if (e != cudaSuccess) return e;                                                                \
-        k<<<tgrid, kTcThreads, tsmem, s>>>(ac, pool.tm_state2, pool.tm_logx2, nring, naux);           \
+        k<<<tgrid, TcShape<NMV>::kThreads, tsmem, s>>>(ac, pool.tm_state2, pool.tm_logx2, nring, naux); \
     } while (0)
         if (bf) {
             if (NM == 16) SSM_TC(__nv_bfloat16, 16);
