@@ -124,6 +124,13 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
     bool bad = false;
     float *cf = a.cf + ((size_t)i * a.G + g) * a.cf_rows * N;
     const int nm = a.cf_nm;
+    // bf16 inputs and the tensor-core kernel: C stays bf16, 64 columns per 128-byte row
+    const bool bf_op = sizeof(TI) == 2 && nm != 0;
+    TI *cfb = reinterpret_cast<TI *>(cf);
+    auto cfb_chunk = [&](int j, int n) -> TI * {  // 8 values (a 16-byte chunk) of row j, columns n .. n + 7
+        const int kb = n >> 6, c = (n & 63) >> 3;
+        return cfb + ((size_t)kb * nm + j) * 64 + ((c ^ (j & 7)) << 3);
+    };
     // fp32 C for the streaming kernels: 4 values (a 16-byte chunk) of row j, columns n .. n + 3
     auto cf_chunk = [&](int j, int n) -> float * {
         if (!nm) return cf + (size_t)j * N + n;
@@ -136,13 +143,24 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
         bad |= V::nonfinite(v);
         float *o = sC + (size_t)j * N + q * EV;
         V::widen(v, o);
+        if (bf_op) {
+            *reinterpret_cast<uint4 *>(cfb_chunk(j, q * EV)) = v;
+        } else {
 #pragma unroll
-        for (int u = 0; u < EV; u += 4)
-            *reinterpret_cast<float4 *>(cf_chunk(j, q * EV + u)) = *reinterpret_cast<const float4 *>(o + u);
+            for (int u = 0; u < EV; u += 4)
+                *reinterpret_cast<float4 *>(cf_chunk(j, q * EV + u)) = *reinterpret_cast<const float4 *>(o + u);
+        }
     }
-    for (int e = threadIdx.x; e < (nm - T1) * (N / 4); e += blockDim.x) {  // padding rows of the MMA operand
-        const int j = T1 + e / (N / 4), n = (e % (N / 4)) * 4;
-        *reinterpret_cast<float4 *>(cf_chunk(j, n)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bf_op) {
+        for (int e = threadIdx.x; e < (nm - T1) * (N / 8); e += blockDim.x) {  // padding rows of the MMA operand
+            const int j = T1 + e / (N / 8), n = (e % (N / 8)) * 8;
+            *reinterpret_cast<uint4 *>(cfb_chunk(j, n)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    } else {
+        for (int e = threadIdx.x; e < (nm - T1) * (N / 4); e += blockDim.x) {
+            const int j = T1 + e / (N / 4), n = (e % (N / 4)) * 4;
+            *reinterpret_cast<float4 *>(cf_chunk(j, n)) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     for (int e = threadIdx.x; e < m * NV; e += blockDim.x) {  // B rows: the log, then the step
         const int s = e / NV, q = e - s * NV;
@@ -540,12 +558,30 @@ constexpr int kTcRing = kTcProd + 1;
 constexpr int kTcMma = kTcRing + 1;
 constexpr int kTcMaxRing = 12;  // checkpoint blocks in flight
 constexpr int kTcMaxAux = 3;    // per-item stages
-constexpr int kTcASlots = 6;    // TMEM operand slots (hi + lo of one 32-column block each)
+constexpr int kTcMaxASlots = 12;  // TMEM operand slots, hi + lo of one 32-column block each (see TcOperand)
 constexpr int kTcDone = 4;      // per-item MMA completion barriers (waiters lag by < 4 items)
 constexpr int kTcDbuf = 4;      // TMEM accumulators: the MMA runs at most 4 items ahead of the epilogue
 constexpr uint32_t kTcCols = 512;
 constexpr uint32_t kTf32Keep = 0xFFFFE000u;  // sign, exponent and the 10 tf32 mantissa bits
+
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) { return *reinterpret_cast<const uint32_t *>(&v); }
 static_assert(kTcDbuf <= kTcDone, "a done barrier must not complete twice ahead of its waiter");
+
+// The product C . h_c per input type.  fp32 inputs: kind::tf32, h_c as tf32 hi
+// + lo in 64 TMEM columns per block (32-bit elements), C fp32 (32 per 128-byte
+// row) and its remainder C_lo.  bf16 inputs: kind::f16 (K = 16 per MMA, half
+// the MMAs), h_c as bf16 hi = rn(v) and lo = rn(v - hi), which carry 16
+// significant bits (|v - hi - lo| <= 2^-17 |v|, far below the bf16 rounding of
+// y), packed two per column in 32 TMEM columns per block; C bf16 as given (64
+// per 128-byte row).
+template <typename TI>
+struct TcOperand {
+    static constexpr bool kF16 = sizeof(TI) == 2;
+    static constexpr int kSlotCols = kF16 ? 32 : 64;
+    static constexpr int kSlots = 384 / kSlotCols;
+    static constexpr int kRowElems = kF16 ? 64 : 32;  // C elements per 128-byte operand row
+};
+static_assert(TcOperand<float>::kSlots <= kTcMaxASlots && TcOperand<__nv_bfloat16>::kSlots <= kTcMaxASlots, "");
 
 // One epilogue group per item, alternating when there are two (group_or groups 0 and 1).
 template <int NM>
@@ -562,7 +598,7 @@ struct TcLayout {
 __host__ __device__ inline TcLayout tc_layout(int N, int NM, int P, int in_b, int wcap, int t1max, int cb_w,
                                              int t1pad, bool split_c, int nring, int naux) {
     TcLayout L;
-    const uint32_t nkb = (uint32_t)N / 32;
+    const uint32_t nkb = (uint32_t)(N * in_b) / 128u;      // 128-byte column blocks of C
     uint32_t o = 0;
     L.Bt = 0;   o = nkb * (uint32_t)NM * 128u;            // NM rows x 128 bytes per column block
     L.Blo = o;  if (split_c) o += nkb * (uint32_t)NM * 128u;
@@ -578,7 +614,7 @@ __host__ __device__ inline TcLayout tc_layout(int N, int NM, int P, int in_b, in
 }
 
 __host__ __device__ inline size_t tc_smem_bytes(const TcLayout &L) {
-    return (size_t)L.bars + (2 * kTcMaxRing + 2 * kTcMaxAux + kTcASlots + kTcDone + kTcDbuf) * 8 + 1024;
+    return (size_t)L.bars + (2 * kTcMaxRing + 2 * kTcMaxAux + kTcMaxASlots + kTcDone + kTcDbuf) * 8 + 1024;
 }
 
 template <typename TI, int NM>
@@ -586,6 +622,8 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
     verify_replay_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap tm_state2,
                             const __grid_constant__ CUtensorMap tm_x2, int nring, int naux) {
     constexpr bool kSplitC = sizeof(TI) == 4;
+    using Op = TcOperand<TI>;
+    constexpr int AS = Op::kSlots, SWC = Op::kSlotCols;
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint32_t s_abort, s_tmem;
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -598,7 +636,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
     uint64_t *rfull = bars, *rempty = rfull + kTcMaxRing;                // checkpoint ring
     uint64_t *xfull = rempty + kTcMaxRing, *xempty = xfull + kTcMaxAux;  // per-item ring
     uint64_t *afull = xempty + kTcMaxAux;                                // TMEM operand slots
-    uint64_t *done = afull + kTcASlots;                                  // MMAs of an item finished
+    uint64_t *done = afull + kTcMaxASlots;                               // MMAs of an item finished
     uint64_t *dempty = done + kTcDone;                                   // TMEM D buffers
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -611,7 +649,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
             mbar_init(&xfull[s], 1);
             mbar_init(&xempty[s], kTcEpiWarps);
         }
-        for (int s = 0; s < kTcASlots; ++s) mbar_init(&afull[s], 4);
+        for (int s = 0; s < AS; ++s) mbar_init(&afull[s], 4);
         for (int s = 0; s < kTcDone; ++s) mbar_init(&done[s], 1);
         for (int s = 0; s < kTcDbuf; ++s) mbar_init(&dempty[s], kTcEpiWarps);
         mbar_fence_init();
@@ -625,7 +663,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
 
     if (warp == kTcProd) {
         // ------------------------------------------------------------ producer
-        const uint32_t cbytes = (uint32_t)nkb * NM * 128u;  // C, already in the operand layout
+        const uint32_t cbytes = (uint32_t)(N / Op::kRowElems) * NM * 128u;  // C, already in the operand layout
         const uint32_t xbytes = cbytes + 2u * a.wcap * P * sizeof(TI) + 2u * a.t1max * a.cb_w * 4u + 2u * a.t1pad * 4u;
         int xlast[kTcMaxAux];
         for (int s = 0; s < kTcMaxAux; ++s) xlast[s] = -1;
@@ -712,7 +750,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
     } else if (warp == kTcMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_tf32_f32(128, NM);
+            constexpr uint32_t idesc = Op::kF16 ? tc::idesc_bf16_f32(128, NM) : tc::idesc_tf32_f32(128, NM);
             int nproc = 0;
             bool alive = true;
             for (int u = 0; alive; ++u) {
@@ -729,8 +767,8 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                 const uint32_t d_tm = tmem + (uint32_t)db * NM;
                 const uint32_t b_hi = smem_addr(X + L.Bt), b_lo = smem_addr(X + L.Blo);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    const int c = nproc * nkb + kb, as = c % kTcASlots;
-                    if (!wait_or_abort(&afull[as], (uint32_t)(c / kTcASlots) & 1u, &s_abort, a.flags)) {
+                    const int c = nproc * nkb + kb, as = c % AS;
+                    if (!wait_or_abort(&afull[as], (uint32_t)(c / AS) & 1u, &s_abort, a.flags)) {
                         if (kb > 0) {  // MMAs of this item are in flight: let them finish first
                             tc::mma_commit(&done[nproc % kTcDone]);
                             mbar_wait(&done[nproc % kTcDone], (uint32_t)(nproc / kTcDone) & 1u);
@@ -739,14 +777,25 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t a_hi = tmem + (uint32_t)kTcDbuf * NM + (uint32_t)as * 64u, a_lo = a_hi + 32u;
+                    const uint32_t a_hi = tmem + (uint32_t)kTcDbuf * NM + (uint32_t)as * SWC;
+                    if constexpr (Op::kF16) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {  // K = 8 tf32 per MMA
-                        const uint32_t boff = (uint32_t)kb * NM * 128 + 32 * kk;
-                        const uint64_t dbh = tc::smem_desc_sw128(b_hi + boff, 1024);
-                        tc::mma_tf32_ta(d_tm, a_hi + 8 * kk, dbh, idesc, (kb | kk) != 0);
-                        tc::mma_tf32_ta(d_tm, a_lo + 8 * kk, dbh, idesc, true);
-                        if (kSplitC) tc::mma_tf32_ta(d_tm, a_hi + 8 * kk, tc::smem_desc_sw128(b_lo + boff, 1024), idesc, true);
+                        for (int kk = 0; kk < 2; ++kk) {  // K = 16 bf16 per MMA: 8 columns of hi (+0) and lo (+16)
+                            const uint32_t boff = (uint32_t)(kb >> 1) * NM * 128 + (kb & 1) * 64 + 32 * kk;
+                            const uint64_t dbh = tc::smem_desc_sw128(b_hi + boff, 1024);
+                            tc::mma_bf16_ta(d_tm, a_hi + 8 * kk, dbh, idesc, (kb | kk) != 0);
+                            tc::mma_bf16_ta(d_tm, a_hi + 16 + 8 * kk, dbh, idesc, true);
+                        }
+                    } else {
+                        const uint32_t a_lo = a_hi + 32u;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {  // K = 8 tf32 per MMA
+                            const uint32_t boff = (uint32_t)kb * NM * 128 + 32 * kk;
+                            const uint64_t dbh = tc::smem_desc_sw128(b_hi + boff, 1024);
+                            tc::mma_tf32_ta(d_tm, a_hi + 8 * kk, dbh, idesc, (kb | kk) != 0);
+                            tc::mma_tf32_ta(d_tm, a_lo + 8 * kk, dbh, idesc, true);
+                            if (kSplitC) tc::mma_tf32_ta(d_tm, a_hi + 8 * kk, tc::smem_desc_sw128(b_lo + boff, 1024), idesc, true);
+                        }
                     }
                 }
                 if (!alive) break;
@@ -784,11 +833,11 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                 tc::fence_proxy_async_smem();
             }
             for (int kb = 0; kb < nkb; ++kb) {
-                const int c = nproc * nkb + kb, rs = c % nring, as = c % kTcASlots;
+                const int c = nproc * nkb + kb, rs = c % nring, as = c % AS;
                 if ((c & 1) != sg) continue;
                 bool ok = wait_or_abort(&rfull[rs], (uint32_t)(c / nring) & 1u, &s_abort, a.flags);
-                if (ok && c >= kTcASlots) {  // the slot's previous block belongs to item (c - slots) / nkb
-                    const int pj = (c - kTcASlots) / nkb;
+                if (ok && c >= AS) {  // the slot's previous block belongs to item (c - slots) / nkb
+                    const int pj = (c - AS) / nkb;
                     ok = wait_or_abort(&done[pj % kTcDone], (uint32_t)(pj / kTcDone) & 1u, &s_abort, a.flags);
                 }
                 if (!ok) {
@@ -798,22 +847,40 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                 tc::fence_after_sync();
                 // this thread's row of the block: 8 chunks of 16 bytes, chunk c at c ^ (row % 8)
                 const unsigned char *blk = smem + (size_t)rs * 16384 + (size_t)row * 128;
-                uint32_t hi[32], lo[32];
+                const uint32_t a_hi = tmem + lane_off + (uint32_t)kTcDbuf * NM + (uint32_t)as * SWC;
+                if constexpr (Op::kF16) {
+                    uint32_t hl[32];  // columns 0-15: hi of elements (2c, 2c + 1); 16-31: lo of the same
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(blk + ((ch ^ (row & 7)) << 4));
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        hi[4 * ch + e] = w[e] & kTf32Keep;
-                        lo[4 * ch + e] = __float_as_uint(__uint_as_float(w[e]) - __uint_as_float(hi[4 * ch + e]));
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const float4 v = *reinterpret_cast<const float4 *>(blk + ((ch ^ (row & 7)) << 4));
+                        const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+                        const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - __low2float(h0), v.y - __high2float(h0));
+                        const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - __low2float(h1), v.w - __high2float(h1));
+                        hl[2 * ch] = bf2_bits(h0);
+                        hl[2 * ch + 1] = bf2_bits(h1);
+                        hl[16 + 2 * ch] = bf2_bits(l0);
+                        hl[16 + 2 * ch + 1] = bf2_bits(l1);
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&rempty[rs]);  // the rows are in registers: free the ring slot
+                    tc::tmem_st32(a_hi, hl);
+                } else {
+                    uint32_t hi[32], lo[32];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(blk + ((ch ^ (row & 7)) << 4));
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            hi[4 * ch + e] = w[e] & kTf32Keep;
+                            lo[4 * ch + e] = __float_as_uint(__uint_as_float(w[e]) - __uint_as_float(hi[4 * ch + e]));
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&rempty[rs]);
+                    tc::tmem_st32(a_hi, hi);
+                    tc::tmem_st32(a_hi + 32u, lo);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&rempty[rs]);  // the rows are in registers: free the ring slot
-                const uint32_t a_hi = tmem + lane_off + (uint32_t)kTcDbuf * NM + (uint32_t)as * 64u;
-                tc::tmem_st32(a_hi, hi);
-                tc::tmem_st32(a_hi + 32u, lo);
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
@@ -985,7 +1052,8 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
     // tensor cores take pairs of heads, at most 32 step tokens, whole W rows of 32
     int NM = 0, nring = 0, naux = 0;
     size_t tsmem = 0;
-    if (pool.tm_tc_ok && T1 <= 32 && T1 <= pool.cf_rows && a.P == 64 && a.cb_w == 32 && a.N <= 128) {
+    if (pool.tm_tc_ok && T1 <= 32 && T1 <= pool.cf_rows && a.P == 64 && a.cb_w == 32 && a.N <= 128 &&
+        (a.N * in_b) % 128 == 0) {
         NM = T1 <= 16 ? 16 : 32;
         if (NM > pool.cf_rows) NM = 0;
         for (int na = kTcMaxAux; NM && na >= 2 && !nring; --na)
