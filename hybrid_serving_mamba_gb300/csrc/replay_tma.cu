@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 //
 // Warps:  0-3 epilogue (TMEM lane quarters 0-3: row = 32 q + lane, q = w % 4),
 //         the log term from the staged x and W rows, y = decay_j D[row][j] +
-//         log term; with 16 step columns a second epilogue group (warps 15-18)
+//         log term; with 16 step columns a second epilogue group (warps 16-19)
 //         takes the odd items, since one group's time per item (log term,
 //         D read, stores) is longer than the checkpoint stream's;
 //         4-7 and 8-11 split, two groups (each over the four lane quarters)
@@ -548,16 +548,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 //           the stream; group 0 also makes C_lo for fp32 inputs;
 //         12 per-item producer (gate inputs prefetched a warp at a time);
 //         13 checkpoint producer;
-//         14 MMA issuer (lane 0) and TMEM owner.
+//         14, 15 MMA issuers (lane 0), taking alternate items, since an issuer's
+//           waits on its barriers take about as long as its MMAs; 14 owns TMEM.
 // TMEM: D buffer b (four) at columns NM b; operand slots of 64 columns (hi at
 // +0, lo at +32) from column 4 NM.
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcSplitGroups = 2;  // split groups take alternate checkpoint blocks
 constexpr int kTcProd = 4 + 4 * kTcSplitGroups;
 constexpr int kTcRing = kTcProd + 1;
-constexpr int kTcMma = kTcRing + 1;
+constexpr int kTcMma = kTcRing + 1;  // and kTcMma + 1: two issuers taking alternate items
+constexpr int kTcMmaWarps = 2;
 constexpr int kTcMaxRing = 12;  // checkpoint blocks in flight
-constexpr int kTcMaxAux = 3;    // per-item stages
+constexpr int kTcMaxAux = 4;    // per-item stages, an even count: stage u % naux then serves items of one
+                                // parity, i.e. one MMA issuer and one epilogue group, and each of them
+                                // sees every phase of its stages' barriers in order
 constexpr int kTcMaxASlots = 12;  // TMEM operand slots, hi + lo of one 32-column block each (see TcOperand)
 constexpr int kTcDone = 4;      // per-item MMA completion barriers (waiters lag by < 4 items)
 constexpr int kTcDbuf = 4;      // TMEM accumulators: the MMA runs at most 4 items ahead of the epilogue
@@ -566,6 +570,8 @@ constexpr uint32_t kTf32Keep = 0xFFFFE000u;  // sign, exponent and the 10 tf32 m
 
 __device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) { return *reinterpret_cast<const uint32_t *>(&v); }
 static_assert(kTcDbuf <= kTcDone, "a done barrier must not complete twice ahead of its waiter");
+static_assert(kTcMaxAux % 2 == 0 && kTcDbuf % kTcMmaWarps == 0 && kTcDone % kTcMmaWarps == 0,
+              "a barrier indexed by item must serve items of one issuer");
 
 // The product C . h_c per input type.  fp32 inputs: kind::tf32, h_c as tf32 hi
 // + lo in 64 TMEM columns per block (32-bit elements), C fp32 (32 per 128-byte
@@ -587,7 +593,7 @@ static_assert(TcOperand<float>::kSlots <= kTcMaxASlots && TcOperand<__nv_bfloat1
 template <int NM>
 struct TcShape {
     static constexpr int kEpiGroups = NM == 16 ? 2 : 1;
-    static constexpr int kThreads = (kTcMma + 1 + 4 * (kEpiGroups - 1)) * 32;
+    static constexpr int kThreads = (kTcMma + kTcMmaWarps + 4 * (kEpiGroups - 1)) * 32;
 };
 
 struct TcLayout {
@@ -747,15 +753,17 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                 if (rlast[s] >= 0 && !mbar_wait(&rfull[s], (uint32_t)(rlast[s] / nring) & 1u))
                     atomicOr(a.flags, SSM_FLAG_TIMEOUT);
         }
-    } else if (warp == kTcMma) {
+    } else if (warp >= kTcMma && warp < kTcMma + kTcMmaWarps) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = Op::kF16 ? tc::idesc_bf16_f32(128, NM) : tc::idesc_tf32_f32(128, NM);
-            int nproc = 0;
+            // every item goes through the MMA, so its position u is also its count of items before it
+            int last = -1;
             bool alive = true;
-            for (int u = 0; alive; ++u) {
+            for (int u = warp - kTcMma; alive; u += kTcMmaWarps) {
                 const int item = blockIdx.x + u * gridDim.x;
                 if (item >= n_items) break;
+                const int nproc = u;
                 const int xs_ = u % naux;
                 if (!wait_or_abort(&xfull[xs_], (uint32_t)(u / naux) & 1u, &s_abort, a.flags)) break;
                 const unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
@@ -800,10 +808,11 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                 }
                 if (!alive) break;
                 tc::mma_commit(&done[nproc % kTcDone]);
-                ++nproc;
+                last = u;
             }
-            // every MMA issued has completed before TMEM is released
-            if (alive && nproc > 0 && !mbar_wait(&done[(nproc - 1) % kTcDone], (uint32_t)((nproc - 1) / kTcDone) & 1u))
+            // every MMA this thread issued has completed before TMEM is released (an item cut short
+            // above was waited for there; the items before it end with this thread's last commit)
+            if (last >= 0 && !mbar_wait(&done[last % kTcDone], (uint32_t)(last / kTcDone) & 1u))
                 atomicOr(a.flags, SSM_FLAG_TIMEOUT);
         }
     } else if (warp >= kTcEpiWarps && warp < kTcProd) {
@@ -889,7 +898,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
             ++nproc;
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 0-3, 15-18)
+        // ------------------------------------------------------------ epilogue (warps 0-3, 16-19)
         constexpr int EG = TcShape<NM>::kEpiGroups;
         const int eg = warp < kTcEpiWarps ? 0 : 1;
         const int q = warp & 3, r = q * 32 + lane, hd = r / 64, p = r - hd * 64;
@@ -1056,7 +1065,7 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         (a.N * in_b) % 128 == 0) {
         NM = T1 <= 16 ? 16 : 32;
         if (NM > pool.cf_rows) NM = 0;
-        for (int na = kTcMaxAux; NM && na >= 2 && !nring; --na)
+        for (int na = kTcMaxAux; NM && na >= 2 && !nring; na -= 2)
             for (int nr = kTcMaxRing; nr >= 4; --nr) {
                 const size_t b =
                     tc_smem_bytes(tc_layout(a.N, NM, a.P, in_b, a.wcap, a.t1max, a.cb_w, a.t1pad, !bf, nr, na));
