@@ -269,22 +269,6 @@ __host__ __device__ inline TmaLayout tma_layout(int P, int N, int in_b, int T1, 
     return L;
 }
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
-            "r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
-        : "memory");
-}
-
 // Bounded wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort,
                                               uint32_t *flags) {
@@ -988,21 +972,27 @@ cudaError_t set_smem(Kernel k, size_t bytes) {
 
 }  // namespace
 
+TensorMapEncode tensor_map_encoder() {
+    static const TensorMapEncode enc = []() -> TensorMapEncode {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<TensorMapEncode>(fn);
+    }();
+    return enc;
+}
+
 bool replay_tma_encode(Pool &p) {
     p.tm_ok = false;
     if (p.cfg.mode != SSM_MODE_REPLAY) return false;
     if (p.N % 32 != 0 || p.N > 128 || p.P % 8 != 0 || p.P > 64 || p.wcap > 8 * kLogPairs ||
         ((size_t)p.P * p.in_bytes) % 16 != 0)
         return false;
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-    using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    const Encode enc = reinterpret_cast<Encode>(fn);
+    const TensorMapEncode enc = tensor_map_encoder();
+    if (!enc) return false;
     // checkpoint: rows (slot, head, p) of N fp32 values; box 32 columns x P rows, 128-byte swizzle
     const cuuint64_t sd[2] = {(cuuint64_t)p.N, (cuuint64_t)p.n_slots * p.H * p.P};
     const cuuint64_t ss[1] = {(cuuint64_t)p.N * 4};

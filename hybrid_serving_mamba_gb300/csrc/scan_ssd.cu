@@ -19,7 +19,12 @@
 // 128-byte-swizzled shared-memory tiles and fp32 accumulators in TMEM
 // (M = 128).  Operands are stored the way their producers write them -- one
 // row per token (C, B, X, w o X) or per state column (S) -- and read K-major
-// or MN-major as each product needs, so no transposes are made.  x, B and C
+// or MN-major as each product needs, so no transposes are made.  C B^T and Z
+// go first, together: C and the state copy are then free, so M takes the
+// place of C and w o X that of the state copy, which keeps a CTA at 100 KiB
+// of shared memory, 256 TMEM columns and 128 registers a thread: two CTAs
+// (two chains) share an SM and each one's waits on the tensor core and on
+// memory overlap the other's work.  x, B and C
 // are bf16 inputs, so C B^T and X are exact; M, w o X and the state copy
 // are rounded to bf16, the state itself stays fp32.
 //
@@ -38,18 +43,18 @@ namespace {
 constexpr int Q = 128, SP = 64, SN = 128;
 constexpr int kThreads = 256;
 constexpr uint32_t kTile128 = 128 * 128;  // one 64-wide (128-byte) column block of a 128-row tile
-constexpr uint32_t OFF_C = 0;                      // C  [i][n]  two n blocks: A of C B^T and of Z (K-major)
+constexpr uint32_t OFF_C = 0;                      // C  [i][n]  two n blocks: A of C B^T and of Z (K-major);
+constexpr uint32_t OFF_M = OFF_C;                  //   then M [i][j], two j blocks: A of Y (K-major)
 constexpr uint32_t OFF_B = OFF_C + 2 * kTile128;   // B  [j][n]  B of C B^T (K-major); A of dS^T (MN-major)
-constexpr uint32_t OFF_M = OFF_B + 2 * kTile128;   // M  [i][j]  two j blocks: A of Y (K-major)
-constexpr uint32_t OFF_X = OFF_M + 2 * kTile128;   // X  [j][p]  B of Y (MN-major)
-constexpr uint32_t OFF_XW = OFF_X + kTile128;      // (w o X) [j][p]  B of dS^T (MN-major)
-constexpr uint32_t OFF_S = OFF_XW + kTile128;      // S  [n][p]  B of Z (MN-major)
+constexpr uint32_t OFF_X = OFF_B + 2 * kTile128;   // X  [j][p]  B of Y (MN-major)
+constexpr uint32_t OFF_S = OFF_X + kTile128;       // S  [n][p]  B of Z (MN-major);
+constexpr uint32_t OFF_XW = OFF_S;                 //   then (w o X) [j][p]: B of dS^T (MN-major)
 constexpr uint32_t OFF_MISC = OFF_S + kTile128;
-// misc: cum[128], dt[128], colf[4][128], wsum[4], safe[4], mbarrier, tmem base, gate
+// misc: cum[128], dt[128], colf[4][128], wsum[4], safe[4], mbarriers (MMA, loads), tmem base, gate
 constexpr uint32_t M_CUM = 0, M_DT = 512, M_COLF = 1024, M_WSUM = 3072, M_SAFE = 3088, M_BAR = 3104,
-                   M_TMEM = 3112, M_GATE = 3116;
+                   M_TMEM = 3112, M_GATE = 3116, M_LDBAR = 3120;
 constexpr uint32_t kSsdSmem = OFF_MISC + 3200 + 1024;  // + slack to align the base to 1024
-constexpr uint32_t kTmemCols = 256;  // [0,128) C B^T, then Z in [0,64) and dS^T in [64,128); Y in [128,192)
+constexpr uint32_t kTmemCols = 256;  // [0,128) C B^T, then dS^T in [64,128); Y in [128,192); Z in [192,256)
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -85,7 +90,9 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int ks) {
 }
 
 template <typename TI>
-__global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_constant__ ScanArgs a) {
+__global__ void __launch_bounds__(kThreads, 2)
+    scan_ssd_kernel(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm_x,
+                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c) {
     static_assert(sizeof(TI) == 2, "tensor-core scan takes bf16 x, B and C");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -98,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_cons
     float *s_wsum = reinterpret_cast<float *>(misc + M_WSUM);
     int *s_safe = reinterpret_cast<int *>(misc + M_SAFE);
     uint64_t *s_bar = reinterpret_cast<uint64_t *>(misc + M_BAR);
+    uint64_t *s_ldbar = reinterpret_cast<uint64_t *>(misc + M_LDBAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc + M_TMEM);
     uint32_t *s_gate = reinterpret_cast<uint32_t *>(misc + M_GATE);
 
@@ -117,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_cons
         else if (a.check_log && a.log_len[slot] != 0) gate = SSM_FLAG_LOG_NOT_EMPTY;
         *s_gate = gate;
         mbar_init(s_bar, 1);
+        mbar_init(s_ldbar, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -160,38 +169,31 @@ __global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_cons
     constexpr uint32_t kIdY = tc::idesc_bf16_f32(128, 64) | (1u << 16);      // B MN-major
     constexpr uint32_t kIdZ = tc::idesc_bf16_f32(128, 64) | (1u << 16);      // B MN-major
     constexpr uint32_t kIdDS = tc::idesc_bf16_f32(128, 64) | (1u << 15) | (1u << 16);  // both MN-major
-    uint32_t phase = 0;
+    uint32_t phase = 0, ld_phase = 0;
     bool bad = false, timeout = false;
     const int L = t1 - t0;
+    // dt of this thread's row, one chunk ahead (a strided load, kept off the chunk's critical path)
+    float dt_next = 0.f;
+    if (half == 1 && row < (L < Q ? L : Q)) dt_next = load_dt(a.dt, (size_t)(t0 + row) * H + h, a.dt_bf16);
     for (int c0 = 0; c0 < L; c0 += Q) {
         const int len = L - c0 < Q ? L - c0 : Q;
         const bool valid = row < len;
         const size_t tok = (size_t)(t0 + c0 + row);
 
-        // ---- P1: rows of C and B (half 0) or of x and dt (half 1); dt prefix sums
-        uint4 xr[8];
+        // ---- P1: the chunk's rows of C, B (two 64-column boxes each) and x by TMA into the
+        // swizzled tiles (the layout chunk_off describes); dt prefix sums meanwhile
+        if (tid == 0) {
+            const int ty = t0 + c0;
+            mbar_arrive_expect_tx(s_ldbar, 5u * kTile128);
+            tma_load_2d(smem + OFF_C, &tm_c, g * SN, ty, s_ldbar);
+            tma_load_2d(smem + OFF_C + kTile128, &tm_c, g * SN + 64, ty, s_ldbar);
+            tma_load_2d(smem + OFF_B, &tm_b, g * SN, ty, s_ldbar);
+            tma_load_2d(smem + OFF_B + kTile128, &tm_b, g * SN + 64, ty, s_ldbar);
+            tma_load_2d(smem + OFF_X, &tm_x, h * SP, ty, s_ldbar);
+        }
         float dtv = 0.f;
-        if (half == 0) {
-            const uint4 *cs = reinterpret_cast<const uint4 *>(Cg + (tok * G + g) * SN);
-            const uint4 *bs = reinterpret_cast<const uint4 *>(Bg + (tok * G + g) * SN);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 cv = valid ? cs[c] : make_uint4(0, 0, 0, 0);
-                const uint4 bv = valid ? bs[c] : make_uint4(0, 0, 0, 0);
-                bad |= nonfinite_bf16x8(cv) | nonfinite_bf16x8(bv);
-                const uint32_t off = (uint32_t)(c >> 3) * kTile128 + chunk_off((uint32_t)row, (uint32_t)c);
-                *reinterpret_cast<uint4 *>(smem + OFF_C + off) = cv;
-                *reinterpret_cast<uint4 *>(smem + OFF_B + off) = bv;
-            }
-        } else {
-            const uint4 *xs = reinterpret_cast<const uint4 *>(xg + (tok * H + h) * SP);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                xr[c] = valid ? xs[c] : make_uint4(0, 0, 0, 0);
-                bad |= nonfinite_bf16x8(xr[c]);
-                *reinterpret_cast<uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c)) = xr[c];
-            }
-            dtv = valid ? load_dt(a.dt, tok * H + h, a.dt_bf16) : 0.f;
+        if (half == 1) {
+            dtv = dt_next;
             bad |= !isfinite(dtv);
             // inclusive prefix sum over the 128 rows (warps 4..7)
             float v = dtv;
@@ -206,6 +208,39 @@ __global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_cons
             for (int w = 0; w < rb; ++w) v += s_wsum[w];
             s_cum[row] = A * v;
         }
+        if (__syncthreads_or(!mbar_wait(s_ldbar, ld_phase & 1u))) {  // uniform across the CTA
+            timeout = true;
+            break;
+        }
+        ++ld_phase;
+        if (!valid) {  // rows past the sequence: the boxes hold the next tokens of the tensor, or zeros
+            if (half == 0) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t off = (uint32_t)(c >> 3) * kTile128 + chunk_off((uint32_t)row, (uint32_t)c);
+                    *reinterpret_cast<uint4 *>(smem + OFF_C + off) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(smem + OFF_B + off) = make_uint4(0, 0, 0, 0);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c)) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        if (valid) {  // the thread's own rows, now in shared memory
+            if (half == 0) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t off = (uint32_t)(c >> 3) * kTile128 + chunk_off((uint32_t)row, (uint32_t)c);
+                    bad |= nonfinite_bf16x8(*reinterpret_cast<const uint4 *>(smem + OFF_C + off)) |
+                           nonfinite_bf16x8(*reinterpret_cast<const uint4 *>(smem + OFF_B + off));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    bad |= nonfinite_bf16x8(*reinterpret_cast<const uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c)));
+            }
+        }
         __syncthreads();
         const float cum_last = s_cum[Q - 1];
         const float cum = s_cum[row];
@@ -218,26 +253,22 @@ __global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_cons
             s_colf[r * Q + row] = row < 32 * r + 32 ? expf(ref - cum) * s_dt[row] : 0.f;
         }
         if (tid < 4) s_safe[tid] = (s_cum[32 * tid] - s_cum[32 * tid + 31]) < 80.f;
-        if (half == 1) {  // w o X, row j = row: weight of token j in the state update
-            const float wt = expf(cum_last - cum) * dtv;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float2 f0 = unpack_bf16(xr[c].x), f1 = unpack_bf16(xr[c].y);
-                const float2 f2 = unpack_bf16(xr[c].z), f3 = unpack_bf16(xr[c].w);
-                *reinterpret_cast<uint4 *>(smem + OFF_XW + chunk_off((uint32_t)row, (uint32_t)c)) =
-                    make_uint4(pack_bf16(f0.x * wt, f0.y * wt), pack_bf16(f1.x * wt, f1.y * wt),
-                               pack_bf16(f2.x * wt, f2.y * wt), pack_bf16(f3.x * wt, f3.y * wt));
-            }
-        }
         tc::fence_proxy_async_smem();
         __syncthreads();
 
-        // ---- P2: C B^T
+        if (half == 1) {  // dt of the next chunk, while this one is on the tensor cores
+            const int c1 = c0 + Q, len1 = L - c1 < Q ? L - c1 : Q;
+            dt_next = row < len1 ? load_dt(a.dt, (size_t)(t0 + c1 + row) * H + h, a.dt_bf16) : 0.f;
+        }
+
+        // ---- P2: C B^T and Z = C S^T (S before the chunk); after them C and S are free
         if (tid == 0) {
             tc::fence_after_sync();
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
+            for (int ks = 0; ks < 8; ++ks) {
                 tc::mma_bf16(tmem, kmajor_desc(sbase + OFF_C, ks), kmajor_desc(sbase + OFF_B, ks), kIdCB, ks > 0);
+                tc::mma_bf16(tmem + 192, kmajor_desc(sbase + OFF_C, ks), mnmajor_desc(sbase + OFF_S, ks), kIdZ, ks > 0);
+            }
             tc::mma_commit(s_bar);
         }
         if (__syncthreads_or(!mbar_wait(s_bar, phase & 1u))) {  // uniform across the CTA
@@ -279,18 +310,28 @@ __global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_cons
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
+            // w o X, row j = row, this half's 4 chunks: weight of token j in the state update
+            const float wt = expf(cum_last - cum) * s_dt[row];
+#pragma unroll
+            for (int c = 4 * half; c < 4 * half + 4; ++c) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c));
+                const float2 f0 = unpack_bf16(xv.x), f1 = unpack_bf16(xv.y);
+                const float2 f2 = unpack_bf16(xv.z), f3 = unpack_bf16(xv.w);
+                *reinterpret_cast<uint4 *>(smem + OFF_XW + chunk_off((uint32_t)row, (uint32_t)c)) =
+                    make_uint4(pack_bf16(f0.x * wt, f0.y * wt), pack_bf16(f1.x * wt, f1.y * wt),
+                               pack_bf16(f2.x * wt, f2.y * wt), pack_bf16(f3.x * wt, f3.y * wt));
+            }
         }
         tc::fence_before_sync();
         tc::fence_proxy_async_smem();
         __syncthreads();
 
-        // ---- P4: Y = M X, Z = C S^T, dS^T = B^T (w o X)
+        // ---- P4: Y = M X, dS^T = B^T (w o X)
         if (tid == 0) {
             tc::fence_after_sync();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 tc::mma_bf16(tmem + 128, kmajor_desc(sbase + OFF_M, ks), mnmajor_desc(sbase + OFF_X, ks), kIdY, ks > 0);
-                tc::mma_bf16(tmem + 0, kmajor_desc(sbase + OFF_C, ks), mnmajor_desc(sbase + OFF_S, ks), kIdZ, ks > 0);
                 tc::mma_bf16(tmem + 64, mnmajor_desc(sbase + OFF_B, ks), mnmajor_desc(sbase + OFF_XW, ks), kIdDS, ks > 0);
             }
             tc::mma_commit(s_bar);
@@ -302,35 +343,44 @@ __global__ void __launch_bounds__(kThreads, 1) scan_ssd_kernel(const __grid_cons
         ++phase;
         tc::fence_after_sync();
 
-        // ---- P5: outputs of row i (this half's 32 columns p), state update of column n = row
+        // ---- P5: outputs of row i (this half's 32 columns p), state update of column n = row,
+        // 16 columns at a time
         {
             const float ecum = expf(cum);
             const float dA = expf(cum_last);
-            float yv[32], zv[32], ds[32];
-            tc::tmem_ld32(tmem + lane_addr + 128u + (uint32_t)p0, yv);
-            tc::tmem_ld32(tmem + lane_addr + 0u + (uint32_t)p0, zv);
-            tc::tmem_ld32(tmem + lane_addr + 64u + (uint32_t)p0, ds);
-            uint4 outc[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint4 xc = *reinterpret_cast<const uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)(4 * half + c)));
-                const uint32_t xw4[4] = {xc.x, xc.y, xc.z, xc.w};
-                uint32_t o[4];
+            for (int hc = 0; hc < 2; ++hc) {
+                float yv[16], zv[16];
+                tc::tmem_ld16(tmem + lane_addr + 128u + (uint32_t)(p0 + 16 * hc), yv);
+                tc::tmem_ld16(tmem + lane_addr + 192u + (uint32_t)(p0 + 16 * hc), zv);
+                uint4 outc[2];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 xf = unpack_bf16(xw4[e]);
-                    const int q = 8 * c + 2 * e;
-                    o[e] = pack_bf16(fmaf(ecum, zv[q], yv[q]) + D * xf.x, fmaf(ecum, zv[q + 1], yv[q + 1]) + D * xf.y);
+                for (int c = 0; c < 2; ++c) {
+                    const uint4 xc = *reinterpret_cast<const uint4 *>(
+                        smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)(4 * half + 2 * hc + c)));
+                    const uint32_t xw4[4] = {xc.x, xc.y, xc.z, xc.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 xf = unpack_bf16(xw4[e]);
+                        const int q = 8 * c + 2 * e;
+                        o[e] = pack_bf16(fmaf(ecum, zv[q], yv[q]) + D * xf.x, fmaf(ecum, zv[q + 1], yv[q + 1]) + D * xf.y);
+                    }
+                    outc[c] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
-                outc[c] = make_uint4(o[0], o[1], o[2], o[3]);
+                if (valid) {
+                    uint4 *yo = reinterpret_cast<uint4 *>(yg + (tok * H + h) * SP + p0 + 16 * hc);
+                    yo[0] = outc[0];
+                    yo[1] = outc[1];
+                }
             }
-            if (valid) {
-                uint4 *yo = reinterpret_cast<uint4 *>(yg + (tok * H + h) * SP + p0);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) yo[c] = outc[c];
+            for (int hc = 0; hc < 2; ++hc) {
+                float ds[16];
+                tc::tmem_ld16(tmem + lane_addr + 64u + (uint32_t)(p0 + 16 * hc), ds);
+#pragma unroll
+                for (int p = 0; p < 16; ++p) S[16 * hc + p] = fmaf(dA, S[16 * hc + p], ds[p]);
             }
-#pragma unroll
-            for (int p = 0; p < 32; ++p) S[p] = fmaf(dA, S[p], ds[p]);
         }
         write_state_copy();
         tc::fence_before_sync();
@@ -360,10 +410,27 @@ bool scan_ssd_supported(const Pool &pool) {
 
 cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s) {
     (void)pool;
+    const TensorMapEncode enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    // tokens of this launch as rows: x [T][H * P], B and C [T][G * N]; 64-column x 128-row boxes,
+    // 128-byte swizzle, zeros past the last token
+    const cuuint64_t T = (cuuint64_t)a.cu[a.n_seq];
+    const cuuint32_t box[2] = {64u, (cuuint32_t)Q};
+    const cuuint32_t es[2] = {1u, 1u};
+    CUtensorMap mx, mb, mc;
+    const cuuint64_t xd[2] = {(cuuint64_t)a.H * SP, T}, xs[1] = {(cuuint64_t)a.H * SP * 2};
+    const cuuint64_t bd[2] = {(cuuint64_t)a.G * SN, T}, bs[1] = {(cuuint64_t)a.G * SN * 2};
+    const auto encode = [&](CUtensorMap *m, const void *base, const cuuint64_t *d, const cuuint64_t *st) {
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), d, st, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (!encode(&mx, a.x, xd, xs) || !encode(&mb, a.B, bd, bs) || !encode(&mc, a.C, bd, bs))
+        return cudaErrorNotSupported;
     auto k = scan_ssd_kernel<__nv_bfloat16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSsdSmem);
     if (e != cudaSuccess) return e;
-    k<<<dim3(a.H, a.n_seq), kThreads, kSsdSmem, s>>>(a);
+    k<<<dim3(a.H, a.n_seq), kThreads, kSsdSmem, s>>>(a, mx, mb, mc);
     return cudaGetLastError();
 }
 

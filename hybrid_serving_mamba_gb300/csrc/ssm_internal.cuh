@@ -158,6 +158,14 @@ struct ScanArgs {
     int32_t slots[kMaxSeqPerLaunch];
 };
 
+// cuTensorMapEncodeTiled, looked up through the runtime's driver entry point
+// once per process; nullptr where the driver does not offer it.
+using TensorMapEncode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                     CUtensorMapFloatOOBfill);
+TensorMapEncode tensor_map_encoder();
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaGetLastError() of its launch(es).
 

@@ -192,6 +192,9 @@ ssm_status ssm_state_gather(ssm_pool pool, int32_t n, const int32_t *slots, floa
  *               a smaller value is SSM_ERR_DUPLICATE, a larger one
  *               SSM_ERR_SEQUENCE (declared mismatch, nothing advances).
  * Replay pools require an empty log on each slot (device check).
+ * bf16 pools with P = 64 and N = 128 take the tensor-core kernel when x, B,
+ * C and y start on 16-byte boundaries, any other call the sequential one
+ * (the same results within the tolerance).
  */
 ssm_status ssm_scan_chunk(ssm_pool pool, int32_t n_seq, const int32_t *cu_seqlens, const int32_t *slots,
                           const int64_t *chunk_seq, const void *x, const void *dt, const void *B,
