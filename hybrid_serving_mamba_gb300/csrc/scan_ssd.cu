@@ -278,7 +278,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         ++phase;
         tc::fence_after_sync();
 
-        // ---- P3: M = C B^T o decay o dt, masked to j <= i (row i = row, columns of this half)
+        // ---- P3: M = C B^T o decay o dt, masked to j <= i (row i = row, columns of this half).
+        // A warp's rows lie in one 32-row block rb, so each 32-column block jb is, for the whole
+        // warp, either right of the diagonal (all zero), left of it (erow x colf, no mask) or the
+        // diagonal block itself (masked; exact exps where the block's range is not safe).
         {
             const int i = row;
             const float erow = expf(cum - s_cum[32 * rb]);  // <= 1
@@ -286,27 +289,45 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float *colf = s_colf + rb * Q;
 #pragma unroll 1
             for (int jb = 64 * half; jb < 64 * half + 64; jb += 32) {
+                uint4 *mrow = reinterpret_cast<uint4 *>(smem + OFF_M + (uint32_t)(jb >> 6) * kTile128);
+                const uint32_t c0q = (uint32_t)(jb & 63) >> 3;  // first 8-column chunk of the block
+                if (jb > 32 * rb) {  // right of the diagonal
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(mrow) +
+                                                   chunk_off((uint32_t)i, c0q + q8)) = make_uint4(0, 0, 0, 0);
+                    continue;
+                }
                 float cb[32];
                 tc::tmem_ld32(tmem + lane_addr + (uint32_t)jb, cb);
+                const bool plain = jb < 32 * rb || safe, diag = jb == 32 * rb;
+                const float4 *c4 = reinterpret_cast<const float4 *>(colf + jb);
 #pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
+                for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns at a time
+                    float f[8];
+                    if (plain) {
+                        const float4 ca = c4[2 * q8], cc = c4[2 * q8 + 1];
+                        f[0] = erow * ca.x; f[1] = erow * ca.y; f[2] = erow * ca.z; f[3] = erow * ca.w;
+                        f[4] = erow * cc.x; f[5] = erow * cc.y; f[6] = erow * cc.z; f[7] = erow * cc.w;
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int j = jb + 8 * q8 + u;
+                            f[u] = expf(cum - s_cum[j]) * s_dt[j];
+                        }
+                    }
+                    if (diag) {  // the diagonal block: j <= i only
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (jb + 8 * q8 + u > i) f[u] = 0.f;
+                    }
                     uint32_t pk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        float mv[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int j = jb + q8 * 8 + 2 * e + u;
-                            float f;
-                            if (j > i) f = 0.f;
-                            else if (j < 32 * rb || safe) f = erow * colf[j];
-                            else f = expf(cum - s_cum[j]) * s_dt[j];
-                            mv[u] = cb[q8 * 8 + 2 * e + u] * f;
-                        }
-                        pk[e] = pack_bf16(mv[0], mv[1]);
+                        const int u = 8 * q8 + 2 * e;
+                        pk[e] = pack_bf16(cb[u] * f[2 * e], cb[u + 1] * f[2 * e + 1]);
                     }
-                    const uint32_t j0 = (uint32_t)(jb + q8 * 8);
-                    *reinterpret_cast<uint4 *>(smem + OFF_M + (j0 >> 6) * kTile128 + chunk_off((uint32_t)i, (j0 >> 3) & 7u)) =
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(mrow) + chunk_off((uint32_t)i, c0q + q8)) =
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
