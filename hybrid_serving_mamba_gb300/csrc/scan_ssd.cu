@@ -28,6 +28,10 @@
 // are bf16 inputs, so C B^T and X are exact; M, w o X and the state copy
 // are rounded to bf16, the state itself stays fp32.
 //
+// Non-finite inputs are found where they surface, in y and in the state
+// increment (each input enters one of them through a product); dt is checked
+// as it is read.
+//
 // exp(cum_i - cum_j) is factored per 32-row block r of the chunk as
 // exp(cum_i - cum_r) * exp(cum_r - cum_j): both factors are at most 1 for
 // j before the block, and inside the block the second factor is bounded by
@@ -64,15 +68,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
     const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&u);
     return __bfloat1622float2(h);
-}
-
-// A NaN or Inf in either bf16 half of w (all exponent bits set).
-__device__ __forceinline__ bool nonfinite_bf16x2(uint32_t w) {
-    return __vcmpeq2(w & 0x7F807F80u, 0x7F807F80u) != 0u;
-}
-
-__device__ __forceinline__ bool nonfinite_bf16x8(uint4 v) {
-    return nonfinite_bf16x2(v.x) | nonfinite_bf16x2(v.y) | nonfinite_bf16x2(v.z) | nonfinite_bf16x2(v.w);
 }
 
 // 16-byte chunk c (of 8 bf16) of row r in a 128-byte-row swizzled block.
@@ -170,27 +165,33 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr uint32_t kIdZ = tc::idesc_bf16_f32(128, 64) | (1u << 16);      // B MN-major
     constexpr uint32_t kIdDS = tc::idesc_bf16_f32(128, 64) | (1u << 15) | (1u << 16);  // both MN-major
     uint32_t phase = 0, ld_phase = 0;
+    // The chunk's tiles, one load phase per chunk: C and B (4 boxes) once the previous chunk's
+    // MMAs have read them, x (1 box) once its outputs are written.
+    auto load_cb = [&](int ty) {
+        mbar_arrive_expect_tx(s_ldbar, 5u * kTile128);
+        tma_load_2d(smem + OFF_C, &tm_c, g * SN, ty, s_ldbar);
+        tma_load_2d(smem + OFF_C + kTile128, &tm_c, g * SN + 64, ty, s_ldbar);
+        tma_load_2d(smem + OFF_B, &tm_b, g * SN, ty, s_ldbar);
+        tma_load_2d(smem + OFF_B + kTile128, &tm_b, g * SN + 64, ty, s_ldbar);
+    };
+    auto load_x = [&](int ty) { tma_load_2d(smem + OFF_X, &tm_x, h * SP, ty, s_ldbar); };
     bool bad = false, timeout = false;
     const int L = t1 - t0;
     // dt of this thread's row, one chunk ahead (a strided load, kept off the chunk's critical path)
     float dt_next = 0.f;
     if (half == 1 && row < (L < Q ? L : Q)) dt_next = load_dt(a.dt, (size_t)(t0 + row) * H + h, a.dt_bf16);
+    if (tid == 0) {
+        load_cb(t0);
+        load_x(t0);
+    }
     for (int c0 = 0; c0 < L; c0 += Q) {
         const int len = L - c0 < Q ? L - c0 : Q;
         const bool valid = row < len;
         const size_t tok = (size_t)(t0 + c0 + row);
 
-        // ---- P1: the chunk's rows of C, B (two 64-column boxes each) and x by TMA into the
-        // swizzled tiles (the layout chunk_off describes); dt prefix sums meanwhile
-        if (tid == 0) {
-            const int ty = t0 + c0;
-            mbar_arrive_expect_tx(s_ldbar, 5u * kTile128);
-            tma_load_2d(smem + OFF_C, &tm_c, g * SN, ty, s_ldbar);
-            tma_load_2d(smem + OFF_C + kTile128, &tm_c, g * SN + 64, ty, s_ldbar);
-            tma_load_2d(smem + OFF_B, &tm_b, g * SN, ty, s_ldbar);
-            tma_load_2d(smem + OFF_B + kTile128, &tm_b, g * SN + 64, ty, s_ldbar);
-            tma_load_2d(smem + OFF_X, &tm_x, h * SP, ty, s_ldbar);
-        }
+        // ---- P1: the chunk's rows of C, B (two 64-column boxes each) and x, issued by TMA into
+        // the swizzled tiles (the layout chunk_off describes) as soon as the previous chunk was
+        // done with each tile; dt prefix sums while they land
         float dtv = 0.f;
         if (half == 1) {
             dtv = dt_next;
@@ -227,21 +228,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                     *reinterpret_cast<uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c)) = make_uint4(0, 0, 0, 0);
             }
         }
-        if (valid) {  // the thread's own rows, now in shared memory
-            if (half == 0) {
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint32_t off = (uint32_t)(c >> 3) * kTile128 + chunk_off((uint32_t)row, (uint32_t)c);
-                    bad |= nonfinite_bf16x8(*reinterpret_cast<const uint4 *>(smem + OFF_C + off)) |
-                           nonfinite_bf16x8(*reinterpret_cast<const uint4 *>(smem + OFF_B + off));
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    bad |= nonfinite_bf16x8(*reinterpret_cast<const uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c)));
-            }
-        }
-        __syncthreads();
         const float cum_last = s_cum[Q - 1];
         const float cum = s_cum[row];
         // column factors colf[r][j] = exp(cum_{32r} - cum_j) dt_j for j < 32 r + 32,
@@ -271,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             tc::mma_commit(s_bar);
         }
+
         if (__syncthreads_or(!mbar_wait(s_bar, phase & 1u))) {  // uniform across the CTA
             timeout = true;
             break;
@@ -364,11 +351,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         ++phase;
         tc::fence_after_sync();
 
+        if (tid == 0 && c0 + Q < L) load_cb(t0 + c0 + Q);  // C (now M) and B are read
+
         // ---- P5: outputs of row i (this half's 32 columns p), state update of column n = row,
         // 16 columns at a time
         {
             const float ecum = expf(cum);
             const float dA = expf(cum_last);
+            // Non-finite inputs show here: every x, B and C value reaches y or the state
+            // increment through a product (a NaN or Inf times anything, zero included, is not
+            // finite), so v * 0 summed over them is NaN exactly when one of them is not finite.
+            float nf = 0.f;
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 float yv[16], zv[16];
@@ -385,7 +378,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int e = 0; e < 4; ++e) {
                         const float2 xf = unpack_bf16(xw4[e]);
                         const int q = 8 * c + 2 * e;
-                        o[e] = pack_bf16(fmaf(ecum, zv[q], yv[q]) + D * xf.x, fmaf(ecum, zv[q + 1], yv[q + 1]) + D * xf.y);
+                        const float v0 = fmaf(ecum, zv[q], yv[q]) + D * xf.x, v1 = fmaf(ecum, zv[q + 1], yv[q + 1]) + D * xf.y;
+                        nf = fmaf(v0, 0.f, fmaf(v1, 0.f, nf));
+                        o[e] = pack_bf16(v0, v1);
                     }
                     outc[c] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
@@ -400,13 +395,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float ds[16];
                 tc::tmem_ld16(tmem + lane_addr + 64u + (uint32_t)(p0 + 16 * hc), ds);
 #pragma unroll
-                for (int p = 0; p < 16; ++p) S[16 * hc + p] = fmaf(dA, S[16 * hc + p], ds[p]);
+                for (int p = 0; p < 16; ++p) {
+                    nf = fmaf(ds[p], 0.f, nf);
+                    S[16 * hc + p] = fmaf(dA, S[16 * hc + p], ds[p]);
+                }
             }
+            bad |= nf != nf;
         }
         write_state_copy();
         tc::fence_before_sync();
         tc::fence_proxy_async_smem();
         __syncthreads();
+        if (tid == 0 && c0 + Q < L) load_x(t0 + c0 + Q);  // x is read
     }
 
     const bool any_bad = __syncthreads_or(bad);

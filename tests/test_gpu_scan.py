@@ -319,3 +319,46 @@ def test_tensor_core_scan_ragged_lengths(lens, dt_dt):
             assert m.ssm_pool_status(sc.pool)[1] == 0
     finally:
         sc.close()
+
+
+@pytest.mark.parametrize("where", ["B", "C", "x", "dt"])
+def test_tensor_core_scan_nonfinite_poisons_slot(where):
+    """bf16 scan on the tensor cores: a NaN or Inf in a sequence's B, C, x or
+    dt flags SSM_FLAG_NONFINITE_INPUT, poisons its slot and leaves the state
+    of every head it reaches as it was; the other sequence of the call
+    advances and matches the oracle."""
+    m = _mod()
+    H, P, N, G = 4, 64, 128, 2
+    seed = SEED1 + 91
+    A, D = synth.head_params(seed, H)
+    sc = Scanner(m, H, P, N, G, synth.BF16, synth.F32, 2, A, D)
+    try:
+        toks = [synth.tokens(seed, i, 300, H, P, G, N, synth.BF16, synth.F32) for i in range(2)]
+        assert sc.scan([0, 1], [_slice(t, 0, 150) for t in toks])[0] == m.SSM_OK
+        assert m.ssm_last_path(sc.pool) == "scan_ssd"
+        before = sc.state([0, 1])
+        bad = [t.copy() for t in _slice(toks[0], 150, 300)]
+        nan16, inf16 = np.uint16(0x7FC0), np.uint16(0x7F80)  # bf16 bit patterns
+        if where == "B":
+            bad[2][140, 0, 5] = nan16      # group 0: heads 0 and 1
+        elif where == "C":
+            bad[3][140, 0, 5] = inf16
+        elif where == "x":
+            bad[0][140, 1, 7] = inf16      # head 1
+        else:
+            bad[1][140, 1] = np.nan
+        assert sc.scan([0, 1], [tuple(bad), _slice(toks[1], 150, 300)])[0] == m.SSM_OK  # found on the device
+        assert m.ssm_last_path(sc.pool) == "scan_ssd"
+        assert m.ssm_pool_status(sc.pool, clear=True)[1] & m.SSM_FLAG_NONFINITE_INPUT
+        after = sc.state([0, 1])
+        for h in ([0, 1] if where in ("B", "C") else [1]):
+            assert np.array_equal(after[0, h], before[0, h]), h
+        meta0 = m.ssm_slot_info(sc.pool, 0)[1]
+        assert meta0.flags & 1
+        if where in ("B", "C"):
+            assert meta0.position == 150
+        _, ref = _oracle_scan(A, D, toks[1], synth.BF16, synth.F32, np.zeros((H, P, N)))
+        check_close(after[1], ref, synth.BF16, "the healthy sequence's state")
+        assert m.ssm_slot_info(sc.pool, 1)[1].flags == 0
+    finally:
+        sc.close()
