@@ -530,6 +530,7 @@ ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, 
     c.n_slots = p.n_slots; c.t1max = p.t1max; c.wcap = p.wcap; c.W = p.cfg.window;
     c.fold_items = p.d_fold_items; c.fold_count = p.d_fold_count;
     c.force_fold = force_fold ? 1 : 0;
+    const char *path = "commit_copy";
     for (int base = 0; base < batch; base += ssm::kMaxSlotsPerLaunch) {
         const int m = std::min(batch - base, ssm::kMaxSlotsPerLaunch);
         c.accept = accept + base;
@@ -539,11 +540,11 @@ ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, 
             c.slots[i] = slots[base + i];
             c.ntok[i] = p.pending_ntok[slots[base + i]];
         }
-        const cudaError_t e = ssm::launch_commit(p, c, s);
+        const cudaError_t e = ssm::launch_commit(p, c, s, &path);
         if (e != cudaSuccess) return cuda_status(e);
     }
     for (int i = 0; i < batch; ++i) p.pending_ntok[slots[i]] = 0;
-    p.last_path = p.cfg.mode == SSM_MODE_COPY ? "commit_copy" : "commit_replay";
+    p.last_path = path;
     return SSM_OK;
 }
 

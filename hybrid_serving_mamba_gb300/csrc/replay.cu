@@ -481,18 +481,24 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s) {
+cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s, const char **path) {
     const bool replay = pool.cfg.mode == SSM_MODE_REPLAY;
     if (replay) {
         const cudaError_t e = cudaMemsetAsync(a.fold_count, 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return e;
     }
     commit_meta_kernel<<<(a.batch + 127) / 128, 128, 0, s>>>(a, replay ? 1 : 0);
+    if (path) *path = "commit_copy";
     if (replay) {
         cudaError_t ep = cudaGetLastError();
         if (ep != cudaSuccess) return ep;
-        ep = launch_fold_pipe(pool, a, s);
+        ep = launch_fold_tc(pool, a, s);
+        if (path) *path = "commit_replay_fold_tc";
         if (ep != cudaErrorNotSupported) return ep;
+        ep = launch_fold_pipe(pool, a, s);
+        if (path) *path = "commit_replay_fold_pipe";
+        if (ep != cudaErrorNotSupported) return ep;
+        if (path) *path = "commit_replay_fold";
         const size_t smem = fold_smem_bytes(pool);
         const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
         SSM_DISPATCH_N(a.N, {

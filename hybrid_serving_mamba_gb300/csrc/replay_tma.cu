@@ -1023,6 +1023,16 @@ bool replay_tma_encode(Pool &p) {
                      enc(&p.tm_logx2, xt, 3, p.log_x, xd, xst, xb2, xe, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        // the fold's B operand: logged rows s of group g, [slot * wcap + s][g][n] bf16, boxes of
+        // 32 rows x 64 columns with the 128-byte swizzle (an MN-major operand tile)
+        if (p.tm_tc_ok && p.cfg.input_dtype == SSM_DTYPE_BF16 && p.N == 128 && p.wcap <= 32) {
+            const cuuint64_t bd[3] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)p.n_slots * p.wcap};
+            const cuuint64_t bst[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2};
+            const cuuint32_t bb[3] = {64u, 1u, 32u};
+            p.tm_fold_ok = enc(&p.tm_logB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.log_B, bd, bst, bb, xe,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
     }
     return true;
 }

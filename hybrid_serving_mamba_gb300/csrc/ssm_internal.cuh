@@ -68,6 +68,8 @@ struct Pool {
     CUtensorMap tm_state2;             // replay, tensor cores: 32 columns x 128 rows (two heads) per box
     CUtensorMap tm_logx2;              // replay, tensor cores: two heads' logs of x rows per box
     bool tm_tc_ok = false;             // the two maps above encoded
+    CUtensorMap tm_logB;               // replay, bf16, N = 128: 32 logged B rows x 64 columns of a group per box
+    bool tm_fold_ok = false;           // tm_state2, tm_logx2 and tm_logB encoded for the tensor-core fold
     int2 *d_fold_items = nullptr;      // (request index, tokens to fold) of one commit launch
     int32_t *d_fold_count = nullptr;
     int sm_count = 1;
@@ -186,7 +188,11 @@ bool replay_tma_encode(Pool &p);
 // Pipelined replay verify (persistent CTAs, bulk-copy ring); returns
 // cudaErrorNotSupported when the shapes or pointers do not allow it.
 cudaError_t launch_verify_replay_pipe(const Pool &pool, const StepArgs &a, cudaStream_t s);
-cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s);
+// The commit; *path names the fold kernel that ran (or "commit_copy").
+cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s, const char **path = nullptr);
+// The fold on the tensor cores (bf16 pools, P = 64, N = 128, window <= 32);
+// cudaErrorNotSupported for other pools.
+cudaError_t launch_fold_tc(const Pool &pool, const CommitArgs &a, cudaStream_t s);
 // Pipelined fold of the requests the commit listed; cudaErrorNotSupported
 // when the shapes or pointers do not allow bulk copies.
 cudaError_t launch_fold_pipe(const Pool &pool, const CommitArgs &a, cudaStream_t s);

@@ -27,7 +27,7 @@ def _wide(x, dt, B, C, dt_in, dt_dt):
 
 
 def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_tok_pattern=None, force_last=True,
-               expect_path=None, y_round_mismatch=None):
+               expect_path=None, y_round_mismatch=None, expect_commit_path=None):
     import torch
     m = _mod()
     n_slots, slots = 8, [6, 1, 3, 0, 7]
@@ -62,6 +62,8 @@ def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_to
             ys.append(to_host(y))
             force = force_last and s == steps - 1
             assert m.ssm_state_commit(pool, slots, torch.from_numpy(acc).cuda(), force, Ad) == m.SSM_OK
+            if expect_commit_path is not None:
+                assert m.ssm_last_path(pool) == expect_commit_path
             _, folded = opool.commit(slots, acc, force_fold=force)
             for sl in range(n_slots):
                 st, meta = m.ssm_slot_info(pool, sl)
@@ -119,8 +121,9 @@ def test_replay_tensor_core_verify(dt_in, T, W, path):
     bf16 for bf16 inputs); at fp32 inputs the oracle's 1e-5 tolerance checks
     that the splits keep fp32 accuracy."""
     m = _mod()
+    fold = "commit_replay_fold_tc" if dt_in == synth.BF16 else "commit_replay_fold_pipe"
     pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, W, T, 0.7, steps=6, H=4, P=64, N=128, G=2, dt_in=dt_in,
-                               expect_path=path)
+                               expect_path=path, expect_commit_path=fold)
     m.ssm_state_destroy(pool)
 
 
