@@ -34,7 +34,8 @@ EXPORTS = (
     "ssm_state_init", "ssm_state_destroy", "ssm_state_reset", "ssm_state_release", "ssm_state_checkpoint",
     "ssm_state_restore", "ssm_slot_info", "ssm_state_gather", "ssm_scan_chunk", "ssm_decode_step",
     "ssm_verify_copy", "ssm_verify_replay", "ssm_state_commit", "ssm_pool_status", "ssm_last_path",
-    "ssm_status_string", "ssm_pool_bytes", "ssm_verify_replay_static",
+    "ssm_status_string", "ssm_pool_bytes", "ssm_verify_replay_static", "ssm_receipt_bytes", "ssm_receipt_encode",
+    "ssm_receipt_decode", "ssm_state_checkpoint_receipt", "ssm_state_restore_receipt",
 )
 
 
@@ -53,6 +54,21 @@ class ssm_config(ctypes.Structure):
 class ssm_slot_meta(ctypes.Structure):
     _fields_ = [("position", ctypes.c_int64), ("next_chunk", ctypes.c_int64), ("epoch", ctypes.c_int64),
                 ("log_len", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class ssm_stream_identity(ctypes.Structure):
+    _fields_ = [("stream_id", ctypes.c_uint64), ("model_revision", ctypes.c_uint64),
+                ("code_revision", ctypes.c_uint64), ("layer", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class ssm_receipt(ctypes.Structure):
+    _fields_ = [("id", ssm_stream_identity), ("schema_version", ctypes.c_uint32), ("state_dtype", ctypes.c_int32),
+                ("input_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32), ("nheads", ctypes.c_int32),
+                ("headdim", ctypes.c_int32), ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32),
+                ("position", ctypes.c_int64), ("next_chunk", ctypes.c_int64), ("checksum", ctypes.c_uint64)]
+
+
+SSM_STATE_SCHEMA_VERSION = 1
 
 
 def _load():
@@ -83,6 +99,11 @@ def _load():
         "ssm_pool_bytes": [V],
         "ssm_verify_replay_static": [I32, I32, I32, I32, I32, I32, I32, I32, I32, V, V, V, V, V,
                                      V, V, V, V, V, V, V, V, V],
+        "ssm_receipt_encode": [ctypes.POINTER(ssm_receipt), V, V, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)],
+        "ssm_receipt_decode": [V, ctypes.c_size_t, ctypes.POINTER(ssm_receipt), ctypes.POINTER(V)],
+        "ssm_state_checkpoint_receipt": [V, I32, V, ctypes.POINTER(ssm_stream_identity), V, ctypes.c_size_t,
+                                         ctypes.POINTER(ctypes.c_size_t), V],
+        "ssm_state_restore_receipt": [V, I32, V, ctypes.c_size_t, ctypes.POINTER(ssm_stream_identity), V],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -91,6 +112,8 @@ def _load():
     lib.ssm_last_path.restype = ctypes.c_char_p
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_pool_bytes.restype = ctypes.c_size_t
+    lib.ssm_receipt_bytes.argtypes = [I32, I32, I32]
+    lib.ssm_receipt_bytes.restype = ctypes.c_size_t
     return lib
 
 
@@ -220,6 +243,56 @@ def ssm_state_restore(pool: Pool, slot: int, host_state: np.ndarray, meta: ssm_s
     h = np.ascontiguousarray(host_state, dtype=np.float32)
     return _lib.ssm_state_restore(pool.handle, int(slot), h.ctypes.data_as(ctypes.c_void_p), h.nbytes,
                                   ctypes.byref(meta), _stream(stream))
+
+
+def stream_identity(stream_id: int, model_revision: int, code_revision: int, layer: int) -> ssm_stream_identity:
+    return ssm_stream_identity(stream_id, model_revision, code_revision, layer, 0)
+
+
+def ssm_receipt_bytes(nheads: int, headdim: int, dstate: int) -> int:
+    return int(_lib.ssm_receipt_bytes(nheads, headdim, dstate))
+
+
+def ssm_receipt_encode(receipt: ssm_receipt, state: np.ndarray):
+    """Host only: (status, bytes) of receipt + state blob; receipt.checksum is filled in."""
+    s = np.ascontiguousarray(state, dtype=np.float32)
+    need = ctypes.c_size_t()
+    _lib.ssm_receipt_encode(ctypes.byref(receipt), s.ctypes.data_as(ctypes.c_void_p), None, 0, ctypes.byref(need))
+    buf = (ctypes.c_ubyte * need.value)()
+    st = _lib.ssm_receipt_encode(ctypes.byref(receipt), s.ctypes.data_as(ctypes.c_void_p), buf, need.value,
+                                 ctypes.byref(need))
+    return st, bytes(buf)
+
+
+def ssm_receipt_decode(blob: bytes):
+    """Host only: (status, ssm_receipt, state ndarray float32 [H][P][N] or None)."""
+    buf = ctypes.create_string_buffer(bytes(blob), len(blob))
+    r = ssm_receipt()
+    ptr = ctypes.c_void_p()
+    st = _lib.ssm_receipt_decode(buf, len(blob), ctypes.byref(r), ctypes.byref(ptr))
+    if st != SSM_OK:
+        return st, r, None
+    off = ptr.value - ctypes.addressof(buf)
+    n = r.nheads * r.headdim * r.dstate
+    state = np.frombuffer(bytes(blob), dtype="<f4", count=n, offset=off).reshape(r.nheads, r.headdim, r.dstate)
+    return st, r, state.copy()
+
+
+def ssm_state_checkpoint_receipt(pool: Pool, slot: int, identity: ssm_stream_identity, A=None, stream=None):
+    """(status, bytes): the slot checkpointed as receipt + state blob."""
+    import torch
+    need = _lib.ssm_receipt_bytes(pool.H, pool.P, pool.N)
+    buf = (ctypes.c_ubyte * need)()
+    written = ctypes.c_size_t()
+    st = _lib.ssm_state_checkpoint_receipt(pool.handle, int(slot), _dev(A, "A", torch.float32, pool.H),
+                                           ctypes.byref(identity), buf, need, ctypes.byref(written), _stream(stream))
+    return st, bytes(buf)[:written.value] if st == SSM_OK else b""
+
+
+def ssm_state_restore_receipt(pool: Pool, slot: int, blob: bytes, expect: ssm_stream_identity, stream=None) -> int:
+    buf = ctypes.create_string_buffer(bytes(blob), len(blob))
+    return _lib.ssm_state_restore_receipt(pool.handle, int(slot), buf, len(blob), ctypes.byref(expect),
+                                          _stream(stream))
 
 
 def ssm_slot_info(pool: Pool, slot: int, stream=None):

@@ -392,6 +392,59 @@ ssm_status ssm_state_restore(ssm_pool pool, int32_t slot, const float *host_stat
     return SSM_OK;
 }
 
+ssm_status ssm_state_checkpoint_receipt(ssm_pool pool, int32_t slot, const float *A, const ssm_stream_identity *id,
+                                        void *buf, size_t cap, size_t *written, ssm_stream_t stream) {
+    if (!pool || !id) return SSM_ERR_INVALID_ARG;
+    Pool &p = pool->p;
+    const size_t need = ssm_receipt_bytes(p.H, p.P, p.N);
+    if (written) *written = need;
+    if (!buf || cap < need) return SSM_ERR_INVALID_ARG;
+    std::vector<float> host(p.hpn);
+    ssm_slot_meta meta;
+    ssm_status st = ssm_state_checkpoint(pool, slot, A, host.data(), host.size() * sizeof(float), &meta, stream);
+    if (st != SSM_OK) return st;
+    ssm_receipt r;
+    std::memset(&r, 0, sizeof(r));
+    r.id = *id;
+    r.schema_version = SSM_STATE_SCHEMA_VERSION;
+    r.state_dtype = SSM_DTYPE_F32;
+    r.input_dtype = p.cfg.input_dtype;
+    r.dt_dtype = p.cfg.dt_dtype;
+    r.nheads = p.H; r.headdim = p.P; r.dstate = p.N; r.ngroups = p.G;
+    r.position = meta.position;
+    r.next_chunk = meta.next_chunk;
+    return ssm_receipt_encode(&r, host.data(), buf, cap, written);
+}
+
+ssm_status ssm_state_restore_receipt(ssm_pool pool, int32_t slot, const void *buf, size_t len,
+                                     const ssm_stream_identity *expect, ssm_stream_t stream) {
+    if (!pool || !buf || !expect || slot < 0 || slot >= pool->p.n_slots) return SSM_ERR_INVALID_ARG;
+    Pool &p = pool->p;
+    ssm_receipt r;
+    const void *payload = nullptr;
+    ssm_status st = ssm_receipt_decode(buf, len, &r, &payload);
+    if (st != SSM_OK) return st;
+    // every semantic field must match: whose state, which layout, precision and shape
+    if (r.id.stream_id != expect->stream_id || r.id.model_revision != expect->model_revision ||
+        r.id.code_revision != expect->code_revision || r.id.layer != expect->layer)
+        return SSM_ERR_SCHEMA;
+    if (r.schema_version != SSM_STATE_SCHEMA_VERSION || r.state_dtype != SSM_DTYPE_F32 ||
+        r.input_dtype != p.cfg.input_dtype || r.dt_dtype != p.cfg.dt_dtype)
+        return SSM_ERR_SCHEMA;
+    if (r.nheads != p.H || r.headdim != p.P || r.dstate != p.N || r.ngroups != p.G) return SSM_ERR_SCHEMA;
+    if (r.position < 0 || r.next_chunk < 0) return SSM_ERR_SCHEMA;
+    std::vector<float> host(p.hpn);
+    std::memcpy(host.data(), payload, p.hpn * sizeof(float));  // the blob holds little-endian fp32
+    ssm_slot_meta meta;
+    std::memset(&meta, 0, sizeof(meta));
+    meta.position = r.position;
+    meta.next_chunk = r.next_chunk;
+    meta.epoch = p.epoch[slot] + 1;  // a new occupant of the slot
+    st = ssm_state_restore(pool, slot, host.data(), host.size() * sizeof(float), &meta, stream);
+    if (st == SSM_OK) p.last_path = "restore_receipt";
+    return st;
+}
+
 ssm_status ssm_state_gather(ssm_pool pool, int32_t n, const int32_t *slots, float *dst, ssm_stream_t stream) {
     if (!pool || !dst) return SSM_ERR_INVALID_ARG;
     ssm_status st = check_slots(pool, slots, n, true);

@@ -166,6 +166,88 @@ ssm_status ssm_state_checkpoint(ssm_pool pool, int32_t slot, const float *A, flo
 ssm_status ssm_state_restore(ssm_pool pool, int32_t slot, const float *host_state, size_t bytes,
                              const ssm_slot_meta *meta, ssm_stream_t stream);
 
+/* ---------------------------------------------------------------- checkpoint receipt */
+
+/*
+ * Whose state it is: given by the caller when it checkpoints and again when
+ * it resumes (Treat Mamba streaming state as a stream-owned record: a state
+ * belongs to one stream under one model, code revision and layer).  The
+ * revisions are the caller's identifiers (for instance hashes of revision
+ * strings); the library only compares them.
+ */
+typedef struct {
+    uint64_t stream_id;
+    uint64_t model_revision;
+    uint64_t code_revision;
+    int32_t layer;
+    int32_t reserved; /* 0 */
+} ssm_stream_identity;
+
+#define SSM_STATE_SCHEMA_VERSION 1u /* layout of the state: fp32 [H][P][N], n fastest */
+
+/*
+ * A checkpoint receipt (Make reset, checkpoint, and cancellation
+ * observable: checkpoint receipt): the identity, the state schema, dtypes,
+ * layer and state dimensions, the absolute position, the chunk sequence and
+ * a checksum of the state.
+ */
+typedef struct {
+    ssm_stream_identity id;
+    uint32_t schema_version; /* SSM_STATE_SCHEMA_VERSION */
+    int32_t state_dtype;     /* SSM_DTYPE_F32 */
+    int32_t input_dtype;     /* the pool's x / B / C dtype */
+    int32_t dt_dtype;
+    int32_t nheads, headdim, dstate, ngroups;
+    int64_t position;        /* tokens applied since the stream began */
+    int64_t next_chunk;      /* chunk sequence number expected next */
+    uint64_t checksum;       /* FNV-1a 64 over the state blob */
+} ssm_receipt;
+
+/*
+ * Serialized checkpoint, little-endian: "SSMR", uint32 format version 1,
+ * then the receipt fields in the order above (uint64 x3, int32 layer,
+ * uint32 schema, int32 x7, int64 x2), uint64 blob bytes, uint64 checksum,
+ * then the state blob in the array format of the SSM.PREFIX state store:
+ * uint32 version = 1, uint32 n_arrays = 1, uint32 ndim = 3, uint32 shape
+ * {H, P, N}, uint32 dtype code 0 (fp32), H*P*N fp32 values.
+ */
+size_t ssm_receipt_bytes(int32_t nheads, int32_t headdim, int32_t dstate);
+
+/*
+ * Host only (no device work).  Serialize *r with the state (host float
+ * [H][P][N] of r's dimensions); the checksum is computed here and written
+ * back into r->checksum.  SSM_ERR_INVALID_ARG if cap is too small
+ * (*written is then the size needed).
+ */
+ssm_status ssm_receipt_encode(ssm_receipt *r, const float *state, void *buf, size_t cap, size_t *written);
+
+/*
+ * Host only.  Parse and check a serialized checkpoint of len bytes: magic,
+ * versions, the blob's array header against the receipt's dimensions, the
+ * lengths and the checksum.  On SSM_OK fills *r and sets *state to the fp32
+ * values inside buf (not necessarily 4-byte aligned).  SSM_ERR_SCHEMA for
+ * anything that does not check.
+ */
+ssm_status ssm_receipt_decode(const void *buf, size_t len, ssm_receipt *r, const void **state);
+
+/*
+ * Checkpoint one slot as receipt + state blob (replay mode folds the log
+ * first; A as for ssm_state_checkpoint).  Synchronous.
+ */
+ssm_status ssm_state_checkpoint_receipt(ssm_pool pool, int32_t slot, const float *A, const ssm_stream_identity *id,
+                                        void *buf, size_t cap, size_t *written, ssm_stream_t stream);
+
+/*
+ * Resume one slot from a serialized checkpoint.  Refused with
+ * SSM_ERR_SCHEMA, nothing changed, unless it decodes, its identity equals
+ * *expect, and its schema, dtypes and dimensions equal the pool's: an
+ * incompatible resume is rejected, never padded or truncated.  Then as
+ * ssm_state_restore, with the position and chunk sequence of the receipt;
+ * the slot's epoch counts the restore as a new occupancy.  Synchronous.
+ */
+ssm_status ssm_state_restore_receipt(ssm_pool pool, int32_t slot, const void *buf, size_t len,
+                                     const ssm_stream_identity *expect, ssm_stream_t stream);
+
 /* Read one slot's metadata (synchronous; no fold). */
 ssm_status ssm_slot_info(ssm_pool pool, int32_t slot, ssm_slot_meta *meta, ssm_stream_t stream);
 
