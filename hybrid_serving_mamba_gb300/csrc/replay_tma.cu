@@ -87,16 +87,21 @@ template <> struct Vec16<float> {
 };
 
 // smem: C [T1][N] | B [mmax][N] | C.B [T1][mmax] | dt per warp [nw][mmax] | prefix sums per warp [nw][mmax] (pairs)
-__host__ __device__ inline size_t gcoef_smem_bytes(int T1, int mmax, int N, int nwarps) {
+// fp32 C, B, C.B and dt rows, the fp32-pair prefix sums, then (16-byte aligned) the step's x
+// of the group's heads as given (xbytes).
+__host__ __device__ inline size_t gcoef_x_offset(int T1, int mmax, int N, int nwarps) {
     size_t f = (size_t)T1 * N + (size_t)mmax * N + (size_t)T1 * mmax + (size_t)nwarps * mmax;
     f = (f + 1) & ~(size_t)1;
-    return f * 4 + (size_t)nwarps * mmax * 8;
+    return (f * 4 + (size_t)nwarps * mmax * 8 + 15) & ~(size_t)15;
+}
+__host__ __device__ inline size_t gcoef_smem_bytes(int T1, int mmax, int N, int nwarps, size_t xbytes) {
+    return gcoef_x_offset(T1, mmax, N, nwarps) + xbytes;
 }
 
 // Rows of x, B, C are moved 16 bytes at a time: the launcher checks that
 // P and N rows are multiples of 16 bytes and the pointers 16-byte aligned.
 template <int N, typename TI>
-__global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(const __grid_constant__ StepArgs a) {
     using V = Vec16<TI>;
     constexpr int EV = V::n;          // elements per 16 bytes
     constexpr int NV = N / EV;        // 16-byte vectors per B or C row
@@ -116,6 +121,20 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
     size_t off = (size_t)T1 * N + (size_t)mmax * N + (size_t)T1 * mmax + (size_t)nwarps * mmax;
     off = (off + 1) & ~(size_t)1;
     Sum2 *sCum = reinterpret_cast<Sum2 *>(reinterpret_cast<float *>(smem4) + off);
+    // the step's x of the group's heads, one contiguous row of hpg P values per token, comes in by
+    // bulk copies, is checked here and goes to the log by bulk copies
+    __shared__ uint64_t s_xbar;
+    TI *sX = reinterpret_cast<TI *>(reinterpret_cast<unsigned char *>(smem4) + gcoef_x_offset(T1, mmax, N, nwarps));
+    const uint32_t xrow = (uint32_t)(hpg * P * (int)sizeof(TI));
+    const TI *sx = reinterpret_cast<const TI *>(a.x);
+    TI *wx = reinterpret_cast<TI *>(a.log_x);
+    if (threadIdx.x == 0) {
+        mbar_init(&s_xbar, 1);
+        mbar_fence_init();
+        mbar_arrive_expect_tx(&s_xbar, (uint32_t)T1 * xrow);
+        for (int t = 0; t < T1; ++t)
+            bulk_g2s(sX + (size_t)t * hpg * P, sx + (((size_t)i * T1 + t) * H + (size_t)g * hpg) * P, xrow, &s_xbar);
+    }
 
     const TI *stepC = reinterpret_cast<const TI *>(a.C);
     const TI *stepB = reinterpret_cast<const TI *>(a.B);
@@ -174,26 +193,29 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
         }
         V::widen(v, sB + (size_t)s * N + q * EV);
     }
-    {  // the step's x of the group's heads (contiguous per token), staged after the log
-        const int rv = hpg * P / EV;  // vectors per token
-        const TI *sx = reinterpret_cast<const TI *>(a.x);
-        TI *wx = reinterpret_cast<TI *>(a.log_x);
-        for (int e = threadIdx.x; e < T1 * rv; e += blockDim.x) {
-            const int t = e / rv, q = e - t * rv;
-            const uint4 v = *reinterpret_cast<const uint4 *>(sx + (((size_t)i * T1 + t) * H + (size_t)g * hpg) * P + q * EV);
-            bad |= V::nonfinite(v);
-            *reinterpret_cast<uint4 *>(wx + (((size_t)slot * a.wcap + k + t) * H + (size_t)g * hpg) * P + q * EV) = v;
+    for (int e = threadIdx.x; e < T1 * hpg; e += blockDim.x) {  // the step's dt, staged after the log
+        const int t = e / hpg, h = g * hpg + (e - t * hpg);
+        const float d = load_dt(a.dt, ((size_t)i * T1 + t) * H + h, a.dt_bf16);
+        bad |= !isfinite(d);
+        a.log_dt[((size_t)slot * a.wcap + k + t) * H + h] = d;
+    }
+    {  // the step's x, once landed: the non-finite check
+        __syncthreads();  // the barrier's initialisation is visible to every thread
+        if (!mbar_wait(&s_xbar, 0u)) {
+            bad = true;
+            if (threadIdx.x == 0) atomicOr(a.flags, SSM_FLAG_TIMEOUT);
         }
-        for (int e = threadIdx.x; e < T1 * hpg; e += blockDim.x) {
-            const int t = e / hpg, h = g * hpg + (e - t * hpg);
-            const float d = load_dt(a.dt, ((size_t)i * T1 + t) * H + h, a.dt_bf16);
-            bad |= !isfinite(d);
-            a.log_dt[((size_t)slot * a.wcap + k + t) * H + h] = d;
-        }
+        const uint4 *x4 = reinterpret_cast<const uint4 *>(sX);
+        for (int e = threadIdx.x; e < T1 * (int)(xrow / 16); e += blockDim.x) bad |= V::nonfinite(x4[e]);
     }
     if (__syncthreads_or(bad)) {
         if (threadIdx.x == 0) raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_NONFINITE_INPUT);
         return;
+    }
+    if (threadIdx.x == 0) {  // x to the log, after the log's k rows; waited for at the end
+        for (int t = 0; t < T1; ++t)
+            bulk_s2g(wx + (((size_t)slot * a.wcap + k + t) * H + (size_t)g * hpg) * P, sX + (size_t)t * hpg * P, xrow);
+        bulk_commit();
     }
     for (int pr = threadIdx.x; pr < T1 * m; pr += blockDim.x) {  // C_j . B_s, one thread per pair
         const int j = pr / m, s = pr - j * m;
@@ -240,6 +262,7 @@ __global__ void __launch_bounds__(kCoefThreads) replay_group_coef_kernel(const _
         for (int j = lane; j < T1; j += 32) a.dec[((size_t)i * H + h) * a.t1pad + j] = expf(A * (cum[k + j].hi + cum[k + j].lo));
         __syncwarp();
     }
+    if (threadIdx.x == 0) bulk_wait0();  // the log's x rows are written before the CTA ends
 }
 
 // ------------------------------------------------------------------ streaming kernel
@@ -1038,7 +1061,8 @@ bool replay_tma_encode(Pool &p) {
 }
 
 size_t replay_coef_smem_bytes(const Pool &pool, int n_tok) {
-    return gcoef_smem_bytes(n_tok, pool.wcap - pool.t1max + n_tok, pool.N, kCoefThreads / 32);
+    return gcoef_smem_bytes(n_tok, pool.wcap - pool.t1max + n_tok, pool.N, kCoefThreads / 32,
+                            (size_t)n_tok * pool.hpg * pool.P * pool.in_bytes);
 }
 
 cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path) {

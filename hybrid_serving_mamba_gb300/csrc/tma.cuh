@@ -114,6 +114,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int
                  : "memory");
 }
 
+// Shared -> global bulk copy (bytes and both addresses multiples of 16), in
+// this thread's bulk async-group.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Until this thread's bulk groups have finished reading shared memory (the
