@@ -236,7 +236,10 @@ def bench_decode(torch, m, dist, args, clocks):
 def bench_decode_e2e(torch, m, args):
     """The same decode workload through the public API with host buffers:
     every token's inputs copied from pinned host memory, its output copied
-    back, inside the timed region."""
+    back, inside the timed region.  Copies overlap the decode the way a
+    serving loop would run them: token t + 1's inputs go up on one copy
+    stream while token t decodes, token t - 1's output comes down on another,
+    with two staging buffers each and events ordering their reuse."""
     c = DEC
     gen = torch.Generator(device="cuda")
     gen.manual_seed(SEED + 91 + 17 * args.rank)
@@ -248,28 +251,49 @@ def bench_decode_e2e(torch, m, args):
     del init
     dev_in = step_inputs(torch, gen, T * R, H, P, G, N)
     host_in = [t.view(T, R, *t.shape[1:]).cpu().pin_memory() for t in dev_in]
-    stage = [torch.empty(t.shape[1:], dtype=t.dtype, device="cuda") for t in host_in]
-    y_dev = torch.empty((R, H, P), dtype=torch.bfloat16, device="cuda")
+    del dev_in
+    stage = [[torch.empty(t.shape[1:], dtype=t.dtype, device="cuda") for t in host_in] for _ in range(2)]
+    y_dev = [torch.empty((R, H, P), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     y_host = torch.empty((T, R, H, P), dtype=torch.bfloat16).pin_memory()
     slots = list(range(R))
     stream = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]
+    in_ready, used, y_ready, y_free = ev(), ev(), ev(), ev()
 
-    def one_step():
+    def one_step(first):
         for t in range(T):
-            for s, h in zip(stage, host_in):
-                s.copy_(h[t], non_blocking=True)
-            m.ssm_decode_step(pool, slots, *stage, A, D, y_dev, stream=stream)
-            y_host[t].copy_(y_dev, non_blocking=True)
+            b = t % 2
+            with torch.cuda.stream(up):  # inputs of token t into buffer b, once token t - 2 has used it
+                if t >= 2 or not first:
+                    up.wait_event(used[b])
+                for s, h in zip(stage[b], host_in):
+                    s.copy_(h[t], non_blocking=True)
+                in_ready[b].record(up)
+            stream.wait_event(in_ready[b])
+            if t >= 2 or not first:
+                stream.wait_event(y_free[b])  # y buffer b read back
+            m.ssm_decode_step(pool, slots, *stage[b], A, D, y_dev[b], stream=stream)
+            used[b].record(stream)
+            y_ready[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(y_ready[b])
+                y_host[t].copy_(y_dev[b], non_blocking=True)
+                y_free[b].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)  # every copy of the step is done before the step ends
 
     steps = max(3, args.steps // 3)
-    for _ in range(max(1, args.warmup)):
-        one_step()
+    for w in range(max(1, args.warmup)):
+        one_step(w == 0)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    up.wait_stream(stream)  # no copy of the timed steps starts before t0
+    down.wait_stream(stream)
     for _ in range(steps):
-        one_step()
+        one_step(False)
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
