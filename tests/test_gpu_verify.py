@@ -286,3 +286,65 @@ def test_config3_full_batch_sampled(T, p, W):
     finally:
         for pl in pools.values():
             m.ssm_state_destroy(pl)
+
+
+@pytest.mark.parametrize("mode,where", [(1, "x"), (1, "B"), (1, "C"), (1, "dt"), (0, "x"), (0, "B")])
+def test_nonfinite_verify_input_poisons_only_its_request(mode, where):
+    """A NaN or Inf in one request's step inputs (bf16 x / B / C, fp32 dt)
+    flags SSM_FLAG_NONFINITE_INPUT and poisons that request's slot; its commit
+    is refused on the device (position and log left as they were); the other
+    requests' outputs, commits and later steps match the oracle."""
+    import torch
+    m = _mod()
+    H, P, N, G, T, W = 4, 64, 128, 2, 4, 8
+    T1 = T + 1
+    slots = [0, 1, 2]
+    A, D = synth.head_params(SEED, H)
+    init = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(3)])
+    pool = m.ssm_state_init(m.make_config(H, P, N, G, synth.BF16, synth.F32, mode, W, T1), 3,
+                            torch.from_numpy(init).cuda())
+    opool = oracle.OraclePool(H, P, N, G, 3, A, D, mode=mode, W=W, max_tokens=T1, init_state=init.astype(np.float64))
+    Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+    verify = m.ssm_verify_copy if mode == m.SSM_MODE_COPY else m.ssm_verify_replay
+    nan16, inf16 = np.uint16(0x7FC0), np.uint16(0x7F80)
+    try:
+        for s in range(4):
+            live = slots if s < 2 else [0, 2]
+            x, dt, B, C = synth.batch_tokens(SEED + 5, s, len(live), T1, H, P, G, N, synth.BF16, synth.F32)
+            if s == 1:  # request 1 of this step
+                if where == "x":
+                    x[1, 2, 3, 5] = inf16
+                elif where == "B":
+                    B[1, 0, 1, 7] = nan16
+                elif where == "C":
+                    C[1, 4, 0, 9] = inf16
+                else:
+                    dt[1, 3, 2] = np.nan
+            y = empty_like_out((len(live), T1, H, P), synth.BF16)
+            assert verify(pool, live, T1, *_dev_inputs(x, dt, B, C, synth.BF16, synth.F32), Ad, Dd, y) == m.SSM_OK
+            good = [i for i, sl in enumerate(live) if not (s == 1 and sl == 1)]
+            gsl = [live[i] for i in good]
+            _, yo = opool.verify(gsl, *[synth.widen(a[good], d) for a, d in
+                                        ((x, synth.BF16), (dt, synth.F32), (B, synth.BF16), (C, synth.BF16))])
+            check_close(to_host(y)[good], yo, synth.BF16, f"y step {s}", positions_axis=1)
+            acc = np.full(len(live), 2, np.int32)
+            if s == 1:
+                before = m.ssm_slot_info(pool, 1)[1]
+            assert m.ssm_state_commit(pool, live, torch.from_numpy(acc).cuda(), False, Ad) == m.SSM_OK
+            opool.commit(gsl, acc[good])
+            st, flags = m.ssm_pool_status(pool, clear=True)
+            if s == 1:
+                assert flags & m.SSM_FLAG_NONFINITE_INPUT, flags
+                meta = m.ssm_slot_info(pool, 1)[1]
+                assert meta.flags & 1
+                assert (meta.position, meta.log_len) == (before.position, before.log_len)
+            else:
+                assert flags == 0, (s, flags)
+            for sl in (0, 2):
+                meta = m.ssm_slot_info(pool, sl)[1]
+                assert meta.position == opool.position[sl] and meta.log_len == opool.log_len[sl] and meta.flags == 0
+        got = torch.empty((3, H, P, N), dtype=torch.float32, device="cuda")
+        assert m.ssm_state_gather(pool, [0, 1, 2], got) == m.SSM_OK
+        check_close(to_host(got)[[0, 2]], opool.state[[0, 2]], synth.BF16, "healthy states")
+    finally:
+        m.ssm_state_destroy(pool)
