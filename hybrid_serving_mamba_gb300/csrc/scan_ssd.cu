@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int t0 = a.cu[i_seq], t1 = a.cu[i_seq + 1];
     if (t1 <= t0) return;  // empty chunk: consumes its sequence number only
     const int slot = a.slots[i_seq];
-    const int H = a.H, G = a.G, g = h / a.hpg;
+    const int H = a.H, g = h / a.hpg;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row = tid & 127;      // token row (P1, P3, P5) or state column n
     const int half = tid >> 7;      // which half of the columns this thread takes
@@ -140,9 +140,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t lane_addr = (uint32_t)(32 * rb) << 16;  // TMEM lane quadrant of this warp
 
     const float A = a.A[h], D = a.D[h];
-    const TI *xg = reinterpret_cast<const TI *>(a.x);
-    const TI *Bg = reinterpret_cast<const TI *>(a.B);
-    const TI *Cg = reinterpret_cast<const TI *>(a.C);
     TI *yg = reinterpret_cast<TI *>(a.y);
     float *st = current_state(a.state, a.snap, a.cur, a.n_slots, (size_t)H * SP * SN, (size_t)SP * SN, slot, h);
 
