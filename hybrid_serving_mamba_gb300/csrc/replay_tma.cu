@@ -106,6 +106,9 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
     constexpr int EV = V::n;          // elements per 16 bytes
     constexpr int NV = N / EV;        // 16-byte vectors per B or C row
     extern __shared__ float4 smem4[];
+    // the streaming kernel may be scheduled as CTAs of this one drain; it waits for this grid's
+    // completion before it reads anything this kernel writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int g = blockIdx.x, i = blockIdx.y;
     const int slot = a.slots[i];
     const int T1 = a.n_tok, H = a.H, P = a.P, hpg = a.hpg;
@@ -680,6 +683,9 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
         const uint32_t xbytes = cbytes + 2u * a.wcap * P * sizeof(TI) + 2u * a.t1max * a.cb_w * 4u + 2u * a.t1pad * 4u;
         int xlast[kTcMaxAux];
         for (int s = 0; s < kTcMaxAux; ++s) xlast[s] = -1;
+        // C in the operand layout, W, decay_j, the staged log rows and the slot flags come from the
+        // coefficient kernel, launched just before this one
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         int my_k = 0;
         uint32_t my_gate = 0;
         bool alive = true;
@@ -1132,7 +1138,18 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         auto k = verify_replay_tc_kernel<TI, NMV>;                                                     \
         e = set_smem(k, tsmem);                                                                        \
         if (e != cudaSuccess) return e;                                                                \
-        k<<<tgrid, TcShape<NMV>::kThreads, tsmem, s>>>(ac, pool.tm_state2, pool.tm_logx2, nring, naux); \
+        cudaLaunchConfig_t cfg = {};                                                                   \
+        cudaLaunchAttribute attr[1];                                                                   \
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                               \
+        attr[0].val.programmaticStreamSerializationAllowed = 1;                                        \
+        cfg.gridDim = dim3(tgrid);                                                                     \
+        cfg.blockDim = dim3(TcShape<NMV>::kThreads);                                                   \
+        cfg.dynamicSmemBytes = tsmem;                                                                  \
+        cfg.stream = s;                                                                                \
+        cfg.attrs = attr;                                                                              \
+        cfg.numAttrs = 1;                                                                              \
+        e = cudaLaunchKernelEx(&cfg, k, ac, pool.tm_state2, pool.tm_logx2, nring, naux);               \
+        if (e != cudaSuccess) return e;                                                                \
     } while (0)
         if (bf) {
             if (NM == 16) SSM_TC(__nv_bfloat16, 16);
