@@ -14,6 +14,9 @@ Also measured in the same run, each in its own timed region:
     batch 512;
   * chunked prefill scan of 8 sequences x 2048 tokens (Mamba-2-130M-shaped
     layer: 24 heads of 64, dstate 128, bf16);
+  * launch cost at small batch: decode (batch 1, 8, 64) and replay verify +
+    commit (batch 8) issued call by call and as a replayed CUDA graph, with
+    the capture's own cost;
   * the oracle (CPU, fp64) on a bounded sample of the decode workload.
 
 Inputs are seeded synthetic data drawn on the device (x, B, C ~ N(0,1),
@@ -543,6 +546,85 @@ def bench_replay_plain_decode(torch, m, args):
     return out
 
 
+def bench_graph_small_batch(torch, m, args, batches=(1, 8, 64), steps=32):
+    """Launch cost at small batch: the same decode steps (and replay verify +
+    commit steps) issued call by call from Python, and captured once as a
+    CUDA graph of `steps` steps and replayed.  Device time per step with CUDA
+    events around the whole loop, so host issue gaps count; capture_ms is the
+    host time to capture and instantiate the graph."""
+    c = DEC
+    H, P, N, G = c["H"], c["P"], c["N"], c["G"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(SEED + 151 + 17 * args.rank)
+    A, D = head_params(torch, gen, H)
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    def timed(fn, reps=3):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return 1000.0 * best / steps
+
+    def measure(pool, body):
+        body(pool)  # first calls outside the capture
+        torch.cuda.synchronize()
+        eager_us = timed(lambda: body(pool))
+        g = torch.cuda.CUDAGraph()
+        t0 = time.perf_counter()
+        with torch.cuda.graph(g):
+            body(pool)
+        torch.cuda.synchronize()
+        capture_ms = 1000.0 * (time.perf_counter() - t0)
+        g.replay()
+        graph_us = timed(g.replay)
+        st, flags = m.ssm_pool_status(pool)
+        assert st == m.SSM_OK and flags == 0, f"graph bench raised device flags {flags}"
+        return dict(eager_us_per_step=eager_us, graph_us_per_step=graph_us, capture_ms=capture_ms,
+                    graph_speedup=eager_us / graph_us)
+
+    for R in batches:
+        slots = list(range(R))
+        x, dt, B, C = step_inputs(torch, gen, steps * R, H, P, G, N)
+        x, dt, B, C = (t.view(steps, R, *t.shape[1:]) for t in (x, dt, B, C))
+        y = torch.empty((steps, R, H, P), dtype=torch.bfloat16, device="cuda")
+        pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, m.SSM_MODE_COPY, 16, 1),
+                                R)
+
+        def decode(p):
+            for s in range(steps):
+                assert m.ssm_decode_step(p, slots, x[s], dt[s], B[s], C[s], A, D, y[s]) == m.SSM_OK
+
+        out[f"decode_b{R}"] = measure(pool, decode)
+        m.ssm_state_destroy(pool)
+        del x, dt, B, C, y
+
+    R, T1, W = 8, 9, 16
+    slots = list(range(R))
+    x, dt, B, C = step_inputs(torch, gen, steps * R, H, P, G, N, n_tok=T1)
+    x, dt, B, C = (t.view(steps, R, *t.shape[1:]) for t in (x, dt, B, C))
+    y = torch.empty((steps, R, T1, H, P), dtype=torch.bfloat16, device="cuda")
+    acc = torch.randint(0, T1, (steps, R), generator=gen, device="cuda", dtype=torch.int32)
+    pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, m.SSM_MODE_REPLAY, W, T1), R)
+
+    def verify(p):
+        for s in range(steps):
+            assert m.ssm_verify_replay(p, slots, T1, x[s], dt[s], B[s], C[s], A, D, y[s]) == m.SSM_OK
+            assert m.ssm_state_commit(p, slots, acc[s], False, A) == m.SSM_OK
+
+    out[f"replay_verify_commit_b{R}_T{T1 - 1}"] = measure(pool, verify)
+    m.ssm_state_destroy(pool)
+    out["config"] = dict(heads=H, headdim=P, dstate=N, groups=G, steps_per_graph=steps, verify_W=W,
+                         timing="best of 3 loops, CUDA events around the loop")
+    return out
+
+
 def cpu_baseline(budget_s=12.0):
     """The oracle (fp64, OpenMP over (request, head)) on a bounded sample of
     the decode workload: all 128 heads of a few requests for a few tokens."""
@@ -605,6 +687,8 @@ def run_case(args):
     elif args.case == "prefill_varlen":
         out = bench_prefill_varlen(torch, m, args)
         print(json.dumps({"case": "prefill_varlen", "ms": out["ms_per_wave"], "path": out["path"]}))
+    elif args.case == "graph":
+        print(json.dumps({"case": "graph", **bench_graph_small_batch(torch, m, args)}))
     else:
         raise SystemExit(f"unknown case {args.case}")
     return 0
@@ -658,7 +742,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extras", action="store_true", help="decode only (no verify / prefill / e2e / cpu)")
-    ap.add_argument("--case", choices=("decode", "verify", "prefill", "prefill_varlen"),
+    ap.add_argument("--case", choices=("decode", "verify", "prefill", "prefill_varlen", "graph"),
                     help="run one workload alone (for profiler captures)")
     ap.add_argument("--batch", type=int, default=0, help="batch / sequence count of --case")
     args = ap.parse_args()
@@ -695,6 +779,7 @@ def main():
         extras["prefill"] = bench_prefill(torch, m, args)
         extras["prefill_varlen"] = bench_prefill_varlen(torch, m, args)
         extras["replay_plain_decode_b256"] = bench_replay_plain_decode(torch, m, args)
+        extras["graph_small_batch"] = bench_graph_small_batch(torch, m, args)
         e2e = bench_decode_e2e(torch, m, args)
     else:
         e2e = None
