@@ -1095,8 +1095,13 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         (a.N * in_b) % 128 == 0) {
         NM = T1 <= 16 ? 16 : 32;
         if (NM > pool.cf_rows) NM = 0;
+        // The ring holds an even number of blocks: the two split groups take alternate blocks, so each
+        // slot then belongs to one group, which takes its blocks in order and has seen the slot's
+        // previous block land before it waits on the slot again (a parity wait cannot tell a phase two
+        // back from the one it waits for).
+        static_assert(kTcMaxRing % 2 == 0, "");
         for (int na = kTcMaxAux; NM && na >= 2 && !nring; na -= 2)
-            for (int nr = kTcMaxRing; nr >= 4; --nr) {
+            for (int nr = kTcMaxRing; nr >= 4; nr -= 2) {
                 const size_t b =
                     tc_smem_bytes(tc_layout(a.N, NM, a.P, in_b, a.wcap, a.t1max, a.cb_w, a.t1pad, !bf, nr, na));
                 if (b <= (size_t)max_smem) {
