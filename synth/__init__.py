@@ -138,3 +138,44 @@ def random_partition(seed: int, stream: int, L: int, max_parts: int = 8, allow_e
     if not allow_empty:
         parts = [q for q in parts if q > 0] or [L]
     return parts
+
+
+# ---------------------------------------------------------------------------
+# Gated delta rule (the second recurrence that unrolls as a decay plus a sum).
+# Distributions of its synthetic workloads:
+#   q, k   ~ N(0, 1) per key head, scaled to unit length (the layer normalizes
+#            them before the recurrence), then stored in the input dtype
+#   v      ~ N(0, 1)
+#   g      = -softplus(N(-2, 0.5)) * exp(U(0, 1.5))   (log of the gate, <= 0)
+#   beta   = sigmoid(N(0, 1))                          (writing strength)
+#   state  ~ N(0, 0.1)
+
+def gdn_tokens(seed: int, stream: int, n_tok: int, H: int, G: int, dk: int, dv: int, in_dtype: int = F32):
+    """Per-token gated-delta-rule inputs of one stream.
+
+    Returns (q [n_tok][G][dk], k [n_tok][G][dk], v [n_tok][H][dv], g [n_tok][H],
+    beta [n_tok][H]); q, k, v fp32 or bf16 bit patterns, g and beta fp32.
+    """
+    r = rng(seed, 7, stream)
+    q = r.standard_normal((n_tok, G, dk), dtype=np.float32)
+    k = r.standard_normal((n_tok, G, dk), dtype=np.float32)
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = r.standard_normal((n_tok, H, dv), dtype=np.float32)
+    sp = np.log1p(np.exp(r.normal(-2.0, 0.5, size=(n_tok, H))))
+    g = (-sp * np.exp(r.uniform(0.0, 1.5, size=(n_tok, H)))).astype(np.float32)
+    beta = (1.0 / (1.0 + np.exp(-r.standard_normal((n_tok, H))))).astype(np.float32)
+    return (_store(q, in_dtype), _store(k, in_dtype), _store(v, in_dtype), g, beta)
+
+
+def gdn_batch_tokens(seed: int, step: int, batch: int, n_tok: int, H: int, G: int, dk: int, dv: int,
+                     in_dtype: int = F32):
+    """Inputs of one batched gated-delta-rule step, shaped [batch][n_tok][...]."""
+    parts = [gdn_tokens(seed, step * 1_000_003 + r, n_tok, H, G, dk, dv, in_dtype) for r in range(batch)]
+    return tuple(np.stack([p[i] for p in parts]) for i in range(5))
+
+
+def gdn_init_state(seed: int, slot: int, H: int, dv: int, dk: int, std: float = 0.1) -> np.ndarray:
+    """Initial fp32 gated-delta-rule state of one slot, N(0, std), shaped [H][dv][dk]."""
+    r = rng(seed, 8, slot)
+    return (r.standard_normal((H, dv, dk), dtype=np.float32) * np.float32(std)).astype(np.float32)
