@@ -36,6 +36,8 @@ EXPORTS = (
     "ssm_verify_copy", "ssm_verify_replay", "ssm_state_commit", "ssm_pool_status", "ssm_last_path",
     "ssm_status_string", "ssm_pool_bytes", "ssm_verify_replay_static", "ssm_receipt_bytes", "ssm_receipt_encode",
     "ssm_receipt_decode", "ssm_state_checkpoint_receipt", "ssm_state_restore_receipt",
+    "ssm_gdn_init", "ssm_gdn_destroy", "ssm_gdn_reset", "ssm_gdn_decode_step", "ssm_gdn_verify_replay",
+    "ssm_gdn_commit", "ssm_gdn_gather", "ssm_gdn_slot_info", "ssm_gdn_status",
 )
 
 
@@ -71,6 +73,12 @@ class ssm_receipt(ctypes.Structure):
 SSM_STATE_SCHEMA_VERSION = 1
 
 
+class ssm_gdn_config(ctypes.Structure):
+    _fields_ = [("nheads", ctypes.c_int32), ("nkheads", ctypes.c_int32), ("dk", ctypes.c_int32),
+                ("dv", ctypes.c_int32), ("input_dtype", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libssmstate is not built ({LIB_PATH} missing); run "
@@ -104,6 +112,15 @@ def _load():
         "ssm_state_checkpoint_receipt": [V, I32, V, ctypes.POINTER(ssm_stream_identity), V, ctypes.c_size_t,
                                          ctypes.POINTER(ctypes.c_size_t), V],
         "ssm_state_restore_receipt": [V, I32, V, ctypes.c_size_t, ctypes.POINTER(ssm_stream_identity), V],
+        "ssm_gdn_init": [ctypes.POINTER(ssm_gdn_config), I32, V, V, ctypes.POINTER(V)],
+        "ssm_gdn_destroy": [V],
+        "ssm_gdn_reset": [V, P_I32, I32, V],
+        "ssm_gdn_decode_step": [V, I32, P_I32, V, V, V, V, V, V, V],
+        "ssm_gdn_verify_replay": [V, I32, I32, P_I32, V, V, V, V, V, V, V],
+        "ssm_gdn_commit": [V, I32, P_I32, V, I32, V],
+        "ssm_gdn_gather": [V, I32, P_I32, V, V],
+        "ssm_gdn_slot_info": [V, I32, P_I64, P_I32, ctypes.POINTER(U32), V],
+        "ssm_gdn_status": [V, ctypes.POINTER(U32), I32, V],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -398,3 +415,103 @@ def ssm_verify_replay_static(batch, n_tok, nheads, headdim, dstate, ngroups, win
         _dev(dt, "dt", tdt, batch * n_tok * H), _dev(B, "B", tin, batch * n_tok * G * N),
         _dev(C, "C", tin, batch * n_tok * G * N), _dev(A, "A", torch.float32, H), _dev(D, "D", torch.float32, H),
         _dev(y, "y", tin, batch * n_tok * H * P), _dev(flags, "flags", torch.int32, 1), _stream(stream))
+
+
+# ------------------------------------------------------------ gated delta rule
+
+@dataclass
+class GdnPool:
+    """Handle returned by ssm_gdn_init, with the config it was made with."""
+    handle: ctypes.c_void_p
+    cfg: ssm_gdn_config
+    n_slots: int
+
+    @property
+    def H(self):
+        return self.cfg.nheads
+
+    @property
+    def G(self):
+        return self.cfg.nkheads
+
+    @property
+    def dk(self):
+        return self.cfg.dk
+
+    @property
+    def dv(self):
+        return self.cfg.dv
+
+
+def make_gdn_config(nheads, nkheads, dk, dv, input_dtype=SSM_DTYPE_F32, window=16, max_tokens=9) -> ssm_gdn_config:
+    return ssm_gdn_config(nheads, nkheads, dk, dv, input_dtype, window, max_tokens)
+
+
+def ssm_gdn_init(cfg: ssm_gdn_config, n_slots: int, init_state=None, stream=None) -> GdnPool:
+    """Create a gated-delta-rule pool (raises SSMError on failure)."""
+    import torch
+    out = ctypes.c_void_p()
+    numel = n_slots * cfg.nheads * cfg.dv * cfg.dk
+    st = _lib.ssm_gdn_init(ctypes.byref(cfg), int(n_slots), _dev(init_state, "init_state", torch.float32, numel),
+                           _stream(stream), ctypes.byref(out))
+    _check(st, "ssm_gdn_init")
+    return GdnPool(out, cfg, int(n_slots))
+
+
+def ssm_gdn_destroy(pool: GdnPool) -> int:
+    return _lib.ssm_gdn_destroy(pool.handle)
+
+
+def ssm_gdn_reset(pool: GdnPool, slots, stream=None) -> int:
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_gdn_reset(pool.handle, psl, len(sl), _stream(stream))
+
+
+def _gdn_inputs(pool: GdnPool, n, q, k, v, g, beta, y):
+    import torch
+    tin = torch.bfloat16 if pool.cfg.input_dtype == SSM_DTYPE_BF16 else torch.float32
+    H, G, dk, dv = pool.H, pool.G, pool.dk, pool.dv
+    return (_dev(q, "q", tin, n * G * dk), _dev(k, "k", tin, n * G * dk), _dev(v, "v", tin, n * H * dv),
+            _dev(g, "g", torch.float32, n * H), _dev(beta, "beta", torch.float32, n * H),
+            _dev(y, "y", tin, n * H * dv))
+
+
+def ssm_gdn_decode_step(pool: GdnPool, slots, q, k, v, g, beta, y, stream=None) -> int:
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_gdn_decode_step(pool.handle, len(sl), psl, *_gdn_inputs(pool, len(sl), q, k, v, g, beta, y),
+                                    _stream(stream))
+
+
+def ssm_gdn_verify_replay(pool: GdnPool, slots, n_tok: int, q, k, v, g, beta, y, stream=None) -> int:
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_gdn_verify_replay(pool.handle, len(sl), int(n_tok), psl,
+                                      *_gdn_inputs(pool, len(sl) * n_tok, q, k, v, g, beta, y), _stream(stream))
+
+
+def ssm_gdn_commit(pool: GdnPool, slots, accept, force_fold: bool = False, stream=None) -> int:
+    import torch
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_gdn_commit(pool.handle, len(sl), psl, _dev(accept, "accept", torch.int32, len(sl)),
+                               1 if force_fold else 0, _stream(stream))
+
+
+def ssm_gdn_gather(pool: GdnPool, slots, dst, stream=None) -> int:
+    import torch
+    sl, psl = _host_i32(slots)
+    return _lib.ssm_gdn_gather(pool.handle, len(sl), psl,
+                               _dev(dst, "dst", torch.float32, len(sl) * pool.H * pool.dv * pool.dk),
+                               _stream(stream))
+
+
+def ssm_gdn_slot_info(pool: GdnPool, slot: int, stream=None):
+    """(status, position, log_len, flags) of one slot (synchronous)."""
+    pos, ll, fl = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_uint32()
+    st = _lib.ssm_gdn_slot_info(pool.handle, int(slot), ctypes.byref(pos), ctypes.byref(ll), ctypes.byref(fl),
+                                _stream(stream))
+    return st, int(pos.value), int(ll.value), int(fl.value)
+
+
+def ssm_gdn_status(pool: GdnPool, clear: bool = False, stream=None):
+    f = ctypes.c_uint32()
+    st = _lib.ssm_gdn_status(pool.handle, ctypes.byref(f), 1 if clear else 0, _stream(stream))
+    return st, int(f.value)

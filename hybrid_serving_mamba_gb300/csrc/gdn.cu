@@ -1,0 +1,784 @@
+// The gated delta rule with a replay log: in-place decode, ReplaySSM verify
+// and commit ("Why Speculative Decoding Slows Hybrid Mamba Models", When the
+// layer is a different kind of recurrence: the update must unroll as a decay
+// plus a sum, and Gated DeltaNet's does).  Per value head h, key head
+// g(h) = h / (H / G):
+//   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t q_t
+// with S fp32 [dv][dk].
+//
+// Every kernel here is bound by the state's bytes, and the state's rows are
+// independent: with the token's k, q and scalars fixed, row p of S_t depends
+// only on row p of S_{t-1} (w = S[p] . k, S[p] <- exp(g) S[p] + (beta v[p] -
+// exp(g) beta w) k), and row p of an output is S[p] . q.  So a warp streams
+// four rows at a time, eight lanes a row; lane s of a row holds the 16-byte
+// pieces n = 4 (s + 8 i) .. + 3 (i < dk / 32), so that each load instruction
+// of the warp covers four whole 128-byte lines, and a row's dot products take
+// three shuffles.
+//
+// Replay verify (The Fix: outputs from the checkpoint and the log, no state
+// written) unrolls the output at position m (the log's K tokens, then the
+// step tokens) as o_m = S_ckpt u_0 + sum_i beta_i (k_i . u_i) v_i, where
+// u_m = q_m and u_{i-1} = exp(g_i) (u_i - beta_i k_i (k_i . u_i)).  A
+// coefficient kernel walks those sweeps (a dk-vector per step token, one warp
+// each) and stages the step after the log; a streaming kernel then reads
+// each checkpoint row once for all step tokens.
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "ssm_gdn.h"
+#include "ssm_internal.cuh"
+
+namespace ssm {
+namespace {
+
+constexpr int kGdnMaxBatch = 1024;  // requests per launch: slot lists travel in kernel parameters
+constexpr int kGdnWarps = 8;
+constexpr int kGdnThreads = 32 * kGdnWarps;
+constexpr int kGdnMaxWindow = 32, kGdnMaxTokens = 32;
+constexpr int kGdnMaxLog = kGdnMaxWindow - 1 + kGdnMaxTokens;  // log entries a slot holds at most
+
+struct GdnArgs {
+    float *state;
+    void *log_k, *log_v;  // [slot][wcap][G][dk], [slot][wcap][H][dv], input dtype
+    float *log_g, *log_b; // [slot][wcap][H]
+    int32_t *log_len;
+    int64_t *position;
+    uint32_t *slot_flags, *flags;
+    float *uq, *cs;       // verify scratch: [request][H][t1max][dk], [request][H][t1max][wcap]
+    int32_t *fold_m;      // commit: tokens to fold per request of the launch (0: none)
+    const void *q, *k, *v;
+    const float *g, *beta;
+    void *y;
+    const int32_t *accept;
+    int H, G, hpg, dv, W, wcap, t1max, n_tok, batch, force_fold;
+    int32_t slots[kGdnMaxBatch];
+    int32_t ntok[kGdnMaxBatch];
+};
+
+__device__ __forceinline__ float red8(float v) {  // sum over the eight lanes of a row
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    return v;
+}
+
+__device__ __forceinline__ float red32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+__device__ __forceinline__ float4 axpy4(float al, float4 x, float c, float4 k) {  // al x + c k
+    return make_float4(fmaf(al, x.x, c * k.x), fmaf(al, x.y, c * k.y), fmaf(al, x.z, c * k.z),
+                       fmaf(al, x.w, c * k.w));
+}
+
+__device__ __forceinline__ void poison(const GdnArgs &a, int slot, uint32_t flag) {
+    atomicOr(a.flags, flag);
+    atomicOr(a.slot_flags + slot, kSlotPoisoned);
+}
+
+// ---------------------------------------------------------------------------- decode
+
+// One token per request, in place.  Grid (H, batch).
+template <int DK, typename TI>
+__global__ void __launch_bounds__(kGdnThreads) gdn_decode_kernel(const __grid_constant__ GdnArgs a) {
+    constexpr int NV = DK / 32;
+    __shared__ __align__(16) float sk[DK], sq[DK];
+    const int h = blockIdx.x, i = blockIdx.y, slot = a.slots[i], kh = h / a.hpg;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
+    if (a.slot_flags[slot] & kSlotPoisoned) {
+        if (tid == 0) atomicOr(a.flags, SSM_FLAG_POISONED_SLOT);
+        return;
+    }
+    if (a.log_len[slot] != 0) {  // the state in place is the checkpoint: tokens in the log would be lost
+        if (tid == 0) poison(a, slot, SSM_FLAG_LOG_NOT_EMPTY);
+        return;
+    }
+    const TI *qg = static_cast<const TI *>(a.q) + ((size_t)i * a.G + kh) * DK;
+    const TI *kg = static_cast<const TI *>(a.k) + ((size_t)i * a.G + kh) * DK;
+    const TI *vh = static_cast<const TI *>(a.v) + ((size_t)i * a.H + h) * a.dv;
+    const float gg = a.g[(size_t)i * a.H + h], bb = a.beta[(size_t)i * a.H + h];
+    bool bad = !(isfinite(gg) && isfinite(bb));
+    for (int n = tid; n < DK; n += kGdnThreads) {
+        sk[n] = to_f(kg[n]);
+        sq[n] = to_f(qg[n]);
+        bad |= !(isfinite(sk[n]) && isfinite(sq[n]));
+    }
+    for (int p = tid; p < a.dv; p += kGdnThreads) bad |= !isfinite(to_f(vh[p]));
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) poison(a, slot, SSM_FLAG_NONFINITE_INPUT);
+        return;
+    }
+    const float alpha = expf(gg), ab = alpha * bb;
+    float4 kr[NV], qr[NV];
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+        kr[e] = *reinterpret_cast<const float4 *>(sk + 4 * (s + 8 * e));
+        qr[e] = *reinterpret_cast<const float4 *>(sq + 4 * (s + 8 * e));
+    }
+    float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
+    TI *yh = static_cast<TI *>(a.y) + ((size_t)i * a.H + h) * a.dv;
+    // two row groups per step of the loop, their loads issued together
+    for (int p0 = 4 * warp; p0 < a.dv; p0 += 8 * kGdnWarps) {
+        const int pa = p0 + r, pb = p0 + 4 * kGdnWarps + r;
+        const bool hb = pb < a.dv;  // dv % 4 == 0: a group is whole or absent
+        float4 sa[NV], sb[NV];
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            sa[e] = ld_stream(st + (size_t)pa * DK + 4 * (s + 8 * e));
+            sb[e] = hb ? ld_stream(st + (size_t)pb * DK + 4 * (s + 8 * e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float wa = 0.f, wb = 0.f;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            wa += dot4(sa[e], kr[e]);
+            wb += dot4(sb[e], kr[e]);
+        }
+        wa = red8(wa);
+        wb = red8(wb);
+        const float ca = bb * to_f(vh[pa]) - ab * wa;
+        const float cb = hb ? bb * to_f(vh[pb]) - ab * wb : 0.f;
+        float oa = 0.f, ob = 0.f;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            sa[e] = axpy4(alpha, sa[e], ca, kr[e]);
+            sb[e] = axpy4(alpha, sb[e], cb, kr[e]);
+            oa += dot4(sa[e], qr[e]);
+            ob += dot4(sb[e], qr[e]);
+        }
+        oa = red8(oa);
+        ob = red8(ob);
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            st_stream(st + (size_t)pa * DK + 4 * (s + 8 * e), sa[e]);
+            if (hb) st_stream(st + (size_t)pb * DK + 4 * (s + 8 * e), sb[e]);
+        }
+        if (s == 0) {
+            yh[pa] = from_f<TI>(oa);
+            if (hb) yh[pb] = from_f<TI>(ob);
+        }
+    }
+    if (h == 0 && tid == 0) a.position[slot] += 1;
+}
+
+// ---------------------------------------------------------------------------- replay verify
+
+__host__ __device__ inline size_t gdn_coef_smem(int DK, int wcap, int t1max) {
+    return ((size_t)wcap * DK + (size_t)t1max * DK + 2 * (size_t)wcap) * sizeof(float);
+}
+
+// Grid (H, batch): checks and stages the step, then walks the sweeps.
+template <int DK, typename TI>
+__global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_constant__ GdnArgs a) {
+    constexpr int NL = DK / 32;  // this lane's contiguous piece of a dk-vector in a sweep
+    extern __shared__ __align__(16) float gsm[];
+    const int h = blockIdx.x, i = blockIdx.y, slot = a.slots[i], kh = h / a.hpg;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T1 = a.n_tok;
+    if (a.slot_flags[slot] & kSlotPoisoned) {
+        if (tid == 0) atomicOr(a.flags, SSM_FLAG_POISONED_SLOT);
+        return;
+    }
+    const int K = a.log_len[slot];
+    float *sk = gsm;                              // [K + T1][DK]: the log's keys, then the step's
+    float *sq = sk + (size_t)a.wcap * DK;         // [T1][DK]
+    float *sal = sq + (size_t)a.t1max * DK;       // [K + T1] exp(g)
+    float *sbe = sal + a.wcap;                    // [K + T1] beta
+    const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK;
+    for (int e = tid; e < K * DK; e += kGdnThreads) {
+        const int t = e / DK, n = e - t * DK;
+        sk[e] = to_f(lk[((size_t)t * a.G + kh) * DK + n]);
+    }
+    for (int t = tid; t < K; t += kGdnThreads) {
+        sal[t] = expf(a.log_g[((size_t)slot * a.wcap + t) * a.H + h]);
+        sbe[t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h];
+    }
+    const TI *qs = static_cast<const TI *>(a.q), *ks = static_cast<const TI *>(a.k);
+    const TI *vs = static_cast<const TI *>(a.v);
+    bool bad = false;
+    for (int e = tid; e < T1 * DK; e += kGdnThreads) {
+        const int j = e / DK, n = e - j * DK;
+        const size_t src = (((size_t)i * T1 + j) * a.G + kh) * DK + n;
+        const float kv = to_f(ks[src]), qv = to_f(qs[src]);
+        bad |= !(isfinite(kv) && isfinite(qv));
+        sk[(size_t)(K + j) * DK + n] = kv;
+        sq[(size_t)j * DK + n] = qv;
+    }
+    for (int j = tid; j < T1; j += kGdnThreads) {
+        const float gv = a.g[((size_t)i * T1 + j) * a.H + h], bv = a.beta[((size_t)i * T1 + j) * a.H + h];
+        bad |= !(isfinite(gv) && isfinite(bv));
+        sal[K + j] = expf(gv);
+        sbe[K + j] = bv;
+    }
+    for (int e = tid; e < T1 * a.dv; e += kGdnThreads) {
+        const int j = e / a.dv, p = e - j * a.dv;
+        bad |= !isfinite(to_f(vs[(((size_t)i * T1 + j) * a.H + h) * a.dv + p]));
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) poison(a, slot, SSM_FLAG_NONFINITE_INPUT);
+        return;
+    }
+    // the step after the log, for the commit: this head's v, g, beta; the key head's k from its first
+    // value head (the others read only the entries before K)
+    TI *lv = static_cast<TI *>(a.log_v);
+    for (int e = tid; e < T1 * a.dv; e += kGdnThreads) {
+        const int j = e / a.dv, p = e - j * a.dv;
+        lv[(((size_t)slot * a.wcap + K + j) * a.H + h) * a.dv + p] = vs[(((size_t)i * T1 + j) * a.H + h) * a.dv + p];
+    }
+    for (int j = tid; j < T1; j += kGdnThreads) {
+        a.log_g[((size_t)slot * a.wcap + K + j) * a.H + h] = a.g[((size_t)i * T1 + j) * a.H + h];
+        a.log_b[((size_t)slot * a.wcap + K + j) * a.H + h] = a.beta[((size_t)i * T1 + j) * a.H + h];
+    }
+    if (h % a.hpg == 0) {
+        TI *lkw = static_cast<TI *>(a.log_k);
+        for (int e = tid; e < T1 * DK; e += kGdnThreads) {
+            const int j = e / DK, n = e - j * DK;
+            lkw[(((size_t)slot * a.wcap + K + j) * a.G + kh) * DK + n] = ks[(((size_t)i * T1 + j) * a.G + kh) * DK + n];
+        }
+    }
+    // the sweeps: warp w takes step tokens j = w, w + 8, ...; lane l holds u[NL l .. NL l + NL - 1]
+    for (int j = warp; j < T1; j += kGdnWarps) {
+        const int mj = K + j + 1;
+        float u[NL];
+#pragma unroll
+        for (int e = 0; e < NL; ++e) u[e] = sq[(size_t)j * DK + NL * lane + e];
+        float *csj = a.cs + (((size_t)i * a.H + h) * a.t1max + j) * a.wcap;
+        for (int t = mj - 1; t >= 0; --t) {
+            const float *kt = sk + (size_t)t * DK + NL * lane;
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < NL; ++e) d = fmaf(kt[e], u[e], d);
+            d = red32(d);
+            const float bd = sbe[t] * d, al = sal[t];
+            if (lane == 0) csj[t] = bd;
+#pragma unroll
+            for (int e = 0; e < NL; ++e) u[e] = al * fmaf(-bd, kt[e], u[e]);
+        }
+        float *uqj = a.uq + (((size_t)i * a.H + h) * a.t1max + j) * DK + NL * lane;
+#pragma unroll
+        for (int e = 0; e < NL; ++e) uqj[e] = u[e];
+    }
+}
+
+__host__ __device__ inline size_t gdn_stream_smem(int DK, int wcap, int t1max) {
+    return ((size_t)t1max * DK + (size_t)t1max * wcap) * sizeof(float);
+}
+
+// Grid (H, batch): every checkpoint row is read once and gives the row's output for each step token:
+// o_j[p] = S[p] . u_j + sum_{t < K + j + 1} c_j[t] v_t[p].
+template <int DK, typename TI>
+__global__ void __launch_bounds__(kGdnThreads) gdn_stream_kernel(const __grid_constant__ GdnArgs a) {
+    constexpr int NV = DK / 32;
+    constexpr int NVL = (kGdnMaxLog + 7) / 8;  // logged values a lane takes per row (t = s + 8 c)
+    extern __shared__ __align__(16) float gsm[];
+    const int h = blockIdx.x, i = blockIdx.y, slot = a.slots[i];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
+    if (a.slot_flags[slot] & kSlotPoisoned) return;  // flagged by the coefficient kernel
+    const int T1 = a.n_tok, K = a.log_len[slot], m = K + T1;
+    float *suq = gsm;                        // [T1][DK]
+    float *scs = suq + (size_t)a.t1max * DK; // [T1][wcap]
+    const float *uq = a.uq + ((size_t)i * a.H + h) * a.t1max * DK;
+    const float *cs = a.cs + ((size_t)i * a.H + h) * a.t1max * a.wcap;
+    for (int e = tid; e < T1 * DK; e += kGdnThreads) suq[e] = uq[e];
+    for (int e = tid; e < T1 * a.wcap; e += kGdnThreads) {
+        const int j = e / a.wcap, t = e - j * a.wcap;
+        scs[e] = t < K + j + 1 ? cs[e] : 0.f;
+    }
+    __syncthreads();
+    const float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
+    const TI *lv = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
+    TI *y = static_cast<TI *>(a.y);
+    for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps) {
+        const int p = p0 + r;
+        float4 sv[NV];
+#pragma unroll
+        for (int e = 0; e < NV; ++e) sv[e] = ld_stream(st + (size_t)p * DK + 4 * (s + 8 * e));
+        float vv[NVL];
+#pragma unroll
+        for (int c = 0; c < NVL; ++c) {
+            const int t = s + 8 * c;
+            vv[c] = t < m ? to_f(lv[((size_t)t * a.H + h) * a.dv + p]) : 0.f;
+        }
+        for (int j = 0; j < T1; ++j) {
+            const float *uj = suq + (size_t)j * DK;
+            const float *cj = scs + (size_t)j * a.wcap;
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) acc += dot4(sv[e], *reinterpret_cast<const float4 *>(uj + 4 * (s + 8 * e)));
+#pragma unroll
+            for (int c = 0; c < NVL; ++c) {
+                const int t = s + 8 * c;
+                if (t < a.wcap) acc = fmaf(cj[t], vv[c], acc);  // zero past K + j
+            }
+            acc = red8(acc);
+            if (s == 0) y[(((size_t)i * T1 + j) * a.H + h) * a.dv + p] = from_f<TI>(acc);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------- commit and fold
+
+// One CTA: per request, append the kept tokens to the log or mark the request for a fold.
+__global__ void gdn_commit_kernel(const __grid_constant__ GdnArgs a) {
+    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
+        const int slot = a.slots[i];
+        a.fold_m[i] = 0;
+        if (a.slot_flags[slot] & kSlotPoisoned) {
+            atomicOr(a.flags, SSM_FLAG_POISONED_SLOT);
+            continue;
+        }
+        const int acc = a.accept[i];
+        if (acc < 0 || acc > a.ntok[i] - 1) {
+            poison(a, slot, SSM_FLAG_BAD_ACCEPT);
+            continue;
+        }
+        const int c = acc + 1, K = a.log_len[slot];
+        a.position[slot] += c;
+        if (K + c < a.W && !a.force_fold) {
+            a.log_len[slot] = K + c;
+        } else {
+            a.fold_m[i] = K + c;
+            a.log_len[slot] = 0;
+        }
+    }
+}
+
+__host__ __device__ inline size_t gdn_fold_smem(int DK, int dv, int wcap) {
+    return ((size_t)wcap * DK + (size_t)wcap * dv + 2 * (size_t)wcap) * sizeof(float);
+}
+
+// Grid (H, batch): the requests marked by the commit apply their M logged tokens to the checkpoint,
+// row by row, in order.
+template <int DK, typename TI>
+__global__ void __launch_bounds__(kGdnThreads) gdn_fold_kernel(const __grid_constant__ GdnArgs a) {
+    constexpr int NV = DK / 32;
+    extern __shared__ __align__(16) float gsm[];
+    const int h = blockIdx.x, i = blockIdx.y;
+    const int M = a.fold_m[i];
+    if (M == 0) return;
+    const int slot = a.slots[i], kh = h / a.hpg;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
+    float *sk = gsm;                          // [M][DK]
+    float *svv = sk + (size_t)a.wcap * DK;    // [M][dv]
+    float *sal = svv + (size_t)a.wcap * a.dv; // [M]
+    float *sbe = sal + a.wcap;                // [M]
+    const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK;
+    const TI *lv = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
+    for (int e = tid; e < M * DK; e += kGdnThreads) {
+        const int t = e / DK, n = e - t * DK;
+        sk[e] = to_f(lk[((size_t)t * a.G + kh) * DK + n]);
+    }
+    for (int e = tid; e < M * a.dv; e += kGdnThreads) {
+        const int t = e / a.dv, p = e - t * a.dv;
+        svv[e] = to_f(lv[((size_t)t * a.H + h) * a.dv + p]);
+    }
+    for (int t = tid; t < M; t += kGdnThreads) {
+        sal[t] = expf(a.log_g[((size_t)slot * a.wcap + t) * a.H + h]);
+        sbe[t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h];
+    }
+    __syncthreads();
+    float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
+    for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps) {
+        const int p = p0 + r;
+        float4 sv[NV];
+#pragma unroll
+        for (int e = 0; e < NV; ++e) sv[e] = ld_stream(st + (size_t)p * DK + 4 * (s + 8 * e));
+        for (int t = 0; t < M; ++t) {
+            const float *kt = sk + (size_t)t * DK;
+            float4 kr[NV];
+            float w = 0.f;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) {
+                kr[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
+                w += dot4(sv[e], kr[e]);
+            }
+            w = red8(w);
+            const float al = sal[t], be = sbe[t];
+            const float c = be * svv[(size_t)t * a.dv + p] - al * be * w;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) sv[e] = axpy4(al, sv[e], c, kr[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < NV; ++e) st_stream(st + (size_t)p * DK + 4 * (s + 8 * e), sv[e]);
+    }
+}
+
+// ---------------------------------------------------------------------------- reset and gather
+
+__global__ void gdn_reset_kernel(const __grid_constant__ GdnArgs a, size_t per_slot) {
+    const int slot = a.slots[blockIdx.y];
+    float4 *st = reinterpret_cast<float4 *>(a.state + (size_t)slot * per_slot);
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < per_slot / 4; e += (size_t)gridDim.x * blockDim.x)
+        st[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        a.log_len[slot] = 0;
+        a.position[slot] = 0;
+        a.slot_flags[slot] = 0u;
+    }
+}
+
+__global__ void gdn_gather_kernel(const __grid_constant__ GdnArgs a, size_t per_slot, float *dst) {
+    const int slot = a.slots[blockIdx.y];
+    const float4 *src = reinterpret_cast<const float4 *>(a.state + (size_t)slot * per_slot);
+    float4 *d = reinterpret_cast<float4 *>(dst + (size_t)blockIdx.y * per_slot);
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < per_slot / 4; e += (size_t)gridDim.x * blockDim.x)
+        d[e] = src[e];
+}
+
+}  // namespace
+}  // namespace ssm
+
+// ---------------------------------------------------------------------------- host: the pool
+
+struct ssm_gdn_pool_s {
+    ssm_gdn_config cfg{};
+    int n_slots = 0, device = 0, wcap = 0, in_b = 4, scratch_rows = 0;
+    size_t per_slot = 0;  // floats of one slot's state
+    float *state = nullptr;
+    void *log_k = nullptr, *log_v = nullptr;
+    float *log_g = nullptr, *log_b = nullptr, *uq = nullptr, *cs = nullptr;
+    int32_t *log_len = nullptr, *fold_m = nullptr;
+    int64_t *position = nullptr;
+    uint32_t *slot_flags = nullptr, *flags = nullptr;
+    std::vector<int> pending_ntok;  // tokens of each slot's last verify (0: none since its commit)
+};
+
+namespace ssm {
+namespace {
+
+struct GdnDevice {  // the pool's device current for the call, the caller's restored after
+    int prev = -1;
+    explicit GdnDevice(int dev) {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    }
+    ~GdnDevice() {
+        int now = -1;
+        if (prev >= 0 && cudaGetDevice(&now) == cudaSuccess && now != prev) cudaSetDevice(prev);
+    }
+};
+
+ssm_status gdn_cuda(cudaError_t e) { return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA; }
+
+void gdn_free(ssm_gdn_pool_s *p) {
+    void *bufs[] = {p->state, p->log_k, p->log_v, p->log_g, p->log_b, p->uq, p->cs,
+                    p->log_len, p->fold_m, p->position, p->slot_flags, p->flags};
+    for (void *b : bufs)
+        if (b) cudaFree(b);
+}
+
+template <typename T>
+cudaError_t gdn_alloc(T **ptr, size_t count) {
+    return cudaMalloc(reinterpret_cast<void **>(ptr), std::max<size_t>(count, 1) * sizeof(T));
+}
+
+GdnArgs gdn_args(const ssm_gdn_pool_s &p) {
+    GdnArgs a;
+    std::memset(&a, 0, offsetof(GdnArgs, slots));
+    a.state = p.state;
+    a.log_k = p.log_k;
+    a.log_v = p.log_v;
+    a.log_g = p.log_g;
+    a.log_b = p.log_b;
+    a.log_len = p.log_len;
+    a.position = p.position;
+    a.slot_flags = p.slot_flags;
+    a.flags = p.flags;
+    a.uq = p.uq;
+    a.cs = p.cs;
+    a.fold_m = p.fold_m;
+    a.H = p.cfg.nheads;
+    a.G = p.cfg.nkheads;
+    a.hpg = p.cfg.nheads / p.cfg.nkheads;
+    a.dv = p.cfg.dv;
+    a.W = p.cfg.window;
+    a.wcap = p.wcap;
+    a.t1max = p.cfg.max_tokens;
+    return a;
+}
+
+ssm_status gdn_check_slots(const ssm_gdn_pool_s *p, const int32_t *slots, int n) {
+    if (!slots || n < 1) return SSM_ERR_INVALID_ARG;
+    std::vector<char> seen((size_t)p->n_slots, 0);
+    for (int i = 0; i < n; ++i) {
+        const int s = slots[i];
+        if (s < 0 || s >= p->n_slots || seen[(size_t)s]) return SSM_ERR_INVALID_ARG;
+        seen[(size_t)s] = 1;
+    }
+    return SSM_OK;
+}
+
+template <typename Kernel>
+cudaError_t gdn_smem(Kernel k, size_t bytes) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// dk and the input type as template arguments
+#define GDN_DISPATCH(p, ...)                                                                   \
+    do {                                                                                       \
+        if ((p).cfg.dk == 128) {                                                               \
+            constexpr int DK = 128;                                                            \
+            if ((p).in_b == 2) { using TI = __nv_bfloat16; __VA_ARGS__; }                      \
+            else { using TI = float; __VA_ARGS__; }                                            \
+        } else {                                                                               \
+            constexpr int DK = 64;                                                             \
+            if ((p).in_b == 2) { using TI = __nv_bfloat16; __VA_ARGS__; }                      \
+            else { using TI = float; __VA_ARGS__; }                                            \
+        }                                                                                      \
+    } while (0)
+
+// Run fn(args, first request, count) over launches of at most kGdnMaxBatch requests.
+template <typename Fn>
+ssm_status gdn_batches(const ssm_gdn_pool_s &p, const int32_t *slots, int batch, Fn fn) {
+    GdnArgs a = gdn_args(p);
+    for (int base = 0; base < batch; base += kGdnMaxBatch) {
+        const int m = std::min(batch - base, kGdnMaxBatch);
+        a.batch = m;
+        for (int i = 0; i < m; ++i) a.slots[i] = slots[base + i];
+        const cudaError_t e = fn(a, base, m);
+        if (e != cudaSuccess) return gdn_cuda(e);
+    }
+    return SSM_OK;
+}
+
+}  // namespace
+}  // namespace ssm
+
+using ssm::GdnArgs;
+
+extern "C" {
+
+ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float *init_state, ssm_stream_t stream,
+                        ssm_gdn_pool *out) {
+    if (!cfg || !out || n_slots < 1) return SSM_ERR_INVALID_ARG;
+    const ssm_gdn_config c = *cfg;
+    if (c.nheads < 1 || c.nkheads < 1 || c.nheads % c.nkheads || (c.dk != 64 && c.dk != 128) || c.dv < 4 ||
+        c.dv > 256 || c.dv % 4 || (c.input_dtype != SSM_DTYPE_F32 && c.input_dtype != SSM_DTYPE_BF16) ||
+        c.window < 1 || c.window > ssm::kGdnMaxWindow || c.max_tokens < 1 || c.max_tokens > ssm::kGdnMaxTokens)
+        return SSM_ERR_INVALID_ARG;
+    auto *p = new (std::nothrow) ssm_gdn_pool_s();
+    if (!p) return SSM_ERR_NO_MEMORY;
+    p->cfg = c;
+    p->n_slots = n_slots;
+    p->wcap = c.window - 1 + c.max_tokens;
+    p->in_b = c.input_dtype == SSM_DTYPE_BF16 ? 2 : 4;
+    p->per_slot = (size_t)c.nheads * c.dv * c.dk;
+    p->scratch_rows = std::min(n_slots, ssm::kGdnMaxBatch);
+    p->pending_ntok.assign((size_t)n_slots, 0);
+    cudaGetDevice(&p->device);
+    const size_t ns = (size_t)n_slots, H = (size_t)c.nheads, G = (size_t)c.nkheads, W = (size_t)p->wcap;
+    const size_t sr = (size_t)p->scratch_rows, T = (size_t)c.max_tokens;
+    cudaError_t e = ssm::gdn_alloc(&p->state, ns * p->per_slot);
+    if (e == cudaSuccess) e = cudaMalloc(&p->log_k, ns * W * G * c.dk * p->in_b);
+    if (e == cudaSuccess) e = cudaMalloc(&p->log_v, ns * W * H * c.dv * p->in_b);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_g, ns * W * H);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_b, ns * W * H);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->uq, sr * H * T * c.dk);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->cs, sr * H * T * W);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_len, ns);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->fold_m, (size_t)ssm::kGdnMaxBatch);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->position, ns);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->slot_flags, ns);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->flags, 1);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (e == cudaSuccess) {
+        e = init_state ? cudaMemcpyAsync(p->state, init_state, ns * p->per_slot * sizeof(float),
+                                         cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(p->state, 0, ns * p->per_slot * sizeof(float), s);
+    }
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->log_len, 0, ns * sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->fold_m, 0, ssm::kGdnMaxBatch * sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->position, 0, ns * sizeof(int64_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->slot_flags, 0, ns * sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->flags, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        ssm::gdn_free(p);
+        delete p;
+        return e == cudaErrorMemoryAllocation ? SSM_ERR_NO_MEMORY : SSM_ERR_CUDA;
+    }
+    *out = p;
+    return SSM_OK;
+}
+
+ssm_status ssm_gdn_destroy(ssm_gdn_pool pool) {
+    if (!pool) return SSM_ERR_INVALID_ARG;
+    ssm::GdnDevice g(pool->device);
+    cudaDeviceSynchronize();
+    ssm::gdn_free(pool);
+    delete pool;
+    return SSM_OK;
+}
+
+ssm_status ssm_gdn_reset(ssm_gdn_pool pool, const int32_t *slots, int32_t n, ssm_stream_t stream) {
+    if (!pool) return SSM_ERR_INVALID_ARG;
+    ssm_status st = ssm::gdn_check_slots(pool, slots, n);
+    if (st != SSM_OK) return st;
+    ssm::GdnDevice g(pool->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t per_slot = pool->per_slot;
+    st = ssm::gdn_batches(*pool, slots, n, [&](const GdnArgs &a, int, int m) {
+        ssm::gdn_reset_kernel<<<dim3(16, m), 256, 0, s>>>(a, per_slot);
+        return cudaGetLastError();
+    });
+    if (st == SSM_OK)
+        for (int i = 0; i < n; ++i) pool->pending_ntok[(size_t)slots[i]] = 0;
+    return st;
+}
+
+ssm_status ssm_gdn_gather(ssm_gdn_pool pool, int32_t n, const int32_t *slots, float *dst, ssm_stream_t stream) {
+    if (!pool || !dst) return SSM_ERR_INVALID_ARG;
+    ssm_status st = ssm::gdn_check_slots(pool, slots, n);
+    if (st != SSM_OK) return st;
+    ssm::GdnDevice g(pool->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t per_slot = pool->per_slot;
+    return ssm::gdn_batches(*pool, slots, n, [&](const GdnArgs &a, int base, int m) {
+        ssm::gdn_gather_kernel<<<dim3(16, m), 256, 0, s>>>(a, per_slot, dst + (size_t)base * per_slot);
+        return cudaGetLastError();
+    });
+}
+
+ssm_status ssm_gdn_decode_step(ssm_gdn_pool pool, int32_t batch, const int32_t *slots, const void *q,
+                               const void *k, const void *v, const float *g, const float *beta, void *y,
+                               ssm_stream_t stream) {
+    if (!pool || !q || !k || !v || !g || !beta || !y) return SSM_ERR_INVALID_ARG;
+    ssm_status st = ssm::gdn_check_slots(pool, slots, batch);
+    if (st != SSM_OK) return st;
+    ssm::GdnDevice dg(pool->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const ssm_gdn_pool_s &p = *pool;
+    const size_t G = (size_t)p.cfg.nkheads, H = (size_t)p.cfg.nheads, dk = (size_t)p.cfg.dk, dv = (size_t)p.cfg.dv;
+    const size_t ib = (size_t)p.in_b;
+    st = ssm::gdn_batches(p, slots, batch, [&](GdnArgs &a, int base, int m) {
+        const size_t b0 = (size_t)base;
+        a.q = static_cast<const char *>(q) + b0 * G * dk * ib;
+        a.k = static_cast<const char *>(k) + b0 * G * dk * ib;
+        a.v = static_cast<const char *>(v) + b0 * H * dv * ib;
+        a.g = g + b0 * H;
+        a.beta = beta + b0 * H;
+        a.y = static_cast<char *>(y) + b0 * H * dv * ib;
+        cudaError_t e = cudaSuccess;
+        GDN_DISPATCH(p, { ssm::gdn_decode_kernel<DK, TI><<<dim3((unsigned)H, m), ssm::kGdnThreads, 0, s>>>(a); });
+        e = cudaGetLastError();
+        return e;
+    });
+    if (st == SSM_OK)
+        for (int i = 0; i < batch; ++i) pool->pending_ntok[(size_t)slots[i]] = 0;
+    return st;
+}
+
+ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok, const int32_t *slots,
+                                 const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                 void *y, ssm_stream_t stream) {
+    if (!pool || !q || !k || !v || !g || !beta || !y) return SSM_ERR_INVALID_ARG;
+    if (n_tok < 1 || n_tok > pool->cfg.max_tokens) return SSM_ERR_INVALID_ARG;
+    ssm_status st = ssm::gdn_check_slots(pool, slots, batch);
+    if (st != SSM_OK) return st;
+    ssm::GdnDevice dg(pool->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const ssm_gdn_pool_s &p = *pool;
+    const size_t G = (size_t)p.cfg.nkheads, H = (size_t)p.cfg.nheads, dk = (size_t)p.cfg.dk, dv = (size_t)p.cfg.dv;
+    const size_t ib = (size_t)p.in_b, T = (size_t)n_tok;
+    const size_t csm = ssm::gdn_coef_smem(p.cfg.dk, p.wcap, p.cfg.max_tokens);
+    const size_t ssm_ = ssm::gdn_stream_smem(p.cfg.dk, p.wcap, p.cfg.max_tokens);
+    st = ssm::gdn_batches(p, slots, batch, [&](GdnArgs &a, int base, int m) {
+        const size_t b0 = (size_t)base;
+        a.n_tok = n_tok;
+        a.q = static_cast<const char *>(q) + b0 * T * G * dk * ib;
+        a.k = static_cast<const char *>(k) + b0 * T * G * dk * ib;
+        a.v = static_cast<const char *>(v) + b0 * T * H * dv * ib;
+        a.g = g + b0 * T * H;
+        a.beta = beta + b0 * T * H;
+        a.y = static_cast<char *>(y) + b0 * T * H * dv * ib;
+        cudaError_t e = cudaSuccess;
+        GDN_DISPATCH(p, {
+            auto kc = ssm::gdn_coef_kernel<DK, TI>;
+            auto ks = ssm::gdn_stream_kernel<DK, TI>;
+            e = ssm::gdn_smem(kc, csm);
+            if (e == cudaSuccess) e = ssm::gdn_smem(ks, ssm_);
+            if (e == cudaSuccess) {
+                kc<<<dim3((unsigned)H, m), ssm::kGdnThreads, csm, s>>>(a);
+                ks<<<dim3((unsigned)H, m), ssm::kGdnThreads, ssm_, s>>>(a);
+                e = cudaGetLastError();
+            }
+        });
+        return e;
+    });
+    if (st == SSM_OK)
+        for (int i = 0; i < batch; ++i) pool->pending_ntok[(size_t)slots[i]] = n_tok;
+    return st;
+}
+
+ssm_status ssm_gdn_commit(ssm_gdn_pool pool, int32_t batch, const int32_t *slots, const int32_t *accept,
+                          int32_t force_fold, ssm_stream_t stream) {
+    if (!pool || !accept) return SSM_ERR_INVALID_ARG;
+    ssm_status st = ssm::gdn_check_slots(pool, slots, batch);
+    if (st != SSM_OK) return st;
+    for (int i = 0; i < batch; ++i)
+        if (pool->pending_ntok[(size_t)slots[i]] < 1) return SSM_ERR_INVALID_STATE;
+    ssm::GdnDevice dg(pool->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const ssm_gdn_pool_s &p = *pool;
+    const size_t fsm = ssm::gdn_fold_smem(p.cfg.dk, p.cfg.dv, p.wcap);
+    const unsigned H = (unsigned)p.cfg.nheads;
+    st = ssm::gdn_batches(p, slots, batch, [&](GdnArgs &a, int base, int m) {
+        a.accept = accept + base;
+        a.force_fold = force_fold ? 1 : 0;
+        for (int i = 0; i < m; ++i) a.ntok[i] = pool->pending_ntok[(size_t)slots[base + i]];
+        ssm::gdn_commit_kernel<<<1, 1024, 0, s>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        GDN_DISPATCH(p, {
+            auto kf = ssm::gdn_fold_kernel<DK, TI>;
+            e = ssm::gdn_smem(kf, fsm);
+            if (e == cudaSuccess) {
+                kf<<<dim3(H, m), ssm::kGdnThreads, fsm, s>>>(a);
+                e = cudaGetLastError();
+            }
+        });
+        return e;
+    });
+    if (st == SSM_OK)
+        for (int i = 0; i < batch; ++i) pool->pending_ntok[(size_t)slots[i]] = 0;
+    return st;
+}
+
+ssm_status ssm_gdn_slot_info(ssm_gdn_pool pool, int32_t slot, int64_t *position, int32_t *log_len,
+                             uint32_t *flags, ssm_stream_t stream) {
+    if (!pool || slot < 0 || slot >= pool->n_slots) return SSM_ERR_INVALID_ARG;
+    ssm::GdnDevice dg(pool->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int64_t pos = 0;
+    int32_t ll = 0;
+    uint32_t fl = 0;
+    cudaError_t e = cudaMemcpyAsync(&pos, pool->position + slot, sizeof(pos), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&ll, pool->log_len + slot, sizeof(ll), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&fl, pool->slot_flags + slot, sizeof(fl), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return SSM_ERR_CUDA;
+    if (position) *position = pos;
+    if (log_len) *log_len = ll;
+    if (flags) *flags = fl;
+    return SSM_OK;
+}
+
+ssm_status ssm_gdn_status(ssm_gdn_pool pool, uint32_t *flags_out, int32_t clear, ssm_stream_t stream) {
+    if (!pool || !flags_out) return SSM_ERR_INVALID_ARG;
+    ssm::GdnDevice dg(pool->device);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t f = 0;
+    cudaError_t e = cudaMemcpyAsync(&f, pool->flags, sizeof(f), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(pool->flags, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return SSM_ERR_CUDA;
+    *flags_out = f;
+    return SSM_OK;
+}
+
+}  // extern "C"
