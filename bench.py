@@ -17,6 +17,9 @@ Also measured in the same run, each in its own timed region:
   * launch cost at small batch: decode (batch 1, 8, 64) and replay verify +
     commit (batch 8) issued call by call and as a replayed CUDA graph, with
     the capture's own cost;
+  * a gated-delta-rule layer (32 value heads, 16 key heads, 128 x 128 state
+    per head, batch 256): in-place decode, the replay pool used for plain
+    decode, and replay verify + commit with 8 drafts;
   * the oracle (CPU, fp64) on a bounded sample of the decode workload.
 
 Inputs are seeded synthetic data drawn on the device (x, B, C ~ N(0,1),
@@ -53,6 +56,8 @@ DEC = dict(H=128, P=64, N=128, G=8, R=256, tokens=64)
 VER = dict(H=128, P=64, N=128, G=8, R=512, T=8, p=0.8, W=16, steps=32)
 # prefill workload (Mamba-2-130M-shaped layer)
 PRE = dict(H=24, P=64, N=128, G=1, R=8, L=2048)
+# gated delta rule layer: 32 value heads, 16 key heads, 128 x 128 fp32 state per head (2 MiB a request)
+GDN = dict(H=32, G=16, dk=128, dv=128, R=256, tokens=64, T=8, p=0.8, W=16, steps=32)
 
 
 def algorithmic_bytes_decode(R, H, P, N, G, in_b=2):
@@ -546,6 +551,111 @@ def bench_replay_plain_decode(torch, m, args):
     return out
 
 
+def gdn_inputs(torch, gen, n, H, G, dk, dv, n_tok=None):
+    """q, k (unit length per key head), v in bf16; g = log gate and beta in fp32."""
+    lead = (n,) if n_tok is None else (n, n_tok)
+    q = torch.nn.functional.normalize(torch.randn(lead + (G, dk), generator=gen, device="cuda"), dim=-1)
+    k = torch.nn.functional.normalize(torch.randn(lead + (G, dk), generator=gen, device="cuda"), dim=-1)
+    v = torch.randn(lead + (H, dv), generator=gen, device="cuda")
+    sp = torch.nn.functional.softplus(torch.randn(lead + (H,), generator=gen, device="cuda") * 0.5 - 2.0)
+    g = -sp * torch.exp(torch.rand(lead + (H,), generator=gen, device="cuda") * 1.5)
+    beta = torch.sigmoid(torch.randn(lead + (H,), generator=gen, device="cuda"))
+    return (q.bfloat16().contiguous(), k.bfloat16().contiguous(), v.bfloat16().contiguous(), g.contiguous(),
+            beta.contiguous())
+
+
+def algorithmic_bytes_gdn_decode(R, H, G, dk, dv, in_b=2):
+    """State read + write, the token's q, k, v, g, beta and the output y, per step of R requests."""
+    return R * (2 * H * dv * dk * 4 + 2 * G * dk * in_b + H * dv * in_b + 2 * H * 4 + H * dv * in_b)
+
+
+def bench_gdn(torch, m, args):
+    """Gated delta rule layer: in-place decode (tok/s, HBM roofline), the replay
+    pool used for plain decode (verify of one token + commit, window W), and
+    speculative verify + commit with T drafts, each in its own timed region."""
+    c = GDN
+    H, G, dk, dv, R, T = c["H"], c["G"], c["dk"], c["dv"], c["R"], c["tokens"]
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(SEED + 171 + 17 * args.rank)
+    stream = torch.cuda.current_stream()
+    q, k, v, g, beta = gdn_inputs(torch, gen, T * R, H, G, dk, dv)
+    q, k, v, g, beta = (t.view(T, R, *t.shape[1:]) for t in (q, k, v, g, beta))
+    y = torch.empty((R, H, dv), dtype=torch.bfloat16, device="cuda")
+    slots = list(range(R))
+    zeros = torch.zeros(R, dtype=torch.int32, device="cuda")
+    out = {}
+
+    def new_pool(W, T1, n):
+        init = (torch.randn((n, H, dv, dk), generator=gen, device="cuda") * 0.1).contiguous()
+        p = m.ssm_gdn_init(m.make_gdn_config(H, G, dk, dv, m.SSM_DTYPE_BF16, W, T1), n, init)
+        del init
+        return p
+
+    def timed(fn, n):
+        fn(min(n, 8))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn(n)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 1000.0 * e0.elapsed_time(e1) / n
+
+    # in place
+    pool = new_pool(c["W"], 1, R)
+
+    def decode(n):
+        for t in range(n):
+            assert m.ssm_gdn_decode_step(pool, slots, q[t % T], k[t % T], v[t % T], g[t % T], beta[t % T], y,
+                                         stream=stream) == m.SSM_OK
+    us = timed(decode, T)
+    alg = algorithmic_bytes_gdn_decode(R, H, G, dk, dv)
+    out["decode"] = dict(us_per_step=us, tok_per_s=R / (us / 1e6), achieved_gbs=alg / (us / 1e6) / 1e9,
+                         algorithmic_bytes=alg)
+    assert m.ssm_gdn_status(pool)[1] == 0
+    m.ssm_gdn_destroy(pool)
+
+    # replay pool used for plain decode
+    pool = new_pool(c["W"], 1, R)
+    yr = torch.empty((R, 1, H, dv), dtype=torch.bfloat16, device="cuda")
+
+    def replay(n):
+        for t in range(n):
+            i = t % T
+            assert m.ssm_gdn_verify_replay(pool, slots, 1, q[i], k[i], v[i], g[i], beta[i], yr,
+                                           stream=stream) == m.SSM_OK
+            assert m.ssm_gdn_commit(pool, slots, zeros, stream=stream) == m.SSM_OK
+    out["replay_plain_decode_us_per_step"] = timed(replay, T)
+    out["replay_speedup_over_decode"] = out["decode"]["us_per_step"] / out["replay_plain_decode_us_per_step"]
+    assert m.ssm_gdn_status(pool)[1] == 0
+    m.ssm_gdn_destroy(pool)
+    del q, k, v, g, beta
+
+    # speculative verify + commit, T drafts
+    T1, S = c["T"] + 1, c["steps"]
+    pool = new_pool(c["W"], T1, R)
+    qs, ks, vs, gs, bs = gdn_inputs(torch, gen, 4 * R, H, G, dk, dv, n_tok=T1)
+    qs, ks, vs, gs, bs = (t.view(4, R, *t.shape[1:]) for t in (qs, ks, vs, gs, bs))
+    hits = torch.rand((S, R, c["T"]), generator=gen, device="cuda") < c["p"]
+    acc = torch.where(hits.all(dim=2), torch.full((S, R), c["T"], device="cuda"),
+                      (~hits).int().argmax(dim=2)).int().contiguous()
+    yv = torch.empty((R, T1, H, dv), dtype=torch.bfloat16, device="cuda")
+
+    def verify(n):
+        for t in range(n):
+            i = t % 4
+            assert m.ssm_gdn_verify_replay(pool, slots, T1, qs[i], ks[i], vs[i], gs[i], bs[i], yv,
+                                           stream=stream) == m.SSM_OK
+            assert m.ssm_gdn_commit(pool, slots, acc[t % S], stream=stream) == m.SSM_OK
+    out["replay_verify_us_per_step"] = timed(verify, S)
+    out["replay_verify_over_decode"] = out["replay_verify_us_per_step"] / out["decode"]["us_per_step"]
+    assert m.ssm_gdn_status(pool)[1] == 0
+    m.ssm_gdn_destroy(pool)
+    out["config"] = dict(batch=R, value_heads=H, key_heads=G, dk=dk, dv=dv, W=c["W"], T=c["T"], p=c["p"],
+                         decode_tokens=T, verify_steps=S, dtype="bf16 q/k/v, fp32 g/beta/state")
+    return out
+
+
 def bench_graph_small_batch(torch, m, args, batches=(1, 8, 64), steps=32):
     """Launch cost at small batch: the same decode steps (and replay verify +
     commit steps) issued call by call from Python, and captured once as a
@@ -689,6 +799,9 @@ def run_case(args):
         print(json.dumps({"case": "prefill_varlen", "ms": out["ms_per_wave"], "path": out["path"]}))
     elif args.case == "graph":
         print(json.dumps({"case": "graph", **bench_graph_small_batch(torch, m, args)}))
+    elif args.case == "gdn":
+        GDN["R"] = args.batch or GDN["R"]
+        print(json.dumps({"case": "gdn", **bench_gdn(torch, m, args)}))
     else:
         raise SystemExit(f"unknown case {args.case}")
     return 0
@@ -742,7 +855,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extras", action="store_true", help="decode only (no verify / prefill / e2e / cpu)")
-    ap.add_argument("--case", choices=("decode", "verify", "prefill", "prefill_varlen", "graph"),
+    ap.add_argument("--case", choices=("decode", "verify", "prefill", "prefill_varlen", "graph", "gdn"),
                     help="run one workload alone (for profiler captures)")
     ap.add_argument("--batch", type=int, default=0, help="batch / sequence count of --case")
     args = ap.parse_args()
@@ -780,6 +893,7 @@ def main():
         extras["prefill_varlen"] = bench_prefill_varlen(torch, m, args)
         extras["replay_plain_decode_b256"] = bench_replay_plain_decode(torch, m, args)
         extras["graph_small_batch"] = bench_graph_small_batch(torch, m, args)
+        extras["gdn_b256"] = bench_gdn(torch, m, args)
         e2e = bench_decode_e2e(torch, m, args)
     else:
         e2e = None

@@ -36,7 +36,6 @@ constexpr int kGdnMaxBatch = 1024;  // requests per launch: slot lists travel in
 constexpr int kGdnWarps = 8;
 constexpr int kGdnThreads = 32 * kGdnWarps;
 constexpr int kGdnMaxWindow = 32, kGdnMaxTokens = 32;
-constexpr int kGdnMaxLog = kGdnMaxWindow - 1 + kGdnMaxTokens;  // log entries a slot holds at most
 
 struct GdnArgs {
     float *state;
@@ -63,14 +62,27 @@ __device__ __forceinline__ float red8(float v) {  // sum over the eight lanes of
     return v;
 }
 
-__device__ __forceinline__ float red32(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
     return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+// x . y accumulated in a pair of partial sums with the two-wide FMA (half the instructions)
+__device__ __forceinline__ float2 dot4x2(float4 x, float4 y, float2 acc) {
+    acc = ffma2(make_float2(x.x, x.y), make_float2(y.x, y.y), acc);
+    return ffma2(make_float2(x.z, x.w), make_float2(y.z, y.w), acc);
+}
+
+// x + c k with the two-wide FMA
+__device__ __forceinline__ float4 add_ck4(float4 x, float c, float4 k) {
+    const float2 lo = ffma2(make_float2(c, c), make_float2(k.x, k.y), make_float2(x.x, x.y));
+    const float2 hi = ffma2(make_float2(c, c), make_float2(k.z, k.w), make_float2(x.z, x.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+__device__ __forceinline__ float4 scale4(float c, float4 x) {
+    const float2 lo = ffma2(make_float2(c, c), make_float2(x.x, x.y), make_float2(0.f, 0.f));
+    const float2 hi = ffma2(make_float2(c, c), make_float2(x.z, x.w), make_float2(0.f, 0.f));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __device__ __forceinline__ float4 axpy4(float al, float4 x, float c, float4 k) {  // al x + c k
@@ -83,11 +95,41 @@ __device__ __forceinline__ void poison(const GdnArgs &a, int slot, uint32_t flag
     atomicOr(a.slot_flags + slot, kSlotPoisoned);
 }
 
+// A warp holds kRG groups of four rows at once (rows p0 + 32 kGdnWarps... apart), so that 8 KiB of
+// loads are in flight per warp; rows past dv are skipped (dv is a multiple of 4: a group is whole or
+// absent).
+constexpr int kRG = 4;
+
+template <int NV>
+__device__ __forceinline__ void load_rows(const float *st, int DK, int dv, int p0, int r, int s, int (&pr)[kRG],
+                                          bool (&ok)[kRG], float4 (&sv)[kRG][NV]) {
+#pragma unroll
+    for (int q = 0; q < kRG; ++q) {
+        pr[q] = p0 + 4 * kGdnWarps * q + r;
+        ok[q] = pr[q] < dv;
+    }
+#pragma unroll
+    for (int q = 0; q < kRG; ++q)
+#pragma unroll
+        for (int e = 0; e < NV; ++e)
+            sv[q][e] = ok[q] ? ld_stream(st + (size_t)pr[q] * DK + 4 * (s + 8 * e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <int NV>
+__device__ __forceinline__ void store_rows(float *st, int DK, const int (&pr)[kRG], const bool (&ok)[kRG], int s,
+                                           const float4 (&sv)[kRG][NV]) {
+#pragma unroll
+    for (int q = 0; q < kRG; ++q)
+        if (ok[q])
+#pragma unroll
+            for (int e = 0; e < NV; ++e) st_stream(st + (size_t)pr[q] * DK + 4 * (s + 8 * e), sv[q][e]);
+}
+
 // ---------------------------------------------------------------------------- decode
 
 // One token per request, in place.  Grid (H, batch).
 template <int DK, typename TI>
-__global__ void __launch_bounds__(kGdnThreads) gdn_decode_kernel(const __grid_constant__ GdnArgs a) {
+__global__ void __launch_bounds__(kGdnThreads, 2) gdn_decode_kernel(const __grid_constant__ GdnArgs a) {
     constexpr int NV = DK / 32;
     __shared__ __align__(16) float sk[DK], sq[DK];
     const int h = blockIdx.x, i = blockIdx.y, slot = a.slots[i], kh = h / a.hpg;
@@ -100,6 +142,12 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_decode_kernel(const __grid_co
         if (tid == 0) poison(a, slot, SSM_FLAG_LOG_NOT_EMPTY);
         return;
     }
+    float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
+    // the warp's first rows are in flight while the token is read and checked
+    int pr[kRG];
+    bool ok[kRG];
+    float4 sv[kRG][NV];
+    load_rows<NV>(st, DK, a.dv, 4 * warp, r, s, pr, ok, sv);
     const TI *qg = static_cast<const TI *>(a.q) + ((size_t)i * a.G + kh) * DK;
     const TI *kg = static_cast<const TI *>(a.k) + ((size_t)i * a.G + kh) * DK;
     const TI *vh = static_cast<const TI *>(a.v) + ((size_t)i * a.H + h) * a.dv;
@@ -116,70 +164,59 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_decode_kernel(const __grid_co
         return;
     }
     const float alpha = expf(gg), ab = alpha * bb;
-    float4 kr[NV], qr[NV];
+    float4 kr[NV];  // q is read from shared memory where it is used (registers go to the rows)
 #pragma unroll
-    for (int e = 0; e < NV; ++e) {
-        kr[e] = *reinterpret_cast<const float4 *>(sk + 4 * (s + 8 * e));
-        qr[e] = *reinterpret_cast<const float4 *>(sq + 4 * (s + 8 * e));
-    }
-    float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
+    for (int e = 0; e < NV; ++e) kr[e] = *reinterpret_cast<const float4 *>(sk + 4 * (s + 8 * e));
     TI *yh = static_cast<TI *>(a.y) + ((size_t)i * a.H + h) * a.dv;
-    // two row groups per step of the loop, their loads issued together
-    for (int p0 = 4 * warp; p0 < a.dv; p0 += 8 * kGdnWarps) {
-        const int pa = p0 + r, pb = p0 + 4 * kGdnWarps + r;
-        const bool hb = pb < a.dv;  // dv % 4 == 0: a group is whole or absent
-        float4 sa[NV], sb[NV];
+    for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps * kRG) {
+        if (p0 != 4 * warp) load_rows<NV>(st, DK, a.dv, p0, r, s, pr, ok, sv);
+        float w[kRG];
 #pragma unroll
-        for (int e = 0; e < NV; ++e) {
-            sa[e] = ld_stream(st + (size_t)pa * DK + 4 * (s + 8 * e));
-            sb[e] = hb ? ld_stream(st + (size_t)pb * DK + 4 * (s + 8 * e)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float wa = 0.f, wb = 0.f;
+        for (int q = 0; q < kRG; ++q) {
+            w[q] = 0.f;
 #pragma unroll
-        for (int e = 0; e < NV; ++e) {
-            wa += dot4(sa[e], kr[e]);
-            wb += dot4(sb[e], kr[e]);
+            for (int e = 0; e < NV; ++e) w[q] += dot4(sv[q][e], kr[e]);
         }
-        wa = red8(wa);
-        wb = red8(wb);
-        const float ca = bb * to_f(vh[pa]) - ab * wa;
-        const float cb = hb ? bb * to_f(vh[pb]) - ab * wb : 0.f;
-        float oa = 0.f, ob = 0.f;
 #pragma unroll
-        for (int e = 0; e < NV; ++e) {
-            sa[e] = axpy4(alpha, sa[e], ca, kr[e]);
-            sb[e] = axpy4(alpha, sb[e], cb, kr[e]);
-            oa += dot4(sa[e], qr[e]);
-            ob += dot4(sb[e], qr[e]);
-        }
-        oa = red8(oa);
-        ob = red8(ob);
+        for (int q = 0; q < kRG; ++q) w[q] = red8(w[q]);
 #pragma unroll
-        for (int e = 0; e < NV; ++e) {
-            st_stream(st + (size_t)pa * DK + 4 * (s + 8 * e), sa[e]);
-            if (hb) st_stream(st + (size_t)pb * DK + 4 * (s + 8 * e), sb[e]);
+        for (int q = 0; q < kRG; ++q) {
+            const float c = ok[q] ? bb * to_f(vh[pr[q]]) - ab * w[q] : 0.f;
+            float o = 0.f;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) {
+                sv[q][e] = axpy4(alpha, sv[q][e], c, kr[e]);
+                o += dot4(sv[q][e], *reinterpret_cast<const float4 *>(sq + 4 * (s + 8 * e)));
+            }
+            w[q] = o;
         }
-        if (s == 0) {
-            yh[pa] = from_f<TI>(oa);
-            if (hb) yh[pb] = from_f<TI>(ob);
-        }
+#pragma unroll
+        for (int q = 0; q < kRG; ++q) w[q] = red8(w[q]);
+        store_rows<NV>(st, DK, pr, ok, s, sv);
+#pragma unroll
+        for (int q = 0; q < kRG; ++q)
+            if (s == 0 && ok[q]) yh[pr[q]] = from_f<TI>(w[q]);
     }
     if (h == 0 && tid == 0) a.position[slot] += 1;
 }
 
 // ---------------------------------------------------------------------------- replay verify
 
-__host__ __device__ inline size_t gdn_coef_smem(int DK, int wcap, int t1max) {
-    return ((size_t)wcap * DK + (size_t)t1max * DK + 2 * (size_t)wcap) * sizeof(float);
+__host__ __device__ inline size_t gdn_coef_smem(int DK, int wcap, int t1max, int hpg) {
+    return ((size_t)wcap * DK + (size_t)t1max * DK + 2 * (size_t)hpg * wcap) * sizeof(float);
 }
 
-// Grid (H, batch): checks and stages the step, then walks the sweeps.
+// Grid (G, batch): one CTA per request and key head, whose logged and step keys serve all its value
+// heads.  It checks and stages the step, then walks the sweeps: sweep (value head, step token) takes
+// the eight lanes of a row group, u in the rows' layout, so that k_t . u takes three shuffles.  A
+// warp's four sweeps run the same number of steps (its longest), the shorter ones idle at the end.
 template <int DK, typename TI>
 __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_constant__ GdnArgs a) {
-    constexpr int NL = DK / 32;  // this lane's contiguous piece of a dk-vector in a sweep
+    constexpr int NV = DK / 32;
     extern __shared__ __align__(16) float gsm[];
-    const int h = blockIdx.x, i = blockIdx.y, slot = a.slots[i], kh = h / a.hpg;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kh = blockIdx.x, i = blockIdx.y, slot = a.slots[i], hpg = a.hpg, h0 = kh * hpg;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
+    const int nthr = blockDim.x, nwarps = nthr >> 5;  // sized by the host to the sweeps
     const int T1 = a.n_tok;
     if (a.slot_flags[slot] & kSlotPoisoned) {
         if (tid == 0) atomicOr(a.flags, SSM_FLAG_POISONED_SLOT);
@@ -188,21 +225,22 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
     const int K = a.log_len[slot];
     float *sk = gsm;                              // [K + T1][DK]: the log's keys, then the step's
     float *sq = sk + (size_t)a.wcap * DK;         // [T1][DK]
-    float *sal = sq + (size_t)a.t1max * DK;       // [K + T1] exp(g)
-    float *sbe = sal + a.wcap;                    // [K + T1] beta
+    float *sal = sq + (size_t)a.t1max * DK;       // [hpg][K + T1] exp(g)
+    float *sbe = sal + (size_t)hpg * a.wcap;      // [hpg][K + T1] beta
     const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK;
-    for (int e = tid; e < K * DK; e += kGdnThreads) {
+    for (int e = tid; e < K * DK; e += nthr) {
         const int t = e / DK, n = e - t * DK;
         sk[e] = to_f(lk[((size_t)t * a.G + kh) * DK + n]);
     }
-    for (int t = tid; t < K; t += kGdnThreads) {
-        sal[t] = expf(a.log_g[((size_t)slot * a.wcap + t) * a.H + h]);
-        sbe[t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h];
+    for (int e = tid; e < hpg * K; e += nthr) {
+        const int hl = e / K, t = e - hl * K;
+        sal[(size_t)hl * a.wcap + t] = expf(a.log_g[((size_t)slot * a.wcap + t) * a.H + h0 + hl]);
+        sbe[(size_t)hl * a.wcap + t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h0 + hl];
     }
     const TI *qs = static_cast<const TI *>(a.q), *ks = static_cast<const TI *>(a.k);
     const TI *vs = static_cast<const TI *>(a.v);
     bool bad = false;
-    for (int e = tid; e < T1 * DK; e += kGdnThreads) {
+    for (int e = tid; e < T1 * DK; e += nthr) {
         const int j = e / DK, n = e - j * DK;
         const size_t src = (((size_t)i * T1 + j) * a.G + kh) * DK + n;
         const float kv = to_f(ks[src]), qv = to_f(qs[src]);
@@ -210,114 +248,157 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
         sk[(size_t)(K + j) * DK + n] = kv;
         sq[(size_t)j * DK + n] = qv;
     }
-    for (int j = tid; j < T1; j += kGdnThreads) {
-        const float gv = a.g[((size_t)i * T1 + j) * a.H + h], bv = a.beta[((size_t)i * T1 + j) * a.H + h];
+    for (int e = tid; e < hpg * T1; e += nthr) {
+        const int hl = e / T1, j = e - hl * T1;
+        const size_t src = ((size_t)i * T1 + j) * a.H + h0 + hl;
+        const float gv = a.g[src], bv = a.beta[src];
         bad |= !(isfinite(gv) && isfinite(bv));
-        sal[K + j] = expf(gv);
-        sbe[K + j] = bv;
+        sal[(size_t)hl * a.wcap + K + j] = expf(gv);
+        sbe[(size_t)hl * a.wcap + K + j] = bv;
     }
-    for (int e = tid; e < T1 * a.dv; e += kGdnThreads) {
-        const int j = e / a.dv, p = e - j * a.dv;
-        bad |= !isfinite(to_f(vs[(((size_t)i * T1 + j) * a.H + h) * a.dv + p]));
+    for (int e = tid; e < T1 * hpg * a.dv; e += nthr) {
+        const int j = e / (hpg * a.dv), rem = e - j * hpg * a.dv;
+        bad |= !isfinite(to_f(vs[(((size_t)i * T1 + j) * a.H + h0) * a.dv + rem]));
     }
     if (__syncthreads_or(bad)) {
         if (tid == 0) poison(a, slot, SSM_FLAG_NONFINITE_INPUT);
         return;
     }
-    // the step after the log, for the commit: this head's v, g, beta; the key head's k from its first
-    // value head (the others read only the entries before K)
+    // the step after the log, for the commit: k, and the value heads' v, g, beta
     TI *lv = static_cast<TI *>(a.log_v);
-    for (int e = tid; e < T1 * a.dv; e += kGdnThreads) {
-        const int j = e / a.dv, p = e - j * a.dv;
-        lv[(((size_t)slot * a.wcap + K + j) * a.H + h) * a.dv + p] = vs[(((size_t)i * T1 + j) * a.H + h) * a.dv + p];
+    TI *lkw = static_cast<TI *>(a.log_k);
+    for (int e = tid; e < T1 * hpg * a.dv; e += nthr) {
+        const int j = e / (hpg * a.dv), rem = e - j * hpg * a.dv;
+        lv[(((size_t)slot * a.wcap + K + j) * a.H + h0) * a.dv + rem] = vs[(((size_t)i * T1 + j) * a.H + h0) * a.dv + rem];
     }
-    for (int j = tid; j < T1; j += kGdnThreads) {
-        a.log_g[((size_t)slot * a.wcap + K + j) * a.H + h] = a.g[((size_t)i * T1 + j) * a.H + h];
-        a.log_b[((size_t)slot * a.wcap + K + j) * a.H + h] = a.beta[((size_t)i * T1 + j) * a.H + h];
+    for (int e = tid; e < hpg * T1; e += nthr) {
+        const int hl = e / T1, j = e - hl * T1;
+        const size_t src = ((size_t)i * T1 + j) * a.H + h0 + hl, dst = ((size_t)slot * a.wcap + K + j) * a.H + h0 + hl;
+        a.log_g[dst] = a.g[src];
+        a.log_b[dst] = a.beta[src];
     }
-    if (h % a.hpg == 0) {
-        TI *lkw = static_cast<TI *>(a.log_k);
-        for (int e = tid; e < T1 * DK; e += kGdnThreads) {
-            const int j = e / DK, n = e - j * DK;
-            lkw[(((size_t)slot * a.wcap + K + j) * a.G + kh) * DK + n] = ks[(((size_t)i * T1 + j) * a.G + kh) * DK + n];
-        }
+    for (int e = tid; e < T1 * DK; e += nthr) {
+        const int j = e / DK, n = e - j * DK;
+        lkw[(((size_t)slot * a.wcap + K + j) * a.G + kh) * DK + n] = ks[(((size_t)i * T1 + j) * a.G + kh) * DK + n];
     }
-    // the sweeps: warp w takes step tokens j = w, w + 8, ...; lane l holds u[NL l .. NL l + NL - 1]
-    for (int j = warp; j < T1; j += kGdnWarps) {
-        const int mj = K + j + 1;
-        float u[NL];
+    // the sweeps: sweep id = 4 * (warp + kGdnWarps * round) + r over hpg * T1 (head hl = id / T1, token j)
+    const int nsw = hpg * T1;
+    for (int base = 4 * warp; base < nsw; base += 4 * nwarps) {
+        const int id = base + r;
+        const bool act = id < nsw;
+        const int hl = act ? id / T1 : 0, j = act ? id - hl * T1 : 0;
+        const int mj = act ? K + j + 1 : 0;
+        // the warp's longest sweep: its last active id has the largest j or a later head (then j runs
+        // from 0 again), so take the largest of the four
+        int mmax = mj;
+        mmax = max(mmax, __shfl_xor_sync(0xffffffffu, mmax, 8));
+        mmax = max(mmax, __shfl_xor_sync(0xffffffffu, mmax, 16));
+        float4 u[NV];
 #pragma unroll
-        for (int e = 0; e < NL; ++e) u[e] = sq[(size_t)j * DK + NL * lane + e];
-        float *csj = a.cs + (((size_t)i * a.H + h) * a.t1max + j) * a.wcap;
-        for (int t = mj - 1; t >= 0; --t) {
-            const float *kt = sk + (size_t)t * DK + NL * lane;
+        for (int e = 0; e < NV; ++e) u[e] = *reinterpret_cast<const float4 *>(sq + (size_t)j * DK + 4 * (s + 8 * e));
+        const float *al = sal + (size_t)hl * a.wcap, *be = sbe + (size_t)hl * a.wcap;
+        float *csj = a.cs + (((size_t)i * a.H + h0 + hl) * a.t1max + j) * a.wcap;
+        for (int t = mmax - 1; t >= 0; --t) {
+            const bool live = t < mj;
+            const float *kt = sk + (size_t)(live ? t : 0) * DK;
+            float4 k4[NV];
             float d = 0.f;
 #pragma unroll
-            for (int e = 0; e < NL; ++e) d = fmaf(kt[e], u[e], d);
-            d = red32(d);
-            const float bd = sbe[t] * d, al = sal[t];
-            if (lane == 0) csj[t] = bd;
+            for (int e = 0; e < NV; ++e) {
+                k4[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
+                d += dot4(k4[e], u[e]);
+            }
+            d = red8(d);
+            if (live) {
+                const float bd = be[t] * d, at = al[t];
+                if (s == 0) csj[t] = bd;
 #pragma unroll
-            for (int e = 0; e < NL; ++e) u[e] = al * fmaf(-bd, kt[e], u[e]);
+                for (int e = 0; e < NV; ++e) u[e] = axpy4(at, u[e], -at * bd, k4[e]);
+            }
         }
-        float *uqj = a.uq + (((size_t)i * a.H + h) * a.t1max + j) * DK + NL * lane;
+        if (act) {
+            float *uqj = a.uq + (((size_t)i * a.H + h0 + hl) * a.t1max + j) * DK;
 #pragma unroll
-        for (int e = 0; e < NL; ++e) uqj[e] = u[e];
+            for (int e = 0; e < NV; ++e) *reinterpret_cast<float4 *>(uqj + 4 * (s + 8 * e)) = u[e];
+        }
     }
 }
 
-__host__ __device__ inline size_t gdn_stream_smem(int DK, int wcap, int t1max) {
-    return ((size_t)t1max * DK + (size_t)t1max * wcap) * sizeof(float);
+// The staged values' rows are dv + 4 floats apart: lane (r, s) of a warp reads token t = s + 8 c at
+// column p0 + r, and the 4-float offset per token spreads the warp's 32 reads over 32 banks.
+__host__ __device__ inline int gdn_vstride(int dv) { return dv + 4; }
+
+__host__ __device__ inline size_t gdn_stream_smem(int DK, int dv, int wcap, int t1max) {
+    return ((size_t)t1max * DK + (size_t)t1max * wcap + (size_t)wcap * gdn_vstride(dv)) * sizeof(float);
 }
 
 // Grid (H, batch): every checkpoint row is read once and gives the row's output for each step token:
 // o_j[p] = S[p] . u_j + sum_{t < K + j + 1} c_j[t] v_t[p].
 template <int DK, typename TI>
-__global__ void __launch_bounds__(kGdnThreads) gdn_stream_kernel(const __grid_constant__ GdnArgs a) {
+__global__ void __launch_bounds__(kGdnThreads, 2) gdn_stream_kernel(const __grid_constant__ GdnArgs a) {
     constexpr int NV = DK / 32;
-    constexpr int NVL = (kGdnMaxLog + 7) / 8;  // logged values a lane takes per row (t = s + 8 c)
     extern __shared__ __align__(16) float gsm[];
     const int h = blockIdx.x, i = blockIdx.y, slot = a.slots[i];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
     if (a.slot_flags[slot] & kSlotPoisoned) return;  // flagged by the coefficient kernel
     const int T1 = a.n_tok, K = a.log_len[slot], m = K + T1;
+    const float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
+    // the warp's first rows are in flight while the coefficients are staged
+    int pr[kRG];
+    bool ok[kRG];
+    float4 sv[kRG][NV];
+    load_rows<NV>(st, DK, a.dv, 4 * warp, r, s, pr, ok, sv);
     float *suq = gsm;                        // [T1][DK]
     float *scs = suq + (size_t)a.t1max * DK; // [T1][wcap]
+    float *svv = scs + (size_t)a.t1max * a.wcap;  // [m][dv]: the logged values, then the step's
     const float *uq = a.uq + ((size_t)i * a.H + h) * a.t1max * DK;
     const float *cs = a.cs + ((size_t)i * a.H + h) * a.t1max * a.wcap;
+    const TI *lv = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
     for (int e = tid; e < T1 * DK; e += kGdnThreads) suq[e] = uq[e];
     for (int e = tid; e < T1 * a.wcap; e += kGdnThreads) {
         const int j = e / a.wcap, t = e - j * a.wcap;
         scs[e] = t < K + j + 1 ? cs[e] : 0.f;
     }
+    const int vst = gdn_vstride(a.dv);
+    for (int e = tid; e < m * a.dv; e += kGdnThreads) {
+        const int t = e / a.dv, p = e - t * a.dv;
+        svv[(size_t)t * vst + p] = to_f(lv[((size_t)t * a.H + h) * a.dv + p]);
+    }
     __syncthreads();
-    const float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
-    const TI *lv = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
     TI *y = static_cast<TI *>(a.y);
-    for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps) {
-        const int p = p0 + r;
-        float4 sv[NV];
-#pragma unroll
-        for (int e = 0; e < NV; ++e) sv[e] = ld_stream(st + (size_t)p * DK + 4 * (s + 8 * e));
-        float vv[NVL];
-#pragma unroll
-        for (int c = 0; c < NVL; ++c) {
-            const int t = s + 8 * c;
-            vv[c] = t < m ? to_f(lv[((size_t)t * a.H + h) * a.dv + p]) : 0.f;
-        }
+    const int nc = (m + 7) / 8;  // logged values a lane takes per row: t = s + 8 c
+    for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps * kRG) {
+        if (p0 != 4 * warp) load_rows<NV>(st, DK, a.dv, p0, r, s, pr, ok, sv);
         for (int j = 0; j < T1; ++j) {
             const float *uj = suq + (size_t)j * DK;
             const float *cj = scs + (size_t)j * a.wcap;
-            float acc = 0.f;
+            float2 acc2[kRG];
 #pragma unroll
-            for (int e = 0; e < NV; ++e) acc += dot4(sv[e], *reinterpret_cast<const float4 *>(uj + 4 * (s + 8 * e)));
+            for (int q = 0; q < kRG; ++q) acc2[q] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < NVL; ++c) {
-                const int t = s + 8 * c;
-                if (t < a.wcap) acc = fmaf(cj[t], vv[c], acc);  // zero past K + j
+            for (int e = 0; e < NV; ++e) {
+                const float4 u4 = *reinterpret_cast<const float4 *>(uj + 4 * (s + 8 * e));
+#pragma unroll
+                for (int q = 0; q < kRG; ++q) acc2[q] = dot4x2(sv[q][e], u4, acc2[q]);
             }
-            acc = red8(acc);
-            if (s == 0) y[(((size_t)i * T1 + j) * a.H + h) * a.dv + p] = from_f<TI>(acc);
+            float acc[kRG];
+#pragma unroll
+            for (int q = 0; q < kRG; ++q) acc[q] = acc2[q].x + acc2[q].y;
+            for (int c = 0; c < nc; ++c) {
+                const int t = s + 8 * c;
+                if (t < m) {  // the weight is zero past K + j
+                    const float cc = cj[t];
+#pragma unroll
+                    for (int q = 0; q < kRG; ++q) acc[q] = fmaf(cc, svv[(size_t)t * vst + (ok[q] ? pr[q] : 0)], acc[q]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kRG; ++q) acc[q] = red8(acc[q]);
+            if (s == 0) {
+#pragma unroll
+                for (int q = 0; q < kRG; ++q)
+                    if (ok[q]) y[(((size_t)i * T1 + j) * a.H + h) * a.dv + pr[q]] = from_f<TI>(acc[q]);
+            }
         }
     }
 }
@@ -356,7 +437,7 @@ __host__ __device__ inline size_t gdn_fold_smem(int DK, int dv, int wcap) {
 // Grid (H, batch): the requests marked by the commit apply their M logged tokens to the checkpoint,
 // row by row, in order.
 template <int DK, typename TI>
-__global__ void __launch_bounds__(kGdnThreads) gdn_fold_kernel(const __grid_constant__ GdnArgs a) {
+__global__ void __launch_bounds__(kGdnThreads, 2) gdn_fold_kernel(const __grid_constant__ GdnArgs a) {
     constexpr int NV = DK / 32;
     extern __shared__ __align__(16) float gsm[];
     const int h = blockIdx.x, i = blockIdx.y;
@@ -364,6 +445,12 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_fold_kernel(const __grid_cons
     if (M == 0) return;
     const int slot = a.slots[i], kh = h / a.hpg;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
+    float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
+    // the warp's first rows are in flight while the logged tokens are staged
+    int pr[kRG];
+    bool ok[kRG];
+    float4 sv[kRG][NV];
+    load_rows<NV>(st, DK, a.dv, 4 * warp, r, s, pr, ok, sv);
     float *sk = gsm;                          // [M][DK]
     float *svv = sk + (size_t)a.wcap * DK;    // [M][dv]
     float *sal = svv + (size_t)a.wcap * a.dv; // [M]
@@ -383,29 +470,56 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_fold_kernel(const __grid_cons
         sbe[t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h];
     }
     __syncthreads();
-    float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
-    for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps) {
-        const int p = p0 + r;
-        float4 sv[NV];
-#pragma unroll
-        for (int e = 0; e < NV; ++e) sv[e] = ld_stream(st + (size_t)p * DK + 4 * (s + 8 * e));
+    for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps * kRG) {
+        if (p0 != 4 * warp) load_rows<NV>(st, DK, a.dv, p0, r, s, pr, ok, sv);
+        // The rows are kept as sigma R with one scale for the whole head (the gate is per head), so
+        // that a token costs one multiply-add per element for S . k and one for the update:
+        //   w = sigma R . k,  sigma <- exp(g) sigma,  R <- R + ((beta v - exp(g) beta w) / sigma) k
+        // (the same S_t = exp(g) S (I - beta k k^T) + beta v k^T); R is rescaled whenever sigma leaves
+        // [2^-60, 1] or a gate is near zero.
+        float sig = 1.f;
         for (int t = 0; t < M; ++t) {
             const float *kt = sk + (size_t)t * DK;
             float4 kr[NV];
-            float w = 0.f;
 #pragma unroll
-            for (int e = 0; e < NV; ++e) {
-                kr[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
-                w += dot4(sv[e], kr[e]);
+            for (int e = 0; e < NV; ++e) kr[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
+            float w[kRG];
+#pragma unroll
+            for (int q = 0; q < kRG; ++q) {
+                float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < NV; ++e) acc2 = dot4x2(sv[q][e], kr[e], acc2);
+                w[q] = acc2.x + acc2.y;
             }
-            w = red8(w);
-            const float al = sal[t], be = sbe[t];
-            const float c = be * svv[(size_t)t * a.dv + p] - al * be * w;
 #pragma unroll
-            for (int e = 0; e < NV; ++e) sv[e] = axpy4(al, sv[e], c, kr[e]);
+            for (int q = 0; q < kRG; ++q) w[q] = red8(w[q]) * sig;
+            const float al = sal[t], be = sbe[t];
+            if (al < 0x1p-20f || sig * al < 0x1p-60f) {
+                // a gate near zero, or a scale about to leave fp32's range: fold the scale into the rows
+                // and take this token's update directly (uniform over the CTA: both are the head's)
+#pragma unroll
+                for (int q = 0; q < kRG; ++q) {
+                    const float c = be * svv[(size_t)t * a.dv + (ok[q] ? pr[q] : 0)] - al * be * w[q];
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) sv[q][e] = axpy4(al * sig, sv[q][e], c, kr[e]);
+                }
+                sig = 1.f;
+            } else {
+                sig *= al;
+                const float inv = 1.f / sig;
+#pragma unroll
+                for (int q = 0; q < kRG; ++q) {
+                    const float c = (be * svv[(size_t)t * a.dv + (ok[q] ? pr[q] : 0)] - al * be * w[q]) * inv;
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) sv[q][e] = add_ck4(sv[q][e], c, kr[e]);
+                }
+            }
         }
 #pragma unroll
-        for (int e = 0; e < NV; ++e) st_stream(st + (size_t)p * DK + 4 * (s + 8 * e), sv[e]);
+        for (int q = 0; q < kRG; ++q)
+#pragma unroll
+            for (int e = 0; e < NV; ++e) sv[q][e] = scale4(sig, sv[q][e]);
+        store_rows<NV>(st, DK, pr, ok, s, sv);
     }
 }
 
@@ -685,8 +799,11 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
     const ssm_gdn_pool_s &p = *pool;
     const size_t G = (size_t)p.cfg.nkheads, H = (size_t)p.cfg.nheads, dk = (size_t)p.cfg.dk, dv = (size_t)p.cfg.dv;
     const size_t ib = (size_t)p.in_b, T = (size_t)n_tok;
-    const size_t csm = ssm::gdn_coef_smem(p.cfg.dk, p.wcap, p.cfg.max_tokens);
-    const size_t ssm_ = ssm::gdn_stream_smem(p.cfg.dk, p.wcap, p.cfg.max_tokens);
+    const size_t csm = ssm::gdn_coef_smem(p.cfg.dk, p.wcap, p.cfg.max_tokens, p.cfg.nheads / p.cfg.nkheads);
+    // the coefficient kernel's block: four sweeps a warp, at least two warps for the staging
+    const int nsw = (p.cfg.nheads / p.cfg.nkheads) * n_tok;
+    const unsigned coef_threads = (unsigned)(32 * std::min(ssm::kGdnWarps, std::max(2, (nsw + 3) / 4)));
+    const size_t ssm_ = ssm::gdn_stream_smem(p.cfg.dk, p.cfg.dv, p.wcap, p.cfg.max_tokens);
     st = ssm::gdn_batches(p, slots, batch, [&](GdnArgs &a, int base, int m) {
         const size_t b0 = (size_t)base;
         a.n_tok = n_tok;
@@ -703,7 +820,7 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
             e = ssm::gdn_smem(kc, csm);
             if (e == cudaSuccess) e = ssm::gdn_smem(ks, ssm_);
             if (e == cudaSuccess) {
-                kc<<<dim3((unsigned)H, m), ssm::kGdnThreads, csm, s>>>(a);
+                kc<<<dim3((unsigned)G, m), coef_threads, csm, s>>>(a);
                 ks<<<dim3((unsigned)H, m), ssm::kGdnThreads, ssm_, s>>>(a);
                 e = cudaGetLastError();
             }
