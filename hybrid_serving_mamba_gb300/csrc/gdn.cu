@@ -19,9 +19,10 @@
 // written) unrolls the output at position m (the log's K tokens, then the
 // step tokens) as o_m = S_ckpt u_0 + sum_i beta_i (k_i . u_i) v_i, where
 // u_m = q_m and u_{i-1} = exp(g_i) (u_i - beta_i k_i (k_i . u_i)).  A
-// coefficient kernel walks those sweeps (a dk-vector per step token, one warp
-// each) and stages the step after the log; a streaming kernel then reads
-// each checkpoint row once for all step tokens.
+// coefficient kernel walks those sweeps (a dk-vector per step token, on eight
+// lanes each), forms the log terms sum_i beta_i (k_i . u_i) v_i and stages the
+// step after the log; a streaming kernel then reads each checkpoint row once
+// for all step tokens.
 #include <algorithm>
 #include <cstring>
 #include <vector>
@@ -44,7 +45,7 @@ struct GdnArgs {
     int32_t *log_len;
     int64_t *position;
     uint32_t *slot_flags, *flags;
-    float *uq, *cs;       // verify scratch: [request][H][t1max][dk], [request][H][t1max][wcap]
+    float *uq, *lt;       // verify scratch: [request][H][t1max][dk] queries, [request][H][t1max][dv] log terms
     int32_t *fold_m;      // commit: tokens to fold per request of the launch (0: none)
     const void *q, *k, *v;
     const float *g, *beta;
@@ -202,8 +203,9 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_decode_kernel(const __grid
 
 // ---------------------------------------------------------------------------- replay verify
 
-__host__ __device__ inline size_t gdn_coef_smem(int DK, int wcap, int t1max, int hpg) {
-    return ((size_t)wcap * DK + (size_t)t1max * DK + 2 * (size_t)hpg * wcap) * sizeof(float);
+__host__ __device__ inline size_t gdn_coef_smem(int DK, int dv, int wcap, int t1max, int hpg) {
+    return ((size_t)wcap * DK + (size_t)t1max * DK + 2 * (size_t)hpg * wcap + (size_t)hpg * t1max * wcap +
+            (size_t)wcap * dv) * sizeof(float);
 }
 
 // Grid (G, batch): one CTA per request and key head, whose logged and step keys serve all its value
@@ -227,6 +229,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
     float *sq = sk + (size_t)a.wcap * DK;         // [T1][DK]
     float *sal = sq + (size_t)a.t1max * DK;       // [hpg][K + T1] exp(g)
     float *sbe = sal + (size_t)hpg * a.wcap;      // [hpg][K + T1] beta
+    float *scw = sbe + (size_t)hpg * a.wcap;      // [hpg][T1][wcap] the weights of the logged values
     const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK;
     for (int e = tid; e < K * DK; e += nthr) {
         const int t = e / DK, n = e - t * DK;
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
 #pragma unroll
         for (int e = 0; e < NV; ++e) u[e] = *reinterpret_cast<const float4 *>(sq + (size_t)j * DK + 4 * (s + 8 * e));
         const float *al = sal + (size_t)hl * a.wcap, *be = sbe + (size_t)hl * a.wcap;
-        float *csj = a.cs + (((size_t)i * a.H + h0 + hl) * a.t1max + j) * a.wcap;
+        float *csj = scw + ((size_t)hl * a.t1max + j) * a.wcap;
         for (int t = mmax - 1; t >= 0; --t) {
             const bool live = t < mj;
             const float *kt = sk + (size_t)(live ? t : 0) * DK;
@@ -322,18 +325,41 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
             for (int e = 0; e < NV; ++e) *reinterpret_cast<float4 *>(uqj + 4 * (s + 8 * e)) = u[e];
         }
     }
+    __syncthreads();  // the weights, and this CTA's staged step values in the log
+    // the log terms lt_j[p] = sum_{t < K + j + 1} w_j[t] v_t[p], a value head at a time: its values
+    // staged in shared memory, one thread per (token, column)
+    const int m = K + T1;
+    float *svl = scw + (size_t)hpg * a.t1max * a.wcap;  // [m][dv]
+    const TI *lvr = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
+    for (int hl = 0; hl < hpg; ++hl) {
+        for (int e = tid; e < m * a.dv; e += nthr) {
+            const int t = e / a.dv, p = e - t * a.dv;
+            svl[e] = to_f(lvr[((size_t)t * a.H + h0 + hl) * a.dv + p]);
+        }
+        __syncthreads();
+        for (int e = tid; e < T1 * a.dv; e += nthr) {
+            const int j = e / a.dv, p = e - j * a.dv;
+            const float *w = scw + ((size_t)hl * a.t1max + j) * a.wcap;
+            const int mj = K + j + 1;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains, so the loads overlap
+            int t = 0;
+            for (; t + 4 <= mj; t += 4)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc[u] = fmaf(w[t + u], svl[(size_t)(t + u) * a.dv + p], acc[u]);
+            for (; t < mj; ++t) acc[0] = fmaf(w[t], svl[(size_t)t * a.dv + p], acc[0]);
+            a.lt[(((size_t)i * a.H + h0 + hl) * a.t1max + j) * a.dv + p] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        __syncthreads();
+    }
 }
 
-// The staged values' rows are dv + 4 floats apart: lane (r, s) of a warp reads token t = s + 8 c at
-// column p0 + r, and the 4-float offset per token spreads the warp's 32 reads over 32 banks.
-__host__ __device__ inline int gdn_vstride(int dv) { return dv + 4; }
-
-__host__ __device__ inline size_t gdn_stream_smem(int DK, int dv, int wcap, int t1max) {
-    return ((size_t)t1max * DK + (size_t)t1max * wcap + (size_t)wcap * gdn_vstride(dv)) * sizeof(float);
+__host__ __device__ inline size_t gdn_stream_smem(int DK, int dv, int t1max) {
+    return ((size_t)t1max * DK + (size_t)t1max * dv) * sizeof(float);
 }
 
 // Grid (H, batch): every checkpoint row is read once and gives the row's output for each step token:
-// o_j[p] = S[p] . u_j + sum_{t < K + j + 1} c_j[t] v_t[p].
+// o_j[p] = S[p] . u_j + lt_j[p], the log term lt_j[p] = sum_{t < K + j + 1} c_j[t] v_t[p] coming from
+// the coefficient kernel.
 template <int DK, typename TI>
 __global__ void __launch_bounds__(kGdnThreads, 2) gdn_stream_kernel(const __grid_constant__ GdnArgs a) {
     constexpr int NV = DK / 32;
@@ -341,7 +367,7 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_stream_kernel(const __grid
     const int h = blockIdx.x, i = blockIdx.y, slot = a.slots[i];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
     if (a.slot_flags[slot] & kSlotPoisoned) return;  // flagged by the coefficient kernel
-    const int T1 = a.n_tok, K = a.log_len[slot], m = K + T1;
+    const int T1 = a.n_tok;
     const float *st = a.state + ((size_t)slot * a.H + h) * a.dv * DK;
     // the warp's first rows are in flight while the coefficients are staged
     int pr[kRG];
@@ -349,29 +375,17 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_stream_kernel(const __grid
     float4 sv[kRG][NV];
     load_rows<NV>(st, DK, a.dv, 4 * warp, r, s, pr, ok, sv);
     float *suq = gsm;                        // [T1][DK]
-    float *scs = suq + (size_t)a.t1max * DK; // [T1][wcap]
-    float *svv = scs + (size_t)a.t1max * a.wcap;  // [m][dv]: the logged values, then the step's
+    float *slt = suq + (size_t)a.t1max * DK; // [T1][dv]
     const float *uq = a.uq + ((size_t)i * a.H + h) * a.t1max * DK;
-    const float *cs = a.cs + ((size_t)i * a.H + h) * a.t1max * a.wcap;
-    const TI *lv = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
+    const float *lt = a.lt + ((size_t)i * a.H + h) * a.t1max * a.dv;
     for (int e = tid; e < T1 * DK; e += kGdnThreads) suq[e] = uq[e];
-    for (int e = tid; e < T1 * a.wcap; e += kGdnThreads) {
-        const int j = e / a.wcap, t = e - j * a.wcap;
-        scs[e] = t < K + j + 1 ? cs[e] : 0.f;
-    }
-    const int vst = gdn_vstride(a.dv);
-    for (int e = tid; e < m * a.dv; e += kGdnThreads) {
-        const int t = e / a.dv, p = e - t * a.dv;
-        svv[(size_t)t * vst + p] = to_f(lv[((size_t)t * a.H + h) * a.dv + p]);
-    }
+    for (int e = tid; e < T1 * a.dv; e += kGdnThreads) slt[e] = lt[e];
     __syncthreads();
     TI *y = static_cast<TI *>(a.y);
-    const int nc = (m + 7) / 8;  // logged values a lane takes per row: t = s + 8 c
     for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps * kRG) {
         if (p0 != 4 * warp) load_rows<NV>(st, DK, a.dv, p0, r, s, pr, ok, sv);
         for (int j = 0; j < T1; ++j) {
             const float *uj = suq + (size_t)j * DK;
-            const float *cj = scs + (size_t)j * a.wcap;
             float2 acc2[kRG];
 #pragma unroll
             for (int q = 0; q < kRG; ++q) acc2[q] = make_float2(0.f, 0.f);
@@ -384,20 +398,14 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_stream_kernel(const __grid
             float acc[kRG];
 #pragma unroll
             for (int q = 0; q < kRG; ++q) acc[q] = acc2[q].x + acc2[q].y;
-            for (int c = 0; c < nc; ++c) {
-                const int t = s + 8 * c;
-                if (t < m) {  // the weight is zero past K + j
-                    const float cc = cj[t];
-#pragma unroll
-                    for (int q = 0; q < kRG; ++q) acc[q] = fmaf(cc, svv[(size_t)t * vst + (ok[q] ? pr[q] : 0)], acc[q]);
-                }
-            }
 #pragma unroll
             for (int q = 0; q < kRG; ++q) acc[q] = red8(acc[q]);
             if (s == 0) {
 #pragma unroll
                 for (int q = 0; q < kRG; ++q)
-                    if (ok[q]) y[(((size_t)i * T1 + j) * a.H + h) * a.dv + pr[q]] = from_f<TI>(acc[q]);
+                    if (ok[q])
+                        y[(((size_t)i * T1 + j) * a.H + h) * a.dv + pr[q]] =
+                            from_f<TI>(acc[q] + slt[(size_t)j * a.dv + pr[q]]);
             }
         }
     }
@@ -556,7 +564,7 @@ struct ssm_gdn_pool_s {
     size_t per_slot = 0;  // floats of one slot's state
     float *state = nullptr;
     void *log_k = nullptr, *log_v = nullptr;
-    float *log_g = nullptr, *log_b = nullptr, *uq = nullptr, *cs = nullptr;
+    float *log_g = nullptr, *log_b = nullptr, *uq = nullptr, *lt = nullptr;
     int32_t *log_len = nullptr, *fold_m = nullptr;
     int64_t *position = nullptr;
     uint32_t *slot_flags = nullptr, *flags = nullptr;
@@ -580,7 +588,7 @@ struct GdnDevice {  // the pool's device current for the call, the caller's rest
 ssm_status gdn_cuda(cudaError_t e) { return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA; }
 
 void gdn_free(ssm_gdn_pool_s *p) {
-    void *bufs[] = {p->state, p->log_k, p->log_v, p->log_g, p->log_b, p->uq, p->cs,
+    void *bufs[] = {p->state, p->log_k, p->log_v, p->log_g, p->log_b, p->uq, p->lt,
                     p->log_len, p->fold_m, p->position, p->slot_flags, p->flags};
     for (void *b : bufs)
         if (b) cudaFree(b);
@@ -604,7 +612,7 @@ GdnArgs gdn_args(const ssm_gdn_pool_s &p) {
     a.slot_flags = p.slot_flags;
     a.flags = p.flags;
     a.uq = p.uq;
-    a.cs = p.cs;
+    a.lt = p.lt;
     a.fold_m = p.fold_m;
     a.H = p.cfg.nheads;
     a.G = p.cfg.nkheads;
@@ -675,6 +683,17 @@ ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float 
         c.dv > 256 || c.dv % 4 || (c.input_dtype != SSM_DTYPE_F32 && c.input_dtype != SSM_DTYPE_BF16) ||
         c.window < 1 || c.window > ssm::kGdnMaxWindow || c.max_tokens < 1 || c.max_tokens > ssm::kGdnMaxTokens)
         return SSM_ERR_INVALID_ARG;
+    {  // the verify and fold kernels' shared-memory working sets must fit one CTA
+        int dev = 0, max_smem = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            max_smem = 0;
+        const int wcap = c.window - 1 + c.max_tokens, hpg = c.nheads / c.nkheads;
+        const size_t need = std::max({ssm::gdn_coef_smem(c.dk, c.dv, wcap, c.max_tokens, hpg),
+                                      ssm::gdn_stream_smem(c.dk, c.dv, c.max_tokens),
+                                      ssm::gdn_fold_smem(c.dk, c.dv, wcap)});
+        if (max_smem > 0 && need + 1024 > (size_t)max_smem) return SSM_ERR_INVALID_ARG;
+    }
     auto *p = new (std::nothrow) ssm_gdn_pool_s();
     if (!p) return SSM_ERR_NO_MEMORY;
     p->cfg = c;
@@ -693,7 +712,7 @@ ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float 
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_g, ns * W * H);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_b, ns * W * H);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->uq, sr * H * T * c.dk);
-    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->cs, sr * H * T * W);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->lt, sr * H * T * (size_t)c.dv);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_len, ns);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->fold_m, (size_t)ssm::kGdnMaxBatch);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->position, ns);
@@ -799,11 +818,12 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
     const ssm_gdn_pool_s &p = *pool;
     const size_t G = (size_t)p.cfg.nkheads, H = (size_t)p.cfg.nheads, dk = (size_t)p.cfg.dk, dv = (size_t)p.cfg.dv;
     const size_t ib = (size_t)p.in_b, T = (size_t)n_tok;
-    const size_t csm = ssm::gdn_coef_smem(p.cfg.dk, p.wcap, p.cfg.max_tokens, p.cfg.nheads / p.cfg.nkheads);
-    // the coefficient kernel's block: four sweeps a warp, at least two warps for the staging
+    const size_t csm = ssm::gdn_coef_smem(p.cfg.dk, p.cfg.dv, p.wcap, p.cfg.max_tokens, p.cfg.nheads / p.cfg.nkheads);
+    // the coefficient kernel's block: four sweeps a warp, at least four warps for the staging and the
+    // log terms
     const int nsw = (p.cfg.nheads / p.cfg.nkheads) * n_tok;
-    const unsigned coef_threads = (unsigned)(32 * std::min(ssm::kGdnWarps, std::max(2, (nsw + 3) / 4)));
-    const size_t ssm_ = ssm::gdn_stream_smem(p.cfg.dk, p.cfg.dv, p.wcap, p.cfg.max_tokens);
+    const unsigned coef_threads = (unsigned)(32 * std::min(ssm::kGdnWarps, std::max(4, (nsw + 3) / 4)));
+    const size_t ssm_ = ssm::gdn_stream_smem(p.cfg.dk, p.cfg.dv, p.cfg.max_tokens);
     st = ssm::gdn_batches(p, slots, batch, [&](GdnArgs &a, int base, int m) {
         const size_t b0 = (size_t)base;
         a.n_tok = n_tok;

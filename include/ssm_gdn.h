@@ -26,7 +26,10 @@
  * SSM_FLAG_* bits, poison the slot and skip its work; calls are
  * asynchronous on the given stream unless marked synchronous.  Supported
  * shapes: dk 64 or 128, dv a multiple of 4 up to 256, G dividing H,
- * max_tokens 1..32, window 1..32.
+ * max_tokens 1..32, window 1..32, and one key head's verify working set in
+ * a CTA's shared memory: 4 * (L (dk + dv) + T dk + hpg L (T + 2)) bytes with
+ * L = window - 1 + max_tokens, T = max_tokens, hpg = H / G (else
+ * ssm_gdn_init returns SSM_ERR_INVALID_ARG).
  */
 #ifndef SSM_GDN_H
 #define SSM_GDN_H
