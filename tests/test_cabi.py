@@ -67,3 +67,33 @@ def test_null_pool_is_rejected(mod):
     assert lib.ssm_pool_status(None, ctypes.byref(f), 0, None) == mod.SSM_ERR_INVALID_ARG
     assert lib.ssm_last_path(None) == b"none"
     assert lib.ssm_pool_bytes(None) == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(nheads=0), dict(nkheads=0), dict(nkheads=3), dict(dk=96), dict(dk=256), dict(dv=0), dict(dv=6),
+    dict(dv=260), dict(input_dtype=1), dict(window=0), dict(window=33), dict(max_tokens=0), dict(max_tokens=33),
+])
+def test_gdn_init_rejects_bad_config(mod, bad):
+    """The gated-delta-rule pool refuses unsupported shapes before any device work."""
+    kw = dict(nheads=4, nkheads=2, dk=64, dv=64, input_dtype=0, window=8, max_tokens=4)
+    kw.update(bad)
+    cfg = mod.ssm_gdn_config(**kw)
+    out = ctypes.c_void_p()
+    st = mod.library().ssm_gdn_init(ctypes.byref(cfg), 4, None, None, ctypes.byref(out))
+    assert st == mod.SSM_ERR_INVALID_ARG and not out.value
+
+
+def test_gdn_null_pool_and_arguments_are_rejected(mod):
+    lib = mod.library()
+    slots = (ctypes.c_int32 * 1)(0)
+    V = ctypes.c_void_p
+    assert lib.ssm_gdn_decode_step(None, 1, slots, V(8), V(8), V(8), V(8), V(8), V(8), None) == mod.SSM_ERR_INVALID_ARG
+    assert lib.ssm_gdn_verify_replay(None, 1, 1, slots, V(8), V(8), V(8), V(8), V(8), V(8),
+                                     None) == mod.SSM_ERR_INVALID_ARG
+    assert lib.ssm_gdn_commit(None, 1, slots, V(8), 0, None) == mod.SSM_ERR_INVALID_ARG
+    assert lib.ssm_gdn_gather(None, 1, slots, V(8), None) == mod.SSM_ERR_INVALID_ARG
+    assert lib.ssm_gdn_reset(None, slots, 1, None) == mod.SSM_ERR_INVALID_ARG
+    assert lib.ssm_gdn_destroy(None) == mod.SSM_ERR_INVALID_ARG
+    f = ctypes.c_uint32()
+    assert lib.ssm_gdn_status(None, ctypes.byref(f), 0, None) == mod.SSM_ERR_INVALID_ARG
+    assert lib.ssm_gdn_slot_info(None, 0, None, None, None, None) == mod.SSM_ERR_INVALID_ARG
