@@ -91,6 +91,84 @@ __device__ __forceinline__ float4 axpy4(float al, float4 x, float c, float4 k) {
                        fmaf(al, x.w, c * k.w));
 }
 
+// rows x cols values (cols a multiple of 4) of a strided global matrix into fp32 shared memory
+// [rows][cols]: four values a load and four loads in flight per thread, since a CTA's staging is
+// otherwise a chain of round trips to memory.  Returns true if a value is not finite.
+template <typename TI>
+__device__ __forceinline__ bool stage_rows(float *dst, const TI *src, size_t stride, int rows, int cols, int tid,
+                                           int nthr) {
+    const int cq = cols >> 2, total = rows * cq;
+    bool bad = false;
+    for (int base = tid; base < total; base += 4 * nthr) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = base + u * nthr;
+            if (e < total) {
+                const int r = e / cq, c = e - r * cq;
+                v[u] = load4(src + (size_t)r * stride, (size_t)4 * c);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = base + u * nthr;
+            if (e < total) {
+                const int r = e / cq, c = e - r * cq;
+                bad |= !finite4(v[u]);
+                *reinterpret_cast<float4 *>(dst + (size_t)r * cols + 4 * c) = v[u];
+            }
+        }
+    }
+    return bad;
+}
+
+// Four values of the input type as one load, and whether one of them is not finite (all exponent bits set).
+template <typename TI> struct Vec4;
+template <> struct Vec4<float> {
+    using T = uint4;
+    __device__ static bool bad(T v) {
+        return ((v.x & 0x7F800000u) == 0x7F800000u) | ((v.y & 0x7F800000u) == 0x7F800000u) |
+               ((v.z & 0x7F800000u) == 0x7F800000u) | ((v.w & 0x7F800000u) == 0x7F800000u);
+    }
+};
+template <> struct Vec4<__nv_bfloat16> {
+    using T = uint2;
+    __device__ static bool bad(T v) {
+        return ((v.x & 0x7F80u) == 0x7F80u) | ((v.x & 0x7F800000u) == 0x7F800000u) | ((v.y & 0x7F80u) == 0x7F80u) |
+               ((v.y & 0x7F800000u) == 0x7F800000u);
+    }
+};
+
+// The same between global matrices in the input type (staging the step into the log), with the check.
+template <typename TI>
+__device__ __forceinline__ bool copy_rows(TI *dst, size_t dstride, const TI *src, size_t sstride, int rows, int cols,
+                                          int tid, int nthr) {
+    using V = typename Vec4<TI>::T;
+    const int cq = cols >> 2, total = rows * cq;
+    bool bad = false;
+    for (int base = tid; base < total; base += 4 * nthr) {
+        V v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = base + u * nthr;
+            if (e < total) {
+                const int r = e / cq, c = e - r * cq;
+                v[u] = *reinterpret_cast<const V *>(src + (size_t)r * sstride + 4 * c);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = base + u * nthr;
+            if (e < total) {
+                const int r = e / cq, c = e - r * cq;
+                bad |= Vec4<TI>::bad(v[u]);
+                *reinterpret_cast<V *>(dst + (size_t)r * dstride + 4 * c) = v[u];
+            }
+        }
+    }
+    return bad;
+}
+
 __device__ __forceinline__ void poison(const GdnArgs &a, int slot, uint32_t flag) {
     atomicOr(a.flags, flag);
     atomicOr(a.slot_flags + slot, kSlotPoisoned);
@@ -231,58 +309,38 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
     float *sbe = sal + (size_t)hpg * a.wcap;      // [hpg][K + T1] beta
     float *scw = sbe + (size_t)hpg * a.wcap;      // [hpg][T1][wcap] the weights of the logged values
     const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK;
-    for (int e = tid; e < K * DK; e += nthr) {
-        const int t = e / DK, n = e - t * DK;
-        sk[e] = to_f(lk[((size_t)t * a.G + kh) * DK + n]);
-    }
+    const TI *qs = static_cast<const TI *>(a.q), *ks = static_cast<const TI *>(a.k);
+    const TI *vs = static_cast<const TI *>(a.v);
+    const size_t kstep = ((size_t)i * T1 * a.G + kh) * DK;  // step token 0's key (and query) of this key head
+    stage_rows(sk, lk + (size_t)kh * DK, (size_t)a.G * DK, K, DK, tid, nthr);  // checked when it was logged
+    bool bad = stage_rows(sk + (size_t)K * DK, ks + kstep, (size_t)a.G * DK, T1, DK, tid, nthr);
+    bad |= stage_rows(sq, qs + kstep, (size_t)a.G * DK, T1, DK, tid, nthr);
     for (int e = tid; e < hpg * K; e += nthr) {
         const int hl = e / K, t = e - hl * K;
         sal[(size_t)hl * a.wcap + t] = expf(a.log_g[((size_t)slot * a.wcap + t) * a.H + h0 + hl]);
         sbe[(size_t)hl * a.wcap + t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h0 + hl];
     }
-    const TI *qs = static_cast<const TI *>(a.q), *ks = static_cast<const TI *>(a.k);
-    const TI *vs = static_cast<const TI *>(a.v);
-    bool bad = false;
-    for (int e = tid; e < T1 * DK; e += nthr) {
-        const int j = e / DK, n = e - j * DK;
-        const size_t src = (((size_t)i * T1 + j) * a.G + kh) * DK + n;
-        const float kv = to_f(ks[src]), qv = to_f(qs[src]);
-        bad |= !(isfinite(kv) && isfinite(qv));
-        sk[(size_t)(K + j) * DK + n] = kv;
-        sq[(size_t)j * DK + n] = qv;
-    }
     for (int e = tid; e < hpg * T1; e += nthr) {
         const int hl = e / T1, j = e - hl * T1;
-        const size_t src = ((size_t)i * T1 + j) * a.H + h0 + hl;
+        const size_t src = ((size_t)i * T1 + j) * a.H + h0 + hl, dst = ((size_t)slot * a.wcap + K + j) * a.H + h0 + hl;
         const float gv = a.g[src], bv = a.beta[src];
         bad |= !(isfinite(gv) && isfinite(bv));
         sal[(size_t)hl * a.wcap + K + j] = expf(gv);
         sbe[(size_t)hl * a.wcap + K + j] = bv;
+        a.log_g[dst] = gv;
+        a.log_b[dst] = bv;
     }
-    for (int e = tid; e < T1 * hpg * a.dv; e += nthr) {
-        const int j = e / (hpg * a.dv), rem = e - j * hpg * a.dv;
-        bad |= !isfinite(to_f(vs[(((size_t)i * T1 + j) * a.H + h0) * a.dv + rem]));
-    }
+    // the step after the log, for the commit (the positions past log_len: a rejected request leaves
+    // nothing behind that a later commit reads): the value heads' v and the key head's k
+    TI *lv = static_cast<TI *>(a.log_v);
+    TI *lkw = static_cast<TI *>(a.log_k);
+    bad |= copy_rows(lv + (((size_t)slot * a.wcap + K) * a.H + h0) * a.dv, (size_t)a.H * a.dv,
+                     vs + ((size_t)i * T1 * a.H + h0) * a.dv, (size_t)a.H * a.dv, T1, hpg * a.dv, tid, nthr);
+    copy_rows(lkw + (((size_t)slot * a.wcap + K) * a.G + kh) * DK, (size_t)a.G * DK, ks + kstep, (size_t)a.G * DK, T1,
+              DK, tid, nthr);
     if (__syncthreads_or(bad)) {
         if (tid == 0) poison(a, slot, SSM_FLAG_NONFINITE_INPUT);
         return;
-    }
-    // the step after the log, for the commit: k, and the value heads' v, g, beta
-    TI *lv = static_cast<TI *>(a.log_v);
-    TI *lkw = static_cast<TI *>(a.log_k);
-    for (int e = tid; e < T1 * hpg * a.dv; e += nthr) {
-        const int j = e / (hpg * a.dv), rem = e - j * hpg * a.dv;
-        lv[(((size_t)slot * a.wcap + K + j) * a.H + h0) * a.dv + rem] = vs[(((size_t)i * T1 + j) * a.H + h0) * a.dv + rem];
-    }
-    for (int e = tid; e < hpg * T1; e += nthr) {
-        const int hl = e / T1, j = e - hl * T1;
-        const size_t src = ((size_t)i * T1 + j) * a.H + h0 + hl, dst = ((size_t)slot * a.wcap + K + j) * a.H + h0 + hl;
-        a.log_g[dst] = a.g[src];
-        a.log_b[dst] = a.beta[src];
-    }
-    for (int e = tid; e < T1 * DK; e += nthr) {
-        const int j = e / DK, n = e - j * DK;
-        lkw[(((size_t)slot * a.wcap + K + j) * a.G + kh) * DK + n] = ks[(((size_t)i * T1 + j) * a.G + kh) * DK + n];
     }
     // the sweeps: sweep id = 4 * (warp + kGdnWarps * round) + r over hpg * T1 (head hl = id / T1, token j)
     const int nsw = hpg * T1;
@@ -332,10 +390,7 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
     float *svl = scw + (size_t)hpg * a.t1max * a.wcap;  // [m][dv]
     const TI *lvr = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
     for (int hl = 0; hl < hpg; ++hl) {
-        for (int e = tid; e < m * a.dv; e += nthr) {
-            const int t = e / a.dv, p = e - t * a.dv;
-            svl[e] = to_f(lvr[((size_t)t * a.H + h0 + hl) * a.dv + p]);
-        }
+        stage_rows(svl, lvr + (size_t)(h0 + hl) * a.dv, (size_t)a.H * a.dv, m, a.dv, tid, nthr);
         __syncthreads();
         for (int e = tid; e < T1 * a.dv; e += nthr) {
             const int j = e / a.dv, p = e - j * a.dv;
@@ -378,8 +433,8 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_stream_kernel(const __grid
     float *slt = suq + (size_t)a.t1max * DK; // [T1][dv]
     const float *uq = a.uq + ((size_t)i * a.H + h) * a.t1max * DK;
     const float *lt = a.lt + ((size_t)i * a.H + h) * a.t1max * a.dv;
-    for (int e = tid; e < T1 * DK; e += kGdnThreads) suq[e] = uq[e];
-    for (int e = tid; e < T1 * a.dv; e += kGdnThreads) slt[e] = lt[e];
+    stage_rows(suq, uq, DK, T1, DK, tid, kGdnThreads);
+    stage_rows(slt, lt, a.dv, T1, a.dv, tid, kGdnThreads);
     __syncthreads();
     TI *y = static_cast<TI *>(a.y);
     for (int p0 = 4 * warp; p0 < a.dv; p0 += 4 * kGdnWarps * kRG) {
@@ -465,14 +520,8 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_fold_kernel(const __grid_c
     float *sbe = sal + a.wcap;                // [M]
     const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK;
     const TI *lv = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
-    for (int e = tid; e < M * DK; e += kGdnThreads) {
-        const int t = e / DK, n = e - t * DK;
-        sk[e] = to_f(lk[((size_t)t * a.G + kh) * DK + n]);
-    }
-    for (int e = tid; e < M * a.dv; e += kGdnThreads) {
-        const int t = e / a.dv, p = e - t * a.dv;
-        svv[e] = to_f(lv[((size_t)t * a.H + h) * a.dv + p]);
-    }
+    stage_rows(sk, lk + (size_t)kh * DK, (size_t)a.G * DK, M, DK, tid, kGdnThreads);
+    stage_rows(svv, lv + (size_t)h * a.dv, (size_t)a.H * a.dv, M, a.dv, tid, kGdnThreads);
     for (int t = tid; t < M; t += kGdnThreads) {
         sal[t] = expf(a.log_g[((size_t)slot * a.wcap + t) * a.H + h]);
         sbe[t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h];
@@ -622,6 +671,12 @@ GdnArgs gdn_args(const ssm_gdn_pool_s &p) {
     a.wcap = p.wcap;
     a.t1max = p.cfg.max_tokens;
     return a;
+}
+
+// q, k, v and y are read and written four values at a time
+bool gdn_aligned(const void *q, const void *k, const void *v, const void *y) {
+    return ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+             reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
 }
 
 ssm_status gdn_check_slots(const ssm_gdn_pool_s *p, const int32_t *slots, int n) {
@@ -780,7 +835,7 @@ ssm_status ssm_gdn_gather(ssm_gdn_pool pool, int32_t n, const int32_t *slots, fl
 ssm_status ssm_gdn_decode_step(ssm_gdn_pool pool, int32_t batch, const int32_t *slots, const void *q,
                                const void *k, const void *v, const float *g, const float *beta, void *y,
                                ssm_stream_t stream) {
-    if (!pool || !q || !k || !v || !g || !beta || !y) return SSM_ERR_INVALID_ARG;
+    if (!pool || !q || !k || !v || !g || !beta || !y || !ssm::gdn_aligned(q, k, v, y)) return SSM_ERR_INVALID_ARG;
     ssm_status st = ssm::gdn_check_slots(pool, slots, batch);
     if (st != SSM_OK) return st;
     ssm::GdnDevice dg(pool->device);
@@ -809,7 +864,7 @@ ssm_status ssm_gdn_decode_step(ssm_gdn_pool pool, int32_t batch, const int32_t *
 ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok, const int32_t *slots,
                                  const void *q, const void *k, const void *v, const float *g, const float *beta,
                                  void *y, ssm_stream_t stream) {
-    if (!pool || !q || !k || !v || !g || !beta || !y) return SSM_ERR_INVALID_ARG;
+    if (!pool || !q || !k || !v || !g || !beta || !y || !ssm::gdn_aligned(q, k, v, y)) return SSM_ERR_INVALID_ARG;
     if (n_tok < 1 || n_tok > pool->cfg.max_tokens) return SSM_ERR_INVALID_ARG;
     ssm_status st = ssm::gdn_check_slots(pool, slots, batch);
     if (st != SSM_OK) return st;

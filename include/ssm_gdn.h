@@ -19,6 +19,7 @@
  *   v, y              [tokens][H][dv]      input dtype
  *   g, beta           float [tokens][H]    (g = log of the gate, <= 0)
  * "tokens" is the batch for a decode step and [batch][n_tok] for a verify.
+ * q, k, v and y must start on 16-byte boundaries (else SSM_ERR_INVALID_ARG).
  *
  * Ownership, errors and asynchrony follow ssm_state.h: the pool owns its
  * memory; host-side checks return before any work is queued; device-side
