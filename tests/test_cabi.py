@@ -97,3 +97,29 @@ def test_gdn_null_pool_and_arguments_are_rejected(mod):
     f = ctypes.c_uint32()
     assert lib.ssm_gdn_status(None, ctypes.byref(f), 0, None) == mod.SSM_ERR_INVALID_ARG
     assert lib.ssm_gdn_slot_info(None, 0, None, None, None, None) == mod.SSM_ERR_INVALID_ARG
+
+
+def _declared_arity():
+    """name -> number of parameters, from every declaration in include/*.h."""
+    out = {}
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+        for m in re.finditer(r"\b(ssm_[a-z_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+            args = m.group(2).strip()
+            out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_the_headers(mod):
+    """Every entry point's ctypes argument list has as many entries as its C
+    declaration has parameters (a mismatch would pass garbage silently)."""
+    lib = mod.library()
+    arity = _declared_arity()
+    assert set(arity) == set(mod.EXPORTS)
+    for name, n in sorted(arity.items()):
+        f = getattr(lib, name)
+        assert f.argtypes is not None, name
+        assert len(f.argtypes) == n, (name, len(f.argtypes), n)
