@@ -149,3 +149,21 @@ def test_pool_commit_keeps_only_accepted_tokens():
     pool.flush([0, 1])
     assert np.allclose(pool.state, ref, rtol=1e-12, atol=1e-12)
     assert list(pool.position) == [7 + int(acc[:, r].sum()) for r in range(2)]
+
+
+def test_input_recipe():
+    """The synthetic gated-delta-rule inputs have the distributions the recipe
+    states: unit q and k per key head (up to bf16 rounding when stored so),
+    a log-gate g <= 0, beta in (0, 1), and the stated shapes and storage."""
+    for code, tol in ((synth.F32, 1e-6), (synth.BF16, 1e-2)):
+        q, k, v, g, b = synth.gdn_batch_tokens(11, 0, 3, 5, 8, 4, 64, 32, code)
+        assert q.shape == k.shape == (3, 5, 4, 64) and v.shape == (3, 5, 8, 32)
+        assert g.shape == b.shape == (3, 5, 8) and g.dtype == b.dtype == np.float32
+        assert q.dtype == (np.uint16 if code == synth.BF16 else np.float32)
+        for a in (q, k):
+            n = np.linalg.norm(synth.widen(a, code), axis=-1)
+            assert np.all(np.abs(n - 1.0) < tol)
+        assert np.all(g < 0) and np.all(g > -20)
+        assert np.all((b > 0) & (b < 1))
+    s = synth.gdn_init_state(3, 0, 8, 32, 64)
+    assert s.shape == (8, 32, 64) and abs(float(s.std()) - 0.1) < 0.01
