@@ -610,8 +610,10 @@ def bench_gdn(torch, m, args):
                                          stream=stream) == m.SSM_OK
     us = timed(decode, T)
     alg = algorithmic_bytes_gdn_decode(R, H, G, dk, dv)
+    hbm_peak, _, peak_kind = measured_peaks()
     out["decode"] = dict(us_per_step=us, tok_per_s=R / (us / 1e6), achieved_gbs=alg / (us / 1e6) / 1e9,
-                         algorithmic_bytes=alg)
+                         algorithmic_bytes=alg, frac_of_hbm=alg / (us / 1e6) / 1e9 / hbm_peak,
+                         hbm_peak_source=peak_kind)
     assert m.ssm_gdn_status(pool)[1] == 0
     m.ssm_gdn_destroy(pool)
 
