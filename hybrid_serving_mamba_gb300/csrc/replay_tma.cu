@@ -1113,7 +1113,12 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
             }
     }
     const TmaLayout L = tma_layout(a.P, a.N, in_b, T1, a.wcap, a.cb_w);
-    const int nstage = std::min(kMaxStages, (int)(((long)max_smem - (long)L.fixed) / (long)L.stage));
+    // The consumer groups take alternate items, so the stage count is a multiple of the group count:
+    // a stage then serves one group, which has consumed the stage's previous item before it waits on
+    // the stage again (a parity wait cannot tell a phase two back from the one it waits for).
+    static_assert(kMaxStages % kGroups == 0, "");
+    const int nstage =
+        std::min(kMaxStages, (int)(((long)max_smem - (long)L.fixed) / (long)L.stage)) / kGroups * kGroups;
     if (!nring && nstage < 2) return cudaErrorNotSupported;
     const size_t smem = (size_t)nstage * L.stage + L.fixed;
     StepArgs ac = a;
