@@ -737,6 +737,22 @@ def bench_graph_small_batch(torch, m, args, batches=(1, 8, 64), steps=32):
     return out
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: implementer and part codes)."""
+    try:
+        text = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    m = re.search(r"^model name\s*:\s*(.+)$", text, flags=re.M)
+    if m:
+        return m.group(1).strip()
+    imp = re.search(r"^CPU implementer\s*:\s*(\S+)", text, flags=re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", text, flags=re.M)
+    if imp and part:
+        return f"Arm implementer {imp.group(1)} part {part.group(1)}"
+    return "unknown"
+
+
 def cpu_baseline(budget_s=12.0):
     """The oracle (fp64, OpenMP over (request, head)) on a bounded sample of
     the decode workload: all 128 heads of a few requests for a few tokens."""
@@ -764,7 +780,7 @@ def cpu_baseline(budget_s=12.0):
     R = int(max(8, min(256, budget_s / max(per, 1e-6) / 4)))
     steps = 4
     secs = run(R, steps)
-    return dict(value=R * steps / secs, unit="tok/s", cores=oracle.threads(), kind="oracle",
+    return dict(value=R * steps / secs, unit="tok/s", cores=oracle.threads(), cpu=cpu_model(), kind="oracle",
                 sample=f"{R} requests x {steps} decode tokens, all {H} heads (fp64 oracle, OpenMP)",
                 seconds=secs)
 
@@ -831,7 +847,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": "decode B=256 H=128 P=64 N=128 G=8 (sampled requests)", "l2": "state > L2"},
-            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": base["cores"], "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": base["cores"], "cpu": base["cpu"], "kind": "oracle",
                              "sample": base["sample"]},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
