@@ -311,23 +311,64 @@ def bench_decode_e2e(torch, m, args):
     return dict(ms=ms, tokens=R * T * steps, h2d=h2d, d2h=d2h)
 
 
-def bench_verify(torch, m, args):
-    """Copy verify vs ReplaySSM verify at batch 512, verify + commit per step."""
+def _verify_bytes(acc_np, R, H, P, N, G, T1, W, S, warm):
+    """Algorithmic bytes per step of copy and replay verify (+ commit).
+    Copy: read the state, write T+1 states, token inputs and outputs.  Replay:
+    read the checkpoint and the k logged entries, token inputs and outputs,
+    stage the step's entries after the log; a fold reads the checkpoint and
+    its m entries and writes the checkpoint.  Log lengths and folds follow the
+    commit rule on the same accept counts (integer bookkeeping only), warm-up
+    steps included so the timed steps start from the logs they leave."""
+    state = H * P * N * 4
+    tok_in = H * P * 2 + H * 4 + 2 * G * N * 2
+    entry = H * P * 2 + H * 4 + G * N * 2
+    y_b = H * P * 2
+    copy_b = R * (state * (T1 + 1) + T1 * (tok_in + y_b))
+    total, folds = 0, 0
+    k = [0] * R
+    for n_run, counted in ((warm, False), (S, True)):
+        for step in range(n_run):
+            for r in range(R):
+                kept = int(acc_np[step % S][r]) + 1
+                b = state + k[r] * entry + T1 * (tok_in + y_b + entry)
+                if k[r] + kept >= W:
+                    b += 2 * state + (k[r] + kept) * entry
+                    k[r] = 0
+                    folds += counted
+                else:
+                    k[r] += kept
+                if counted:
+                    total += b
+    return copy_b, total / S, folds / S
+
+
+def bench_verify(torch, m, args, T=None, p=None, windows=None, static=False):
+    """Copy verify vs ReplaySSM verify at batch 512, verify + commit per step,
+    at one (T, p) and the given windows (the copy flavour does not depend on
+    the window).  With static, also the replay verify through the entry point
+    that allocates nothing, on caller-owned checkpoint and log buffers."""
     import synth
     c = VER
-    H, P, N, G, R, T, W, S = c["H"], c["P"], c["N"], c["G"], c["R"], c["T"], c["W"], c["steps"]
+    H, P, N, G, R, S = c["H"], c["P"], c["N"], c["G"], c["R"], c["steps"]
+    T = c["T"] if T is None else T
+    p = c["p"] if p is None else p
+    windows = [c["W"]] if windows is None else list(windows)
     T1 = T + 1
     gen = torch.Generator(device="cuda")
     gen.manual_seed(SEED + 33 + 17 * args.rank)
     A, D = head_params(torch, gen, H)
-    acc = torch.from_numpy(synth.accept_counts(SEED, S, R, T, c["p"])).cuda()
+    acc = torch.from_numpy(synth.accept_counts(SEED, S, R, T, p)).cuda()
+    acc_np = acc.cpu().numpy()
     n_sets = 4  # distinct step inputs, cycled
     ins = [step_inputs(torch, gen, R, H, P, G, N, n_tok=T1) for _ in range(n_sets)]
     y = torch.empty((R, T1, H, P), dtype=torch.bfloat16, device="cuda")
     slots = list(range(R))
     stream = torch.cuda.current_stream()
-    out = {}
-    for mode, name in ((m.SSM_MODE_COPY, "copy"), (m.SSM_MODE_REPLAY, "replay")):
+    peak, _, kind = measured_peaks()
+    warm = 3
+    out = {"replay": {}}
+    runs = [(m.SSM_MODE_COPY, "copy", windows[0])] + [(m.SSM_MODE_REPLAY, "replay", W) for W in windows]
+    for mode, name, W in runs:
         init = (torch.randn((R, H, P, N), generator=gen, device="cuda") * 0.1).contiguous()
         pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, mode, W, T1), R, init)
         del init
@@ -339,7 +380,7 @@ def bench_verify(torch, m, args):
                 verify(pool, slots, T1, x, dt, B, C, A, D, y, stream=stream)
                 m.ssm_state_commit(pool, slots, acc[s % S], False, A, stream=stream)
 
-        run(3)
+        run(warm)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -347,10 +388,18 @@ def bench_verify(torch, m, args):
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
+        paths = m.ssm_last_path(pool)
         st, flags = m.ssm_pool_status(pool)
         assert st == m.SSM_OK and flags == 0, f"{name} verify raised device flags {flags}"
-        out[name] = dict(us_per_step=1000.0 * ms / S)
-        if mode == m.SSM_MODE_COPY:  # plain decode step at the same batch, for the ratio
+        copy_b, replay_b, folds = _verify_bytes(acc_np, R, H, P, N, G, T1, W, S, warm)
+        b = copy_b if mode == m.SSM_MODE_COPY else replay_b
+        us = 1000.0 * ms / S
+        gbs = b / (us * 1e-6) / 1e9
+        rec = dict(us_per_step=us, algorithmic_bytes=b, achieved_gbs=gbs, frac_of_hbm=gbs / peak,
+                   frac_of_nominal_8tbs=gbs / 8000.0)
+        if mode == m.SSM_MODE_COPY:
+            out["copy"] = rec
+            # plain decode step at the same batch, for the ratios
             xd, dtd, Bd, Cd = (t[:, 0].contiguous() for t in ins[0])
             yd = torch.empty((R, H, P), dtype=torch.bfloat16, device="cuda")
             for _ in range(3):
@@ -362,43 +411,61 @@ def bench_verify(torch, m, args):
             e1.record(stream)
             torch.cuda.synchronize()
             out["plain_decode_us"] = 1000.0 * e0.elapsed_time(e1) / S
+        else:
+            rec.update(W=W, folds_per_step=folds, commit_path=paths,
+                       over_plain=us / out["plain_decode_us"], copy_over_replay=out["copy"]["us_per_step"] / us)
+            out["replay"][str(W)] = rec
         m.ssm_state_destroy(pool)
-    # algorithmic bytes per step.  Copy: read the state, write T+1 states,
-    # token inputs and outputs.  Replay: read the checkpoint and the k logged
-    # entries, token inputs and outputs, stage the step's entries after the
-    # log; a fold reads the checkpoint and its m entries and writes the
-    # checkpoint.  Log lengths and folds follow the commit rule on the same
-    # accept counts (integer bookkeeping only).
-    state = H * P * N * 4
-    tok_in = H * P * 2 + H * 4 + 2 * G * N * 2
-    entry = H * P * 2 + H * 4 + G * N * 2
-    y_b = H * P * 2
-    copy_b = R * (state * (T1 + 1) + T1 * (tok_in + y_b))
-    accs = acc.cpu().numpy()
-    total = 0
-    k = [0] * R
-    for n_run, counted in ((3, False), (S, True)):  # the warm-up run, then the timed one
-        for step in range(n_run):
-            for r in range(R):
-                kept = int(accs[step % S][r]) + 1
-                b = state + k[r] * entry + T1 * (tok_in + y_b + entry)
-                if k[r] + kept >= W:
-                    b += 2 * state + (k[r] + kept) * entry
-                    k[r] = 0
-                else:
-                    k[r] += kept
-                if counted:
-                    total += b
-    replay_b = total / S
-    peak, _, kind = measured_peaks()
-    for name, b in (("copy", copy_b), ("replay", replay_b)):
-        gbs = b / (out[name]["us_per_step"] * 1e-6) / 1e9
-        out[name].update(algorithmic_bytes=b, achieved_gbs=gbs, frac_of_hbm=gbs / peak)
+    if static:
+        # the entry point that allocates nothing: verify only (the caller folds), logs of the lengths the
+        # commit rule gives mid-run, against the pool's verify alone at the same lengths
+        W = windows[0]
+        Wc = W - 1 + T1
+        ckpt = (torch.randn((R, H, P, N), generator=gen, device="cuda") * 0.1).contiguous()
+        log_x = torch.randn((R, Wc, H, P), generator=gen, device="cuda").bfloat16()
+        log_dt = torch.full((R, Wc, H), 0.1, device="cuda")
+        log_B = torch.randn((R, Wc, G, N), generator=gen, device="cuda").bfloat16()
+        log_len = torch.randint(0, W, (R,), generator=gen, device="cuda", dtype=torch.int32)
+        flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def run_static(n):
+            for s in range(n):
+                x, dt, B, C = ins[s % n_sets]
+                assert m.ssm_verify_replay_static(R, T1, H, P, N, G, W, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, ckpt,
+                                                  log_x, log_dt, log_B, log_len, x, dt, B, C, A, D, y, flags,
+                                                  stream=stream) == m.SSM_OK
+        run_static(warm)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run_static(S)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert int(flags.item()) == 0
+        out["static_verify_us"] = 1000.0 * e0.elapsed_time(e1) / S
+        out["static_path"] = m.ssm_last_path(None)
+        del ckpt, log_x, log_dt, log_B
     out["hbm_peak_source"] = kind
     out["copy_over_plain"] = out["copy"]["us_per_step"] / out["plain_decode_us"]
-    out["replay_over_plain"] = out["replay"]["us_per_step"] / out["plain_decode_us"]
-    out["config"] = dict(batch=R, T=T, p=c["p"], W=W, steps=S, heads=H, headdim=P, dstate=N, groups=G)
+    out["config"] = dict(batch=R, T=T, p=p, windows=windows, steps=S, heads=H, headdim=P, dstate=N, groups=G)
     return out
+
+
+def bench_verify_sweep(torch, m, args):
+    """Every (T, p, W) point of the speculative verify workload at batch 512:
+    T in {4, 8}, p in {0.6, 0.8}, W in {8, 16, 32}; verify + commit per step."""
+    pts = []
+    for T in (4, 8):
+        for p in (0.6, 0.8):
+            r = bench_verify(torch, m, args, T=T, p=p, windows=(8, 16, 32))
+            for W, rec in r["replay"].items():
+                pts.append(dict(T=T, p=p, W=int(W), copy_us=r["copy"]["us_per_step"],
+                                copy_frac_of_hbm=r["copy"]["frac_of_hbm"], replay_us=rec["us_per_step"],
+                                replay_frac_of_hbm=rec["frac_of_hbm"], replay_frac_of_nominal=rec["frac_of_nominal_8tbs"],
+                                folds_per_step=rec["folds_per_step"], copy_over_replay=rec["copy_over_replay"],
+                                replay_over_plain=rec["over_plain"], commit_path=rec["commit_path"]))
+    return dict(points=pts, config=dict(batch=VER["R"], steps=VER["steps"], heads=VER["H"], headdim=VER["P"],
+                                        dstate=VER["N"], groups=VER["G"]))
 
 
 def bench_prefill(torch, m, args):
@@ -440,16 +507,17 @@ def bench_prefill(torch, m, args):
     alg = 2 * R * L * H * P * 2 + R * L * (H * 2 + 2 * G * N * 2) + R * H * P * N * 4
     return dict(us_per_scan=1000 * ms, tokens_per_s=R * L / (ms / 1000), path=path,
                 achieved_gbs=alg / (ms / 1000) / 1e9, algorithmic_bytes=alg,
+                frac_of_hbm=alg / (ms / 1000) / 1e9 / measured_peaks()[0],
                 config=dict(seqs=R, seqlen=L, heads=H, headdim=P, dstate=N, groups=G, includes="reset + scan"))
 
 
-def bench_prefill_varlen(torch, m, args):
-    """2.7B-shaped layer (80 heads of 64, dstate 128, one group): 64 packed
-    sequences with lengths U(512, 8192), fed as user chunks of 1024 tokens
-    (each call packs the next chunk of every live sequence).  Time per wave
-    of all 64 sequences, from reset."""
+def bench_prefill_varlen(torch, m, args, chunk=1024, S=64):
+    """2.7B-shaped layer (80 heads of 64, dstate 128, one group): S packed
+    sequences (64 in the workload) with lengths U(512, 8192), fed as user
+    chunks of `chunk` tokens (each call packs the next chunk of every live
+    sequence).  Time per wave of all sequences, from reset."""
     import synth
-    H, P, N, G, S, chunk = 80, 64, 128, 1, 64, 1024
+    H, P, N, G = 80, 64, 128, 1
     lens = synth.varlen_lengths(SEED + 4000, S, 512, 8192)
     total = int(lens.sum())
     gen = torch.Generator(device="cuda")
@@ -501,6 +569,7 @@ def bench_prefill_varlen(torch, m, args):
     alg = 2 * total * H * P * 2 + total * (H * 2 + 2 * G * N * 2) + S * H * P * N * 4
     return dict(ms_per_wave=ms, tokens=total, tokens_per_s=total / (ms / 1000), path=path,
                 achieved_gbs=alg / (ms / 1000) / 1e9, algorithmic_bytes=alg, calls_per_wave=len(calls),
+                frac_of_hbm=alg / (ms / 1000) / 1e9 / measured_peaks()[0],
                 config=dict(seqs=S, lengths="U(512, 8192)", user_chunk=chunk, heads=H, headdim=P, dstate=N,
                             groups=G, includes="reset + every chunk call"))
 
@@ -753,36 +822,128 @@ def cpu_model():
     return "unknown"
 
 
-def cpu_baseline(budget_s=12.0):
-    """The oracle (fp64, OpenMP over (request, head)) on a bounded sample of
-    the decode workload: all 128 heads of a few requests for a few tokens."""
+def _cpu_inputs(R, T1, H, P, N, G, seed):
+    """Widened (exact) bf16 x / B / C and fp32 dt of R requests x T1 tokens, from synth."""
+    import synth
+    x, dt, B, C = synth.batch_tokens(seed, 0, R, T1, H, P, G, N, synth.BF16, synth.F32)
+    return (synth.widen(x, synth.BF16), synth.widen(dt, synth.F32), synth.widen(B, synth.BF16),
+            synth.widen(C, synth.BF16))
+
+
+def _time_cpu(fn, budget_s):
+    """Run fn() (one unit of work, returning the units it did) until about budget_s has passed."""
+    units, t0 = 0, time.perf_counter()
+    while True:
+        units += fn()
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return units, el
+
+
+def cpu_workloads(budget_s=1.5):
+    """The oracle's fp32 instantiation (the same loops with fp32 values and
+    accumulators, OpenMP over independent (request, head) pairs, or a thread
+    per (sequence, head) for the scans) on the host cores, on bounded samples
+    of each workload, on all cores and on one core.  Rates are scaled to each
+    workload's own unit (tokens per second, or microseconds per step of the
+    whole batch)."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
     import synth
+    all_cores = oracle.f32_threads()
+    out = {}
+    # decode (batch 256 at Nemotron heads): tok/s
     c = DEC
     H, P, N, G = c["H"], c["P"], c["N"], c["G"]
     A, D = synth.head_params(SEED, H)
+    x, dt, B, C = (a[:, 0] for a in _cpu_inputs(32, 1, H, P, N, G, SEED + 1))
+    for name, n_thr in (("all_cores", all_cores), ("one_core", 1)):
+        oracle.f32_set_threads(n_thr)
+        R = 32 if n_thr > 1 else 4
+        st = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(R)]).astype(np.float32)
+        xs, dts, Bs, Cs = x[:R], dt[:R], B[:R], C[:R]
+        units, el = _time_cpu(lambda: (oracle.f32_decode_step(st, xs, dts, Bs, Cs, A, D), R)[1], budget_s)
+        out.setdefault("decode", {})[name] = dict(value=units / el, unit="tok/s", threads=n_thr,
+                                                   sample=f"{R} requests x all {H} heads per token")
+    # speculative verify at batch 512, T = 8 (copy: T+1 states written; replay: checkpoint + log, fold when
+    # the window fills): microseconds per verify step of all 512 requests
+    v = VER
+    T1, W, Rfull = v["T"] + 1, v["W"], v["R"]
+    xs, dts, Bs, Cs = _cpu_inputs(8, T1, H, P, N, G, SEED + 2)
+    acc = synth.accept_counts(SEED, 64, 8, v["T"], v["p"])
+    Wc = W - 1 + T1
+    for name, n_thr in (("all_cores", all_cores), ("one_core", 1)):
+        oracle.f32_set_threads(n_thr)
+        R = 8 if n_thr > 1 else 1
+        st = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(R)]).astype(np.float32)
+        units, el = _time_cpu(lambda: (oracle.f32_verify_copy(st, xs[:R], dts[:R], Bs[:R], Cs[:R], A, D), R)[1],
+                              budget_s)
+        out.setdefault("verify_copy_b512", {})[name] = dict(
+            value=1e6 * el / units * Rfull, unit="us/step", threads=n_thr,
+            sample=f"{R} requests x 1 verify step of {T1} tokens (T={v['T']}), scaled to {Rfull} requests")
+        lx = np.zeros((R, Wc, H, P), np.float32)
+        ldt = np.zeros((R, Wc, H), np.float32)
+        lB = np.zeros((R, Wc, G, N), np.float32)
+        k = np.zeros(R, np.int32)
+        step = [0]
 
-    def run(R, steps):
-        st = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(R)]).astype(np.float64)
-        ins = [tuple(a[:, 0] for a in synth.batch_tokens(SEED, s, R, 1, H, P, G, N, synth.BF16, synth.F32))
-               for s in range(steps)]
-        ins = [tuple(synth.widen(a, code) for a, code in zip(t, (synth.BF16, synth.F32, synth.BF16, synth.BF16)))
-               for t in ins]
-        t0 = time.perf_counter()
-        for x, dt, B, C in ins:
-            oracle.decode_step(st, x, dt, B, C, A, D)
-        return time.perf_counter() - t0
+        def replay_step():  # verify, then the commit rule: append below the window, else fold
+            s_ = step[0] % 64
+            oracle.f32_verify_replay(st, k, lx, ldt, lB, xs[:R], dts[:R], Bs[:R], Cs[:R], A, D)
+            cnt = acc[s_][:R] + 1
+            fold = (k + cnt >= W).astype(np.int32)
+            if fold.any():
+                oracle.f32_fold(st, k, cnt, fold, lx, ldt, lB, xs[:R], dts[:R], Bs[:R], A)
+            for r in range(R):
+                if fold[r]:
+                    k[r] = 0
+                else:
+                    lx[r, k[r]:k[r] + cnt[r]] = xs[r, :cnt[r]]
+                    ldt[r, k[r]:k[r] + cnt[r]] = dts[r, :cnt[r]]
+                    lB[r, k[r]:k[r] + cnt[r]] = Bs[r, :cnt[r]]
+                    k[r] += cnt[r]
+            step[0] += 1
+            return R
+        units, el = _time_cpu(replay_step, budget_s)
+        out.setdefault("verify_replay_b512", {})[name] = dict(
+            value=1e6 * el / units * Rfull, unit="us/step", threads=n_thr,
+            sample=f"{R} requests x {step[0]} verify + commit steps (T={v['T']}, p={v['p']}, W={W}), "
+                   f"scaled to {Rfull} requests")
+    # prefill: one thread per (sequence, head) sequential scan; tok/s of the whole layer
+    for key, (Hh, L) in (("prefill_130m", (PRE["H"], 512)), ("prefill_2p7b_varlen", (80, 512))):
+        xs, dts, Bs, Cs = (np.ascontiguousarray(a[0], np.float32) for a in _cpu_inputs(1, L, Hh, 64, 128, 1, SEED + 3))
+        Ah, Dh = synth.head_params(SEED, Hh)
+        for name, n_thr in (("all_cores", all_cores), ("one_core", 1)):
+            heads = list(range(Hh)) if n_thr > 1 else [0, 1]
 
-    probe = run(8, 1)
-    per = probe / 8
-    R = int(max(8, min(256, budget_s / max(per, 1e-6) / 4)))
-    steps = 4
-    secs = run(R, steps)
-    return dict(value=R * steps / secs, unit="tok/s", cores=oracle.threads(), cpu=cpu_model(), kind="oracle",
-                sample=f"{R} requests x {steps} decode tokens, all {H} heads (fp64 oracle, OpenMP)",
-                seconds=secs)
+            def scan_all():
+                y = np.empty((L, Hh, 64), np.float32)
+
+                def one(h):
+                    st = np.zeros((64, 128), np.float32)
+                    oracle.f32_scan_head(st, xs[:, h], dts[:, h], Bs[:, 0], Cs[:, 0], Ah[h], Dh[h],
+                                         Hh * 64, Hh, 128, y[:, h], Hh * 64)
+                with cf.ThreadPoolExecutor(max_workers=n_thr) as ex:
+                    list(ex.map(one, heads))
+                return L * len(heads) / Hh  # tokens of the whole layer (all heads)
+            units, el = _time_cpu(scan_all, budget_s)
+            out.setdefault(key, {})[name] = dict(value=units / el, unit="tok/s", threads=n_thr,
+                                                 sample=f"1 sequence x {L} tokens x {len(heads)} of {Hh} heads")
+    oracle.f32_set_threads(all_cores)
+    return out
+
+
+def cpu_baseline(budget_s=1.5):
+    """CPU baseline of every workload (the oracle's fp32 instantiation on all
+    host cores and on one), with the decode rate on all cores as the headline."""
+    w = cpu_workloads(budget_s)
+    dec = w["decode"]["all_cores"]
+    return dict(value=dec["value"], unit="tok/s", cores=dec["threads"], cpu=cpu_model(), kind="oracle",
+                precision="fp32 values and accumulators (the fp64 parity oracle is not the speed baseline)",
+                sample=dec["sample"], workloads=w)
 
 
 # ---------------------------------------------------------------------------
@@ -805,15 +966,15 @@ def run_case(args):
     elif args.case == "verify":
         VER["R"] = args.batch or VER["R"]
         VER["steps"] = 4
-        out = bench_verify(torch, m, args)
+        out = bench_verify(torch, m, args, T=args.T or None, windows=[args.W] if args.W else None)
         print(json.dumps({"case": "verify", "batch": VER["R"], "copy_us": out["copy"]["us_per_step"],
-                          "replay_us": out["replay"]["us_per_step"]}))
+                          "replay_us": {w: r["us_per_step"] for w, r in out["replay"].items()}}))
     elif args.case == "prefill":
         PRE["R"] = args.batch or PRE["R"]
         out = bench_prefill(torch, m, args)
         print(json.dumps({"case": "prefill", "seqs": PRE["R"], "us": out["us_per_scan"], "path": out["path"]}))
     elif args.case == "prefill_varlen":
-        out = bench_prefill_varlen(torch, m, args)
+        out = bench_prefill_varlen(torch, m, args, chunk=args.chunk or 1024, S=args.batch or 64)
         print(json.dumps({"case": "prefill_varlen", "ms": out["ms_per_wave"], "path": out["path"]}))
     elif args.case == "graph":
         print(json.dumps({"case": "graph", **bench_graph_small_batch(torch, m, args)}))
@@ -826,29 +987,46 @@ def run_case(args):
 
 
 def run_reference(args):
-    """The oracle as the reference arm: rank 0 times it on the host cores."""
+    """The oracle as the reference arm: rank 0 times its fp32 instantiation
+    (OpenMP over (request, head) on all host cores) on the decode workload,
+    W untimed warm-up steps and K timed steps, each step a bounded sample of
+    the batch-256 decode (a few requests, all heads, one token)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    import numpy as np
+
+    import oracle
+    import synth
     steps, warmup = max(1, args.steps), max(0, args.warmup)
-    # each step: a bounded sample of the decode workload
-    base = cpu_baseline(budget_s=6.0)
+    c = DEC
+    H, P, N, G = c["H"], c["P"], c["N"], c["G"]
+    A, D = synth.head_params(SEED, H)
+    R = 16
+    st = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(R)]).astype(np.float32)
+    x, dt, B, C = (a[:, 0] for a in _cpu_inputs(R, 1, H, P, N, G, SEED + 1))
+    cores = oracle.f32_threads()
+
+    def one_step():
+        t0 = time.perf_counter()
+        oracle.f32_decode_step(st, x, dt, B, C, A, D)
+        return time.perf_counter() - t0
+
     for _ in range(warmup):
-        pass
-    vals = [base["value"]]
-    t_total = base["seconds"]
-    for _ in range(min(steps, 3) - 1):
-        b = cpu_baseline(budget_s=6.0)
-        vals.append(b["value"])
-        t_total += b["seconds"]
-    v = statistics.median(vals)
+        one_step()
+    secs = [one_step() for _ in range(steps)]
+    total = sum(secs)
+    v = R * steps / total
+    sample = f"{R} of the 256 requests x all {H} heads, one decode token per step (fp32 oracle, OpenMP)"
     line = {"impl": "reference", "metric": "decode state-update tok/s", "value": v, "unit": "tok/s",
-            "n_gpus": args.gpus, "steps": len(vals), "warmup": warmup, "ms_per_step": 1000 * t_total / len(vals),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "n_gpus": args.gpus, "steps": steps, "warmup": warmup, "ms_per_step": 1000 * total / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": "decode B=256 H=128 P=64 N=128 G=8 (sampled requests)", "l2": "state > L2"},
-            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": base["cores"], "cpu": base["cpu"], "kind": "oracle",
-                             "sample": base["sample"]},
+            "config": {"workload": "batched decode, 256 requests x 64 successive tokens, heads 128 x headdim 64 x "
+                                   "dstate 128, 8 groups, bf16 x/B/C, fp32 dt and state (sampled requests)",
+                       "l2": "state > L2"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": cores, "cpu": cpu_model(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -876,6 +1054,9 @@ def main():
     ap.add_argument("--case", choices=("decode", "verify", "prefill", "prefill_varlen", "graph", "gdn"),
                     help="run one workload alone (for profiler captures)")
     ap.add_argument("--batch", type=int, default=0, help="batch / sequence count of --case")
+    ap.add_argument("--T", type=int, default=0, help="drafts per verify step of --case verify")
+    ap.add_argument("--chunk", type=int, default=0, help="user chunk of --case prefill_varlen (256 or 1024)")
+    ap.add_argument("--W", type=int, default=0, help="replay window of --case verify")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -906,9 +1087,11 @@ def main():
 
     extras = {}
     if not args.no_extras:
-        extras["verify_b512"] = bench_verify(torch, m, args)
+        extras["verify_b512"] = bench_verify(torch, m, args, static=True)
+        extras["verify_b512_sweep"] = bench_verify_sweep(torch, m, args)
         extras["prefill"] = bench_prefill(torch, m, args)
-        extras["prefill_varlen"] = bench_prefill_varlen(torch, m, args)
+        extras["prefill_varlen"] = bench_prefill_varlen(torch, m, args, chunk=1024)
+        extras["prefill_varlen_chunk256"] = bench_prefill_varlen(torch, m, args, chunk=256)
         extras["replay_plain_decode_b256"] = bench_replay_plain_decode(torch, m, args)
         extras["graph_small_batch"] = bench_graph_small_batch(torch, m, args)
         extras["gdn_b256"] = bench_gdn(torch, m, args)
@@ -950,7 +1133,6 @@ def main():
     line.update(extras)
     if not args.no_extras:
         line["cpu_baseline"] = cpu_baseline()
-        line["cpu_baseline"].pop("seconds", None)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

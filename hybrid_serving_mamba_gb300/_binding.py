@@ -384,8 +384,10 @@ def ssm_pool_status(pool: Pool, clear: bool = False, stream=None):
     return st, int(f.value)
 
 
-def ssm_last_path(pool: Pool) -> str:
-    return _lib.ssm_last_path(pool.handle).decode()
+def ssm_last_path(pool) -> str:
+    """Kernel path of the pool's last hot-path call; with pool None, that of
+    this thread's last ssm_verify_replay_static call."""
+    return _lib.ssm_last_path(None if pool is None else pool.handle).decode()
 
 
 def ssm_pool_bytes(pool: Pool) -> int:

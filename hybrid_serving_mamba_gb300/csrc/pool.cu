@@ -614,7 +614,7 @@ ssm_status ssm_pool_status(ssm_pool pool, uint32_t *flags_out, int32_t clear, ss
     return SSM_OK;
 }
 
-const char *ssm_last_path(ssm_pool pool) { return pool ? pool->p.last_path : "none"; }
+const char *ssm_last_path(ssm_pool pool) { return pool ? pool->p.last_path : ssm::static_last_path(); }
 
 size_t ssm_pool_bytes(ssm_pool pool) { return pool ? pool->p.bytes : 0; }
 

@@ -547,21 +547,47 @@ static __device__ __align__(256) float g_noalloc_scratch[kStaticScratchFloats];
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float *g_noalloc_ptr[kMaxDevices] = {};
+CUcontext g_noalloc_ctx[kMaxDevices] = {};
+thread_local const char *g_noalloc_path = "none";
+
+using CtxGetCurrent = CUresult (*)(CUcontext *);
+
+// The driver's cuCtxGetCurrent, looked up through the runtime once per process.
+CtxGetCurrent ctx_get_current() {
+    static const CtxGetCurrent fn = []() -> CtxGetCurrent {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<CtxGetCurrent>(f);
+    }();
+    return fn;
+}
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a stand-in for the symbol, so the address is
-// looked up once per device, with that device current.
+// looked up with the device current: once per device, and again whenever
+// the device's context is not the one the address was taken in (after a
+// cudaDeviceReset the runtime makes a new primary context, in which the
+// library's module, and so the array, may sit at another address).
 cudaError_t noalloc_scratch(float **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const CtxGetCurrent get = ctx_get_current();
+    if (!get) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;  // null until the runtime has made the device's context current
+    if (get(&ctx) != CUDA_SUCCESS) return cudaErrorNotSupported;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!ctx || !g_noalloc_ptr[dev] || g_noalloc_ctx[dev] != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // also makes the primary context current
         if (e != cudaSuccess) return e;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorNotSupported;
         g_noalloc_ptr[dev] = static_cast<float *>(p);
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = g_noalloc_ptr[dev];
     return cudaSuccess;
@@ -594,6 +620,7 @@ extern "C" ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int
 
     // launch geometry only: a Pool describing the caller's buffers (no allocation)
     Pool view;
+    view.device = 0;
     view.cfg.nheads = nheads; view.cfg.headdim = headdim; view.cfg.dstate = dstate; view.cfg.ngroups = ngroups;
     view.cfg.input_dtype = input_dtype; view.cfg.dt_dtype = dt_dtype; view.cfg.mode = SSM_MODE_REPLAY;
     view.cfg.window = window; view.cfg.max_tokens = n_tok;
@@ -601,8 +628,11 @@ extern "C" ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int
     view.t1max = n_tok; view.wcap = wcap; view.n_slots = batch; view.cb_w = cb_w;
     int dev = 0, max_smem = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&view.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SSM_ERR_CUDA;
+    view.device = dev;
+    if (view.sm_count < 1) view.sm_count = 1;  // the persistent kernels size their grids by it
     if (replay_smem_bytes(view, n_tok) > (size_t)max_smem || replay_prep_smem_bytes(view, n_tok) > (size_t)max_smem)
         return SSM_ERR_INVALID_ARG;
 
@@ -631,6 +661,12 @@ extern "C" ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int
     a.check_log = 1;
     a.batch = batch;
     for (int i = 0; i < batch; ++i) a.slots[i] = i;  // request i owns row i of every caller buffer
-    const cudaError_t e = launch_verify_replay(view, a, s);
+    const char *path = "verify_replay";
+    const cudaError_t e = launch_verify_replay(view, a, s, &path);
+    g_noalloc_path = e == cudaSuccess ? path : "none";
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
+
+namespace ssm {
+const char *static_last_path() { return g_noalloc_path; }
+}  // namespace ssm

@@ -122,13 +122,27 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
     if (warp == ncw) {
         // ------------------------------------------------------------ producer
         const size_t in_b = sizeof(TI);
+        // the last item issued to each stage: before the producer leaves, normally or after a wait
+        // that ran out, every copy it issued has landed (bounded waits), so none is still writing
+        // shared memory when the CTA exits, even if the consumers have already left
+        int last[kStages];
+        for (int s = 0; s < kStages; ++s) last[s] = -1;
+        auto drain = [&]() {
+            if (lane == 0)
+                for (int s = 0; s < kStages; ++s)
+                    if (last[s] >= 0 && !mbar_wait(&full[s], (uint32_t)(last[s] / kStages) & 1u))
+                        atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+            __syncwarp();
+        };
         int n = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int st = n % kStages;
             if (n >= kStages && !mbar_wait(&empty[st], (uint32_t)((n / kStages) - 1) & 1u)) {
                 if (lane == 0) atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+                drain();
                 return;
             }
+            last[st] = n;
             const int i = item / H, h = item - i * H;
             const int slot = a.slots[i];
             const int g = h / a.hpg;
@@ -188,6 +202,7 @@ __global__ void __launch_bounds__(kPipeMaxThreads) verify_replay_pipe_kernel(con
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
         }
+        drain();
         return;
     }
 
@@ -370,13 +385,25 @@ __global__ void __launch_bounds__(kPipeMaxThreads) fold_pipe_kernel(const __grid
         const size_t in_b = sizeof(TI);
         const TI *lx = reinterpret_cast<const TI *>(a.log_x);
         const TI *lB = reinterpret_cast<const TI *>(a.log_B);
+        // as in the verify's producer: every issued copy has landed before the producer leaves
+        int last[kStages];
+        for (int s = 0; s < kStages; ++s) last[s] = -1;
+        auto drain = [&]() {
+            if (lane == 0)
+                for (int s = 0; s < kStages; ++s)
+                    if (last[s] >= 0 && !mbar_wait(&full[s], (uint32_t)(last[s] / kStages) & 1u))
+                        atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+            __syncwarp();
+        };
         int n = 0;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int st = n % kStages;
             if (n >= kStages && !mbar_wait(&empty[st], (uint32_t)((n / kStages) - 1) & 1u)) {
                 if (lane == 0) atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+                drain();
                 return;
             }
+            last[st] = n;
             const int f = item / H, h = item - f * H;
             const int2 it = a.fold_items[f];
             const int m = it.y;
@@ -407,6 +434,7 @@ __global__ void __launch_bounds__(kPipeMaxThreads) fold_pipe_kernel(const __grid
             __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
         }
+        drain();
         return;
     }
 

@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
 
 constexpr int kMaxStages = 8;
 constexpr int kLogPairs = 4;  // log tokens per warp = 2 * kLogPairs, so the log capacity is at most 32
+constexpr int kMaxTmaLog = 64;  // log capacity the tensor-core kernel and the fold take (a box is <= 256 rows)
 
 // Byte offsets inside one ring stage, and of the areas after the ring.
 struct TmaLayout {
@@ -1015,35 +1016,38 @@ TensorMapEncode tensor_map_encoder() {
 }
 
 bool replay_tma_encode(Pool &p) {
-    p.tm_ok = false;
+    p.tm_ok = p.tm_tc_ok = p.tm_fold_ok = false;
+    p.fold_kp = 0;
     if (p.cfg.mode != SSM_MODE_REPLAY) return false;
-    if (p.N % 32 != 0 || p.N > 128 || p.P % 8 != 0 || p.P > 64 || p.wcap > 8 * kLogPairs ||
+    if (p.N % 32 != 0 || p.N > 128 || p.P % 8 != 0 || p.P > 64 || p.wcap > kMaxTmaLog ||
         ((size_t)p.P * p.in_bytes) % 16 != 0)
         return false;
     const TensorMapEncode enc = tensor_map_encoder();
     if (!enc) return false;
-    // checkpoint: rows (slot, head, p) of N fp32 values; box 32 columns x P rows, 128-byte swizzle
     const cuuint64_t sd[2] = {(cuuint64_t)p.N, (cuuint64_t)p.n_slots * p.H * p.P};
     const cuuint64_t ss[1] = {(cuuint64_t)p.N * 4};
-    const cuuint32_t sb[2] = {32u, (cuuint32_t)p.P};
     const cuuint32_t se[2] = {1u, 1u};
-    if (enc(&p.tm_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.state, sd, ss, sb, se, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-        CUDA_SUCCESS)
-        return false;
-    // log x: [slot * wcap + s][head][p]; box = one head's whole log (wcap rows of P)
     const cuuint64_t xd[3] = {(cuuint64_t)p.P, (cuuint64_t)p.H, (cuuint64_t)p.n_slots * p.wcap};
     const cuuint64_t xst[2] = {(cuuint64_t)p.P * p.in_bytes, (cuuint64_t)p.H * p.P * p.in_bytes};
-    const cuuint32_t xb[3] = {(cuuint32_t)p.P, 1u, (cuuint32_t)p.wcap};
     const cuuint32_t xe[3] = {1u, 1u, 1u};
     const CUtensorMapDataType xt =
         p.cfg.input_dtype == SSM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    if (enc(&p.tm_logx, xt, 3, p.log_x, xd, xst, xb, xe, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
-    p.tm_ok = true;
-    // tensor-core kernel: pairs of heads of P = 64 rows, 32-column boxes of both heads' rows
-    if (p.P == 64 && p.H % 2 == 0 && p.hpg % 2 == 0 && p.cb_w == 32) {
+    // CUDA-core kernel (it holds the log's x rows in registers, so the log capacity is at most 32):
+    // checkpoint rows (slot, head, p) of N fp32 values, box 32 columns x P rows, 128-byte swizzle;
+    // log x [slot * wcap + s][head][p], box = one head's whole log (wcap rows of P)
+    if (p.wcap <= 8 * kLogPairs) {
+        const cuuint32_t sb[2] = {32u, (cuuint32_t)p.P};
+        const cuuint32_t xb[3] = {(cuuint32_t)p.P, 1u, (cuuint32_t)p.wcap};
+        p.tm_ok = enc(&p.tm_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.state, sd, ss, sb, se,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+                  enc(&p.tm_logx, xt, 3, p.log_x, xd, xst, xb, xe, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    // tensor-core kernel: pairs of heads of P = 64 rows, 32-column boxes of both heads' rows, and both
+    // heads' whole logs of x rows (any capacity up to kMaxTmaLog)
+    if (p.P == 64 && p.H % 2 == 0 && p.hpg % 2 == 0) {
         const cuuint32_t sb2[2] = {32u, 128u};
         const cuuint32_t xb2[3] = {(cuuint32_t)p.P, 2u, (cuuint32_t)p.wcap};
         p.tm_tc_ok = enc(&p.tm_state2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.state, sd, ss, sb2, se,
@@ -1053,17 +1057,20 @@ bool replay_tma_encode(Pool &p) {
                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         // the fold's B operand: logged rows s of group g, [slot * wcap + s][g][n] bf16, boxes of
-        // 32 rows x 64 columns with the 128-byte swizzle (an MN-major operand tile)
-        if (p.tm_tc_ok && p.cfg.input_dtype == SSM_DTYPE_BF16 && p.N == 128 && p.wcap <= 32) {
+        // fold_kp rows (the log capacity rounded up to a K step multiple: 32, 48 or 64) x 64 columns
+        // with the 128-byte swizzle (an MN-major operand tile)
+        const int kp = p.wcap <= 32 ? 32 : (p.wcap + 15) / 16 * 16;
+        if (p.tm_tc_ok && p.cfg.input_dtype == SSM_DTYPE_BF16 && p.N == 128 && kp <= kMaxFoldK) {
             const cuuint64_t bd[3] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)p.n_slots * p.wcap};
             const cuuint64_t bst[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2};
-            const cuuint32_t bb[3] = {64u, 1u, 32u};
+            const cuuint32_t bb[3] = {64u, 1u, (cuuint32_t)kp};
             p.tm_fold_ok = enc(&p.tm_logB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.log_B, bd, bst, bb, xe,
                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            if (p.tm_fold_ok) p.fold_kp = kp;
         }
     }
-    return true;
+    return p.tm_ok || p.tm_tc_ok;
 }
 
 size_t replay_coef_smem_bytes(const Pool &pool, int n_tok) {
@@ -1072,10 +1079,10 @@ size_t replay_coef_smem_bytes(const Pool &pool, int n_tok) {
 }
 
 cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path) {
-    if (!pool.tm_ok || !a.wsc || !a.cf || !a.dec) return cudaErrorNotSupported;
+    if ((!pool.tm_ok && !pool.tm_tc_ok) || !a.wsc || !a.cf || !a.dec) return cudaErrorNotSupported;
     const bool bf = pool.cfg.input_dtype == SSM_DTYPE_BF16;
     const int in_b = bf ? 2 : 4;
-    if (a.N > 128 || a.wcap > 8 * kLogPairs || (a.hpg * a.P * in_b) % 16 || (a.N * in_b) % 16)
+    if (a.N > 128 || a.wcap > kMaxTmaLog || (a.hpg * a.P * in_b) % 16 || (a.N * in_b) % 16)
         return cudaErrorNotSupported;
     if (reinterpret_cast<uintptr_t>(a.x) % 16 || reinterpret_cast<uintptr_t>(a.B) % 16 ||
         reinterpret_cast<uintptr_t>(a.C) % 16)
@@ -1088,10 +1095,11 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
     if (csmem > (size_t)max_smem) return cudaErrorNotSupported;
 
     // the streaming kernel first, since it fixes the layout the coefficient kernel writes C in:
-    // tensor cores take pairs of heads, at most 32 step tokens, whole W rows of 32
+    // tensor cores take pairs of heads and at most 32 step tokens; W rows are whole float4 (cb_w a
+    // multiple of 4, zero past each row's length)
     int NM = 0, nring = 0, naux = 0;
     size_t tsmem = 0;
-    if (pool.tm_tc_ok && T1 <= 32 && T1 <= pool.cf_rows && a.P == 64 && a.cb_w == 32 && a.N <= 128 &&
+    if (pool.tm_tc_ok && T1 <= 32 && T1 <= pool.cf_rows && a.P == 64 && a.cb_w % 4 == 0 && a.N <= 128 &&
         (a.N * in_b) % 128 == 0) {
         NM = T1 <= 16 ? 16 : 32;
         if (NM > pool.cf_rows) NM = 0;
@@ -1112,6 +1120,7 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
                 }
             }
     }
+    if (!nring && (!pool.tm_ok || a.wcap > 8 * kLogPairs)) return cudaErrorNotSupported;
     const TmaLayout L = tma_layout(a.P, a.N, in_b, T1, a.wcap, a.cb_w);
     // The consumer groups take alternate items, so the stage count is a multiple of the group count:
     // a stage then serves one group, which has consumed the stage's previous item before it waits on

@@ -11,7 +11,7 @@
 //   M[i][j] = CB[i][j] exp(cum_i - cum_j) dt_j, j <= i  (CUDA cores, to bf16)
 //   Y       = M X                                      (128 x 64,  K = 128)
 //   Z       = C S^T           (S = state before the chunk, bf16 copy)
-//   dS^T    = B^T (w o X)     w_j = exp(cum_last - cum_j) dt_j
+//   dS^T    = B^T (w o X)     w_j = exp(cum_last - cum_j) dt_j, w o X as bf16 hi + lo
 //   y_i     = Y_i + exp(cum_i) Z_i + D x_i
 //   S      <- exp(cum_last) S + dS
 //
@@ -52,11 +52,14 @@ constexpr uint32_t OFF_M = OFF_C;                  //   then M [i][j], two j blo
 constexpr uint32_t OFF_B = OFF_C + 2 * kTile128;   // B  [j][n]  B of C B^T (K-major); A of dS^T (MN-major)
 constexpr uint32_t OFF_X = OFF_B + 2 * kTile128;   // X  [j][p]  B of Y (MN-major)
 constexpr uint32_t OFF_S = OFF_X + kTile128;       // S  [n][p]  B of Z (MN-major);
-constexpr uint32_t OFF_XW = OFF_S;                 //   then (w o X) [j][p]: B of dS^T (MN-major)
+constexpr uint32_t OFF_XW = OFF_S;                 //   then (w o X)_hi [j][p]: B of dS^T (MN-major)
+constexpr uint32_t OFF_XWLO = OFF_M;               // (w o X)_lo [j][p] in M's first block, once Y has read M
 constexpr uint32_t OFF_MISC = OFF_S + kTile128;
 // misc: cum[128], dt[128], colf[4][128], wsum[4], safe[4], mbarriers (MMA, loads), tmem base, gate
 constexpr uint32_t M_CUM = 0, M_DT = 512, M_COLF = 1024, M_WSUM = 3072, M_SAFE = 3088, M_BAR = 3104,
-                   M_TMEM = 3112, M_GATE = 3116, M_LDBAR = 3120;
+                   M_TMEM = 3112, M_GATE = 3116, M_LDBAR = 3120, M_CMAX = 3136, M_CMIN = 3152;
+// the factored form is taken while exp(+-kFactorRange) stays far inside fp32 (max about exp(88))
+constexpr float kFactorRange = 70.f;
 constexpr uint32_t kSsdSmem = OFF_MISC + 3200 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 256;  // [0,128) C B^T, then dS^T in [64,128); Y in [128,192); Z in [192,256)
 
@@ -103,6 +106,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *s_ldbar = reinterpret_cast<uint64_t *>(misc + M_LDBAR);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(misc + M_TMEM);
     uint32_t *s_gate = reinterpret_cast<uint32_t *>(misc + M_GATE);
+    float *s_cmax = reinterpret_cast<float *>(misc + M_CMAX);  // [4] per row block
+    float *s_cmin = reinterpret_cast<float *>(misc + M_CMIN);  // [4]
 
     const int h = blockIdx.x, i_seq = blockIdx.y;
     const int t0 = a.cu[i_seq], t1 = a.cu[i_seq + 1];
@@ -148,14 +153,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     float S[32];
 #pragma unroll
     for (int p = 0; p < 32; ++p) S[p] = st[(size_t)(p0 + p) * SN + n_col];
-    auto write_state_copy = [&]() {  // bf16 copy, row n of the [n][p] tile, this half's 4 chunks
+    // bf16 copy of sc * S, row n of the [n][p] tile, this half's 4 chunks (the B operand of Z)
+    auto write_state_copy = [&](float sc) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4 *>(smem + OFF_S + chunk_off(n_col, 4 * half + c)) =
-                make_uint4(pack_bf16(S[8 * c + 0], S[8 * c + 1]), pack_bf16(S[8 * c + 2], S[8 * c + 3]),
-                           pack_bf16(S[8 * c + 4], S[8 * c + 5]), pack_bf16(S[8 * c + 6], S[8 * c + 7]));
+                make_uint4(pack_bf16(sc * S[8 * c + 0], sc * S[8 * c + 1]), pack_bf16(sc * S[8 * c + 2], sc * S[8 * c + 3]),
+                           pack_bf16(sc * S[8 * c + 4], sc * S[8 * c + 5]), pack_bf16(sc * S[8 * c + 6], sc * S[8 * c + 7]));
     };
-    write_state_copy();
 
     constexpr uint32_t kIdCB = tc::idesc_bf16_f32(128, 128);                 // K-major x K-major
     constexpr uint32_t kIdY = tc::idesc_bf16_f32(128, 64) | (1u << 16);      // B MN-major
@@ -174,26 +179,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto load_x = [&](int ty) { tma_load_2d(smem + OFF_X, &tm_x, h * SP, ty, s_ldbar); };
     bool bad = false, timeout = false;
     const int L = t1 - t0;
-    // dt of this thread's row, one chunk ahead (a strided load, kept off the chunk's critical path)
-    float dt_next = 0.f;
-    if (half == 1 && row < (L < Q ? L : Q)) dt_next = load_dt(a.dt, (size_t)(t0 + row) * H + h, a.dt_bf16);
-    if (tid == 0) {
-        load_cb(t0);
-        load_x(t0);
-    }
-    for (int c0 = 0; c0 < L; c0 += Q) {
-        const int len = L - c0 < Q ? L - c0 : Q;
-        const bool valid = row < len;
-        const size_t tok = (size_t)(t0 + c0 + row);
 
-        // ---- P1: the chunk's rows of C, B (two 64-column boxes each) and x, issued by TMA into
-        // the swizzled tiles (the layout chunk_off describes) as soon as the previous chunk was
-        // done with each tile; dt prefix sums while they land
-        float dtv = 0.f;
+    // One chunk's dt (rows: warps 4..7): prefix sums cum_i = A (dt_0 + .. + dt_i), and the range of
+    // cum, from which every thread takes the chunk's reference point and whether the factored form
+    // below is safe for it.  Called by every thread.
+    auto chunk_setup = [&](float dtv) {
         if (half == 1) {
-            dtv = dt_next;
             bad |= !isfinite(dtv);
-            // inclusive prefix sum over the 128 rows (warps 4..7)
             float v = dtv;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -204,8 +196,58 @@ __global__ void __launch_bounds__(kThreads, 2)
             s_dt[row] = dtv;
             bar_sync_named(1, 128);
             for (int w = 0; w < rb; ++w) v += s_wsum[w];
-            s_cum[row] = A * v;
+            const float c = A * v;
+            s_cum[row] = c;
+            float mx = c, mn = c;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            }
+            if (lane == 0) {
+                s_cmax[rb] = mx;
+                s_cmin[rb] = mn;
+            }
         }
+        __syncthreads();
+    };
+    // The factored form: exp(cum_i - cum_j) = exp(cum_i - ref) exp(ref - cum_j) with ref = cum at the
+    // middle row of the chunk, so that the decay-masked product is a plain causal mask of C B^T,
+    // shared by every row's scale.  Safe while both factors, and exp(ref) that scales the state copy,
+    // stay far inside fp32 (a NaN range is not safe either: the exact path finds the NaN).
+    auto fast_ok = [&](int len, float &ref_out) -> bool {
+        const float ref = s_cum[(len - 1) >> 1];
+        const float mx = fmaxf(fmaxf(s_cmax[0], s_cmax[1]), fmaxf(s_cmax[2], s_cmax[3]));
+        const float mn = fminf(fminf(s_cmin[0], s_cmin[1]), fminf(s_cmin[2], s_cmin[3]));
+        ref_out = ref;
+        return (mx - ref <= kFactorRange) && (ref - mn <= kFactorRange) && (ref >= -kFactorRange);
+    };
+
+    // chunk 0: its dt, its form, the state copy its Z reads, its tiles
+    float ref = 0.f;
+    bool fast;
+    {
+        const float d0 = (half == 1 && row < (L < Q ? L : Q)) ? load_dt(a.dt, (size_t)(t0 + row) * H + h, a.dt_bf16)
+                                                             : 0.f;
+        chunk_setup(d0);
+        fast = fast_ok(L < Q ? L : Q, ref);
+        write_state_copy(fast ? expf(ref) : 1.f);
+    }
+    float dt_next = 0.f;
+    if (tid == 0) {
+        load_cb(t0);
+        load_x(t0);
+    }
+    for (int c0 = 0; c0 < L; c0 += Q) {
+        const int len = L - c0 < Q ? L - c0 : Q;
+        const bool valid = row < len;
+        const size_t tok = (size_t)(t0 + c0 + row);
+
+        // ---- P1: dt of the next chunk (a strided load, off the critical path); the chunk's rows
+        // of C, B (two 64-column boxes each) and x, issued by TMA into the swizzled tiles as soon as
+        // the previous chunk was done with each tile
+        const int c1 = c0 + Q, len1 = L - c1 < Q ? L - c1 : Q;
+        if (half == 1) dt_next = row < len1 ? load_dt(a.dt, (size_t)(t0 + c1 + row) * H + h, a.dt_bf16) : 0.f;
         if (__syncthreads_or(!mbar_wait(s_ldbar, ld_phase & 1u))) {  // uniform across the CTA
             timeout = true;
             break;
@@ -227,30 +269,30 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const float cum_last = s_cum[Q - 1];
         const float cum = s_cum[row];
-        // column factors colf[r][j] = exp(cum_{32r} - cum_j) dt_j for j < 32 r + 32,
-        // and whether block r's own range keeps them finite
+        const float dtr = s_dt[row];
+        if (!fast) {
+            // exact form: column factors colf[r][j] = exp(cum_{32r} - cum_j) dt_j for j < 32 r + 32,
+            // and whether block r's own range keeps them finite
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int r = 2 * half + q;
-            const float ref = s_cum[32 * r];
-            s_colf[r * Q + row] = row < 32 * r + 32 ? expf(ref - cum) * s_dt[row] : 0.f;
+            for (int q = 0; q < 2; ++q) {
+                const int r = 2 * half + q;
+                const float rf = s_cum[32 * r];
+                s_colf[r * Q + row] = row < 32 * r + 32 ? expf(rf - cum) * dtr : 0.f;
+            }
+            if (tid < 4) s_safe[tid] = (s_cum[32 * tid] - s_cum[32 * tid + 31]) < 80.f;
         }
-        if (tid < 4) s_safe[tid] = (s_cum[32 * tid] - s_cum[32 * tid + 31]) < 80.f;
         tc::fence_proxy_async_smem();
         __syncthreads();
 
-        if (half == 1) {  // dt of the next chunk, while this one is on the tensor cores
-            const int c1 = c0 + Q, len1 = L - c1 < Q ? L - c1 : Q;
-            dt_next = row < len1 ? load_dt(a.dt, (size_t)(t0 + c1 + row) * H + h, a.dt_bf16) : 0.f;
-        }
-
-        // ---- P2: C B^T and Z = C S^T (S before the chunk); after them C and S are free
+        // ---- P2: C B^T and Z = C (sc S)^T (S before the chunk; sc = exp(ref) in the factored form,
+        // whose Z shares the accumulator of Y); after them C and the state copy are free
+        const uint32_t zcol = fast ? 128u : 192u;
         if (tid == 0) {
             tc::fence_after_sync();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 tc::mma_bf16(tmem, kmajor_desc(sbase + OFF_C, ks), kmajor_desc(sbase + OFF_B, ks), kIdCB, ks > 0);
-                tc::mma_bf16(tmem + 192, kmajor_desc(sbase + OFF_C, ks), mnmajor_desc(sbase + OFF_S, ks), kIdZ, ks > 0);
+                tc::mma_bf16(tmem + zcol, kmajor_desc(sbase + OFF_C, ks), mnmajor_desc(sbase + OFF_S, ks), kIdZ, ks > 0);
             }
             tc::mma_commit(s_bar);
         }
@@ -262,13 +304,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         ++phase;
         tc::fence_after_sync();
 
-        // ---- P3: M = C B^T o decay o dt, masked to j <= i (row i = row, columns of this half).
-        // A warp's rows lie in one 32-row block rb, so each 32-column block jb is, for the whole
-        // warp, either right of the diagonal (all zero), left of it (erow x colf, no mask) or the
-        // diagonal block itself (masked; exact exps where the block's range is not safe).
+        uint4 xw_lo[4];  // this thread's lo half of the state operand, row `row`, chunks 4 half .. 4 half + 3
+        // ---- P3: the causal product operand (row i = row, columns of this half) and the state
+        // operand.  A warp's rows lie in one 32-row block rb, so each 32-column block jb is, for the
+        // whole warp, either right of the diagonal (all zero), left of it (no mask) or the diagonal
+        // block itself (masked to j <= i).
+        //   factored:  L[i][j] = C B^T[i][j] (j <= i);  X~_j = exp(ref - cum_j) dt_j x_j
+        //   exact:     M[i][j] = C B^T[i][j] exp(cum_i - cum_j) dt_j (j <= i);  (w o X)_j = exp(cum_last - cum_j) dt_j x_j
         {
             const int i = row;
-            const float erow = expf(cum - s_cum[32 * rb]);  // <= 1
+            const float erow = fast ? 1.f : expf(cum - s_cum[32 * rb]);  // <= 1
             const bool safe = s_safe[rb] != 0;
             const float *colf = s_colf + rb * Q;
 #pragma unroll 1
@@ -284,7 +329,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 float cb[32];
                 tc::tmem_ld32(tmem + lane_addr + (uint32_t)jb, cb);
-                const bool plain = jb < 32 * rb || safe, diag = jb == 32 * rb;
+                const bool diag = jb == 32 * rb;
+                if (fast) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        float f[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) f[u] = (diag && jb + 8 * q8 + u > i) ? 0.f : cb[8 * q8 + u];
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(mrow) +
+                                                   chunk_off((uint32_t)i, c0q + q8)) =
+                            make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                                       pack_bf16(f[6], f[7]));
+                    }
+                    continue;
+                }
+                const bool plain = jb < 32 * rb || safe;
                 const float4 *c4 = reinterpret_cast<const float4 *>(colf + jb);
 #pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns at a time
@@ -315,28 +374,41 @@ __global__ void __launch_bounds__(kThreads, 2)
                         make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
-            // w o X, row j = row, this half's 4 chunks: weight of token j in the state update
-            const float wt = expf(cum_last - cum) * s_dt[row];
+            // the state operand, row j = row, this half's 4 chunks, as hi (to the tile now) and lo
+            // (kept for the second product)
+            const float wt = (fast ? expf(ref - cum) : expf(cum_last - cum)) * dtr;
 #pragma unroll
-            for (int c = 4 * half; c < 4 * half + 4; ++c) {
-                const uint4 xv = *reinterpret_cast<const uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)c));
-                const float2 f0 = unpack_bf16(xv.x), f1 = unpack_bf16(xv.y);
-                const float2 f2 = unpack_bf16(xv.z), f3 = unpack_bf16(xv.w);
-                *reinterpret_cast<uint4 *>(smem + OFF_XW + chunk_off((uint32_t)row, (uint32_t)c)) =
-                    make_uint4(pack_bf16(f0.x * wt, f0.y * wt), pack_bf16(f1.x * wt, f1.y * wt),
-                               pack_bf16(f2.x * wt, f2.y * wt), pack_bf16(f3.x * wt, f3.y * wt));
+            for (int c = 0; c < 4; ++c) {
+                const uint4 xv =
+                    *reinterpret_cast<const uint4 *>(smem + OFF_X + chunk_off((uint32_t)row, (uint32_t)(4 * half + c)));
+                const uint32_t xw4[4] = {xv.x, xv.y, xv.z, xv.w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack_bf16(xw4[e]);
+                    const float v0 = f.x * wt, v1 = f.y * wt;
+                    hi[e] = pack_bf16(v0, v1);
+                    const float2 hf = unpack_bf16(hi[e]);
+                    lo[e] = pack_bf16(v0 - hf.x, v1 - hf.y);
+                }
+                *reinterpret_cast<uint4 *>(smem + OFF_XW + chunk_off((uint32_t)row, (uint32_t)(4 * half + c))) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                xw_lo[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         tc::fence_before_sync();
         tc::fence_proxy_async_smem();
         __syncthreads();
 
-        // ---- P4: Y = M X, dS^T = B^T (w o X)
+        // ---- P4: factored: Y~ = L X~_hi into Z's accumulator; exact: Y = M X.  dS^T = B^T (hi operand)
         if (tid == 0) {
             tc::fence_after_sync();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                tc::mma_bf16(tmem + 128, kmajor_desc(sbase + OFF_M, ks), mnmajor_desc(sbase + OFF_X, ks), kIdY, ks > 0);
+                if (fast)
+                    tc::mma_bf16(tmem + 128, kmajor_desc(sbase + OFF_M, ks), mnmajor_desc(sbase + OFF_XW, ks), kIdY, true);
+                else
+                    tc::mma_bf16(tmem + 128, kmajor_desc(sbase + OFF_M, ks), mnmajor_desc(sbase + OFF_X, ks), kIdY, ks > 0);
                 tc::mma_bf16(tmem + 64, mnmajor_desc(sbase + OFF_B, ks), mnmajor_desc(sbase + OFF_XW, ks), kIdDS, ks > 0);
             }
             tc::mma_commit(s_bar);
@@ -346,24 +418,36 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
         }
         ++phase;
+        // ---- P4b: with M / L read, the lo operand into its tile and dS^T += B^T (lo operand); waited
+        // for only before the state update, so it runs under the outputs below
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4 *>(smem + OFF_XWLO + chunk_off((uint32_t)row, (uint32_t)(4 * half + c))) = xw_lo[c];
+        tc::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + 64, mnmajor_desc(sbase + OFF_B, ks), mnmajor_desc(sbase + OFF_XWLO, ks), kIdDS, true);
+            tc::mma_commit(s_bar);
+        }
         tc::fence_after_sync();
 
-        if (tid == 0 && c0 + Q < L) load_cb(t0 + c0 + Q);  // C (now M) and B are read
-
-        // ---- P5: outputs of row i (this half's 32 columns p), state update of column n = row,
-        // 16 columns at a time
+        // ---- P5: outputs of row i (this half's 32 columns p), 16 columns at a time
+        //   factored: y_i = exp(cum_i - ref) (Z~ + Y~)_i + D x_i;  exact: y_i = Y_i + exp(cum_i) Z_i + D x_i
+        // Non-finite inputs show here and in the state increment: every x, B and C value reaches one
+        // of them through a product (a NaN or Inf times anything, zero included, is not finite), so
+        // v * 0 summed over them is NaN exactly when one of them is not finite.
+        float nf = 0.f;
         {
-            const float ecum = expf(cum);
-            const float dA = expf(cum_last);
-            // Non-finite inputs show here: every x, B and C value reaches y or the state
-            // increment through a product (a NaN or Inf times anything, zero included, is not
-            // finite), so v * 0 summed over them is NaN exactly when one of them is not finite.
-            float nf = 0.f;
+            const float rs = fast ? expf(cum - ref) : 1.f;
+            const float ecum = fast ? 0.f : expf(cum);
 #pragma unroll
             for (int hc = 0; hc < 2; ++hc) {
                 float yv[16], zv[16];
                 tc::tmem_ld16(tmem + lane_addr + 128u + (uint32_t)(p0 + 16 * hc), yv);
-                tc::tmem_ld16(tmem + lane_addr + 192u + (uint32_t)(p0 + 16 * hc), zv);
+                if (!fast) tc::tmem_ld16(tmem + lane_addr + 192u + (uint32_t)(p0 + 16 * hc), zv);
                 uint4 outc[2];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -375,7 +459,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int e = 0; e < 4; ++e) {
                         const float2 xf = unpack_bf16(xw4[e]);
                         const int q = 8 * c + 2 * e;
-                        const float v0 = fmaf(ecum, zv[q], yv[q]) + D * xf.x, v1 = fmaf(ecum, zv[q + 1], yv[q + 1]) + D * xf.y;
+                        float v0, v1;
+                        if (fast) {
+                            v0 = fmaf(rs, yv[q], D * xf.x);
+                            v1 = fmaf(rs, yv[q + 1], D * xf.y);
+                        } else {
+                            v0 = fmaf(ecum, zv[q], yv[q]) + D * xf.x;
+                            v1 = fmaf(ecum, zv[q + 1], yv[q + 1]) + D * xf.y;
+                        }
                         nf = fmaf(v0, 0.f, fmaf(v1, 0.f, nf));
                         o[e] = pack_bf16(v0, v1);
                     }
@@ -387,23 +478,45 @@ __global__ void __launch_bounds__(kThreads, 2)
                     yo[1] = outc[1];
                 }
             }
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {
-                float ds[16];
-                tc::tmem_ld16(tmem + lane_addr + 64u + (uint32_t)(p0 + 16 * hc), ds);
-#pragma unroll
-                for (int p = 0; p < 16; ++p) {
-                    nf = fmaf(ds[p], 0.f, nf);
-                    S[16 * hc + p] = fmaf(dA, S[16 * hc + p], ds[p]);
-                }
-            }
-            bad |= nf != nf;
         }
-        write_state_copy();
+        // this chunk's state factors, then the next chunk's dt, form and reference point (every
+        // thread is done with this chunk's cum)
+        const float dA = expf(cum_last);
+        const float cds = fast ? expf(cum_last - ref) : 1.f;
+        bool fast_next = fast;
+        float ref_next = ref;
+        __syncthreads();
+        if (len1 > 0) {
+            chunk_setup(dt_next);
+            fast_next = fast_ok(len1, ref_next);
+        }
+        // the state increment (both products), then C and B of the next chunk may land
+        if (__syncthreads_or(!mbar_wait(s_bar, phase & 1u))) {
+            timeout = true;
+            break;
+        }
+        ++phase;
+        tc::fence_after_sync();
+        if (tid == 0 && len1 > 0) load_cb(t0 + c1);
+        // ---- state update of column n = row: S <- exp(cum_last) S + cds dS, 16 columns at a time
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+            float ds[16];
+            tc::tmem_ld16(tmem + lane_addr + 64u + (uint32_t)(p0 + 16 * hc), ds);
+#pragma unroll
+            for (int p = 0; p < 16; ++p) {
+                nf = fmaf(ds[p], 0.f, nf);
+                S[16 * hc + p] = fmaf(dA, S[16 * hc + p], cds * ds[p]);
+            }
+        }
+        bad |= nf != nf;
+        if (len1 > 0) write_state_copy(fast_next ? expf(ref_next) : 1.f);
+        fast = fast_next;
+        ref = ref_next;
         tc::fence_before_sync();
         tc::fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0 && c0 + Q < L) load_x(t0 + c0 + Q);  // x is read
+        if (tid == 0 && len1 > 0) load_x(t0 + c1);  // x is read
     }
 
     const bool any_bad = __syncthreads_or(bad);

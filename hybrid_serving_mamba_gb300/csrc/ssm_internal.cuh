@@ -28,6 +28,7 @@ constexpr int kMaxSeqPerLaunch = 1024;
 constexpr int kRowsPerThread = 2;
 constexpr int kMaxThreads = 512;  // per CTA of the state-streaming kernels
 constexpr uint32_t kSlotPoisoned = 1u;
+constexpr int kMaxFoldK = 64;  // largest K extent (log capacity rounded up to 16) of the tensor-core fold
 
 // ---------------------------------------------------------------- pool
 
@@ -68,8 +69,9 @@ struct Pool {
     CUtensorMap tm_state2;             // replay, tensor cores: 32 columns x 128 rows (two heads) per box
     CUtensorMap tm_logx2;              // replay, tensor cores: two heads' logs of x rows per box
     bool tm_tc_ok = false;             // the two maps above encoded
-    CUtensorMap tm_logB;               // replay, bf16, N = 128: 32 logged B rows x 64 columns of a group per box
+    CUtensorMap tm_logB;               // replay, bf16, N = 128: fold_kp logged B rows x 64 columns of a group per box
     bool tm_fold_ok = false;           // tm_state2, tm_logx2 and tm_logB encoded for the tensor-core fold
+    int fold_kp = 0;                   // K extent of the tensor-core fold (32, 48 or 64 >= the log capacity)
     int2 *d_fold_items = nullptr;      // (request index, tokens to fold) of one commit launch
     int32_t *d_fold_count = nullptr;
     int sm_count = 1;
@@ -190,7 +192,7 @@ bool replay_tma_encode(Pool &p);
 cudaError_t launch_verify_replay_pipe(const Pool &pool, const StepArgs &a, cudaStream_t s);
 // The commit; *path names the fold kernel that ran (or "commit_copy").
 cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s, const char **path = nullptr);
-// The fold on the tensor cores (bf16 pools, P = 64, N = 128, window <= 32);
+// The fold on the tensor cores (bf16 pools, P = 64, N = 128, log capacity <= 64);
 // cudaErrorNotSupported for other pools.
 cudaError_t launch_fold_tc(const Pool &pool, const CommitArgs &a, cudaStream_t s);
 // Pipelined fold of the requests the commit listed; cudaErrorNotSupported
@@ -202,6 +204,9 @@ bool scan_ssd_supported(const Pool &pool);
 cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s);
 cudaError_t launch_reset(const Pool &pool, const int32_t *slots, int n, cudaStream_t s);
 cudaError_t launch_gather(const Pool &pool, const int32_t *slots, int n, float *dst, cudaStream_t s);
+
+// Kernel path of the calling thread's last ssm_verify_replay_static call.
+const char *static_last_path();
 
 size_t replay_smem_bytes(const Pool &pool, int n_tok);
 size_t replay_prep_smem_bytes(const Pool &pool, int n_tok);

@@ -361,10 +361,13 @@ ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, 
  * batch * G * n_tok * Wc4 <= SSM_STATIC_SCRATCH_FLOATS, with Wc4 = Wc rounded
  * up to a multiple of 4, else
  * SSM_ERR_INVALID_ARG.  The first call on a device looks up the array's
- * device address (once per device, with that device current); make that
- * first call before any stream capture.  All calls share the array, which
- * keeps the last call's contents: calls that overlap on the GPU race.
- * Asynchronous on stream.
+ * device address (once per device, with that device current, and again if
+ * the device's context has changed since, as after cudaDeviceReset); make
+ * that first call before any stream capture.  All calls share the array,
+ * which keeps the last call's contents: calls that overlap on the GPU race.
+ * Launches are sized by the device's SM count, as the pool's are;
+ * ssm_last_path(NULL) names the kernel path of the calling thread's last
+ * call.  Asynchronous on stream.
  */
 #define SSM_STATIC_SCRATCH_FLOATS 1047552
 ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int32_t nheads, int32_t headdim, int32_t dstate,
@@ -379,7 +382,8 @@ ssm_status ssm_verify_replay_static(int32_t batch, int32_t n_tok, int32_t nheads
 /* Read (and if clear != 0, clear) the pool's sticky device flags.  Synchronous. */
 ssm_status ssm_pool_status(ssm_pool pool, uint32_t *flags_out, int32_t clear, ssm_stream_t stream);
 
-/* Name of the kernel path the last hot-path call used (static string). */
+/* Name of the kernel path the last hot-path call used (static string); with
+ * pool == NULL, that of the calling thread's last ssm_verify_replay_static. */
 const char *ssm_last_path(ssm_pool pool);
 
 /* Static text of a status code. */

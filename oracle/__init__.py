@@ -7,7 +7,12 @@ imports it.
 
 The arithmetic lives in ``ssm_oracle.c`` (plain fp64 scalar loops); this
 module compiles it with gcc on first use, marshals numpy arrays, and models
-the pool's lifecycle rules on the host:
+the pool's lifecycle rules on the host.  The same source also builds with
+every value in fp32 (``f32_*`` functions below): that build serves only as the
+CPU speed baseline, never as a parity reference.  Functions that return
+outputs y can also return their condition scale ``cond`` (sum over n of
+|C[n] h[p, n]| plus |D x[p]|, h the state after the token), against which the
+parity tests take their relative tolerance:
 
 * ``OraclePool`` follows the streaming-state contract of "Mamba Streaming
   State That Survives Chunking": separate init / reset / checkpoint /
@@ -36,9 +41,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ssm_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
-_LIB_PATH = os.path.join(_OUT_DIR, "libssm_oracle.so")
+_LIB_PATHS = {"f64": os.path.join(_OUT_DIR, "libssm_oracle.so"),
+              "f32": os.path.join(_OUT_DIR, "libssm_oracle_f32.so")}
 _lock = threading.Lock()
-_lib = None
+_libs = {}
 
 # status codes mirrored by the pool model (same meaning as the library's)
 OK, ERR_INVALID_ARG, ERR_INVALID_CHUNK, ERR_INVALID_STATE, ERR_SEQUENCE, ERR_DUPLICATE = 0, 1, 2, 3, 4, 5
@@ -47,36 +53,44 @@ COPY, REPLAY = 0, 1
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (fp64, no FMA contraction, OpenMP)."""
+    """Compile the oracle with gcc (no FMA contraction, OpenMP): the fp64
+    parity oracle and the fp32 instantiation of the same source."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
-                               "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    for prec, path in _LIB_PATHS.items():
+        if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+            tmp = path + ".tmp%d" % os.getpid()
+            extra = ["-DORACLE_F32"] if prec == "f32" else []
+            subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+                                   "-ffp-contract=off", "-fno-fast-math", *extra, "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, path)
+    return _LIB_PATHS["f64"]
 
 
-def lib():
-    global _lib
+def lib(prec: str = "f64"):
     with _lock:
-        if _lib is None:
-            L = ctypes.CDLL(build())
-            d, i, l = ctypes.c_double, ctypes.c_int, ctypes.c_long
+        if prec not in _libs:
+            build()
+            L = ctypes.CDLL(_LIB_PATHS[prec])
+            d = ctypes.c_double if prec == "f64" else ctypes.c_float
+            i, l = ctypes.c_int, ctypes.c_long
             P_ = ctypes.c_void_p
-            L.oracle_scan_head.argtypes = [i, i, l, d, d, P_, l, P_, l, P_, P_, l, P_, P_, l]
-            L.oracle_decode_step.argtypes = [i, i, i, i, i, P_, P_, P_, P_, P_, P_, P_, P_]
-            L.oracle_verify_copy.argtypes = [i, i, i, i, i, i, P_, P_, P_, P_, P_, P_, P_, P_, P_]
-            L.oracle_replay_head.argtypes = [i, i, i, i, d, d, P_, P_, P_, P_, P_, P_]
+            L.oracle_scan_head.argtypes = [i, i, l, d, d, P_, l, P_, l, P_, P_, l, P_, P_, l, P_]
+            L.oracle_decode_step.argtypes = [i, i, i, i, i, P_, P_, P_, P_, P_, P_, P_, P_, P_]
+            L.oracle_verify_copy.argtypes = [i, i, i, i, i, i, P_, P_, P_, P_, P_, P_, P_, P_, P_, P_]
+            L.oracle_replay_head.argtypes = [i, i, i, i, d, d, P_, P_, P_, P_, P_, P_, P_]
             L.oracle_verify_replay.argtypes = [i, i, i, i, i, i, i, P_, P_, P_, P_, P_,
-                                               P_, P_, P_, P_, P_, P_, P_]
+                                               P_, P_, P_, P_, P_, P_, P_, P_]
             L.oracle_fold.argtypes = [i, i, i, i, i, i, i, P_, P_, P_, P_, P_, P_, P_, P_, P_, P_, P_]
             for f in ("oracle_scan_head", "oracle_decode_step", "oracle_verify_copy",
                       "oracle_replay_head", "oracle_verify_replay", "oracle_fold"):
                 getattr(L, f).restype = None
             L.oracle_max_threads.restype = ctypes.c_int
-            _lib = L
-    return _lib
+            L.oracle_set_threads.argtypes = [i]
+            L.oracle_set_threads.restype = None
+            L.oracle_real_bytes.restype = ctypes.c_int
+            assert L.oracle_real_bytes() == (8 if prec == "f64" else 4)
+            _libs[prec] = L
+    return _libs[prec]
 
 
 def threads() -> int:
@@ -99,56 +113,74 @@ def group_of(h: int, H: int, G: int) -> int:
 # ---------------------------------------------------------------------------
 # the recurrence in its forms
 
-def scan_head(state: np.ndarray, x, dt, B, C, A: float, D: float, want_y: bool = True):
+def scan_head(state: np.ndarray, x, dt, B, C, A: float, D: float, want_y: bool = True, want_cond: bool = False):
     """Sequential recurrence of one (sequence, head).
 
     state [P][N] (updated in place, fp64); x [L][P]; dt [L]; B, C [L][N].
-    Returns y [L][P] (or None).
+    Returns y [L][P] (or None), and with want_cond (y, cond).
     """
     x, dt, B, C = _f64(x), _f64(dt), _f64(B), _f64(C)
     L, P = x.shape
     N = B.shape[1]
     assert state.dtype == np.float64 and state.flags.c_contiguous and state.shape == (P, N)
     y = np.empty((L, P), np.float64) if want_y else None
+    cond = np.empty((L, P), np.float64) if want_cond else None
     lib().oracle_scan_head(P, N, L, float(A), float(D), _ptr(x), P, _ptr(dt), 1,
-                           _ptr(B), _ptr(C), N, _ptr(state), _ptr(y) if want_y else None, P)
-    return y
+                           _ptr(B), _ptr(C), N, _ptr(state), _ptr(y) if want_y else None, P,
+                           _ptr(cond) if want_cond else None)
+    return (y, cond) if want_cond else y
 
 
-def scan(state: np.ndarray, x, dt, B, C, A, D):
+def scan(state: np.ndarray, x, dt, B, C, A, D, want_cond: bool = False):
     """Sequential recurrence of one sequence, all heads.
 
     state [H][P][N] fp64 in/out; x [L][H][P]; dt [L][H]; B, C [L][G][N];
-    A, D [H].  Returns y [L][H][P].
+    A, D [H].  Returns y [L][H][P], and with want_cond (y, cond).
     """
     x, dt, B, C = _f64(x), _f64(dt), _f64(B), _f64(C)
     L, H, P = x.shape
     G, N = B.shape[1], B.shape[2]
     y = np.empty((L, H, P), np.float64)
-    for h in range(H):
+    cond = np.empty((L, H, P), np.float64) if want_cond else None
+
+    def one(h):  # heads are independent: one C call each, spread over threads (no change to any result)
         g = group_of(h, H, G)
         st = np.ascontiguousarray(state[h])
-        y[:, h, :] = scan_head(st, x[:, h, :], dt[:, h], B[:, g, :], C[:, g, :], A[h], D[h])
+        r = scan_head(st, x[:, h, :], dt[:, h], B[:, g, :], C[:, g, :], A[h], D[h], want_cond=want_cond)
+        if want_cond:
+            y[:, h, :], cond[:, h, :] = r
+        else:
+            y[:, h, :] = r
         state[h] = st
-    return y
+
+    if H > 1 and L * P * N > (1 << 16):
+        import concurrent.futures as cf
+        with cf.ThreadPoolExecutor(max_workers=min(H, os.cpu_count() or 1)) as ex:
+            list(ex.map(one, range(H)))
+    else:
+        for h in range(H):
+            one(h)
+    return (y, cond) if want_cond else y
 
 
-def decode_step(state: np.ndarray, x, dt, B, C, A, D):
-    """One token for R requests. state [R][H][P][N] fp64 in/out; returns y [R][H][P]."""
+def decode_step(state: np.ndarray, x, dt, B, C, A, D, want_cond: bool = False):
+    """One token for R requests. state [R][H][P][N] fp64 in/out; returns y [R][H][P] (and cond)."""
     assert state.dtype == np.float64 and state.flags.c_contiguous
     x, dt, B, C, A, D = _f64(x), _f64(dt), _f64(B), _f64(C), _f64(A), _f64(D)
     R, H, P, N = state.shape
     G = B.shape[1]
     y = np.empty((R, H, P), np.float64)
+    cond = np.empty((R, H, P), np.float64) if want_cond else None
     lib().oracle_decode_step(R, H, P, N, G, _ptr(state), _ptr(x), _ptr(dt), _ptr(B), _ptr(C),
-                             _ptr(A), _ptr(D), _ptr(y))
-    return y
+                             _ptr(A), _ptr(D), _ptr(y), _ptr(cond) if want_cond else None)
+    return (y, cond) if want_cond else y
 
 
-def verify_copy(state: np.ndarray, x, dt, B, C, A, D):
+def verify_copy(state: np.ndarray, x, dt, B, C, A, D, want_cond: bool = False):
     """Copy verify. state [R][H][P][N]; x [R][T1][H][P] ...
 
-    Returns (snapshots [T1][R][H][P][N], y [R][T1][H][P]).
+    Returns (snapshots [T1][R][H][P][N], y [R][T1][H][P]) and with want_cond
+    also cond [R][T1][H][P].
     """
     state = _f64(state)
     x, dt, B, C, A, D = _f64(x), _f64(dt), _f64(B), _f64(C), _f64(A), _f64(D)
@@ -156,25 +188,27 @@ def verify_copy(state: np.ndarray, x, dt, B, C, A, D):
     T1, G = x.shape[1], B.shape[2]
     snap = np.empty((T1, R, H, P, N), np.float64)
     y = np.empty((R, T1, H, P), np.float64)
+    cond = np.empty((R, T1, H, P), np.float64) if want_cond else None
     lib().oracle_verify_copy(R, T1, H, P, N, G, _ptr(state), _ptr(x), _ptr(dt), _ptr(B), _ptr(C),
-                             _ptr(A), _ptr(D), _ptr(snap), _ptr(y))
-    return snap, y
+                             _ptr(A), _ptr(D), _ptr(snap), _ptr(y), _ptr(cond) if want_cond else None)
+    return (snap, y, cond) if want_cond else (snap, y)
 
 
-def replay_head(hc, ux, udt, uB, Cq, k: int, A: float, D: float):
+def replay_head(hc, ux, udt, uB, Cq, k: int, A: float, D: float, want_cond: bool = False):
     """ReplaySSM closed form for one (request, head); see ssm_oracle.c."""
     hc, ux, udt, uB, Cq = _f64(hc), _f64(ux), _f64(udt), _f64(uB), _f64(Cq)
     P, N = hc.shape
     n_tok = Cq.shape[0]
     assert ux.shape == (k + n_tok, P) and uB.shape == (k + n_tok, N)
     y = np.empty((n_tok, P), np.float64)
+    cond = np.empty((n_tok, P), np.float64) if want_cond else None
     lib().oracle_replay_head(P, N, k, n_tok, float(A), float(D), _ptr(hc), _ptr(ux), _ptr(udt),
-                             _ptr(uB), _ptr(Cq), _ptr(y))
-    return y
+                             _ptr(uB), _ptr(Cq), _ptr(y), _ptr(cond) if want_cond else None)
+    return (y, cond) if want_cond else y
 
 
-def verify_replay(ckpt, log_len, lx, ldt, lB, x, dt, B, C, A, D):
-    """Replay verify over R requests; returns y [R][T1][H][P]."""
+def verify_replay(ckpt, log_len, lx, ldt, lB, x, dt, B, C, A, D, want_cond: bool = False):
+    """Replay verify over R requests; returns y [R][T1][H][P] (and cond)."""
     ckpt = _f64(ckpt)
     log_len = np.ascontiguousarray(log_len, dtype=np.int32)
     lx, ldt, lB = _f64(lx), _f64(ldt), _f64(lB)
@@ -182,9 +216,11 @@ def verify_replay(ckpt, log_len, lx, ldt, lB, x, dt, B, C, A, D):
     R, H, P, N = ckpt.shape
     T1, G, Wc = x.shape[1], B.shape[2], lx.shape[1]
     y = np.empty((R, T1, H, P), np.float64)
+    cond = np.empty((R, T1, H, P), np.float64) if want_cond else None
     lib().oracle_verify_replay(R, T1, H, P, N, G, Wc, _ptr(ckpt), _ptr(log_len), _ptr(lx), _ptr(ldt),
-                               _ptr(lB), _ptr(x), _ptr(dt), _ptr(B), _ptr(C), _ptr(A), _ptr(D), _ptr(y))
-    return y
+                               _ptr(lB), _ptr(x), _ptr(dt), _ptr(B), _ptr(C), _ptr(A), _ptr(D), _ptr(y),
+                               _ptr(cond) if want_cond else None)
+    return (y, cond) if want_cond else y
 
 
 def fold(ckpt: np.ndarray, log_len, c, do_fold, lx, ldt, lB, x, dt, B, A):
@@ -221,6 +257,76 @@ def copy_break_even(p: float, T: int) -> float:
 
 
 # ---------------------------------------------------------------------------
+# the fp32 instantiation (CPU speed baseline only; never a parity reference)
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def f32_threads() -> int:
+    return int(lib("f32").oracle_max_threads())
+
+
+def f32_set_threads(n: int) -> None:
+    """Threads of the fp32 build's parallel loops (timing only)."""
+    lib("f32").oracle_set_threads(int(n))
+
+
+def f32_decode_step(state, x, dt, B, C, A, D):
+    """decode_step in fp32; state [R][H][P][N] float32 in/out."""
+    x, dt, B, C, A, D = _f32(x), _f32(dt), _f32(B), _f32(C), _f32(A), _f32(D)
+    R, H, P, N = state.shape
+    y = np.empty((R, H, P), np.float32)
+    lib("f32").oracle_decode_step(R, H, P, N, B.shape[1], _ptr(state), _ptr(x), _ptr(dt), _ptr(B), _ptr(C),
+                                  _ptr(A), _ptr(D), _ptr(y), None)
+    return y
+
+
+def f32_verify_copy(state, x, dt, B, C, A, D):
+    state = _f32(state)
+    x, dt, B, C, A, D = _f32(x), _f32(dt), _f32(B), _f32(C), _f32(A), _f32(D)
+    R, H, P, N = state.shape
+    T1, G = x.shape[1], B.shape[2]
+    snap = np.empty((T1, R, H, P, N), np.float32)
+    y = np.empty((R, T1, H, P), np.float32)
+    lib("f32").oracle_verify_copy(R, T1, H, P, N, G, _ptr(state), _ptr(x), _ptr(dt), _ptr(B), _ptr(C),
+                                  _ptr(A), _ptr(D), _ptr(snap), _ptr(y), None)
+    return snap, y
+
+
+def f32_verify_replay(ckpt, log_len, lx, ldt, lB, x, dt, B, C, A, D):
+    ckpt = _f32(ckpt)
+    log_len = np.ascontiguousarray(log_len, dtype=np.int32)
+    lx, ldt, lB = _f32(lx), _f32(ldt), _f32(lB)
+    x, dt, B, C, A, D = _f32(x), _f32(dt), _f32(B), _f32(C), _f32(A), _f32(D)
+    R, H, P, N = ckpt.shape
+    T1, G, Wc = x.shape[1], B.shape[2], lx.shape[1]
+    y = np.empty((R, T1, H, P), np.float32)
+    lib("f32").oracle_verify_replay(R, T1, H, P, N, G, Wc, _ptr(ckpt), _ptr(log_len), _ptr(lx), _ptr(ldt),
+                                    _ptr(lB), _ptr(x), _ptr(dt), _ptr(B), _ptr(C), _ptr(A), _ptr(D), _ptr(y), None)
+    return y
+
+
+def f32_fold(ckpt, log_len, c, do_fold, lx, ldt, lB, x, dt, B, A):
+    log_len = np.ascontiguousarray(log_len, dtype=np.int32)
+    c = np.ascontiguousarray(c, dtype=np.int32)
+    do_fold = np.ascontiguousarray(do_fold, dtype=np.int32)
+    lx, ldt, lB, x, dt, B, A = _f32(lx), _f32(ldt), _f32(lB), _f32(x), _f32(dt), _f32(B), _f32(A)
+    R, H, P, N = ckpt.shape
+    T1, G, Wc = x.shape[1], B.shape[2], lx.shape[1]
+    lib("f32").oracle_fold(R, T1, H, P, N, G, Wc, _ptr(ckpt), _ptr(log_len), _ptr(c), _ptr(do_fold),
+                           _ptr(lx), _ptr(ldt), _ptr(lB), _ptr(x), _ptr(dt), _ptr(B), _ptr(A))
+
+
+def f32_scan_head(state, x, dt, B, C, A, D, xs, dts, bcs, y, ys):
+    """scan_head in fp32 on strided views: x token t at x + t * xs (elements), etc."""
+    P, N = state.shape[-2], state.shape[-1]
+    L = y.shape[0]
+    lib("f32").oracle_scan_head(P, N, L, float(A), float(D), _ptr(x), xs, _ptr(dt), dts, _ptr(B), _ptr(C), bcs,
+                                _ptr(state), _ptr(y), ys, None)
+
+
+# ---------------------------------------------------------------------------
 # the pool's lifecycle, on the host
 
 class OraclePool:
@@ -228,6 +334,8 @@ class OraclePool:
 
     Slot metadata: position (tokens applied), next_chunk (next chunk sequence
     number expected), epoch (resets), log_len (replay mode), released flag.
+    ``last_cond`` holds the condition scale of the last call's outputs (an
+    array shaped like y; a list of them for scan_chunk).
     """
 
     def __init__(self, H, P, N, G, n_slots, A, D, mode=COPY, W=16, max_tokens=9, init_state=None):
@@ -248,6 +356,7 @@ class OraclePool:
         self.ldt = np.zeros((n_slots, cap, H))
         self.lB = np.zeros((n_slots, cap, G, N))
         self._pending = {}
+        self.last_cond = None
 
     # -- lifecycle ---------------------------------------------------------
     def _check_slots(self, slots):
@@ -299,11 +408,14 @@ class OraclePool:
                 return ERR_INVALID_CHUNK, None
         if self.mode == REPLAY and any(self.log_len[s] != 0 for s in slots):
             return ERR_INVALID_STATE, None
-        ys = []
+        ys, conds = [], []
         for s, (x, dt, B, C) in zip(slots, chunks):
-            ys.append(scan(self.state[s], x, dt, B, C, self.A, self.D))
+            y, cond = scan(self.state[s], x, dt, B, C, self.A, self.D, want_cond=True)
+            ys.append(y)
+            conds.append(cond)
             self.position[s] += np.asarray(x).shape[0]
             self.next_chunk[s] += 1
+        self.last_cond = conds
         return OK, ys
 
     def decode(self, slots, x, dt, B, C):
@@ -312,7 +424,7 @@ class OraclePool:
             return st, None
         sl = list(slots)
         sub = np.ascontiguousarray(self.state[sl])
-        y = decode_step(sub, x, dt, B, C, self.A, self.D)
+        y, self.last_cond = decode_step(sub, x, dt, B, C, self.A, self.D, want_cond=True)
         self.state[sl] = sub
         self.position[sl] += 1
         return OK, y
@@ -325,12 +437,12 @@ class OraclePool:
         sl = list(slots)
         T1 = np.asarray(x).shape[1]
         if self.mode == COPY:
-            snap, y = verify_copy(self.state[sl], x, dt, B, C, self.A, self.D)
+            snap, y, self.last_cond = verify_copy(self.state[sl], x, dt, B, C, self.A, self.D, want_cond=True)
             for i, s in enumerate(sl):
                 self._pending[s] = ("copy", snap[:, i].copy(), T1)
         else:
-            y = verify_replay(self.state[sl], self.log_len[sl], self.lx[sl], self.ldt[sl], self.lB[sl],
-                              x, dt, B, C, self.A, self.D)
+            y, self.last_cond = verify_replay(self.state[sl], self.log_len[sl], self.lx[sl], self.ldt[sl],
+                                              self.lB[sl], x, dt, B, C, self.A, self.D, want_cond=True)
             xs, dts, Bs = _f64(x), _f64(dt), _f64(B)
             for i, s in enumerate(sl):
                 self._pending[s] = ("replay", (xs[i], dts[i], Bs[i]), T1)

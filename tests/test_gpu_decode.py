@@ -53,7 +53,7 @@ def test_decode_matches_oracle(H, P, N, G, dt_in, dt_dt):
             assert st == m.SSM_OK
             _, yo = opool.decode(slots, synth.widen(x, dt_in), synth.widen(dt, dt_dt), synth.widen(B, dt_in),
                                  synth.widen(C, dt_in))
-            check_close(to_host(y), yo, dt_in, f"y step {s}")
+            check_close(to_host(y), yo, dt_in, f"y step {s}", cond=opool.last_cond)
         got = torch.empty((n_slots, H, P, N), dtype=torch.float32, device="cuda")
         assert m.ssm_state_gather(pool, list(range(n_slots)), got) == m.SSM_OK
         check_close(to_host(got), opool.state, dt_in, "state")
@@ -89,9 +89,10 @@ def test_decode_nemotron_shape_full_batch_sampled():
             st = m.ssm_decode_step(pool, slots, to_device(x, synth.BF16), to_device(dt, synth.F32),
                                    to_device(B, synth.BF16), to_device(C, synth.BF16), Ad, Dd, y)
             assert st == m.SSM_OK
-            yo = oracle.decode_step(ost, synth.widen(x[sample], synth.BF16), synth.widen(dt[sample], synth.F32),
-                                    synth.widen(B[sample], synth.BF16), synth.widen(C[sample], synth.BF16), A, D)
-            check_close(to_host(y[sample]), yo, synth.BF16, f"y step {s}")
+            yo, yc = oracle.decode_step(ost, synth.widen(x[sample], synth.BF16), synth.widen(dt[sample], synth.F32),
+                                        synth.widen(B[sample], synth.BF16), synth.widen(C[sample], synth.BF16), A, D,
+                                        want_cond=True)
+            check_close(to_host(y[sample]), yo, synth.BF16, f"y step {s}", cond=yc)
         got = torch.empty((len(sample), H, P, N), dtype=torch.float32, device="cuda")
         assert m.ssm_state_gather(pool, sample, got) == m.SSM_OK
         check_close(to_host(got), ost, synth.BF16, "state after 64 steps")

@@ -69,7 +69,7 @@ def test_decode_matches_oracle(dt_in, H, G, dk, dv):
             y = _out((len(slots), H, dv), dt_in)
             assert m.ssm_gdn_decode_step(pool, slots, *_dev(one, dt_in), y) == m.SSM_OK
             yo = opool.decode(slots, *_wide(one, dt_in))
-            check_close(to_host(y), yo, dt_in, f"y step {s}")
+            check_close(to_host(y), yo, dt_in, f"y step {s}", cond=opool.last_cond)
         check_close(_states(m, pool, slots), opool.state[slots], dt_in, "states")
         for sl in slots:
             st, pos, ll, fl = m.ssm_gdn_slot_info(pool, sl)
@@ -89,7 +89,7 @@ def _run_verify(m, dt_in, H, G, dk, dv, W, T1, p, steps, slots, n_slots=8, force
         y = _out((len(slots), T1, H, dv), dt_in)
         assert m.ssm_gdn_verify_replay(pool, slots, T1, *_dev(parts, dt_in), y) == m.SSM_OK
         yo = opool.verify(slots, *_wide(parts, dt_in))
-        check_close(to_host(y), yo, dt_in, f"y step {s}", positions_axis=1)
+        check_close(to_host(y), yo, dt_in, f"y step {s}", positions_axis=1, cond=opool.last_cond)
         a = torch.from_numpy(np.ascontiguousarray(acc[s], dtype=np.int32)).cuda()
         ff = s in force_at
         assert m.ssm_gdn_commit(pool, slots, a, ff) == m.SSM_OK
@@ -172,7 +172,7 @@ def test_nonfinite_input_poisons_only_its_request(which):
         assert m.ssm_gdn_slot_info(pool, 1)[3] & 1 and m.ssm_gdn_slot_info(pool, 0)[3] == 0
         good = [0, 2]
         yo = opool.verify(good, *(a[good] for a in _wide(tuple(parts), dt_in)))
-        check_close(to_host(y)[good], yo, dt_in, "the other requests")
+        check_close(to_host(y)[good], yo, dt_in, "the other requests", cond=opool.last_cond)
         assert m.ssm_gdn_commit(pool, slots, torch.zeros(3, dtype=torch.int32, device="cuda")) == m.SSM_OK
         assert m.ssm_gdn_slot_info(pool, 1)[1] == 0 and m.ssm_gdn_slot_info(pool, 0)[1] == 1
         assert m.ssm_gdn_reset(pool, [1]) == m.SSM_OK
@@ -222,7 +222,7 @@ def test_full_size_sampled_requests():
             y = _out((R, T1, H, dv), dt_in)
             assert m.ssm_gdn_verify_replay(pool, slots, T1, *_dev(parts, dt_in), y) == m.SSM_OK
             yo = opool.verify(list(range(len(sample))), *(a[sample] for a in _wide(parts, dt_in)))
-            check_close(to_host(y)[sample], yo, dt_in, f"sampled y step {s}", positions_axis=1)
+            check_close(to_host(y)[sample], yo, dt_in, f"sampled y step {s}", positions_axis=1, cond=opool.last_cond)
             assert m.ssm_gdn_commit(pool, slots, torch.from_numpy(acc[s]).cuda()) == m.SSM_OK
             opool.commit(list(range(len(sample))), acc[s][sample])
         assert m.ssm_gdn_status(pool)[1] == 0

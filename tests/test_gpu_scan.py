@@ -2,6 +2,8 @@
 CPU oracle, on the partitions and lifecycle cases of Mamba Streaming State
 That Survives Chunking (Let the full scan define legal chunking; Make reset,
 checkpoint, and cancellation observable)."""
+import functools
+
 import numpy as np
 import pytest
 
@@ -80,16 +82,17 @@ def _slice(tok, a, b):
 
 
 def _oracle_scan(A, D, tok, dt_in, dt_dt, h0):
+    """(y, final state, condition scale of y) of one sequence from h0."""
     st = np.array(h0, np.float64, copy=True)
-    y = oracle.scan(st, synth.widen(tok[0], dt_in), synth.widen(tok[1], dt_dt), synth.widen(tok[2], dt_in),
-                    synth.widen(tok[3], dt_in), A, D)
-    return y, st
+    y, cond = oracle.scan(st, synth.widen(tok[0], dt_in), synth.widen(tok[1], dt_dt), synth.widen(tok[2], dt_in),
+                          synth.widen(tok[3], dt_in), A, D, want_cond=True)
+    return y, st, cond
 
 
 def test_config0_every_listed_partition():
     m = _mod()
     (H, P, N, G, L), A, D, tok = _cfg0()
-    y_ref, s_ref = _oracle_scan(A, D, tok, synth.F32, synth.F32, np.zeros((H, P, N)))
+    y_ref, s_ref, c_ref = _oracle_scan(A, D, tok, synth.F32, synth.F32, np.zeros((H, P, N)))
     parts_list = [[L], [1] * L, [0, L], [32, 0, 32], [7, 13, 43, 1], [L, 0], [63, 1], [2, 3, 5, 7, 11, 13, 17, 6]]
     sc = Scanner(m, H, P, N, G, synth.F32, synth.F32, len(parts_list), A, D)
     try:
@@ -100,7 +103,7 @@ def test_config0_every_listed_partition():
                 assert st == m.SSM_OK
                 ys.append(y[0])
                 a += q
-            check_close(np.concatenate(ys), y_ref, synth.F32, f"y {parts}", positions_axis=0)
+            check_close(np.concatenate(ys), y_ref, synth.F32, f"y {parts}", positions_axis=0, cond=c_ref)
             check_close(sc.state([slot])[0], s_ref, synth.F32, f"state {parts}")
             _, meta = m.ssm_slot_info(sc.pool, slot)
             assert meta.position == L and meta.next_chunk == len(parts)
@@ -124,8 +127,8 @@ def test_config0_reset_swap_duplicate():
         _, yab = sc.scan([2], [_slice(tok, 0, 24)])
         _, yab2 = sc.scan([2], [_slice(tok, 24, L)])
         assert np.abs(yab2[0] - yb_fresh[0]).max() > 1e-3
-        yb_ref, _ = _oracle_scan(A, D, _slice(tok, 24, L), synth.F32, synth.F32, np.zeros((H, P, N)))
-        check_close(yb_reset[0], yb_ref, synth.F32, "B after reset")
+        yb_ref, _, yb_cond = _oracle_scan(A, D, _slice(tok, 24, L), synth.F32, synth.F32, np.zeros((H, P, N)))
+        check_close(yb_reset[0], yb_ref, synth.F32, "B after reset", cond=yb_cond)
         assert m.ssm_slot_info(sc.pool, 0)[1].epoch == 1
         # swapped chunk order gives a different sequence
         _, y1 = sc.scan([3], [_slice(tok, 24, L)])
@@ -190,21 +193,22 @@ def test_config1_130m_prefill_chunked_and_partitioned():
     """Mamba-2-130M-shaped layer: d_inner 1536 (24 heads of 64), dstate 128,
     one group, 8 sequences of 2048 bf16 tokens.  Full scan in one call, user
     chunks of 256 with handoff, and seeded random partitions per sequence;
-    the oracle follows three sequences with all heads."""
+    every sequence and head is checked against the oracle, and the three ways
+    of cutting it against each other (at twice the bound, against the
+    oracle's condition scale)."""
     m = _mod()
     H, P, N, G, Bt, L = 24, 64, 128, 1, 8, 2048
     A, D = synth.head_params(SEED1, H)
     toks = [synth.tokens(SEED1, b, L, H, P, G, N, synth.BF16, synth.BF16) for b in range(Bt)]
-    sample = [0, 3, 7]
-    refs = {b: _oracle_scan(A, D, toks[b], synth.BF16, synth.BF16, np.zeros((H, P, N))) for b in sample}
+    refs = {b: _oracle_scan(A, D, toks[b], synth.BF16, synth.BF16, np.zeros((H, P, N))) for b in range(Bt)}
     sc = Scanner(m, H, P, N, G, synth.BF16, synth.BF16, 3 * Bt, A, D)
     try:
         # full-sequence scan of all 8 sequences in one call
         st, ys_full = sc.scan(list(range(Bt)), toks)
         assert st == m.SSM_OK
         s_full = sc.state(list(range(Bt)))
-        for b in sample:
-            check_close(ys_full[b], refs[b][0], synth.BF16, f"full y seq {b}", positions_axis=0)
+        for b in range(Bt):
+            check_close(ys_full[b], refs[b][0], synth.BF16, f"full y seq {b}", positions_axis=0, cond=refs[b][2])
             check_close(s_full[b], refs[b][1], synth.BF16, f"full state seq {b}")
         # user chunks of 256 tokens: one call per chunk, all sequences packed
         slots = list(range(Bt, 2 * Bt))
@@ -216,10 +220,11 @@ def test_config1_130m_prefill_chunked_and_partitioned():
                 ys[b].append(yc[b])
         s_chunk = sc.state(slots)
         for b in range(Bt):
-            if b in refs:
-                check_close(np.concatenate(ys[b]), refs[b][0], synth.BF16, f"chunk-256 seq {b}", positions_axis=0)
-                check_close(s_chunk[b], refs[b][1], synth.BF16, f"chunk-256 state seq {b}")
-            check_close(np.concatenate(ys[b]), ys_full[b], synth.BF16, f"chunk-256 vs full seq {b}", pair=True)
+            check_close(np.concatenate(ys[b]), refs[b][0], synth.BF16, f"chunk-256 seq {b}", positions_axis=0,
+                        cond=refs[b][2])
+            check_close(s_chunk[b], refs[b][1], synth.BF16, f"chunk-256 state seq {b}")
+            check_close(np.concatenate(ys[b]), ys_full[b], synth.BF16, f"chunk-256 vs full seq {b}", pair=True,
+                        cond=refs[b][2])
             check_close(s_chunk[b], s_full[b], synth.BF16, f"chunk-256 state seq {b}", pair=True)
         # seeded random partitions (with empty chunks) per sequence
         for b in range(Bt):
@@ -231,20 +236,30 @@ def test_config1_130m_prefill_chunked_and_partitioned():
                 assert st == m.SSM_OK
                 out.append(yc[0])
                 a += q
-            if b in refs:
-                check_close(np.concatenate(out), refs[b][0], synth.BF16, f"partition {parts} seq {b}")
-                check_close(sc.state([slot])[0], refs[b][1], synth.BF16, f"partition state seq {b}")
-            check_close(np.concatenate(out), ys_full[b], synth.BF16, f"partition {parts} vs full seq {b}", pair=True)
+            check_close(np.concatenate(out), refs[b][0], synth.BF16, f"partition {parts} seq {b}", cond=refs[b][2])
+            check_close(sc.state([slot])[0], refs[b][1], synth.BF16, f"partition state seq {b}")
+            check_close(np.concatenate(out), ys_full[b], synth.BF16, f"partition {parts} vs full seq {b}", pair=True,
+                        cond=refs[b][2])
             check_close(sc.state([slot])[0], s_full[b], synth.BF16, f"partition state vs full seq {b}", pair=True)
         assert m.ssm_pool_status(sc.pool)[1] == 0
     finally:
         sc.close()
 
 
-def test_config4_varlen_packed_with_slot_reuse():
+@functools.lru_cache(maxsize=2)
+def _config4_wave(wave):
+    """Tokens of the 64 sequences of one wave of the 2.7B-shaped varlen workload."""
+    H, P, N, G, S = 80, 64, 128, 1, 64
+    lens = synth.varlen_lengths(SEED4, S, 512, 8192)
+    return tuple(synth.tokens(SEED4, 1000 * wave + i, int(lens[i]), H, P, G, N, synth.BF16, synth.BF16)
+                 for i in range(S))
+
+
+@pytest.mark.parametrize("chunk", [256, 1024])
+def test_config4_varlen_packed_with_slot_reuse(chunk):
     """Mamba-2-2.7B-shaped layer: d_inner 5120 (80 heads of 64), dstate 128,
     one group; 64 packed sequences with lengths U(512, 8192) fed as user
-    chunks of 1024 tokens (every call packs the next chunk of each live
+    chunks of 256 or 1024 tokens (every call packs the next chunk of each live
     sequence).  Then the 64 slots are reset and reused by a second wave,
     each checked against a fresh-state scan; a control wave without the
     reset must differ."""
@@ -253,12 +268,10 @@ def test_config4_varlen_packed_with_slot_reuse():
     A, D = synth.head_params(SEED4, H)
     lens = synth.varlen_lengths(SEED4, S, 512, 8192)
     sc = Scanner(m, H, P, N, G, synth.BF16, synth.BF16, 2 * S, A, D)
-    chunk = 1024
     heads = [0, 41, 79]
     try:
         for wave in range(2):
-            toks = [synth.tokens(SEED4, 1000 * wave + i, int(lens[i]), H, P, G, N, synth.BF16, synth.BF16)
-                    for i in range(S)]
+            toks = list(_config4_wave(wave))
             if wave == 1:
                 sc.reset(list(range(S)))
             ys = [[] for _ in range(S)]
@@ -275,10 +288,11 @@ def test_config4_varlen_packed_with_slot_reuse():
                 for h in heads:
                     t = toks[i]
                     st0 = np.zeros((P, N))
-                    yo = oracle.scan_head(st0, synth.widen(t[0][:, h], synth.BF16), synth.widen(t[1][:, h], synth.BF16),
-                                          synth.widen(t[2][:, 0], synth.BF16), synth.widen(t[3][:, 0], synth.BF16),
-                                          A[h], D[h])
-                    check_close(y_all[:, h], yo, synth.BF16, f"wave {wave} seq {i} head {h}", positions_axis=0)
+                    yo, yc = oracle.scan_head(st0, synth.widen(t[0][:, h], synth.BF16),
+                                              synth.widen(t[1][:, h], synth.BF16), synth.widen(t[2][:, 0], synth.BF16),
+                                              synth.widen(t[3][:, 0], synth.BF16), A[h], D[h], want_cond=True)
+                    check_close(y_all[:, h], yo, synth.BF16, f"chunk {chunk} wave {wave} seq {i} head {h}",
+                                positions_axis=0, cond=yc)
                     check_close(states[i, h], st0, synth.BF16, f"wave {wave} seq {i} head {h} state")
             if wave == 1:
                 # control: wave-2 tokens of sequence 0 on a slot still holding
@@ -313,8 +327,44 @@ def test_tensor_core_scan_ragged_lengths(lens, dt_dt):
                 assert m.ssm_last_path(sc.pool) == "scan_ssd"
             got = sc.state(list(range(S)))
             for i in range(S):
-                y_ref, states[i] = _oracle_scan(A, D, toks[i], synth.BF16, dt_dt, states[i])
-                check_close(ys[i], y_ref, synth.BF16, f"call {call} seq {i} (L={lens[i]}) y", positions_axis=0)
+                y_ref, states[i], y_cond = _oracle_scan(A, D, toks[i], synth.BF16, dt_dt, states[i])
+                check_close(ys[i], y_ref, synth.BF16, f"call {call} seq {i} (L={lens[i]}) y", positions_axis=0,
+                            cond=y_cond)
+                check_close(got[i], states[i], synth.BF16, f"call {call} seq {i} state")
+            assert m.ssm_pool_status(sc.pool)[1] == 0
+    finally:
+        sc.close()
+
+
+def test_tensor_core_scan_fast_decay_takes_the_exact_form():
+    """The tensor-core scan factors exp(cum_i - cum_j) around a reference
+    point of each 128-token chunk only while both factors stay far inside
+    fp32; chunks whose decay over the chunk is steeper (here heads with
+    A = -40 and -400, and a stretch of one sequence with 30 times larger dt)
+    take the exact per-block form instead.  Both forms, mixed within one
+    sequence and across its calls, match the oracle."""
+    m = _mod()
+    H, P, N, G = 4, 64, 128, 2
+    seed = SEED1 + 79
+    _, D = synth.head_params(seed, H)
+    A = np.array([-1.0, -3.0, -40.0, -400.0], np.float32)
+    lens = [300, 129, 384]
+    S = len(lens)
+    sc = Scanner(m, H, P, N, G, synth.BF16, synth.F32, S, A, D)
+    try:
+        states = [np.zeros((H, P, N)) for _ in range(S)]
+        for call in range(2):
+            toks = [list(synth.tokens(seed, 100 * call + i, L, H, P, G, N, synth.BF16, synth.F32))
+                    for i, L in enumerate(lens)]
+            toks[0][1] = toks[0][1].copy()
+            toks[0][1][150:260] *= np.float32(30.0)   # dt: a steep stretch in the middle of sequence 0
+            toks = [tuple(t) for t in toks]
+            st, ys = sc.scan(list(range(S)), toks)
+            assert st == m.SSM_OK and m.ssm_last_path(sc.pool) == "scan_ssd"
+            got = sc.state(list(range(S)))
+            for i in range(S):
+                y_ref, states[i], y_cond = _oracle_scan(A, D, toks[i], synth.BF16, synth.F32, states[i])
+                check_close(ys[i], y_ref, synth.BF16, f"call {call} seq {i} y", positions_axis=0, cond=y_cond)
                 check_close(got[i], states[i], synth.BF16, f"call {call} seq {i} state")
             assert m.ssm_pool_status(sc.pool)[1] == 0
     finally:
@@ -357,7 +407,7 @@ def test_tensor_core_scan_nonfinite_poisons_slot(where):
         assert meta0.flags & 1
         if where in ("B", "C"):
             assert meta0.position == 150
-        _, ref = _oracle_scan(A, D, toks[1], synth.BF16, synth.F32, np.zeros((H, P, N)))
+        _, ref, _ = _oracle_scan(A, D, toks[1], synth.BF16, synth.F32, np.zeros((H, P, N)))
         check_close(after[1], ref, synth.BF16, "the healthy sequence's state")
         assert m.ssm_slot_info(sc.pool, 1)[1].flags == 0
     finally:

@@ -42,7 +42,7 @@ def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_to
     Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
     acc_all = synth.accept_counts(SEED, steps, R, T, p)
     verify = m.ssm_verify_copy if mode == m.SSM_MODE_COPY else m.ssm_verify_replay
-    ys = []
+    ys, conds = [], []
     try:
         for s in range(steps):
             nt = T1 if n_tok_pattern is None else n_tok_pattern[s % len(n_tok_pattern)]
@@ -53,13 +53,14 @@ def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_to
             if expect_path is not None:
                 assert m.ssm_last_path(pool) == expect_path
             _, yo = opool.verify(slots, *_wide(x, dt, B, C, dt_in, synth.F32))
-            check_close(to_host(y), yo, dt_in, f"y step {s}", positions_axis=1)
+            check_close(to_host(y), yo, dt_in, f"y step {s}", positions_axis=1, cond=opool.last_cond)
             if y_round_mismatch is not None:  # share of outputs that differ from the oracle rounded to bf16
                 g = np.asarray(to_host(y), np.float64)
                 o16 = synth.bf16_to_f32(synth.f32_to_bf16(np.asarray(yo, np.float32))).astype(np.float64)
                 frac = float(np.mean(g != o16))
                 assert frac <= y_round_mismatch, (s, frac, y_round_mismatch)
             ys.append(to_host(y))
+            conds.append(opool.last_cond)
             force = force_last and s == steps - 1
             assert m.ssm_state_commit(pool, slots, torch.from_numpy(acc).cuda(), force, Ad) == m.SSM_OK
             if expect_commit_path is not None:
@@ -76,7 +77,7 @@ def _run_small(mode, W, T, p, steps, H=4, P=16, N=32, G=2, dt_in=synth.F32, n_to
         check_close(to_host(got), opool.state, dt_in, "state")
         st, flags = m.ssm_pool_status(pool)
         assert st == m.SSM_OK and flags == 0
-        return pool, opool, ys, (A, D)
+        return pool, opool, (ys, conds), (A, D)
     except BaseException:
         m.ssm_state_destroy(pool)
         raise
@@ -127,6 +128,22 @@ def test_replay_tensor_core_verify(dt_in, T, W, path):
     m.ssm_state_destroy(pool)
 
 
+@pytest.mark.parametrize("dt_in,T,W,fold", [
+    (synth.BF16, 8, 32, "commit_replay_fold_tc"),    # log capacity 40: the fold's K = 48
+    (synth.F32, 8, 32, "commit_replay_fold_pipe"),
+    (synth.BF16, 4, 32, "commit_replay_fold_tc"),    # capacity 36
+    (synth.BF16, 19, 40, "commit_replay_fold_tc"),   # capacity 59: K = 64, 32 MMA columns
+])
+def test_replay_tensor_core_wide_window(dt_in, T, W, fold):
+    """Windows whose log holds more than 32 tokens (W - 1 + T + 1 > 32) stay on
+    the tensor-core verify and, for bf16 pools, the tensor-core fold; 16 steps
+    so the log fills and folds at least once before the final forced fold."""
+    m = _mod()
+    pool, _, _, _ = _run_small(m.SSM_MODE_REPLAY, W, T, 0.7, steps=16, H=4, P=64, N=128, G=2, dt_in=dt_in,
+                               expect_path="verify_replay_tc", expect_commit_path=fold)
+    m.ssm_state_destroy(pool)
+
+
 @pytest.mark.parametrize("T,W", [(8, 16), (19, 8)])
 def test_replay_tensor_core_bf16_product_keeps_fp32_grade(T, W):
     """bf16 inputs run C_j . h_c as kind::f16 MMAs with the fp32 checkpoint
@@ -170,11 +187,11 @@ def test_copy_and_replay_agree_on_gpu():
     after a final forced fold, so do the states (The Fix: the same math)."""
     import torch
     m = _mod()
-    pc, _, yc, _ = _run_small(m.SSM_MODE_COPY, 16, 4, 0.7, steps=8)
-    pr, _, yr, _ = _run_small(m.SSM_MODE_REPLAY, 4, 4, 0.7, steps=8)
+    pc, _, (yc, cc), _ = _run_small(m.SSM_MODE_COPY, 16, 4, 0.7, steps=8)
+    pr, _, (yr, _), _ = _run_small(m.SSM_MODE_REPLAY, 4, 4, 0.7, steps=8)
     try:
-        for a, b in zip(yc, yr):
-            check_close(b, a, synth.F32, "replay vs copy y", pair=True)
+        for a, b, c in zip(yc, yr, cc):
+            check_close(b, a, synth.F32, "replay vs copy y", pair=True, cond=c)
         sc = torch.empty((8, 4, 16, 32), dtype=torch.float32, device="cuda")
         sr = torch.empty_like(sc)
         m.ssm_state_gather(pc, list(range(8)), sc)
@@ -226,15 +243,19 @@ def test_verify_host_side_errors():
         m.ssm_state_destroy(pool)
 
 
-@pytest.mark.parametrize("T,p,W", [(8, 0.8, 16), (4, 0.6, 8)])
+@pytest.mark.parametrize("T,p,W", [(T, p, W) for T in (4, 8) for p in (0.6, 0.8) for W in (8, 16, 32)])
 def test_config3_full_batch_sampled(T, p, W):
     """Speculative verify at batch 512 with Nemotron-shaped heads, bf16 token
-    inputs, fp32 state: copy and replay flavours on the same inputs and
-    accept counts; three requests followed by the oracle; every slot's
-    position and log length checked against the oracle's commit rule."""
+    inputs, fp32 state, at every (T, p, W) point of the workload: copy and
+    replay flavours on the same inputs and accept counts; three requests
+    followed by the oracle; every slot's position and log length checked
+    against the oracle's commit rule.  Replay runs the tensor-core verify and
+    fold at every window (a log of up to 40 tokens at W = 32); enough steps
+    that the window fills (W = 32 needs about 32 / E[1 + accept] steps)."""
     import torch
     m = _mod()
-    H, P, N, G, R, steps = 128, 64, 128, 8, 512, 6
+    H, P, N, G, R = 128, 64, 128, 8, 512
+    steps = {8: 6, 16: 8, 32: 14}[W]
     T1 = T + 1
     A, D = synth.head_params(SEED, H)
     init = np.stack([synth.init_state(SEED, s, H, P, N) for s in range(R)])
@@ -251,6 +272,7 @@ def test_config3_full_batch_sampled(T, p, W):
     Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
     acc_all = synth.accept_counts(SEED, steps, R, T, p)
     slots = list(range(R))
+    n_folds = 0
     try:
         for s in range(steps):
             x, dt, B, C = synth.batch_tokens(SEED, s, R, T1, H, P, G, N, synth.BF16, synth.F32)
@@ -262,15 +284,19 @@ def test_config3_full_batch_sampled(T, p, W):
                 assert fn(pools[md], slots, T1, *dev, Ad, Dd, y) == m.SSM_OK
                 assert m.ssm_last_path(pools[md]) == ("verify_copy" if md == 0 else "verify_replay_tc")
                 assert m.ssm_state_commit(pools[md], slots, acc, False, Ad) == m.SSM_OK
+                assert m.ssm_last_path(pools[md]) == ("commit_copy" if md == 0 else "commit_replay_fold_tc")
                 ys[md] = y
                 _, yo = osample[md].verify(list(range(len(sample))),
                                            *_wide(x[sample], dt[sample], B[sample], C[sample], synth.BF16, synth.F32))
                 osample[md].commit(list(range(len(sample))), acc_all[s][sample])
-                check_close(to_host(y[sample]), yo, synth.BF16, f"mode {md} y step {s}", positions_axis=1)
+                check_close(to_host(y[sample]), yo, synth.BF16, f"mode {md} y step {s}", positions_axis=1,
+                            cond=osample[md].last_cond)
             check_close(to_host(ys[1]), to_host(ys[0]), synth.BF16, f"replay vs copy step {s}", pair=True)
             z = np.zeros((R, T1, 1, 1))
             meta_rule.verify(slots, z, np.zeros((R, T1, 1)), np.zeros((R, T1, 1, 16)), np.zeros((R, T1, 1, 16)))
-            meta_rule.commit(slots, acc_all[s])
+            _, folded = meta_rule.commit(slots, acc_all[s])
+            n_folds += int(folded.sum())
+        assert n_folds > 0, "the window never filled"
         torch.cuda.synchronize()
         for md in (0, 1):
             st, flags = m.ssm_pool_status(pools[md])
@@ -326,7 +352,7 @@ def test_nonfinite_verify_input_poisons_only_its_request(mode, where):
             gsl = [live[i] for i in good]
             _, yo = opool.verify(gsl, *[synth.widen(a[good], d) for a, d in
                                         ((x, synth.BF16), (dt, synth.F32), (B, synth.BF16), (C, synth.BF16))])
-            check_close(to_host(y)[good], yo, synth.BF16, f"y step {s}", positions_axis=1)
+            check_close(to_host(y)[good], yo, synth.BF16, f"y step {s}", positions_axis=1, cond=opool.last_cond)
             acc = np.full(len(live), 2, np.int32)
             if s == 1:
                 before = m.ssm_slot_info(pool, 1)[1]

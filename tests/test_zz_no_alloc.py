@@ -74,16 +74,64 @@ def test_static_scratch_replay_matches_pool_entry_point():
         st = m.ssm_verify_replay_static(R, T1, H, P, N, G, W, BF, F, ckpt, log_x, log_dt, log_B, log_len,
                                         *dev[s], Ad, Dd, y, flags)
         assert st == m.SSM_OK
+        # the bulk-copy pipelined kernel (the tensor-map kernels need the pool's larger scratch)
+        assert m.ssm_last_path(None) == "verify_replay_pipe"
         torch.cuda.synchronize()
-        check_close(to_host(y), to_host(y_pool[s]), BF, f"static call {call} (verify step {s})", positions_axis=1)
+        check_close(to_host(y), to_host(y_pool[s]), BF, f"static call {call} (verify step {s})", positions_axis=1,
+                    pair=True)
         if s == 1:
             log_len += torch.from_numpy(acc2 + 1).cuda()
     assert int(flags.item()) == 0
     assert torch.equal(ckpt, init_t)   # the checkpoint is read only
 
-    # requests beyond the built-in scratch are refused before any work
+    # requests beyond the built-in scratch are refused before any work; each limit on its own
     lib = m.library()
     p = ctypes.c_void_p(ckpt.data_ptr())
-    big = lib.ssm_verify_replay_static(1024, 64, 64, 64, 128, 8, 1024, BF, F, *([p] * 14), None)
-    assert big == m.SSM_ERR_INVALID_ARG
-    assert lib.ssm_verify_replay_static(1025, 1, 8, 64, 128, 8, 1, BF, F, *([p] * 14), None) == m.SSM_ERR_INVALID_ARG
+    ptrs = [p] * 13  # ckpt .. y; flags and the stream follow
+    # the batch limit alone (everything else in range, the scratch need small)
+    assert lib.ssm_verify_replay_static(1025, 1, 8, 64, 128, 1, 1, BF, F, *ptrs, p, None) == m.SSM_ERR_INVALID_ARG
+    # the scratch size alone: batch 1024, G 8, 9 tokens, Wc4 = 24 -> 1,769,472 floats > 1,047,552
+    assert lib.ssm_verify_replay_static(1024, 9, 64, 64, 128, 8, 16, BF, F, *ptrs, p, None) == m.SSM_ERR_INVALID_ARG
+    assert 1024 * 8 * 9 * 24 > m.SSM_STATIC_SCRATCH_FLOATS >= 1024 * 8 * 1 * 4
+
+
+def test_static_scratch_replay_at_serving_batch():
+    """At batch 512 with Nemotron-shaped heads, 8 drafts and window 16 (the
+    speculative verify workload) the static entry point runs the persistent
+    bulk-copy kernel over the whole GPU and gives the outputs of the pool's
+    verify on the same checkpoints and empty logs, on two calls in a row."""
+    import torch
+
+    import hybrid_serving_mamba_gb300 as m
+    H, P, N, G, R, T1, W = 128, 64, 128, 8, 512, 9, 16  # scratch: 512 * 8 * 9 * 24 floats
+    BF, F = synth.BF16, synth.F32
+    seed = synth.BASE_SEED + 7100
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    A = -torch.exp(torch.rand(H, generator=gen, device="cuda") * 1.5)
+    D = torch.randn(H, generator=gen, device="cuda")
+    ckpt = (torch.randn((R, H, P, N), generator=gen, device="cuda") * 0.1).contiguous()
+    x = torch.randn((R, T1, H, P), generator=gen, device="cuda").bfloat16()
+    dt = torch.nn.functional.softplus(torch.randn((R, T1, H), generator=gen, device="cuda") * 0.5 - 2.0)
+    B = torch.randn((R, T1, G, N), generator=gen, device="cuda").bfloat16()
+    C = torch.randn((R, T1, G, N), generator=gen, device="cuda").bfloat16()
+    pool = m.ssm_state_init(m.make_config(H, P, N, G, BF, F, m.SSM_MODE_REPLAY, W, T1), R, ckpt)
+    try:
+        y_pool = torch.empty((R, T1, H, P), dtype=torch.bfloat16, device="cuda")
+        assert m.ssm_verify_replay(pool, list(range(R)), T1, x, dt, B, C, A, D, y_pool) == m.SSM_OK
+    finally:
+        m.ssm_state_destroy(pool)
+    Wc = W - 1 + T1
+    log_x = torch.zeros((R, Wc, H, P), dtype=torch.bfloat16, device="cuda")
+    log_dt = torch.zeros((R, Wc, H), device="cuda")
+    log_B = torch.zeros((R, Wc, G, N), dtype=torch.bfloat16, device="cuda")
+    log_len = torch.zeros(R, dtype=torch.int32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call in range(2):
+        y = torch.empty_like(y_pool)
+        assert m.ssm_verify_replay_static(R, T1, H, P, N, G, W, BF, F, ckpt, log_x, log_dt, log_B, log_len,
+                                          x, dt, B, C, A, D, y, flags) == m.SSM_OK
+        assert m.ssm_last_path(None) == "verify_replay_pipe"
+        torch.cuda.synchronize()
+        assert int(flags.item()) == 0
+        check_close(to_host(y), to_host(y_pool), BF, f"static call {call} at batch {R}", pair=True)
