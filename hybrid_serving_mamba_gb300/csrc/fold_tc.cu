@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
             if (lane == 0) mbar_arrive(&hful[st]);
         }
     }
+    __syncwarp();  // warps whose lane 0 ran a role alone arrive at the block barrier converged
     tc::fence_before_sync();
     __syncthreads();
     if (warp == kFtMma) {

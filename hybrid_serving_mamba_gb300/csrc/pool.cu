@@ -490,14 +490,15 @@ ssm_status ssm_scan_chunk(ssm_pool pool, int32_t n_seq, const int32_t *cu_seqlen
             // the tensor-core scan moves x, B, C and y in 16-byte pieces
             const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(B) |
                                    reinterpret_cast<uintptr_t>(C) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+            const char *path = "scan_seq";
             bool ssd = aligned && ssm::scan_ssd_supported(p);
-            cudaError_t e = ssd ? ssm::launch_scan_ssd(p, a, s) : cudaErrorNotSupported;
+            cudaError_t e = ssd ? ssm::launch_scan_ssd(p, a, s, &path) : cudaErrorNotSupported;
             if (e == cudaErrorNotSupported) {  // no tensor maps for these buffers: the sequential scan
-                ssd = false;
+                path = "scan_seq";
                 e = ssm::launch_scan_seq(p, a, s);
             }
             if (e != cudaSuccess) return cuda_status(e);
-            p.last_path = ssd ? "scan_ssd" : "scan_seq";
+            p.last_path = path;
         }
     }
     for (int i = 0; i < n_seq; ++i) {

@@ -987,6 +987,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
             }
         }
     }
+    __syncwarp();  // warps whose lane 0 ran a role alone arrive at the block barrier converged
     tc::fence_before_sync();
     __syncthreads();
     if (warp == kTcMma) {

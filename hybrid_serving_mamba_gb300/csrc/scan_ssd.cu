@@ -539,7 +539,7 @@ bool scan_ssd_supported(const Pool &pool) {
     return pool.cfg.input_dtype == SSM_DTYPE_BF16 && pool.P == SP && pool.N == SN;
 }
 
-cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s) {
+cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s, const char **path) {
     (void)pool;
     const TensorMapEncode enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
@@ -562,6 +562,7 @@ cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSsdSmem);
     if (e != cudaSuccess) return e;
     k<<<dim3(a.H, a.n_seq), kThreads, kSsdSmem, s>>>(a, mx, mb, mc);
+    if (path) *path = "scan_ssd";
     return cudaGetLastError();
 }
 

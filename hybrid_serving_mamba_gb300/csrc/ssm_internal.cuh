@@ -201,7 +201,8 @@ cudaError_t launch_fold_pipe(const Pool &pool, const CommitArgs &a, cudaStream_t
 cudaError_t launch_scan_seq(const Pool &pool, const ScanArgs &a, cudaStream_t s);
 // Tensor-core chunked scan (bf16 x / B / C, headdim 64, dstate 128).
 bool scan_ssd_supported(const Pool &pool);
-cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s);
+// *path names the kernel ("scan_ssd").
+cudaError_t launch_scan_ssd(const Pool &pool, const ScanArgs &a, cudaStream_t s, const char **path);
 cudaError_t launch_reset(const Pool &pool, const int32_t *slots, int n, cudaStream_t s);
 cudaError_t launch_gather(const Pool &pool, const int32_t *slots, int n, float *dst, cudaStream_t s);
 

@@ -306,13 +306,18 @@ def test_config4_varlen_packed_with_slot_reuse(chunk):
         sc.close()
 
 
+# head counts and groups of the tensor-core scan cases: two groups of two heads, one group of three
+KERNELS = [(4, 2, "scan_ssd"), (3, 1, "scan_ssd")]
+
+
+@pytest.mark.parametrize("H,G,path", KERNELS)
 @pytest.mark.parametrize("lens,dt_dt", [([1, 5, 127, 128, 129, 300], synth.F32), ([0, 64, 256, 383], synth.BF16)])
-def test_tensor_core_scan_ragged_lengths(lens, dt_dt):
+def test_tensor_core_scan_ragged_lengths(lens, dt_dt, H, G, path):
     """The tensor-core chunked scan (bf16 x/B/C, headdim 64, dstate 128) on
-    lengths around its 128-token kernel chunk, with two groups, then a second
-    call that continues every sequence from its handed-off state."""
+    lengths around its 128-token kernel chunk, then a second call that
+    continues every sequence from its handed-off state."""
     m = _mod()
-    H, P, N, G = 4, 64, 128, 2
+    P, N = 64, 128
     seed = SEED1 + 77
     A, D = synth.head_params(seed, H)
     S = len(lens)
@@ -324,7 +329,7 @@ def test_tensor_core_scan_ragged_lengths(lens, dt_dt):
             st, ys = sc.scan(list(range(S)), toks)
             assert st == m.SSM_OK
             if any(lens):
-                assert m.ssm_last_path(sc.pool) == "scan_ssd"
+                assert m.ssm_last_path(sc.pool) == path
             got = sc.state(list(range(S)))
             for i in range(S):
                 y_ref, states[i], y_cond = _oracle_scan(A, D, toks[i], synth.BF16, dt_dt, states[i])
@@ -336,18 +341,20 @@ def test_tensor_core_scan_ragged_lengths(lens, dt_dt):
         sc.close()
 
 
-def test_tensor_core_scan_fast_decay_takes_the_exact_form():
+@pytest.mark.parametrize("H,G,path", KERNELS)
+def test_tensor_core_scan_fast_decay_takes_the_exact_form(H, G, path):
     """The tensor-core scan factors exp(cum_i - cum_j) around a reference
     point of each 128-token chunk only while both factors stay far inside
-    fp32; chunks whose decay over the chunk is steeper (here heads with
-    A = -40 and -400, and a stretch of one sequence with 30 times larger dt)
-    take the exact per-block form instead.  Both forms, mixed within one
-    sequence and across its calls, match the oracle."""
+    fp32; where the decay over the chunk is steeper (here heads with A = -40
+    and -400, and a stretch of one sequence with 30 times larger dt) the
+    two-head kernel cuts the chunk into shorter passes and the one-head
+    kernel takes its exact per-block form.  Mixed within one sequence and
+    across its calls, they match the oracle."""
     m = _mod()
-    H, P, N, G = 4, 64, 128, 2
+    P, N = 64, 128
     seed = SEED1 + 79
     _, D = synth.head_params(seed, H)
-    A = np.array([-1.0, -3.0, -40.0, -400.0], np.float32)
+    A = np.array([-1.0, -3.0, -40.0, -400.0][-H:], np.float32)
     lens = [300, 129, 384]
     S = len(lens)
     sc = Scanner(m, H, P, N, G, synth.BF16, synth.F32, S, A, D)
@@ -360,7 +367,7 @@ def test_tensor_core_scan_fast_decay_takes_the_exact_form():
             toks[0][1][150:260] *= np.float32(30.0)   # dt: a steep stretch in the middle of sequence 0
             toks = [tuple(t) for t in toks]
             st, ys = sc.scan(list(range(S)), toks)
-            assert st == m.SSM_OK and m.ssm_last_path(sc.pool) == "scan_ssd"
+            assert st == m.SSM_OK and m.ssm_last_path(sc.pool) == path
             got = sc.state(list(range(S)))
             for i in range(S):
                 y_ref, states[i], y_cond = _oracle_scan(A, D, toks[i], synth.BF16, synth.F32, states[i])
@@ -371,26 +378,27 @@ def test_tensor_core_scan_fast_decay_takes_the_exact_form():
         sc.close()
 
 
+@pytest.mark.parametrize("H,G,path", KERNELS)
 @pytest.mark.parametrize("where", ["B", "C", "x", "dt"])
-def test_tensor_core_scan_nonfinite_poisons_slot(where):
+def test_tensor_core_scan_nonfinite_poisons_slot(where, H, G, path):
     """bf16 scan on the tensor cores: a NaN or Inf in a sequence's B, C, x or
     dt flags SSM_FLAG_NONFINITE_INPUT, poisons its slot and leaves the state
     of every head it reaches as it was; the other sequence of the call
     advances and matches the oracle."""
     m = _mod()
-    H, P, N, G = 4, 64, 128, 2
+    P, N = 64, 128
     seed = SEED1 + 91
     A, D = synth.head_params(seed, H)
     sc = Scanner(m, H, P, N, G, synth.BF16, synth.F32, 2, A, D)
     try:
         toks = [synth.tokens(seed, i, 300, H, P, G, N, synth.BF16, synth.F32) for i in range(2)]
         assert sc.scan([0, 1], [_slice(t, 0, 150) for t in toks])[0] == m.SSM_OK
-        assert m.ssm_last_path(sc.pool) == "scan_ssd"
+        assert m.ssm_last_path(sc.pool) == path
         before = sc.state([0, 1])
         bad = [t.copy() for t in _slice(toks[0], 150, 300)]
         nan16, inf16 = np.uint16(0x7FC0), np.uint16(0x7F80)  # bf16 bit patterns
         if where == "B":
-            bad[2][140, 0, 5] = nan16      # group 0: heads 0 and 1
+            bad[2][140, 0, 5] = nan16      # group 0: heads 0 and 1 (and 2 with one group)
         elif where == "C":
             bad[3][140, 0, 5] = inf16
         elif where == "x":
@@ -398,7 +406,7 @@ def test_tensor_core_scan_nonfinite_poisons_slot(where):
         else:
             bad[1][140, 1] = np.nan
         assert sc.scan([0, 1], [tuple(bad), _slice(toks[1], 150, 300)])[0] == m.SSM_OK  # found on the device
-        assert m.ssm_last_path(sc.pool) == "scan_ssd"
+        assert m.ssm_last_path(sc.pool) == path
         assert m.ssm_pool_status(sc.pool, clear=True)[1] & m.SSM_FLAG_NONFINITE_INPUT
         after = sc.state([0, 1])
         for h in ([0, 1] if where in ("B", "C") else [1]):
