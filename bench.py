@@ -505,7 +505,11 @@ def bench_prefill(torch, m, args):
     path = m.ssm_last_path(pool)
     m.ssm_state_destroy(pool)
     alg = 2 * R * L * H * P * 2 + R * L * (H * 2 + 2 * G * N * 2) + R * H * P * N * 4
-    return dict(us_per_scan=1000 * ms, tokens_per_s=R * L / (ms / 1000), path=path,
+    # DRAM bytes of one scan from the profile (taken at 16 sequences, traffic in proportion to them)
+    prof = profiled_traffic("scan_ssd_kernel_130m.md", "hybrid_serving_mamba_gb300/csrc/scan_ssd.cu",
+                            "hybrid_serving_mamba_gb300/csrc/tc.cuh", "hybrid_serving_mamba_gb300/csrc/tma.cuh")
+    traffic = prof * R / 16 if prof is not None else None
+    return dict(us_per_scan=1000 * ms, tokens_per_s=R * L / (ms / 1000), path=path, traffic=traffic,
                 achieved_gbs=alg / (ms / 1000) / 1e9, algorithmic_bytes=alg,
                 frac_of_hbm=alg / (ms / 1000) / 1e9 / measured_peaks()[0],
                 config=dict(seqs=R, seqlen=L, heads=H, headdim=P, dstate=N, groups=G, includes="reset + scan"))
