@@ -242,12 +242,11 @@ def bench_decode(torch, m, dist, args, clocks):
 
 
 def bench_decode_e2e(torch, m, args):
-    """The same decode workload through the public API with host buffers:
-    every token's inputs copied from pinned host memory, its output copied
-    back, inside the timed region.  Copies overlap the decode the way a
-    serving loop would run them: token t + 1's inputs go up on one copy
-    stream while token t decodes, token t - 1's output comes down on another,
-    with two staging buffers each and events ordering their reuse."""
+    """The same decode workload through the C ABI's host-buffer entry
+    (ssm_decode_steps_host): every token's inputs go up from pinned host
+    memory and its output comes back inside the timed region, the library
+    overlapping token t + 1's upload and token t - 1's readback with token t's
+    decode on its own copy streams."""
     c = DEC
     gen = torch.Generator(device="cuda")
     gen.manual_seed(SEED + 91 + 17 * args.rank)
@@ -258,57 +257,33 @@ def bench_decode_e2e(torch, m, args):
                             R, init)
     del init
     dev_in = step_inputs(torch, gen, T * R, H, P, G, N)
-    host_in = [t.view(T, R, *t.shape[1:]).cpu().pin_memory() for t in dev_in]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
     del dev_in
-    stage = [[torch.empty(t.shape[1:], dtype=t.dtype, device="cuda") for t in host_in] for _ in range(2)]
-    y_dev = [torch.empty((R, H, P), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     y_host = torch.empty((T, R, H, P), dtype=torch.bfloat16).pin_memory()
     slots = list(range(R))
     stream = torch.cuda.current_stream()
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = lambda: [torch.cuda.Event() for _ in range(2)]
-    in_ready, used, y_ready, y_free = ev(), ev(), ev(), ev()
 
-    def one_step(first):
-        for t in range(T):
-            b = t % 2
-            with torch.cuda.stream(up):  # inputs of token t into buffer b, once token t - 2 has used it
-                if t >= 2 or not first:
-                    up.wait_event(used[b])
-                for s, h in zip(stage[b], host_in):
-                    s.copy_(h[t], non_blocking=True)
-                in_ready[b].record(up)
-            stream.wait_event(in_ready[b])
-            if t >= 2 or not first:
-                stream.wait_event(y_free[b])  # y buffer b read back
-            m.ssm_decode_step(pool, slots, *stage[b], A, D, y_dev[b], stream=stream)
-            used[b].record(stream)
-            y_ready[b].record(stream)
-            with torch.cuda.stream(down):
-                down.wait_event(y_ready[b])
-                y_host[t].copy_(y_dev[b], non_blocking=True)
-                y_free[b].record(down)
-        stream.wait_stream(up)
-        stream.wait_stream(down)  # every copy of the step is done before the step ends
+    def one_step():
+        st = m.ssm_decode_steps_host(pool, slots, T, *host_in, A, D, y_host, stream=stream)
+        assert st == m.SSM_OK, f"ssm_decode_steps_host returned {st}"
 
-    steps = max(3, args.steps // 3)
-    for w in range(max(1, args.warmup)):
-        one_step(w == 0)
+    for _ in range(max(1, args.warmup)):
+        one_step()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    up.wait_stream(stream)  # no copy of the timed steps starts before t0
-    down.wait_stream(stream)
-    for _ in range(steps):
-        one_step(False)
+    for _ in range(args.steps):
+        one_step()
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
+    st, flags = m.ssm_pool_status(pool)
+    assert st == m.SSM_OK and flags == 0, f"host-buffer decode raised device flags {flags}"
     m.ssm_state_destroy(pool)
-    h2d = sum(h[0].numel() * h.element_size() for h in host_in) * T
-    d2h = R * H * P * 2 * T
-    return dict(ms=ms, tokens=R * T * steps, h2d=h2d, d2h=d2h)
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = y_host.numel() * y_host.element_size()
+    return dict(ms=ms, tokens=R * T * args.steps, h2d=h2d, d2h=d2h)
 
 
 def _verify_bytes(acc_np, R, H, P, N, G, T1, W, S, warm):
@@ -1133,7 +1108,8 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = {"value": e2e["tokens"] / (e2e["ms"] / 1000.0), "unit": "tok/s",
-                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "entry": "ssm_decode_steps_host", "steps": args.steps}
     line.update(extras)
     if not args.no_extras:
         line["cpu_baseline"] = cpu_baseline()

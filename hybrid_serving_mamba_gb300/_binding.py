@@ -33,6 +33,7 @@ SSM_FLAG_LOG_NOT_EMPTY, SSM_FLAG_TIMEOUT = 8, 16
 EXPORTS = (
     "ssm_state_init", "ssm_state_destroy", "ssm_state_reset", "ssm_state_release", "ssm_state_checkpoint",
     "ssm_state_restore", "ssm_slot_info", "ssm_state_gather", "ssm_scan_chunk", "ssm_decode_step",
+    "ssm_decode_steps_host",
     "ssm_verify_copy", "ssm_verify_replay", "ssm_state_commit", "ssm_pool_status", "ssm_last_path",
     "ssm_status_string", "ssm_pool_bytes", "ssm_verify_replay_static", "ssm_receipt_bytes", "ssm_receipt_encode",
     "ssm_receipt_decode", "ssm_state_checkpoint_receipt", "ssm_state_restore_receipt",
@@ -98,6 +99,7 @@ def _load():
         "ssm_state_gather": [V, I32, P_I32, V, V],
         "ssm_scan_chunk": [V, I32, P_I32, P_I32, P_I64, V, V, V, V, V, V, V, V],
         "ssm_decode_step": [V, I32, P_I32, V, V, V, V, V, V, V, V],
+        "ssm_decode_steps_host": [V, I32, P_I32, I32, V, V, V, V, V, V, V, V],
         "ssm_verify_copy": [V, I32, I32, P_I32, V, V, V, V, V, V, V, V],
         "ssm_verify_replay": [V, I32, I32, P_I32, V, V, V, V, V, V, V, V],
         "ssm_state_commit": [V, I32, P_I32, V, I32, V, V],
@@ -355,6 +357,32 @@ def ssm_decode_step(pool: Pool, slots, x, dt, B, C, A, D, y, stream=None) -> int
     sl, psl = _host_i32(slots)
     return _lib.ssm_decode_step(pool.handle, len(sl), psl, *_inputs(pool, len(sl), x, dt, B, C, A, D, y),
                                 _stream(stream))
+
+
+def _pinned(t, name, dtype, numel):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements, got {t.numel()}")
+    return ctypes.c_void_p(t.data_ptr())  # page-locked or not: the library checks and refuses
+
+
+def ssm_decode_steps_host(pool: Pool, slots, n_steps: int, x, dt, B, C, A, D, y, stream=None) -> int:
+    """n_steps decode tokens over the same slots, x / dt / B / C / y host tensors (page-locked), step-major."""
+    import torch
+    sl, psl = _host_i32(slots)
+    n = len(sl) * int(n_steps)
+    td, tdt = pool.torch_dtype(), pool.torch_dtype(pool.cfg.dt_dtype)
+    H, P, N, G = pool.H, pool.P, pool.N, pool.G
+    return _lib.ssm_decode_steps_host(pool.handle, len(sl), psl, int(n_steps), _pinned(x, "x", td, n * H * P),
+                                      _pinned(dt, "dt", tdt, n * H), _pinned(B, "B", td, n * G * N),
+                                      _pinned(C, "C", td, n * G * N), _dev(A, "A", torch.float32, H),
+                                      _dev(D, "D", torch.float32, H), _pinned(y, "y", td, n * H * P),
+                                      _stream(stream))
 
 
 def ssm_verify_copy(pool: Pool, slots, n_tok: int, x, dt, B, C, A, D, y, stream=None) -> int:

@@ -67,6 +67,14 @@ void free_all(Pool &p) {
     cudaFree(p.d_cf);
     cudaFree(p.d_fold_items);
     cudaFree(p.d_fold_count);
+    Pool::HostPipe &h = p.hpipe;
+    cudaFree(h.buf);
+    for (cudaEvent_t e : {h.start, h.in_ready[0], h.in_ready[1], h.used[0], h.used[1], h.y_ready[0], h.y_ready[1],
+                          h.y_free[0], h.y_free[1]})
+        if (e) cudaEventDestroy(e);
+    if (h.up) cudaStreamDestroy(h.up);
+    if (h.down) cudaStreamDestroy(h.down);
+    h = Pool::HostPipe{};
 }
 
 int warps_needed(int N, int P) {
@@ -520,6 +528,114 @@ ssm_status ssm_decode_step(ssm_pool pool, int32_t batch, const int32_t *slots, c
     fill_step(p, a, x, dt, B, C, A, D, y, 1);
     st = run_step(p, a, slots, batch, 1, ssm::launch_decode, reinterpret_cast<cudaStream_t>(stream));
     if (st != SSM_OK) return st;
+    for (int i = 0; i < batch; ++i) p.pending_ntok[slots[i]] = 0;
+    p.last_path = "decode";
+    return SSM_OK;
+}
+
+// The host pipe's streams and events, and staging sets of at least set_bytes
+// (re-allocated once the previous sets are idle).
+static cudaError_t host_pipe_ready(Pool &p, size_t set_bytes) {
+    Pool::HostPipe &h = p.hpipe;
+    cudaError_t e = cudaSuccess;
+    if (!h.up) {
+        e = cudaStreamCreateWithFlags(&h.up, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.down, cudaStreamNonBlocking);
+        cudaEvent_t *evs[] = {&h.start, &h.in_ready[0], &h.in_ready[1], &h.used[0], &h.used[1],
+                              &h.y_ready[0], &h.y_ready[1], &h.y_free[0], &h.y_free[1]};
+        for (cudaEvent_t *ev : evs)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+    }
+    if (set_bytes <= h.set_cap) return cudaSuccess;
+    if (h.buf) {  // queued copies and decodes of earlier calls may still touch the old sets
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            e = cudaEventSynchronize(h.used[b]);
+            if (e == cudaSuccess) e = cudaEventSynchronize(h.y_free[b]);
+        }
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h.up);
+        if (e != cudaSuccess) return e;
+        cudaFree(h.buf);
+        p.bytes -= 2 * h.set_cap;
+        h.buf = nullptr;
+        h.set_cap = 0;
+    }
+    const size_t cap = (set_bytes + 255) / 256 * 256;
+    e = cudaMalloc(reinterpret_cast<void **>(&h.buf), 2 * cap);
+    if (e != cudaSuccess) {
+        h.buf = nullptr;
+        return e;
+    }
+    p.bytes += 2 * cap;
+    h.set_cap = cap;
+    return cudaSuccess;
+}
+
+static bool page_locked(const void *ptr) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+
+ssm_status ssm_decode_steps_host(ssm_pool pool, int32_t batch, const int32_t *slots, int32_t n_steps,
+                                 const void *x, const void *dt, const void *B, const void *C, const float *A,
+                                 const float *D, void *y, ssm_stream_t stream) {
+    if (!pool || !x || !dt || !B || !C || !A || !D || !y || n_steps < 1) return SSM_ERR_INVALID_ARG;
+    ssm_status st = check_slots(pool, slots, batch, false);
+    if (st != SSM_OK) return st;
+    Pool &p = pool->p;
+    DeviceGuard g(p.device);
+    for (const void *ptr : {x, dt, B, C, static_cast<const void *>(y)})
+        if (!page_locked(ptr)) return SSM_ERR_INVALID_ARG;
+    const size_t in_b = in_elem(p.cfg.input_dtype), dt_b = in_elem(p.cfg.dt_dtype);
+    // one step's bytes of each array; each starts on a 256-byte boundary in a staging set
+    const size_t nb[5] = {(size_t)batch * p.H * p.P * in_b, (size_t)batch * p.H * dt_b,
+                          (size_t)batch * p.G * p.N * in_b, (size_t)batch * p.G * p.N * in_b,
+                          (size_t)batch * p.H * p.P * in_b};
+    size_t off[5], set_bytes = 0;
+    for (int i = 0; i < 5; ++i) {
+        off[i] = set_bytes;
+        set_bytes += (nb[i] + 255) / 256 * 256;
+    }
+    cudaError_t e = host_pipe_ready(p, set_bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+    Pool::HostPipe &h = p.hpipe;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const char *src[4] = {static_cast<const char *>(x), static_cast<const char *>(dt),
+                          static_cast<const char *>(B), static_cast<const char *>(C)};
+    char *dst = static_cast<char *>(y);
+    e = cudaEventRecord(h.start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h.up, h.start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h.down, h.start, 0);
+    int b = 0;
+    for (int t = 0; t < n_steps && e == cudaSuccess; ++t) {
+        b = t & 1;
+        char *set = h.buf + b * h.set_cap;
+        // inputs of step t into set b, once the decode that last read it is done
+        e = cudaStreamWaitEvent(h.up, h.used[b], 0);
+        for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+            e = cudaMemcpyAsync(set + off[i], src[i] + t * nb[i], nb[i], cudaMemcpyHostToDevice, h.up);
+        if (e == cudaSuccess) e = cudaEventRecord(h.in_ready[b], h.up);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h.in_ready[b], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h.y_free[b], 0);  // set b's output read back
+        if (e != cudaSuccess) break;
+        ssm::StepArgs a;
+        fill_step(p, a, set + off[0], set + off[1], set + off[2], set + off[3], A, D, set + off[4], 1);
+        st = run_step(p, a, slots, batch, 1, ssm::launch_decode, s);
+        if (st != SSM_OK) return st;
+        e = cudaEventRecord(h.used[b], s);
+        if (e == cudaSuccess) e = cudaEventRecord(h.y_ready[b], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h.down, h.y_ready[b], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dst + t * nb[4], set + off[4], nb[4], cudaMemcpyDeviceToHost, h.down);
+        if (e == cudaSuccess) e = cudaEventRecord(h.y_free[b], h.down);
+    }
+    // the last output copy ends after every earlier one (one stream); every input copy was waited on
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h.y_free[b], 0);
+    if (e != cudaSuccess) return cuda_status(e);
     for (int i = 0; i < batch; ++i) p.pending_ntok[slots[i]] = 0;
     p.last_path = "decode";
     return SSM_OK;

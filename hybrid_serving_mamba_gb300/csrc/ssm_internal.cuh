@@ -77,6 +77,15 @@ struct Pool {
     int sm_count = 1;
     size_t bytes = 0;
 
+    // host-buffer decode: two staging sets, each x | dt | B | C | y of one step, and the copy streams
+    struct HostPipe {
+        cudaStream_t up = nullptr, down = nullptr;
+        // start; then per set: inputs landed, inputs consumed, output written, output read back
+        cudaEvent_t start = nullptr, in_ready[2] = {}, used[2] = {}, y_ready[2] = {}, y_free[2] = {};
+        char *buf = nullptr;  // [2][set_cap]
+        size_t set_cap = 0;
+    } hpipe;
+
     // host mirror
     std::vector<int64_t> next_chunk, epoch;
     std::vector<uint8_t> released;

@@ -293,6 +293,29 @@ ssm_status ssm_decode_step(ssm_pool pool, int32_t batch, const int32_t *slots, c
                            const float *D, void *y, ssm_stream_t stream);
 
 /*
+ * n_steps decode tokens for the same `batch` requests with the token inputs
+ * and outputs in page-locked host memory (cudaHostAlloc, cudaHostRegister):
+ * step t is ssm_decode_step on row t of x [n_steps][batch][H][P],
+ * dt [n_steps][batch][H], B, C [n_steps][batch][G][N] and
+ * y [n_steps][batch][H][P] (dtypes as there); A and D stay device pointers.
+ * The rows pass through two device staging sets owned by the pool: step
+ * t + 1's inputs go up on one copy stream while step t decodes on `stream`
+ * and step t - 1's output comes down on another, events ordering each reuse.
+ * Copies start after the work queued on `stream` before the call.  The call
+ * returns once everything is queued; `stream` is then ordered after the last
+ * output copy, so y is complete once `stream` is synchronized, and the host
+ * buffers must stay valid and unchanged until then.  Staging is allocated
+ * the first time a call needs more than the pool holds (that call waits for
+ * the previous staging to go idle).
+ * SSM_ERR_INVALID_ARG: a null pointer, n_steps < 1, or x, dt, B, C or y not
+ * page-locked host memory; slot errors as ssm_decode_step.  An error after
+ * some steps were queued leaves those steps applied.
+ */
+ssm_status ssm_decode_steps_host(ssm_pool pool, int32_t batch, const int32_t *slots, int32_t n_steps,
+                                 const void *x, const void *dt, const void *B, const void *C,
+                                 const float *A, const float *D, void *y, ssm_stream_t stream);
+
+/*
  * Speculative verify, copy flavour (copy pools only): each request walks its
  * n_tok = T + 1 tokens (the pending real token, then T drafts) from its
  * current state and keeps a full state copy after every token (Why

@@ -63,6 +63,8 @@ def test_null_pool_is_rejected(mod):
     slots = (ctypes.c_int32 * 1)(0)
     assert lib.ssm_decode_step(None, 1, slots, None, None, None, None, None, None, None, None) == mod.SSM_ERR_INVALID_ARG
     assert lib.ssm_state_commit(None, 1, slots, None, 0, None, None) == mod.SSM_ERR_INVALID_ARG
+    V = ctypes.c_void_p
+    assert lib.ssm_decode_steps_host(None, 1, slots, 1, *([V(8)] * 7), None) == mod.SSM_ERR_INVALID_ARG
     f = ctypes.c_uint32()
     assert lib.ssm_pool_status(None, ctypes.byref(f), 0, None) == mod.SSM_ERR_INVALID_ARG
     assert lib.ssm_last_path(None) == b"none"

@@ -67,6 +67,58 @@ def test_decode_matches_oracle(H, P, N, G, dt_in, dt_dt):
         m.ssm_state_destroy(pool)
 
 
+@pytest.mark.parametrize("dt_in,dt_dt", [(synth.F32, synth.F32), (synth.BF16, synth.F32), (synth.BF16, synth.BF16)])
+def test_decode_from_host_buffers_equals_device_path(dt_in, dt_dt):
+    """ssm_decode_steps_host over n steps (inputs and outputs in page-locked
+    host memory) gives bit for bit the outputs and states of n ssm_decode_step
+    calls on the same rows, and follows the oracle; a later call with a larger
+    batch regrows the staging; pageable host memory is refused and changes
+    nothing."""
+    import torch
+    m = _mod()
+    H, P, N, G, n_slots = 8, 64, 128, 4, 7
+    A, D = synth.head_params(SEED + 1, H)
+    init = np.stack([synth.init_state(SEED + 1, s, H, P, N) for s in range(n_slots)])
+    pd = _pool(m, H, P, N, G, dt_in, dt_dt, n_slots, init)
+    ph = _pool(m, H, P, N, G, dt_in, dt_dt, n_slots, init)
+    opool = oracle.OraclePool(H, P, N, G, n_slots, A, D, init_state=init.astype(np.float64))
+    Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+    side = torch.cuda.Stream()
+    try:
+        for call, (slots, steps) in enumerate((([5, 0, 3], 5), ([1, 2, 4, 6, 5, 0, 3], 3))):
+            R = len(slots)
+            rows = [_step_inputs(SEED + 1, 10 * call + t, R, H, P, G, N, dt_in, dt_dt) for t in range(steps)]
+            host = [torch.stack([to_device(r[i], code, "cpu") for r in rows]).pin_memory()
+                    for i, code in enumerate((dt_in, dt_dt, dt_in, dt_in))]
+            y_host = empty_like_out((steps, R, H, P), dt_in, "cpu").pin_memory()
+            if call == 1:  # pageable buffers: refused before anything is queued
+                st = m.ssm_decode_steps_host(ph, slots, steps, *(h.clone() for h in host), Ad, Dd, y_host.clone())
+                assert st == m.SSM_ERR_INVALID_ARG
+            with torch.cuda.stream(side):
+                st = m.ssm_decode_steps_host(ph, slots, steps, *host, Ad, Dd, y_host, stream=side)
+            assert st == m.SSM_OK
+            side.synchronize()
+            for t, (x, dt, B, C) in enumerate(rows):
+                y = empty_like_out((R, H, P), dt_in)
+                assert m.ssm_decode_step(pd, slots, to_device(x, dt_in), to_device(dt, dt_dt), to_device(B, dt_in),
+                                         to_device(C, dt_in), Ad, Dd, y) == m.SSM_OK
+                assert torch.equal(y.cpu(), y_host[t]), f"call {call} step {t}: host path differs"
+                _, yo = opool.decode(slots, synth.widen(x, dt_in), synth.widen(dt, dt_dt), synth.widen(B, dt_in),
+                                     synth.widen(C, dt_in))
+                check_close(to_host(y_host[t]), yo, dt_in, f"host path y call {call} step {t}", cond=opool.last_cond)
+        gd = torch.empty((n_slots, H, P, N), device="cuda")
+        gh = torch.empty_like(gd)
+        assert m.ssm_state_gather(pd, list(range(n_slots)), gd) == m.SSM_OK
+        assert m.ssm_state_gather(ph, list(range(n_slots)), gh) == m.SSM_OK
+        assert torch.equal(gd, gh)
+        for s in range(n_slots):
+            assert m.ssm_slot_info(ph, s)[1].position == m.ssm_slot_info(pd, s)[1].position
+        assert m.ssm_pool_status(ph) == (m.SSM_OK, 0)
+    finally:
+        m.ssm_state_destroy(pd)
+        m.ssm_state_destroy(ph)
+
+
 def test_decode_nemotron_shape_full_batch_sampled():
     """Batched decode, Nemotron-shaped (H=128, P=64, N=128, G=8), batch 256,
     64 successive steps, bf16 x/B/C, fp32 dt and N(0, 0.1) fp32 state; the
