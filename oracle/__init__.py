@@ -338,9 +338,12 @@ class OraclePool:
     array shaped like y; a list of them for scan_chunk).
     """
 
-    def __init__(self, H, P, N, G, n_slots, A, D, mode=COPY, W=16, max_tokens=9, init_state=None):
+    def __init__(self, H, P, N, G, n_slots, A, D, mode=COPY, W=16, max_tokens=9, init_state=None,
+                 fold_in_verify=False):
         self.H, self.P, self.N, self.G = H, P, N, G
         self.n_slots, self.mode, self.W, self.T1max = n_slots, mode, W, max_tokens
+        # replay: a commit that fills the window leaves the log full, and the next verify folds it
+        self.fold_in_verify = bool(fold_in_verify)
         self.A, self.D = _f64(A), _f64(D)
         self.state = np.zeros((n_slots, H, P, N), np.float64)
         if init_state is not None:
@@ -441,6 +444,8 @@ class OraclePool:
             for i, s in enumerate(sl):
                 self._pending[s] = ("copy", snap[:, i].copy(), T1)
         else:
+            if self.fold_in_verify:  # a log of W or more tokens goes into the checkpoint first
+                self.flush([s for s in sl if self.log_len[s] >= self.W])
             y, self.last_cond = verify_replay(self.state[sl], self.log_len[sl], self.lx[sl], self.ldt[sl],
                                               self.lB[sl], x, dt, B, C, self.A, self.D, want_cond=True)
             xs, dts, Bs = _f64(x), _f64(dt), _f64(B)
@@ -454,7 +459,11 @@ class OraclePool:
         Copy mode: the state after the last accepted token becomes current.
         Replay mode: if log_len + c < W (and no forced fold) the c accepted
         tokens are appended to the log; otherwise the log and the c tokens
-        are folded into the checkpoint and the log empties.
+        are folded into the checkpoint and the log empties.  With
+        fold_in_verify the c tokens are appended whatever the length (unless
+        forced), and the next verify folds a log of W or more tokens before
+        it replays (the same states and outputs, the checkpoint written one
+        call later).
         Returns (status, folded flags).
         """
         st = self._check_slots(slots)
@@ -474,7 +483,7 @@ class OraclePool:
             else:
                 xs, dts, Bs = payload
                 k = int(self.log_len[s])
-                if k + c < self.W and not force_fold:
+                if (k + c < self.W or self.fold_in_verify) and not force_fold:
                     self.lx[s, k:k + c] = xs[:c]
                     self.ldt[s, k:k + c] = dts[:c]
                     self.lB[s, k:k + c] = Bs[:c]

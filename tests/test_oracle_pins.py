@@ -332,6 +332,49 @@ def test_replay_equals_copy(W):
     np.testing.assert_array_equal(copy.position, (acc + 1).sum(axis=0))
 
 
+@pytest.mark.parametrize("W", [1, 3, 4, 8])
+def test_fold_in_verify_equals_fold_at_commit(W):
+    """The deferred rule (a commit that fills the window leaves the log full,
+    the next verify folds it first) gives the outputs of the at-commit rule
+    and the sequential recurrence, and right after each verify its log holds
+    what the at-commit pool's log holds: the fold only moves one call later
+    (Why Speculative Decoding Slows Hybrid Mamba Models, The Fix)."""
+    H, P, N, G, R, T, steps = 4, 6, 8, 2, 3, 3, 11
+    seed = 4343
+    A, D = synth.head_params(seed, H)
+    h0 = np.stack([synth.init_state(seed, s, H, P, N) for s in range(R)]).astype(np.float64)
+    acc = synth.accept_counts(seed, steps, R, T, 0.7)
+    now = oracle.OraclePool(H, P, N, G, R, A, D, mode=oracle.REPLAY, W=W, init_state=h0, max_tokens=T + 1)
+    late = oracle.OraclePool(H, P, N, G, R, A, D, mode=oracle.REPLAY, W=W, init_state=h0, max_tokens=T + 1,
+                             fold_in_verify=True)
+    copy = oracle.OraclePool(H, P, N, G, R, A, D, mode=oracle.COPY, init_state=h0, max_tokens=T + 1)
+    slots = list(range(R))
+    deferred = 0
+    for s in range(steps):
+        x, dt, B, C = (synth.widen(a, synth.F32) for a in synth.batch_tokens(seed, s, R, T + 1, H, P, G, N))
+        _, yn = now.verify(slots, x, dt, B, C)
+        _, yl = late.verify(slots, x, dt, B, C)
+        _, yc = copy.verify(slots, x, dt, B, C)
+        np.testing.assert_allclose(yl, yn, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(yl, yc, rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(late.log_len, now.log_len)
+        np.testing.assert_allclose(late.state, now.state, rtol=1e-12, atol=1e-12)
+        now.commit(slots, acc[s])
+        _, folded = late.commit(slots, acc[s])
+        copy.commit(slots, acc[s])
+        assert not folded.any()  # folds happen in the verify only
+        assert np.all(late.log_len <= W - 1 + T + 1)
+        deferred += int(np.sum(late.log_len >= W))
+    assert deferred > 0, "no log filled the window"
+    late.flush(slots)
+    np.testing.assert_allclose(late.state, copy.state, rtol=1e-12, atol=1e-12)
+    # a forced fold still folds at the commit
+    x, dt, B, C = (synth.widen(a, synth.F32) for a in synth.batch_tokens(seed, steps, R, T + 1, H, P, G, N))
+    late.verify(slots, x, dt, B, C)
+    _, folded = late.commit(slots, [0] * R, force_fold=True)
+    assert folded.all() and np.all(late.log_len == 0)
+
+
 def test_fold_rule_is_exact_in_counts():
     """Plain decode through replay (one token per step) folds every W steps."""
     H, P, N, G, W = 2, 4, 4, 1, 5
