@@ -317,6 +317,33 @@ def _verify_bytes(acc_np, R, H, P, N, G, T1, W, S, warm):
     return copy_b, total / S, folds / S
 
 
+def _verify_bytes_fold_in_verify(acc_np, R, H, P, N, G, T1, W, S, warm):
+    """Algorithmic bytes per step of replay verify (+ commit) when the verify
+    folds a full log: read the checkpoint and the k logged entries, token
+    inputs and outputs, stage the step's entries; a request whose log holds W
+    or more tokens also writes its new checkpoint (its log was read above).
+    The commit only appends.  Log lengths follow that rule on the same accept
+    counts, warm-up steps included."""
+    state = H * P * N * 4
+    tok_in = H * P * 2 + H * 4 + 2 * G * N * 2
+    entry = H * P * 2 + H * 4 + G * N * 2
+    y_b = H * P * 2
+    total, folds = 0, 0
+    k = [0] * R
+    for n_run, counted in ((warm, False), (S, True)):
+        for step in range(n_run):
+            for r in range(R):
+                b = state + k[r] * entry + T1 * (tok_in + y_b + entry)
+                if k[r] >= W:
+                    b += state
+                    k[r] = 0
+                    folds += counted
+                k[r] += int(acc_np[step % S][r]) + 1
+                if counted:
+                    total += b
+    return total / S, folds / S
+
+
 def bench_verify(torch, m, args, T=None, p=None, windows=None, static=False):
     """Copy verify vs ReplaySSM verify at batch 512, verify + commit per step,
     at one (T, p) and the given windows (the copy flavour does not depend on
@@ -341,11 +368,14 @@ def bench_verify(torch, m, args, T=None, p=None, windows=None, static=False):
     stream = torch.cuda.current_stream()
     peak, _, kind = measured_peaks()
     warm = 3
-    out = {"replay": {}}
-    runs = [(m.SSM_MODE_COPY, "copy", windows[0])] + [(m.SSM_MODE_REPLAY, "replay", W) for W in windows]
-    for mode, name, W in runs:
+    out = {"replay": {}, "replay_fold_in_verify": {}}
+    runs = ([(m.SSM_MODE_COPY, "copy", windows[0], m.SSM_FOLD_AT_COMMIT)] +
+            [(m.SSM_MODE_REPLAY, "replay", W, m.SSM_FOLD_AT_COMMIT) for W in windows] +
+            [(m.SSM_MODE_REPLAY, "replay_fold_in_verify", W, m.SSM_FOLD_IN_VERIFY) for W in windows])
+    for mode, name, W, fold in runs:
         init = (torch.randn((R, H, P, N), generator=gen, device="cuda") * 0.1).contiguous()
-        pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, mode, W, T1), R, init)
+        pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, mode, W, T1,
+                                              fold=fold), R, init)
         del init
         verify = m.ssm_verify_copy if mode == m.SSM_MODE_COPY else m.ssm_verify_replay
 
@@ -367,6 +397,8 @@ def bench_verify(torch, m, args, T=None, p=None, windows=None, static=False):
         st, flags = m.ssm_pool_status(pool)
         assert st == m.SSM_OK and flags == 0, f"{name} verify raised device flags {flags}"
         copy_b, replay_b, folds = _verify_bytes(acc_np, R, H, P, N, G, T1, W, S, warm)
+        if fold == m.SSM_FOLD_IN_VERIFY:
+            replay_b, folds = _verify_bytes_fold_in_verify(acc_np, R, H, P, N, G, T1, W, S, warm)
         b = copy_b if mode == m.SSM_MODE_COPY else replay_b
         us = 1000.0 * ms / S
         gbs = b / (us * 1e-6) / 1e9
@@ -389,7 +421,9 @@ def bench_verify(torch, m, args, T=None, p=None, windows=None, static=False):
         else:
             rec.update(W=W, folds_per_step=folds, commit_path=paths,
                        over_plain=us / out["plain_decode_us"], copy_over_replay=out["copy"]["us_per_step"] / us)
-            out["replay"][str(W)] = rec
+            if fold == m.SSM_FOLD_IN_VERIFY:
+                rec["vs_fold_at_commit"] = out["replay"][str(W)]["us_per_step"] / us
+            out[name][str(W)] = rec
         m.ssm_state_destroy(pool)
     if static:
         # the entry point that allocates nothing: verify only (the caller folds), logs of the lengths the
@@ -438,7 +472,9 @@ def bench_verify_sweep(torch, m, args):
                                 copy_frac_of_hbm=r["copy"]["frac_of_hbm"], replay_us=rec["us_per_step"],
                                 replay_frac_of_hbm=rec["frac_of_hbm"], replay_frac_of_nominal=rec["frac_of_nominal_8tbs"],
                                 folds_per_step=rec["folds_per_step"], copy_over_replay=rec["copy_over_replay"],
-                                replay_over_plain=rec["over_plain"], commit_path=rec["commit_path"]))
+                                replay_over_plain=rec["over_plain"], commit_path=rec["commit_path"],
+                                fold_in_verify_us=r["replay_fold_in_verify"][W]["us_per_step"],
+                                fold_in_verify_frac_of_hbm=r["replay_fold_in_verify"][W]["frac_of_hbm"]))
     return dict(points=pts, config=dict(batch=VER["R"], steps=VER["steps"], heads=VER["H"], headdim=VER["P"],
                                         dstate=VER["N"], groups=VER["G"]))
 
@@ -947,7 +983,8 @@ def run_case(args):
         VER["steps"] = 4
         out = bench_verify(torch, m, args, T=args.T or None, windows=[args.W] if args.W else None)
         print(json.dumps({"case": "verify", "batch": VER["R"], "copy_us": out["copy"]["us_per_step"],
-                          "replay_us": {w: r["us_per_step"] for w, r in out["replay"].items()}}))
+                          "replay_us": {w: r["us_per_step"] for w, r in out["replay"].items()},
+                          "fold_in_verify_us": {w: r["us_per_step"] for w, r in out["replay_fold_in_verify"].items()}}))
     elif args.case == "prefill":
         PRE["R"] = args.batch or PRE["R"]
         out = bench_prefill(torch, m, args)

@@ -26,6 +26,7 @@ SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_INVALID_CHUNK, SSM_ERR_INVALID_STATE = 0, 1
 SSM_ERR_SEQUENCE, SSM_ERR_DUPLICATE, SSM_ERR_SCHEMA, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_NO_MEMORY = 4, 5, 6, 7, 8, 9
 SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 2
 SSM_MODE_COPY, SSM_MODE_REPLAY = 0, 1
+SSM_FOLD_AT_COMMIT, SSM_FOLD_IN_VERIFY = 0, 1
 SSM_FLAG_NONFINITE_INPUT, SSM_FLAG_POISONED_SLOT, SSM_FLAG_BAD_ACCEPT = 1, 2, 4
 SSM_FLAG_LOG_NOT_EMPTY, SSM_FLAG_TIMEOUT = 8, 16
 
@@ -51,7 +52,8 @@ class SSMError(RuntimeError):
 class ssm_config(ctypes.Structure):
     _fields_ = [("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32), ("dstate", ctypes.c_int32),
                 ("ngroups", ctypes.c_int32), ("input_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32),
-                ("mode", ctypes.c_int32), ("window", ctypes.c_int32), ("max_tokens", ctypes.c_int32)]
+                ("mode", ctypes.c_int32), ("window", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("fold", ctypes.c_int32)]
 
 
 class ssm_slot_meta(ctypes.Structure):
@@ -215,8 +217,8 @@ class Pool:
 
 
 def make_config(nheads, headdim, dstate, ngroups, input_dtype=SSM_DTYPE_F32, dt_dtype=SSM_DTYPE_F32,
-                mode=SSM_MODE_COPY, window=16, max_tokens=9) -> ssm_config:
-    return ssm_config(nheads, headdim, dstate, ngroups, input_dtype, dt_dtype, mode, window, max_tokens)
+                mode=SSM_MODE_COPY, window=16, max_tokens=9, fold=SSM_FOLD_AT_COMMIT) -> ssm_config:
+    return ssm_config(nheads, headdim, dstate, ngroups, input_dtype, dt_dtype, mode, window, max_tokens, fold)
 
 
 # ---------------------------------------------------------------- lifecycle

@@ -9,7 +9,7 @@
 // a rank-m update of the P x N fp32 checkpoint.  An item is a pair of heads
 // (h0, h0 + 1) of one request (the same group, so the same logged B rows):
 // D = W B on the tensor cores with W[row][s] = w_s x_s[p] for the 128 rows
-// (head, p) and B[s][n] the group's logged rows, K = KP (the log capacity
+// (head, p) and B[s][n] the group's logged rows, K = KP (the longest window
 // rounded up to 32, 48 or 64; zero past m), then h <- d h + D row by row.
 //
 // W is fp32; it enters kind::f16 MMAs as three bf16 terms hi = rn(v),
@@ -50,7 +50,7 @@ struct FtLayout {
 };
 
 // Per stage: checkpoint boxes, B boxes of kp rows x 128 bytes (1024-aligned
-// for the swizzle), the two heads' logged x rows [wcap][2][P] bf16; after the
+// for the swizzle), the two heads' logged x rows [wwin][2][P] bf16; after the
 // stages the barriers.
 __host__ __device__ inline FtLayout ft_layout(int wcap, int P, int kp) {
     FtLayout L;
@@ -112,7 +112,7 @@ __device__ __forceinline__ void ft_store_cols(uint32_t taddr, const uint32_t *v)
     if constexpr (n % 16 != 0) tc::tmem_st8(taddr + (n - 8), v + (n - 8));
 }
 
-// KP: the K extent (32, 48 or 64), at least the log capacity.
+// KP: the K extent (32, 48 or 64), at least the longest window.
 template <int KP>
 __global__ void __launch_bounds__(kFtThreads, 1)
     fold_tc_kernel(const __grid_constant__ CommitArgs a, const __grid_constant__ CUtensorMap tm_state,
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
     __shared__ uint32_t s_abort, s_tmem;
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const int P = a.P, H = a.H;
-    const FtLayout L = ft_layout(a.wcap, P, KP);
+    const FtLayout L = ft_layout(a.wwin, P, KP);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);  // tiles landed
     uint64_t *wful = full + kFtStages;                              // W in TMEM, B tile trimmed
     uint64_t *done = wful + kFtStages;                              // MMAs finished
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
     if (warp == kFtProd) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint32_t bytes = kFtHBytes + 2u * L.bbox + (uint32_t)a.wcap * 2u * (uint32_t)P * 2u;
+            const uint32_t bytes = kFtHBytes + 2u * L.bbox + (uint32_t)a.wwin * 2u * (uint32_t)P * 2u;
             int loaded[kFtStages];
             for (int s = 0; s < kFtStages; ++s) loaded[s] = -1;
             bool alive = true;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kFtThreads, 1)
             if (item >= n_items) break;
             const int st = u % kFtStages;
             const FtItem it = ft_item(a, item);
-            const int h = it.h0 + hd, m = it.m;  // 1 <= m <= wcap <= KP
+            const int h = it.h0 + hd, m = it.m;  // 1 <= m <= wwin <= KP
             const float A = a.A[h];
             // dt of the head's logged tokens s = lane (and s = lane + 32 when KP > 32); prefix sums as
             // fp32 pairs, so that each difference is as exact as fp32 can hold
@@ -333,9 +333,9 @@ __global__ void __launch_bounds__(kFtThreads, 1)
 
 cudaError_t launch_fold_tc(const Pool &pool, const CommitArgs &a, cudaStream_t s) {
     const int kp = pool.fold_kp;
-    if (!pool.tm_fold_ok || a.P != 64 || a.N != 128 || a.wcap > kp || (a.H & 1) || (a.hpg & 1))
+    if (!pool.tm_fold_ok || a.P != 64 || a.N != 128 || a.wwin > kp || (a.H & 1) || (a.hpg & 1))
         return cudaErrorNotSupported;
-    const FtLayout L = ft_layout(a.wcap, a.P, kp);
+    const FtLayout L = ft_layout(a.wwin, a.P, kp);
     int dev = 0, max_smem = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);

@@ -67,6 +67,11 @@ void free_all(Pool &p) {
     cudaFree(p.d_cf);
     cudaFree(p.d_fold_items);
     cudaFree(p.d_fold_count);
+    cudaFree(p.d_stage_pos);
+    cudaFree(p.d_plain);
+    cudaFree(p.d_fv_items);
+    cudaFree(p.d_moves);
+    cudaFree(p.d_counts);
     Pool::HostPipe &h = p.hpipe;
     cudaFree(h.buf);
     for (cudaEvent_t e : {h.start, h.in_ready[0], h.in_ready[1], h.used[0], h.used[1], h.y_ready[0], h.y_ready[1],
@@ -122,6 +127,32 @@ void fill_step(const Pool &p, ssm::StepArgs &a, const void *x, const void *dt, c
     a.n_tok = n_tok;
     a.dt_bf16 = p.cfg.dt_dtype == SSM_DTYPE_BF16;
     a.check_log = p.cfg.mode == SSM_MODE_REPLAY;
+    a.wwin = p.wwin;
+    if (p.fold_in_verify) {
+        a.fold_w = p.cfg.window;
+        a.stage_pos = p.d_stage_pos;
+        a.plain = p.d_plain;
+        a.fv_items = p.d_fv_items;
+        a.counts = p.d_counts;
+    }
+}
+
+void fill_commit(const Pool &p, ssm::CommitArgs &c, const float *A) {
+    std::memset(&c, 0, offsetof(ssm::CommitArgs, slots));
+    c.A = A; c.state = p.state;
+    c.log_x = p.log_x; c.log_dt = p.log_dt; c.log_B = p.log_B;
+    c.position = p.d_position; c.log_len = p.d_log_len; c.cur = p.d_cur;
+    c.slot_flags = p.d_slot_flags; c.flags = p.d_flags;
+    c.H = p.H; c.P = p.P; c.N = p.N; c.G = p.G; c.hpg = p.hpg;
+    c.n_slots = p.n_slots; c.t1max = p.t1max; c.wcap = p.wcap; c.W = p.cfg.window;
+    c.fold_items = p.d_fold_items; c.fold_count = p.d_fold_count;
+    c.wwin = p.wwin;
+    if (p.fold_in_verify) {
+        c.fold_w = p.cfg.window;
+        c.stage_pos = p.d_stage_pos;
+        c.moves = p.d_moves;
+        c.counts = p.d_counts;
+    }
 }
 
 size_t in_elem(int dtype) { return dtype == SSM_DTYPE_BF16 ? 2 : 4; }
@@ -184,6 +215,11 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     if (c.mode != SSM_MODE_COPY && c.mode != SSM_MODE_REPLAY) return SSM_ERR_INVALID_ARG;
     if (c.max_tokens < 1 || c.max_tokens > 64) return SSM_ERR_INVALID_ARG;
     if (c.mode == SSM_MODE_REPLAY && (c.window < 1 || c.window > 1024)) return SSM_ERR_INVALID_ARG;
+    if (c.fold != SSM_FOLD_AT_COMMIT && c.fold != SSM_FOLD_IN_VERIFY) return SSM_ERR_INVALID_ARG;
+    const bool fiv = c.fold == SSM_FOLD_IN_VERIFY;
+    if (fiv && (c.mode != SSM_MODE_REPLAY || c.input_dtype != SSM_DTYPE_BF16 || c.headdim != 64 || c.dstate != 128 ||
+                (c.nheads / c.ngroups) % 2 != 0 || c.max_tokens > 32 || c.window - 1 + 2 * c.max_tokens > 64))
+        return SSM_ERR_INVALID_ARG;
     if (32 * warps_needed(c.dstate, c.headdim) > ssm::kMaxThreads) return SSM_ERR_INVALID_ARG;
 
     ssm_pool_s *pool = new (std::nothrow) ssm_pool_s();
@@ -195,9 +231,12 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     p.pn = (size_t)p.P * p.N;
     p.hpn = (size_t)p.H * p.pn;
     p.t1max = c.max_tokens;
-    p.wcap = c.mode == SSM_MODE_REPLAY ? c.window - 1 + c.max_tokens : 0;
-    p.cb_w = (p.wcap + 3) / 4 * 4;
-    if (c.mode == SSM_MODE_REPLAY && p.wcap <= 32) p.cb_w = 32;  // whole-row float4 reads of the W rows
+    p.fold_in_verify = fiv;
+    p.wwin = c.mode == SSM_MODE_REPLAY ? c.window - 1 + c.max_tokens : 0;
+    // a verify that folds stages its tokens after a log of up to W - 1 + t1max
+    p.wcap = p.wwin + (fiv ? c.max_tokens : 0);
+    p.cb_w = (p.wwin + 3) / 4 * 4;
+    if (c.mode == SSM_MODE_REPLAY && p.wwin <= 32) p.cb_w = 32;  // whole-row float4 reads of the W rows
     p.t1pad = (p.t1max + 3) / 4 * 4;
     p.cf_rows = (p.t1max + 15) / 16 * 16;
     p.in_bytes = in_elem(c.input_dtype);
@@ -206,7 +245,7 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         p.sm_count = 1;
     p.cb_rows = std::min(n_slots, ssm::kMaxSlotsPerLaunch);
 
-    if (c.mode == SSM_MODE_REPLAY) {
+    if (c.mode == SSM_MODE_REPLAY && !fiv) {  // the kernels a pool that folds in its verify never runs
         int max_smem = 0;
         cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device);
         if (ssm::replay_smem_bytes(p, c.max_tokens) > (size_t)max_smem ||
@@ -236,6 +275,13 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         if (e == cudaSuccess) e = alloc(&p.d_fold_items, (size_t)ssm::kMaxSlotsPerLaunch, b);
         if (e == cudaSuccess) e = alloc(&p.d_fold_count, 1, b);
     }
+    if (e == cudaSuccess && fiv) {
+        e = alloc(&p.d_stage_pos, ns, b);
+        if (e == cudaSuccess) e = alloc(&p.d_plain, (size_t)ssm::kMaxSlotsPerLaunch, b);
+        if (e == cudaSuccess) e = alloc(&p.d_fv_items, (size_t)ssm::kMaxSlotsPerLaunch, b);
+        if (e == cudaSuccess) e = alloc(&p.d_moves, (size_t)ssm::kMaxSlotsPerLaunch, b);
+        if (e == cudaSuccess) e = alloc(&p.d_counts, 4, b);
+    }
     if (e == cudaSuccess) e = alloc(&p.d_position, ns, b);
     if (e == cudaSuccess) e = alloc(&p.d_log_len, ns, b);
     if (e == cudaSuccess) e = alloc(&p.d_cur, ns, b);
@@ -252,6 +298,8 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
     if (e == cudaSuccess) e = cudaMemsetAsync(p.d_cur, 0xff, ns * sizeof(int32_t), s);  // -1: base state
     if (e == cudaSuccess) e = cudaMemsetAsync(p.d_slot_flags, 0, ns * sizeof(uint32_t), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(p.d_flags, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess && fiv) e = cudaMemsetAsync(p.d_stage_pos, 0, ns * sizeof(int32_t), s);
+    if (e == cudaSuccess && fiv) e = cudaMemsetAsync(p.d_counts, 0, 4 * sizeof(int32_t), s);
     if (e == cudaSuccess && c.mode == SSM_MODE_REPLAY) {  // padding rows of the scratch read as zeros
         e = cudaMemsetAsync(p.d_cf, 0, (size_t)p.cb_rows * p.G * p.cf_rows * p.N * sizeof(float), s);
         if (e == cudaSuccess) e = cudaMemsetAsync(p.d_wsc, 0, (size_t)p.cb_rows * p.H * p.t1max * p.cb_w * sizeof(float), s);
@@ -264,6 +312,11 @@ ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *i
         return cuda_status(e);
     }
     if (c.mode == SSM_MODE_REPLAY) ssm::replay_tma_encode(p);  // else the bulk-copy / plain kernels serve
+    if (fiv && (!p.tm_tc_ok || !p.tm_fold_ok || !ssm::fold_verify_fits(p))) {  // the verify's fold needs them
+        free_all(p);
+        delete pool;
+        return SSM_ERR_INVALID_ARG;
+    }
     p.next_chunk.assign(ns, 0);
     p.epoch.assign(ns, 0);
     p.released.assign(ns, 0);
@@ -351,14 +404,8 @@ ssm_status ssm_state_checkpoint(ssm_pool pool, int32_t slot, const float *A, flo
     if (p.cfg.mode == SSM_MODE_REPLAY && m0.log_len > 0) {
         if (!A) return SSM_ERR_INVALID_ARG;
         ssm::CommitArgs c;
-        std::memset(&c, 0, offsetof(ssm::CommitArgs, slots));
-        c.A = A; c.state = p.state;
-        c.log_x = p.log_x; c.log_dt = p.log_dt; c.log_B = p.log_B;
-        c.position = p.d_position; c.log_len = p.d_log_len; c.cur = p.d_cur;
-        c.slot_flags = p.d_slot_flags; c.flags = p.d_flags;
-        c.H = p.H; c.P = p.P; c.N = p.N; c.G = p.G; c.hpg = p.hpg;
-        c.n_slots = p.n_slots; c.t1max = p.t1max; c.wcap = p.wcap; c.W = p.cfg.window;
-        c.fold_items = p.d_fold_items; c.fold_count = p.d_fold_count; c.fold_grid = p.H;
+        fill_commit(p, c, A);
+        c.fold_grid = p.H;
         c.flush = 1; c.batch = 1;
         c.slots[0] = slot;
         c.ntok[0] = 1;
@@ -648,6 +695,9 @@ static ssm_status verify_common(ssm_pool pool, int32_t batch, int32_t n_tok, con
     Pool &p = pool->p;
     if (p.cfg.mode != mode) return SSM_ERR_INVALID_ARG;
     if (n_tok < 1 || n_tok > p.t1max) return SSM_ERR_INVALID_ARG;
+    if (p.fold_in_verify && (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(B) % 16 ||
+                             reinterpret_cast<uintptr_t>(C) % 16))
+        return SSM_ERR_INVALID_ARG;  // the tensor-core path, the only one that folds, moves rows in 16 bytes
     ssm_status st = check_slots(pool, slots, batch, false);
     if (st != SSM_OK) return st;
     DeviceGuard g(p.device);
@@ -691,14 +741,7 @@ ssm_status ssm_state_commit(ssm_pool pool, int32_t batch, const int32_t *slots, 
     DeviceGuard g(p.device);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     ssm::CommitArgs c;
-    std::memset(&c, 0, offsetof(ssm::CommitArgs, slots));
-    c.A = A; c.state = p.state;
-    c.log_x = p.log_x; c.log_dt = p.log_dt; c.log_B = p.log_B;
-    c.position = p.d_position; c.log_len = p.d_log_len; c.cur = p.d_cur;
-    c.slot_flags = p.d_slot_flags; c.flags = p.d_flags;
-    c.H = p.H; c.P = p.P; c.N = p.N; c.G = p.G; c.hpg = p.hpg;
-    c.n_slots = p.n_slots; c.t1max = p.t1max; c.wcap = p.wcap; c.W = p.cfg.window;
-    c.fold_items = p.d_fold_items; c.fold_count = p.d_fold_count;
+    fill_commit(p, c, A);
     c.force_fold = force_fold ? 1 : 0;
     const char *path = "commit_copy";
     for (int base = 0; base < batch; base += ssm::kMaxSlotsPerLaunch) {

@@ -287,7 +287,49 @@ __device__ __forceinline__ bool commit_decision(const CommitArgs &a, int i, int 
     return true;
 }
 
-// One thread per request: the index side of the commit (bit exact).
+// Fold in verify: the kept tokens' log rows of one slot move from row `from`
+// to row `to` (to < from): x, B and dt rows each form one contiguous range.
+// Disjoint ranges are copied in kMoveParts slices by as many CTAs; ranges
+// that overlap (from < to + c, possible when W < the step's tokens) are
+// copied by one CTA row by row in increasing order, a barrier between rows,
+// so that every source row is read before it is overwritten.
+constexpr int kMoveParts = 8;
+constexpr int kMoveThreads = 256;
+
+template <typename V>
+__device__ void move_range(char *base, size_t row_bytes, int from, int to, int c, bool overlap) {
+    const V *src = reinterpret_cast<const V *>(base + (size_t)from * row_bytes);
+    V *dst = reinterpret_cast<V *>(base + (size_t)to * row_bytes);
+    const size_t rw = row_bytes / sizeof(V);
+    if (!overlap) {
+        const size_t n = rw * (size_t)c, per = (n + kMoveParts - 1) / kMoveParts;
+        const size_t e0 = per * blockIdx.y, e1 = min(n, e0 + per);
+        for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) dst[e] = src[e];
+        return;
+    }
+    if (blockIdx.y != 0) return;
+    for (int r = 0; r < c; ++r) {
+        for (size_t e = threadIdx.x; e < rw; e += blockDim.x) dst[(size_t)r * rw + e] = src[(size_t)r * rw + e];
+        __syncthreads();
+    }
+}
+
+// CTA (listed move, slice).
+__global__ void __launch_bounds__(kMoveThreads) log_move_kernel(const __grid_constant__ CommitArgs a) {
+    if ((int)blockIdx.x >= a.counts[2]) return;
+    const int4 mv = a.moves[blockIdx.x];
+    const int slot = a.slots[mv.x], from = mv.y, to = mv.z, c = mv.w;
+    const bool overlap = from < to + c;
+    const size_t xrow = (size_t)a.H * a.P * 2, brow = (size_t)a.G * a.N * 2, drow = (size_t)a.H * 4;  // bf16 x, B
+    move_range<uint4>(static_cast<char *>(a.log_x) + (size_t)slot * a.wcap * xrow, xrow, from, to, c, overlap);
+    move_range<uint4>(static_cast<char *>(a.log_B) + (size_t)slot * a.wcap * brow, brow, from, to, c, overlap);
+    move_range<float>(reinterpret_cast<char *>(a.log_dt) + (size_t)slot * a.wcap * drow, drow, from, to, c,
+                      overlap);
+}
+
+// One thread per request: the index side of the commit (bit exact).  kMoves:
+// a commit of a pool that folds in its verify (appends, moving staged tokens).
+template <bool kMoves>
 __global__ void commit_meta_kernel(const __grid_constant__ CommitArgs a, int replay) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.batch) return;
@@ -304,6 +346,21 @@ __global__ void commit_meta_kernel(const __grid_constant__ CommitArgs a, int rep
         if (k < 0 || k + c > a.wcap) {  // corrupted log length
             raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_BAD_ACCEPT);
             return;
+        }
+        if constexpr (kMoves) {
+            // fold in verify: the window fills in the next verify, and this commit appends; the
+            // verify staged its tokens after the log as it then was, and where that log has since
+            // gone into the checkpoint (folded by the verify or a checkpoint read) the kept tokens
+            // move to the end of the log first
+            const int sp = a.stage_pos[slot];
+            if (sp != k) {
+                if (sp < 0 || sp + c > a.wcap) {
+                    raise_flag(a.flags, a.slot_flags, slot, SSM_FLAG_BAD_ACCEPT);
+                    return;
+                }
+                a.moves[atomicAdd(&a.counts[2], 1)] = make_int4(i, sp, k, c);
+            }
+            fold = a.force_fold != 0;
         }
         if (fold) a.fold_items[atomicAdd(a.fold_count, 1)] = make_int2(i, k + c);
         a.log_len[slot] = fold ? 0 : k + c;
@@ -441,6 +498,7 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
     {  // the tensor-map path brings its own C . B and staging
         const cudaError_t e = launch_verify_replay_tma(pool, a, s, path);
         if (e != cudaErrorNotSupported) return e;
+        if (pool.fold_in_verify) return cudaErrorInvalidValue;  // no other path folds in the verify
     }
     const size_t smem = replay_smem_bytes(pool, a.n_tok);
     const size_t psmem = replay_prep_smem_bytes(pool, a.n_tok);
@@ -483,15 +541,25 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
 
 cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s, const char **path) {
     const bool replay = pool.cfg.mode == SSM_MODE_REPLAY;
+    const bool moves = a.fold_w && !a.flush;
     if (replay) {
-        const cudaError_t e = cudaMemsetAsync(a.fold_count, 0, sizeof(int32_t), s);
+        cudaError_t e = cudaMemsetAsync(a.fold_count, 0, sizeof(int32_t), s);
+        if (e == cudaSuccess && moves) e = cudaMemsetAsync(&a.counts[2], 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return e;
     }
-    commit_meta_kernel<<<(a.batch + 127) / 128, 128, 0, s>>>(a, replay ? 1 : 0);
+    if (moves) commit_meta_kernel<true><<<(a.batch + 127) / 128, 128, 0, s>>>(a, 1);
+    else commit_meta_kernel<false><<<(a.batch + 127) / 128, 128, 0, s>>>(a, replay ? 1 : 0);
     if (path) *path = "commit_copy";
     if (replay) {
         cudaError_t ep = cudaGetLastError();
         if (ep != cudaSuccess) return ep;
+        if (moves) {
+            log_move_kernel<<<dim3(a.batch, kMoveParts), kMoveThreads, 0, s>>>(a);
+            ep = cudaGetLastError();
+            if (ep != cudaSuccess) return ep;
+            if (path) *path = "commit_replay_append";
+            if (!a.force_fold) return cudaSuccess;  // nothing folds here
+        }
         ep = launch_fold_tc(pool, a, s);
         if (path) *path = "commit_replay_fold_tc";
         if (ep != cudaErrorNotSupported) return ep;

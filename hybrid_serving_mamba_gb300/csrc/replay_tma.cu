@@ -100,7 +100,7 @@ __host__ __device__ inline size_t gcoef_smem_bytes(int T1, int mmax, int N, int 
 
 // Rows of x, B, C are moved 16 bytes at a time: the launcher checks that
 // P and N rows are multiples of 16 bytes and the pointers 16-byte aligned.
-template <int N, typename TI>
+template <int N, typename TI, bool kFiv>
 __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(const __grid_constant__ StepArgs a) {
     using V = Vec16<TI>;
     constexpr int EV = V::n;          // elements per 16 bytes
@@ -114,9 +114,24 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
     const int T1 = a.n_tok, H = a.H, P = a.P, hpg = a.hpg;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int wmax = a.wcap - a.t1max, mmax = wmax + T1;
-    const int k = a.log_len[slot];
-    if ((a.slot_flags[slot] & kSlotPoisoned) || k < 0 || k > wmax) return;  // the streaming kernel reports it
+    const int kl = a.log_len[slot];
+    // fold in verify (kFiv): a log of W or more tokens is folded by this verify (fold_verify_tc_kernel),
+    // whose outputs then come from the new checkpoint over the step alone; the step is staged after the
+    // log either way, and the commit moves the kept tokens to the end of the (then empty) log
+    bool fold_now = false;
+    if constexpr (kFiv) {
+        fold_now = kl >= a.fold_w && kl <= wmax;
+        if (g == 0 && threadIdx.x == 0) {
+            a.stage_pos[slot] = kl;
+            if (fold_now) a.fv_items[atomicAdd(&a.counts[1], 1)] = make_int2(i, kl);
+            else a.plain[atomicAdd(&a.counts[0], 1)] = i;
+        }
+    }
+    if ((a.slot_flags[slot] & kSlotPoisoned) || kl < 0 || kl > wmax) return;  // the streaming kernel reports it
+    const int k = fold_now ? 0 : kl;  // logged tokens in the window of the outputs
     const int m = k + T1;
+    // log row of window position s (s < k: the log; then the step, staged from row kl)
+    auto lrow = [&](int s) { return s < k ? s : kl + (s - k); };
     float *sC = reinterpret_cast<float *>(smem4);
     float *sB = sC + (size_t)T1 * N;
     float *sCB = sB + (size_t)mmax * N;
@@ -192,7 +207,7 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
         } else {
             v = *reinterpret_cast<const uint4 *>(stepB + (((size_t)i * T1 + (s - k)) * a.G + g) * N + q * EV);
             bad |= V::nonfinite(v);
-            *reinterpret_cast<uint4 *>(wB + ((size_t)s * a.G + g) * N + q * EV) = v;  // staged after the log
+            *reinterpret_cast<uint4 *>(wB + ((size_t)lrow(s) * a.G + g) * N + q * EV) = v;  // staged after the log
         }
         V::widen(v, sB + (size_t)s * N + q * EV);
     }
@@ -200,7 +215,7 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
         const int t = e / hpg, h = g * hpg + (e - t * hpg);
         const float d = load_dt(a.dt, ((size_t)i * T1 + t) * H + h, a.dt_bf16);
         bad |= !isfinite(d);
-        a.log_dt[((size_t)slot * a.wcap + k + t) * H + h] = d;
+        a.log_dt[((size_t)slot * a.wcap + kl + t) * H + h] = d;
     }
     {  // the step's x, once landed: the non-finite check
         __syncthreads();  // the barrier's initialisation is visible to every thread
@@ -217,7 +232,7 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
     }
     if (threadIdx.x == 0) {  // x to the log, after the log's k rows; waited for at the end
         for (int t = 0; t < T1; ++t)
-            bulk_s2g(wx + (((size_t)slot * a.wcap + k + t) * H + (size_t)g * hpg) * P, sX + (size_t)t * hpg * P, xrow);
+            bulk_s2g(wx + (((size_t)slot * a.wcap + kl + t) * H + (size_t)g * hpg) * P, sX + (size_t)t * hpg * P, xrow);
         bulk_commit();
     }
     for (int pr = threadIdx.x; pr < T1 * m; pr += blockDim.x) {  // C_j . B_s, one thread per pair
@@ -244,7 +259,7 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
     for (int hh = warp; hh < hpg; hh += nwarps) {
         const int h = g * hpg + hh;
         const float A = a.A[h], D = a.D[h];
-        for (int s = lane; s < m; s += 32) dts[s] = a.log_dt[((size_t)slot * a.wcap + s) * H + h];
+        for (int s = lane; s < m; s += 32) dts[s] = a.log_dt[((size_t)slot * a.wcap + lrow(s)) * H + h];
         __syncwarp();
         warp_prefix_sum2(dts, cum, m, lane);  // differences of these are exact to fp32
         __syncwarp();
@@ -634,7 +649,7 @@ __host__ __device__ inline size_t tc_smem_bytes(const TcLayout &L) {
     return (size_t)L.bars + (2 * kTcMaxRing + 2 * kTcMaxAux + kTcMaxASlots + kTcDone + kTcDbuf) * 8 + 1024;
 }
 
-template <typename TI, int NM>
+template <typename TI, int NM, bool kList>
 __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
     verify_replay_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ CUtensorMap tm_state2,
                             const __grid_constant__ CUtensorMap tm_x2, int nring, int naux) {
@@ -647,8 +662,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
     const int P = a.P, N = a.N, T1 = a.n_tok, H = a.H;
     const int nkb = N / 32, hp = H / 2;
     const int wmax = a.wcap - a.t1max;
-    const int n_items = a.batch * hp;
-    const TcLayout L = tc_layout(N, NM, P, (int)sizeof(TI), a.wcap, a.t1max, a.cb_w, a.t1pad, kSplitC, nring, naux);
+    const TcLayout L = tc_layout(N, NM, P, (int)sizeof(TI), a.wwin, a.t1max, a.cb_w, a.t1pad, kSplitC, nring, naux);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *rfull = bars, *rempty = rfull + kTcMaxRing;                // checkpoint ring
     uint64_t *xfull = rempty + kTcMaxRing, *xempty = xfull + kTcMaxAux;  // per-item ring
@@ -677,11 +691,22 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = s_tmem;
+    // kList (the verify folds full logs): the coefficient kernel lists the other requests; every role
+    // reads the list, so every role waits for that kernel (else only the per-item producer does)
+    int n_items = a.batch * hp;
+    if constexpr (kList) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        n_items = *(volatile const int32_t *)&a.counts[0] * hp;
+    }
+    auto request = [&](int item) {
+        if constexpr (kList) return a.plain[item / hp];
+        else return item / hp;
+    };
 
     if (warp == kTcProd) {
         // ------------------------------------------------------------ producer
         const uint32_t cbytes = (uint32_t)(N / Op::kRowElems) * NM * 128u;  // C, already in the operand layout
-        const uint32_t xbytes = cbytes + 2u * a.wcap * P * sizeof(TI) + 2u * a.t1max * a.cb_w * 4u + 2u * a.t1pad * 4u;
+        const uint32_t xbytes = cbytes + 2u * a.wwin * P * sizeof(TI) + 2u * a.t1max * a.cb_w * 4u + 2u * a.t1pad * 4u;
         int xlast[kTcMaxAux];
         for (int s = 0; s < kTcMaxAux; ++s) xlast[s] = -1;
         // C in the operand layout, W, decay_j, the staged log rows and the slot flags come from the
@@ -698,7 +723,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                 my_k = 0;
                 my_gate = 0;
                 if (it2 < n_items) {
-                    const int sl = a.slots[it2 / hp];
+                    const int sl = a.slots[request(it2)];
                     my_k = a.log_len[sl];
                     if (a.slot_flags[sl] & kSlotPoisoned) my_gate = SSM_FLAG_POISONED_SLOT;
                     else if (my_k < 0 || my_k > wmax) my_gate = SSM_FLAG_BAD_ACCEPT;
@@ -708,7 +733,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
             const uint32_t gate = __shfl_sync(0xffffffffu, my_gate, u & 31);
             if (lane == 0) {
                 const int xs_ = u % naux;
-                const int i = item / hp, h0 = 2 * (item - i * hp);
+                const int i = request(item), h0 = 2 * (item % hp);
                 const int slot = a.slots[i];
                 const int g = h0 / a.hpg;
                 if (u >= naux && !wait_or_abort(&xempty[xs_], (uint32_t)((u / naux) - 1) & 1u, &s_abort, a.flags)) {
@@ -748,7 +773,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
             for (int u = 0; alive; ++u) {
                 const int item = blockIdx.x + u * gridDim.x;
                 if (item >= n_items) break;
-                const int i = item / hp, h0 = 2 * (item - i * hp);
+                const int i = request(item), h0 = 2 * (item % hp);
                 const int row0 = (a.slots[i] * H + h0) * P;
                 for (int kb = 0; kb < nkb; ++kb, ++nblk) {
                     const int rs = nblk % nring;
@@ -926,7 +951,7 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
             const unsigned char *X = smem + L.aux_base + (size_t)xs_ * L.aux;
             const int gate = reinterpret_cast<const int *>(X + L.hdr)[0];
             const int k = reinterpret_cast<const int *>(X + L.hdr)[1];
-            const int i = item / hp, h0 = 2 * (item - i * hp);
+            const int i = request(item), h0 = 2 * (item % hp);
             if (gate && r == 0) raise_flag(a.flags, a.slot_flags, a.slots[i], (uint32_t)gate);
             const int m = gate ? 0 : k + T1;
             // log term sum_s W[j][s] x_s[p], s in quads (the W rows, zero past s = k + j, as float4),
@@ -1047,10 +1072,10 @@ bool replay_tma_encode(Pool &p) {
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
     // tensor-core kernel: pairs of heads of P = 64 rows, 32-column boxes of both heads' rows, and both
-    // heads' whole logs of x rows (any capacity up to kMaxTmaLog)
+    // heads' logs of x rows as far as the longest window reaches (up to kMaxTmaLog rows)
     if (p.P == 64 && p.H % 2 == 0 && p.hpg % 2 == 0) {
         const cuuint32_t sb2[2] = {32u, 128u};
-        const cuuint32_t xb2[3] = {(cuuint32_t)p.P, 2u, (cuuint32_t)p.wcap};
+        const cuuint32_t xb2[3] = {(cuuint32_t)p.P, 2u, (cuuint32_t)p.wwin};
         p.tm_tc_ok = enc(&p.tm_state2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.state, sd, ss, sb2, se,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
@@ -1058,9 +1083,9 @@ bool replay_tma_encode(Pool &p) {
                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         // the fold's B operand: logged rows s of group g, [slot * wcap + s][g][n] bf16, boxes of
-        // fold_kp rows (the log capacity rounded up to a K step multiple: 32, 48 or 64) x 64 columns
+        // fold_kp rows (the longest window rounded up to a K step multiple: 32, 48 or 64) x 64 columns
         // with the 128-byte swizzle (an MN-major operand tile)
-        const int kp = p.wcap <= 32 ? 32 : (p.wcap + 15) / 16 * 16;
+        const int kp = p.wwin <= 32 ? 32 : (p.wwin + 15) / 16 * 16;
         if (p.tm_tc_ok && p.cfg.input_dtype == SSM_DTYPE_BF16 && p.N == 128 && kp <= kMaxFoldK) {
             const cuuint64_t bd[3] = {(cuuint64_t)p.N, (cuuint64_t)p.G, (cuuint64_t)p.n_slots * p.wcap};
             const cuuint64_t bst[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.G * p.N * 2};
@@ -1069,6 +1094,13 @@ bool replay_tma_encode(Pool &p) {
                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
             if (p.tm_fold_ok) p.fold_kp = kp;
+        }
+        // fold in verify: both heads' whole logs (the step is staged after a full log)
+        if (p.tm_fold_ok && p.fold_in_verify) {
+            const cuuint32_t xbf[3] = {(cuuint32_t)p.P, 2u, (cuuint32_t)p.wcap};
+            p.tm_fold_ok = enc(&p.tm_logx_fv, xt, 3, p.log_x, xd, xst, xbf, xe, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
     }
     return p.tm_ok || p.tm_tc_ok;
@@ -1112,7 +1144,7 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         for (int na = kTcMaxAux; NM && na >= 2 && !nring; na -= 2)
             for (int nr = kTcMaxRing; nr >= 4; nr -= 2) {
                 const size_t b =
-                    tc_smem_bytes(tc_layout(a.N, NM, a.P, in_b, a.wcap, a.t1max, a.cb_w, a.t1pad, !bf, nr, na));
+                    tc_smem_bytes(tc_layout(a.N, NM, a.P, in_b, a.wwin, a.t1max, a.cb_w, a.t1pad, !bf, nr, na));
                 if (b <= (size_t)max_smem) {
                     nring = nr;
                     naux = na;
@@ -1133,16 +1165,22 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
     const size_t smem = (size_t)nstage * L.stage + L.fixed;
     StepArgs ac = a;
     ac.cf_nm = nring ? NM : 0;
+    if (pool.fold_in_verify && !nring) return cudaErrorNotSupported;
 
     cudaError_t e = cudaSuccess;
+    if (pool.fold_in_verify) {  // the coefficient kernel lists the requests of the two streaming kernels
+        e = cudaMemsetAsync(a.counts, 0, 2 * sizeof(int32_t), s);
+        if (e != cudaSuccess) return e;
+    }
     SSM_DISPATCH_N(a.N, {
         if (bf) {
-            auto k = replay_group_coef_kernel<NN, __nv_bfloat16>;
+            auto k = pool.fold_in_verify ? replay_group_coef_kernel<NN, __nv_bfloat16, true>
+                                         : replay_group_coef_kernel<NN, __nv_bfloat16, false>;
             e = set_smem(k, csmem);
             if (e != cudaSuccess) return e;
             k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(ac);
         } else {
-            auto k = replay_group_coef_kernel<NN, float>;
+            auto k = replay_group_coef_kernel<NN, float, false>;
             e = set_smem(k, csmem);
             if (e != cudaSuccess) return e;
             k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(ac);
@@ -1153,9 +1191,9 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
 
     if (nring) {
         const int tgrid = std::min(a.batch * (a.H / 2), pool.sm_count);
-#define SSM_TC(TI, NMV)                                                                                \
+#define SSM_TC(TI, NMV, LIST)                                                                          \
     do {                                                                                               \
-        auto k = verify_replay_tc_kernel<TI, NMV>;                                                     \
+        auto k = verify_replay_tc_kernel<TI, NMV, LIST>;                                               \
         e = set_smem(k, tsmem);                                                                        \
         if (e != cudaSuccess) return e;                                                                \
         cudaLaunchConfig_t cfg = {};                                                                   \
@@ -1172,14 +1210,24 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
         if (e != cudaSuccess) return e;                                                                \
     } while (0)
         if (bf) {
-            if (NM == 16) SSM_TC(__nv_bfloat16, 16);
-            else SSM_TC(__nv_bfloat16, 32);
+            if (pool.fold_in_verify) {
+                if (NM == 16) SSM_TC(__nv_bfloat16, 16, true);
+                else SSM_TC(__nv_bfloat16, 32, true);
+            } else {
+                if (NM == 16) SSM_TC(__nv_bfloat16, 16, false);
+                else SSM_TC(__nv_bfloat16, 32, false);
+            }
         } else {
-            if (NM == 16) SSM_TC(float, 16);
-            else SSM_TC(float, 32);
+            if (NM == 16) SSM_TC(float, 16, false);
+            else SSM_TC(float, 32, false);
         }
 #undef SSM_TC
         if (path) *path = "verify_replay_tc";
+        if (pool.fold_in_verify) {  // the requests whose full log this verify folds
+            e = launch_fold_verify_tc(pool, ac, NM, s);
+            if (e != cudaSuccess) return e == cudaErrorNotSupported ? cudaErrorInvalidValue : e;
+            if (path) *path = "verify_replay_tc_fold";
+        }
         return cudaGetLastError();
     }
 

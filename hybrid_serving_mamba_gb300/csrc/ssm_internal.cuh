@@ -40,7 +40,9 @@ struct Pool {
     size_t pn = 0;    // P * N floats per head
     size_t hpn = 0;   // H * P * N floats per slot
     int t1max = 0;    // max tokens per verify step
-    int wcap = 0;     // replay log capacity: W - 1 + t1max
+    int wcap = 0;     // replay log capacity: W - 1 + t1max (W - 1 + 2 t1max when the verify folds)
+    int wwin = 0;     // replay: longest window a verify replays, W - 1 + t1max
+    bool fold_in_verify = false;  // SSM_FOLD_IN_VERIFY
     size_t in_bytes = 0;  // bytes per x / B / C element
 
     float *state = nullptr;      // [n_slots][H][P][N]
@@ -57,7 +59,7 @@ struct Pool {
     // replay scratch: C_j . B_s of one launch's requests, [cb_rows][G][t1max][wcap]
     float *d_cb = nullptr;
     int cb_rows = 0;
-    int cb_w = 0;                      // row stride of d_cb: wcap rounded up to 4 floats
+    int cb_w = 0;                      // row stride of d_cb: wwin rounded up to 4 floats
     float *d_wsc = nullptr;            // replay: W[j][s] per head, [cb_rows][H][t1max][cb_w]
     float *d_dec = nullptr;            // replay: decay_j per head, [cb_rows][H][t1pad]
     float *d_cf = nullptr;             // replay: C_j in fp32 per group, [cb_rows][G][cf_rows][N]
@@ -71,9 +73,18 @@ struct Pool {
     bool tm_tc_ok = false;             // the two maps above encoded
     CUtensorMap tm_logB;               // replay, bf16, N = 128: fold_kp logged B rows x 64 columns of a group per box
     bool tm_fold_ok = false;           // tm_state2, tm_logx2 and tm_logB encoded for the tensor-core fold
-    int fold_kp = 0;                   // K extent of the tensor-core fold (32, 48 or 64 >= the log capacity)
+    int fold_kp = 0;                   // K extent of the tensor-core fold (32, 48 or 64 >= the longest window)
     int2 *d_fold_items = nullptr;      // (request index, tokens to fold) of one commit launch
     int32_t *d_fold_count = nullptr;
+    // fold in verify: where each slot's last verify staged its tokens; the verify's request lists
+    // (plain requests; (request, log length) of the requests whose full log it folds) and, for the
+    // commit, (request, from, to, count) of staged tokens to move to the end of the log
+    int32_t *d_stage_pos = nullptr;    // [n_slots]
+    int32_t *d_plain = nullptr;        // [kMaxSlotsPerLaunch]
+    int2 *d_fv_items = nullptr;        // [kMaxSlotsPerLaunch]
+    int4 *d_moves = nullptr;           // [kMaxSlotsPerLaunch]
+    int32_t *d_counts = nullptr;       // plain, fold-in-verify, moves
+    CUtensorMap tm_logx_fv;            // both heads' whole logs (wcap rows) per box
     int sm_count = 1;
     size_t bytes = 0;
 
@@ -123,6 +134,12 @@ struct StepArgs {  // decode, copy verify, replay verify
     int n_tok;        // tokens per request in this call (1 for decode)
     int dt_bf16;      // dt dtype is bf16
     int check_log;    // replay pool: in-place updates need an empty log
+    int wwin;         // replay: longest window (rows of the log boxes the tensor-core kernels load)
+    int fold_w;       // fold in verify: W (a log of at least W tokens is folded by this verify); 0: off
+    int32_t *stage_pos;   // fold in verify: see Pool
+    int32_t *plain;
+    int2 *fv_items;
+    int32_t *counts;
     int batch;
     int32_t slots[kMaxSlotsPerLaunch];
 };
@@ -146,6 +163,11 @@ struct CommitArgs {
     int fold_grid;    // CTAs of the persistent fold kernel
     int force_fold;
     int flush;        // fold the log only (checkpoint); accept is ignored
+    int wwin;         // longest window (rows of the log boxes the tensor-core fold loads)
+    int fold_w;       // fold in verify: W; the commit appends unless forced, moving staged tokens first
+    int32_t *stage_pos;
+    int4 *moves;
+    int32_t *counts;
     int batch;
     int32_t slots[kMaxSlotsPerLaunch];
     int32_t ntok[kMaxSlotsPerLaunch];
@@ -204,6 +226,12 @@ cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s,
 // The fold on the tensor cores (bf16 pools, P = 64, N = 128, log capacity <= 64);
 // cudaErrorNotSupported for other pools.
 cudaError_t launch_fold_tc(const Pool &pool, const CommitArgs &a, cudaStream_t s);
+// Fold in verify: the requests the coefficient kernel listed as holding a
+// full log (StepArgs::fv_items) get the log folded into the checkpoint and
+// the step's outputs from the new checkpoint, in one checkpoint read and one
+// write (fold_verify.cu).  cudaErrorNotSupported when it cannot run.
+cudaError_t launch_fold_verify_tc(const Pool &pool, const StepArgs &a, int NM, cudaStream_t s);
+bool fold_verify_fits(const Pool &pool);
 // Pipelined fold of the requests the commit listed; cudaErrorNotSupported
 // when the shapes or pointers do not allow bulk copies.
 cudaError_t launch_fold_pipe(const Pool &pool, const CommitArgs &a, cudaStream_t s);

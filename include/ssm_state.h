@@ -77,6 +77,14 @@ enum {
     SSM_MODE_REPLAY = 1  /* verify reads checkpoint + input log; commit appends or folds */
 };
 
+/* when a replay pool writes a full window into the checkpoint (The Fix: the
+ * full state is written only when the window fills) */
+enum {
+    SSM_FOLD_AT_COMMIT = 0, /* the commit that fills the window folds it (a checkpoint read + write) */
+    SSM_FOLD_IN_VERIFY = 1  /* the commit appends; the next verify, which reads the checkpoint anyway,
+                               folds a log of W or more tokens and writes the checkpoint once */
+};
+
 /* sticky device flag bits (ssm_pool_status) */
 enum {
     SSM_FLAG_NONFINITE_INPUT = 1u << 0, /* a NaN or Inf in x, dt, B or C */
@@ -96,6 +104,7 @@ typedef struct {
     int32_t mode;        /* SSM_MODE_COPY or SSM_MODE_REPLAY */
     int32_t window;      /* replay window W >= 1 (replay mode; ignored otherwise) */
     int32_t max_tokens;  /* largest n_tok (= T + 1) of one verify step, 1..64 */
+    int32_t fold;        /* replay mode: SSM_FOLD_AT_COMMIT or SSM_FOLD_IN_VERIFY (0 otherwise) */
 } ssm_config;
 
 /* per-slot metadata (Make reset, checkpoint, and cancellation observable:
@@ -104,7 +113,8 @@ typedef struct {
     int64_t position;   /* tokens applied since the last reset */
     int64_t next_chunk; /* chunk sequence number ssm_scan_chunk expects next */
     int64_t epoch;      /* number of resets of this slot */
-    int32_t log_len;    /* replay mode: tokens in the input log (0..W-1) */
+    int32_t log_len;    /* replay mode: tokens in the input log (0..W-1; up to W - 1 + max_tokens
+                           between a commit and the next verify with SSM_FOLD_IN_VERIFY) */
     uint32_t flags;     /* bit 0: poisoned; bit 1: released */
 } ssm_slot_meta;
 
@@ -118,7 +128,11 @@ typedef struct ssm_pool_s *ssm_pool;
  * reset, checkpoint, and cancellation observable: initialization).
  * init_state: device float [n_slots][H][P][N] copied in, or NULL for zeros.
  * Copy mode also allocates 2 x max_tokens snapshot states per slot; replay
- * mode allocates a log of W - 1 + max_tokens entries per slot.
+ * mode allocates a log of W - 1 + max_tokens entries per slot
+ * (W - 1 + 2 max_tokens with SSM_FOLD_IN_VERIFY).  SSM_FOLD_IN_VERIFY needs
+ * the tensor-core replay path: bf16 inputs, headdim 64, dstate 128, an even
+ * number of heads per group, max_tokens <= 32 and W - 1 + 2 max_tokens <= 64
+ * (SSM_ERR_INVALID_ARG otherwise).
  * Synchronous.  *out is set only on SSM_OK.
  */
 ssm_status ssm_state_init(const ssm_config *cfg, int32_t n_slots, const float *init_state,
@@ -338,6 +352,12 @@ ssm_status ssm_verify_copy(ssm_pool pool, int32_t batch, int32_t n_tok, const in
  *          + D * x_j[p]
  * over the logged tokens and step tokens 0..j.  The step's x, dt and B are
  * staged after the log for the commit.  Arguments as ssm_verify_copy.
+ * SSM_FOLD_IN_VERIFY pools: a request whose log holds W or more tokens has
+ * them folded into its checkpoint here, in the same pass that reads the
+ * checkpoint (one checkpoint read and one write instead of the commit's read
+ * and write plus this call's read); its log then counts as empty and its
+ * outputs come from the new checkpoint.  Such pools need x, B and C on
+ * 16-byte boundaries (SSM_ERR_INVALID_ARG otherwise).
  */
 ssm_status ssm_verify_replay(ssm_pool pool, int32_t batch, int32_t n_tok, const int32_t *slots,
                              const void *x, const void *dt, const void *B, const void *C,
@@ -354,7 +374,9 @@ ssm_status ssm_verify_replay(ssm_pool pool, int32_t batch, int32_t n_tok, const 
  *                appended to the log; otherwise the log and the c tokens are
  *                folded into the checkpoint and the log empties (The Fix:
  *                the full state is written only when the window is full).
- *                Rejected drafts never enter the log.
+ *                SSM_FOLD_IN_VERIFY pools append the c tokens unless
+ *                force_fold, and leave the fold of a full log to the next
+ *                verify.  Rejected drafts never enter the log.
  * Every slot must have had a verify since its last commit or reset
  * (SSM_ERR_INVALID_STATE otherwise).  A is the same float [H] as the verify's.
  */

@@ -48,6 +48,9 @@ def test_status_strings(mod):
     dict(nheads=0), dict(headdim=0), dict(headdim=300), dict(dstate=48), dict(ngroups=3),
     dict(input_dtype=1), dict(dt_dtype=7), dict(mode=2), dict(max_tokens=0), dict(max_tokens=65),
     dict(mode=1, window=0),
+    dict(fold=2), dict(fold=1), dict(mode=1, fold=1),  # fold in verify: replay, bf16, P 64, N 128 only
+    dict(mode=1, fold=1, input_dtype=2, headdim=64, dstate=128, max_tokens=33),
+    dict(mode=1, fold=1, input_dtype=2, headdim=64, dstate=128, window=40, max_tokens=13),  # log > 64
 ])
 def test_init_rejects_bad_config(mod, bad):
     kw = dict(nheads=4, headdim=16, dstate=16, ngroups=2, input_dtype=0, dt_dtype=0, mode=0, window=4, max_tokens=4)
