@@ -605,9 +605,12 @@ def bench_replay_plain_decode(torch, m, args):
     slots = list(range(R))
     stream = torch.cuda.current_stream()
     out = {}
-    for name, mode in (("decode", m.SSM_MODE_COPY), ("replay", m.SSM_MODE_REPLAY)):
+    for name, mode, fold in (("decode", m.SSM_MODE_COPY, m.SSM_FOLD_AT_COMMIT),
+                             ("replay", m.SSM_MODE_REPLAY, m.SSM_FOLD_AT_COMMIT),
+                             ("replay_fold_in_verify", m.SSM_MODE_REPLAY, m.SSM_FOLD_IN_VERIFY)):
         init = (torch.randn((R, H, P, N), generator=gen, device="cuda") * 0.1).contiguous()
-        pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, mode, 16, 1), R, init)
+        pool = m.ssm_state_init(m.make_config(H, P, N, G, m.SSM_DTYPE_BF16, m.SSM_DTYPE_F32, mode, 16, 1,
+                                              fold=fold), R, init)
         del init
 
         def run(n):
@@ -631,6 +634,8 @@ def bench_replay_plain_decode(torch, m, args):
         assert st == m.SSM_OK and flags == 0, f"{name} raised device flags {flags}"
         m.ssm_state_destroy(pool)
     out["replay_speedup_over_decode"] = out["decode_us_per_step"] / out["replay_us_per_step"]
+    out["replay_fold_in_verify_speedup_over_decode"] = (out["decode_us_per_step"] /
+                                                       out["replay_fold_in_verify_us_per_step"])
     out["config"] = dict(batch=R, W=16, tokens=T, heads=H, headdim=P, dstate=N, groups=G)
     return out
 

@@ -39,7 +39,7 @@ EXPORTS = (
     "ssm_status_string", "ssm_pool_bytes", "ssm_verify_replay_static", "ssm_receipt_bytes", "ssm_receipt_encode",
     "ssm_receipt_decode", "ssm_state_checkpoint_receipt", "ssm_state_restore_receipt",
     "ssm_gdn_init", "ssm_gdn_destroy", "ssm_gdn_reset", "ssm_gdn_decode_step", "ssm_gdn_verify_replay",
-    "ssm_gdn_commit", "ssm_gdn_gather", "ssm_gdn_slot_info", "ssm_gdn_status",
+    "ssm_gdn_commit", "ssm_gdn_gather", "ssm_gdn_slot_info", "ssm_gdn_status", "ssm_gdn_last_path",
 )
 
 
@@ -124,6 +124,7 @@ def _load():
         "ssm_gdn_commit": [V, I32, P_I32, V, I32, V],
         "ssm_gdn_gather": [V, I32, P_I32, V, V],
         "ssm_gdn_slot_info": [V, I32, P_I64, P_I32, ctypes.POINTER(U32), V],
+        "ssm_gdn_last_path": [V],
         "ssm_gdn_status": [V, ctypes.POINTER(U32), I32, V],
     }
     for name, args in sig.items():
@@ -131,6 +132,7 @@ def _load():
         f.argtypes = args
         f.restype = ctypes.c_int
     lib.ssm_last_path.restype = ctypes.c_char_p
+    lib.ssm_gdn_last_path.restype = ctypes.c_char_p
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_pool_bytes.restype = ctypes.c_size_t
     lib.ssm_receipt_bytes.argtypes = [I32, I32, I32]
@@ -541,6 +543,11 @@ def ssm_gdn_slot_info(pool: GdnPool, slot: int, stream=None):
     st = _lib.ssm_gdn_slot_info(pool.handle, int(slot), ctypes.byref(pos), ctypes.byref(ll), ctypes.byref(fl),
                                 _stream(stream))
     return st, int(pos.value), int(ll.value), int(fl.value)
+
+
+def ssm_gdn_last_path(pool) -> str:
+    """Kernel path of the gated-delta-rule pool's last verify."""
+    return _lib.ssm_gdn_last_path(pool.handle if pool is not None else None).decode()
 
 
 def ssm_gdn_status(pool: GdnPool, clear: bool = False, stream=None):

@@ -29,6 +29,8 @@
 
 #include "ssm_gdn.h"
 #include "ssm_internal.cuh"
+#include "tc.cuh"
+#include "tma.cuh"
 
 namespace ssm {
 namespace {
@@ -46,6 +48,9 @@ struct GdnArgs {
     int64_t *position;
     uint32_t *slot_flags, *flags;
     float *uq, *lt;       // verify scratch: [request][H][t1max][dk] queries, [request][H][t1max][dv] log terms
+    int uq_nm;            // 0: uq as above; else uq_rows rows per (request, head) in the tensor-core
+    int uq_rows;          // kernel's operand layout: [4 blocks of 32 columns][uq_nm rows][32], 16-byte chunk c
+                          // of row j at c ^ (j % 8)
     int32_t *fold_m;      // commit: tokens to fold per request of the launch (0: none)
     const void *q, *k, *v;
     const float *g, *beta;
@@ -298,6 +303,9 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 3, s = lane & 7;
     const int nthr = blockDim.x, nwarps = nthr >> 5;  // sized by the host to the sweeps
     const int T1 = a.n_tok;
+    // the tensor-core streaming kernel may start its checkpoint loads as this grid drains; it waits for
+    // this grid's completion before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (a.slot_flags[slot] & kSlotPoisoned) {
         if (tid == 0) atomicOr(a.flags, SSM_FLAG_POISONED_SLOT);
         return;
@@ -377,10 +385,15 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
                 for (int e = 0; e < NV; ++e) u[e] = axpy4(at, u[e], -at * bd, k4[e]);
             }
         }
-        if (act) {
+        if (act && a.uq_nm == 0) {
             float *uqj = a.uq + (((size_t)i * a.H + h0 + hl) * a.t1max + j) * DK;
 #pragma unroll
             for (int e = 0; e < NV; ++e) *reinterpret_cast<float4 *>(uqj + 4 * (s + 8 * e)) = u[e];
+        } else if (act) {  // the tensor-core operand: columns 4 (s + 8 e) .. + 3 are block e, chunk s
+            float *ub = a.uq + ((size_t)i * a.H + h0 + hl) * a.uq_rows * DK;
+#pragma unroll
+            for (int e = 0; e < NV; ++e)
+                *reinterpret_cast<float4 *>(ub + ((size_t)e * a.uq_nm + j) * 32 + ((s ^ (j & 7)) << 2)) = u[e];
         }
     }
     __syncthreads();  // the weights, and this CTA's staged step values in the log
@@ -463,6 +476,245 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_stream_kernel(const __grid
                             from_f<TI>(acc[q] + slt[(size_t)j * a.dv + pr[q]]);
             }
         }
+    }
+}
+
+// ---------------------------------------------------------------------------- replay verify, tensor cores
+//
+// gdn_stream_tc_kernel: the streaming product o_j = S u_j + lt_j of bf16 pools with dk = dv = 128 on the
+// 5th-generation tensor cores.  An item is one (request, value head): its 128 x 128 fp32 checkpoint is the
+// A operand (M = 128 rows p, K = 128), read in place from four 32-column TMA boxes whose 128-byte swizzle
+// is the K-major operand layout of kind::tf32; B is U, the swept queries, NM rows written in the same layout
+// by the coefficient kernel.  kind::tf32 takes each fp32 operand through its top 19 bits (the low 13
+// mantissa bits dropped), at most 2^-10 of each product, below the bf16 rounding of the outputs; fp32
+// pools keep the CUDA-core kernel above.
+// Warps: 0-3 epilogue (TMEM lane quarter w, thread = row p = 32 w + lane): o_j[p] = D[p][j] + lt_j[p];
+//        4 per-item producer: U and the log terms of an item into a small ring (after the coefficient
+//          kernel's completion);
+//        5 checkpoint producer: 16 KiB boxes into a ring, a slot refilled once the MMAs of the item that
+//          held it are done (so no per-slot release is needed);
+//        6 MMA issuer (lane 0), 16 MMAs and one commit per item; TMEM owner.
+constexpr int kGtProd = 4, kGtRing = 5, kGtMma = 6, kGtThreads = 7 * 32;
+constexpr int kGtMaxRing = 12, kGtAux = 3, kGtDone = 4, kGtDbuf = 4;
+constexpr int kGtMinTokens = 4;
+constexpr uint32_t kGtCols = 128;  // kGtDbuf accumulators of up to 32 columns
+
+struct GtLayout {
+    uint32_t u, lt, hdr, aux, aux_base, bars;
+};
+
+// Per-item stage: U [4 column blocks][NM rows][32 fp32], the log terms [t1max][dv], a header (the gate).
+__host__ __device__ inline GtLayout gt_layout(int NM, int t1max, int dv, int nring) {
+    GtLayout L;
+    L.u = 0;
+    L.lt = 4u * (uint32_t)NM * 128u;
+    L.hdr = L.lt + (uint32_t)t1max * (uint32_t)dv * 4u;
+    L.aux = (L.hdr + 16u + 1023u) & ~1023u;
+    L.aux_base = (uint32_t)nring * 16384u;
+    L.bars = L.aux_base + kGtAux * L.aux;
+    return L;
+}
+
+__host__ __device__ inline size_t gt_smem(const GtLayout &L) {
+    return (size_t)L.bars + (kGtMaxRing + 2 * kGtAux + kGtDone + kGtDbuf) * 8 + 1024;
+}
+
+__device__ __forceinline__ bool gt_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort, uint32_t *flags) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u && *abort) return false;
+    }
+    *abort = 1u;
+    atomicOr(flags, SSM_FLAG_TIMEOUT);
+    return false;
+}
+
+// The epilogue warps' barrier (named barrier 1, 128 threads) that ORs a predicate.
+__device__ __forceinline__ bool gt_epi_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+template <int NM>
+__global__ void __launch_bounds__(kGtThreads, 1)
+    gdn_stream_tc_kernel(const __grid_constant__ GdnArgs a, const __grid_constant__ CUtensorMap tm_state, int nring) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ uint32_t s_abort, s_tmem;
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int H = a.H, T1 = a.n_tok, dv = a.dv;  // dv = 128
+    const int n_items = a.batch * H;
+    const GtLayout L = gt_layout(NM, a.t1max, dv, nring);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *rfull = bars;                                     // checkpoint ring
+    uint64_t *xfull = rfull + kGtMaxRing, *xempty = xfull + kGtAux;  // per-item ring
+    uint64_t *done = xempty + kGtAux;                           // MMAs of an item finished
+    uint64_t *dempty = done + kGtDone;                          // accumulators read
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nring; ++s) mbar_init(&rfull[s], 1);
+        for (int s = 0; s < kGtAux; ++s) {
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], 4);
+        }
+        for (int s = 0; s < kGtDone; ++s) mbar_init(&done[s], 1);
+        for (int s = 0; s < kGtDbuf; ++s) mbar_init(&dempty[s], 4);
+        mbar_fence_init();
+        s_abort = 0u;
+    }
+    if (warp == kGtMma) tc::tmem_alloc(&s_tmem, kGtCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == kGtProd) {
+        // ------------------------------------------------------------ per-item producer
+        if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");  // U, the log terms and the flags are written
+            int xlast[kGtAux];
+            for (int s = 0; s < kGtAux; ++s) xlast[s] = -1;
+            const uint32_t ubytes = 4u * NM * 128u, lbytes = (uint32_t)T1 * dv * 4u;
+            for (int u = 0;; ++u) {
+                const int item = blockIdx.x + u * gridDim.x;
+                if (item >= n_items) break;
+                const int i = item / H, h = item - i * H, slot = a.slots[i];
+                const int xs = u % kGtAux;
+                if (u >= kGtAux && !gt_wait(&xempty[xs], (uint32_t)((u / kGtAux) - 1) & 1u, &s_abort, a.flags)) break;
+                unsigned char *X = smem + L.aux_base + (size_t)xs * L.aux;
+                const int gate = (a.slot_flags[slot] & kSlotPoisoned) ? 1 : 0;
+                *reinterpret_cast<int *>(X + L.hdr) = gate;
+                if (gate) {
+                    mbar_arrive(&xfull[xs]);
+                } else {
+                    mbar_arrive_expect_tx(&xfull[xs], ubytes + lbytes);
+                    bulk_g2s(X + L.u, a.uq + ((size_t)i * H + h) * a.uq_rows * 128, ubytes, &xfull[xs]);
+                    bulk_g2s(X + L.lt, a.lt + ((size_t)i * H + h) * a.t1max * dv, lbytes, &xfull[xs]);
+                    xlast[xs] = u;
+                }
+            }
+            for (int s = 0; s < kGtAux; ++s)  // no copy may still be landing when the CTA exits
+                if (xlast[s] >= 0 && !mbar_wait(&xfull[s], (uint32_t)(xlast[s] / kGtAux) & 1u))
+                    atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else if (warp == kGtRing) {
+        // ------------------------------------------------------------ checkpoint producer
+        if (lane == 0) {
+            int rlast[kGtMaxRing];
+            for (int s = 0; s < kGtMaxRing; ++s) rlast[s] = -1;
+            int nblk = 0;
+            bool alive = true;
+            for (int u = 0; alive; ++u) {
+                const int item = blockIdx.x + u * gridDim.x;
+                if (item >= n_items) break;
+                const int i = item / H, h = item - i * H;
+                const int row0 = (a.slots[i] * H + h) * dv;
+                for (int kb = 0; kb < 4; ++kb, ++nblk) {
+                    const int rs = nblk % nring;
+                    if (nblk >= nring) {  // the slot's last block belonged to item pu: its MMAs are done
+                        const int pu = (nblk - nring) >> 2;
+                        if (!gt_wait(&done[pu % kGtDone], (uint32_t)(pu / kGtDone) & 1u, &s_abort, a.flags)) {
+                            alive = false;
+                            break;
+                        }
+                    }
+                    mbar_arrive_expect_tx(&rfull[rs], 16384u);
+                    tma_load_2d(smem + (size_t)rs * 16384, &tm_state, kb * 32, row0, &rfull[rs]);
+                    rlast[rs] = nblk;
+                }
+            }
+            for (int s = 0; s < nring; ++s)  // no copy may still be landing when the CTA exits
+                if (rlast[s] >= 0 && !mbar_wait(&rfull[s], (uint32_t)(rlast[s] / nring) & 1u))
+                    atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else if (warp == kGtMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_tf32_f32(128, NM);
+            int last = -1;
+            for (int u = 0;; ++u) {
+                const int item = blockIdx.x + u * gridDim.x;
+                if (item >= n_items) break;
+                const int xs = u % kGtAux, db = u % kGtDbuf;
+                if (!gt_wait(&xfull[xs], (uint32_t)(u / kGtAux) & 1u, &s_abort, a.flags)) break;
+                if (u >= kGtDbuf && !gt_wait(&dempty[db], (uint32_t)((u / kGtDbuf) - 1) & 1u, &s_abort, a.flags))
+                    break;
+                const uint32_t d = tmem + (uint32_t)db * NM;
+                const uint32_t ub = smem_addr(smem + L.aux_base + (size_t)xs * L.aux + L.u);
+                bool ok = true;
+                for (int kb = 0; kb < 4 && ok; ++kb) {
+                    const int c = 4 * u + kb, rs = c % nring;
+                    ok = gt_wait(&rfull[rs], (uint32_t)(c / nring) & 1u, &s_abort, a.flags);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t ab = smem_addr(smem + (size_t)rs * 16384);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // K = 8 tf32 per MMA
+                        tc::mma_tf32(d, tc::smem_desc_sw128(ab + 32 * kk, 1024),
+                                     tc::smem_desc_sw128(ub + (uint32_t)kb * NM * 128 + 32 * kk, 1024), idesc,
+                                     (kb | kk) != 0);
+                }
+                tc::mma_commit(&done[u % kGtDone]);  // also when cut short: what was issued completes first
+                last = u;
+                if (!ok) break;
+            }
+            // every MMA issued has completed before TMEM is released
+            if (last >= 0 && !mbar_wait(&done[last % kGtDone], (uint32_t)(last / kGtDone) & 1u))
+                atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 0-3)
+        const int p = 32 * warp + lane;
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(a.y);
+        for (int u = 0;; ++u) {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) break;
+            const int xs = u % kGtAux, db = u % kGtDbuf;
+            const bool ok = gt_wait(&xfull[xs], (uint32_t)(u / kGtAux) & 1u, &s_abort, a.flags);
+            if (gt_epi_or(!ok)) break;
+            const unsigned char *X = smem + L.aux_base + (size_t)xs * L.aux;
+            const int gate = *reinterpret_cast<const int *>(X + L.hdr);
+            const int i = item / H, h = item - i * H;
+            const bool okd = gt_wait(&done[u % kGtDone], (uint32_t)(u / kGtDone) & 1u, &s_abort, a.flags);
+            if (gt_epi_or(!okd)) break;
+            tc::fence_after_sync();
+            float d[NM];
+#pragma unroll
+            for (int c = 0; c < NM; c += 16) {
+                float part[16];
+                tc::tmem_ld16(tmem + lane_off + (uint32_t)db * NM + c, part);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) d[c + q] = part[q];
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[db]);
+            if (!gate) {
+                const float *lt = reinterpret_cast<const float *>(X + L.lt);
+                __nv_bfloat16 *yr = y + ((size_t)i * T1 * H + h) * dv + p;
+#pragma unroll
+                for (int j = 0; j < NM; ++j)
+                    if (j < T1) yr[(size_t)j * H * dv] = __float2bfloat16_rn(d[j] + lt[(size_t)j * dv + p]);
+            }
+            __syncwarp();  // the stage is read (U by the MMAs, done above; the log terms here)
+            if (lane == 0) mbar_arrive(&xempty[xs]);
+        }
+    }
+    __syncwarp();  // warps whose lane 0 ran a role alone arrive at the block barrier converged
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kGtMma) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kGtCols);
     }
 }
 
@@ -618,6 +870,12 @@ struct ssm_gdn_pool_s {
     int64_t *position = nullptr;
     uint32_t *slot_flags = nullptr, *flags = nullptr;
     std::vector<int> pending_ntok;  // tokens of each slot's last verify (0: none since its commit)
+    // bf16 pools with dk = dv = 128: the tensor-core streaming verify (rows of 128 fp32, 32-column boxes,
+    // 128-byte swizzle) and the rows of U per (request, head) in its operand layout
+    CUtensorMap tm_state;
+    bool tc_ok = false;
+    int uq_rows = 0;
+    const char *last_path = "none";
 };
 
 namespace ssm {
@@ -766,7 +1024,9 @@ ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float 
     if (e == cudaSuccess) e = cudaMalloc(&p->log_v, ns * W * H * c.dv * p->in_b);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_g, ns * W * H);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_b, ns * W * H);
-    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->uq, sr * H * T * c.dk);
+    const bool tc_shape = p->in_b == 2 && c.dk == 128 && c.dv == 128 && c.max_tokens <= 32;
+    p->uq_rows = tc_shape ? (c.max_tokens <= 16 ? 16 : 32) : c.max_tokens;
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->uq, sr * H * (size_t)p->uq_rows * c.dk);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->lt, sr * H * T * (size_t)c.dv);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_len, ns);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->fold_m, (size_t)ssm::kGdnMaxBatch);
@@ -789,6 +1049,15 @@ ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float 
         ssm::gdn_free(p);
         delete p;
         return e == cudaErrorMemoryAllocation ? SSM_ERR_NO_MEMORY : SSM_ERR_CUDA;
+    }
+    if (tc_shape) {  // else (or with no encoder in the driver) the CUDA-core streaming kernel serves
+        const ssm::TensorMapEncode enc = ssm::tensor_map_encoder();
+        const cuuint64_t dims[2] = {(cuuint64_t)c.dk, (cuuint64_t)ns * H * c.dv};
+        const cuuint64_t strides[1] = {(cuuint64_t)c.dk * 4};
+        const cuuint32_t box[2] = {32u, 128u}, es[2] = {1u, 1u};
+        p->tc_ok = enc && enc(&p->tm_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p->state, dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
     *out = p;
     return SSM_OK;
@@ -879,9 +1148,30 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
     const int nsw = (p.cfg.nheads / p.cfg.nkheads) * n_tok;
     const unsigned coef_threads = (unsigned)(32 * std::min(ssm::kGdnWarps, std::max(4, (nsw + 3) / 4)));
     const size_t ssm_ = ssm::gdn_stream_smem(p.cfg.dk, p.cfg.dv, p.cfg.max_tokens);
+    // the tensor-core streaming kernel: as many 16 KiB checkpoint slots as fit beside its per-item ring
+    const int NM = n_tok <= 16 ? 16 : 32;
+    int nring = 0;
+    size_t tsm = 0;
+    // (from four step tokens: below that the CUDA-core kernel's few products per state element are cheaper
+    // than the tensor-core kernel's per-item pipeline)
+    if (p.tc_ok && n_tok >= ssm::kGtMinTokens && n_tok <= 32 && NM <= p.uq_rows) {
+        int max_smem = 0;
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device);
+        for (int nr = ssm::kGtMaxRing; nr >= 8 && !nring; --nr) {
+            const size_t b = ssm::gt_smem(ssm::gt_layout(NM, p.cfg.max_tokens, p.cfg.dv, nr));
+            if (b <= (size_t)max_smem) {
+                nring = nr;
+                tsm = b;
+            }
+        }
+    }
+    int sms = 1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
     st = ssm::gdn_batches(p, slots, batch, [&](GdnArgs &a, int base, int m) {
         const size_t b0 = (size_t)base;
         a.n_tok = n_tok;
+        a.uq_nm = nring ? NM : 0;
+        a.uq_rows = p.uq_rows;
         a.q = static_cast<const char *>(q) + b0 * T * G * dk * ib;
         a.k = static_cast<const char *>(k) + b0 * T * G * dk * ib;
         a.v = static_cast<const char *>(v) + b0 * T * H * dv * ib;
@@ -896,14 +1186,34 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
             if (e == cudaSuccess) e = ssm::gdn_smem(ks, ssm_);
             if (e == cudaSuccess) {
                 kc<<<dim3((unsigned)G, m), coef_threads, csm, s>>>(a);
-                ks<<<dim3((unsigned)H, m), ssm::kGdnThreads, ssm_, s>>>(a);
-                e = cudaGetLastError();
+                if (nring) {  // bf16, dk = dv = 128: the tensor-core streaming kernel
+                    auto kt = NM == 16 ? ssm::gdn_stream_tc_kernel<16> : ssm::gdn_stream_tc_kernel<32>;
+                    e = ssm::gdn_smem(kt, tsm);
+                    if (e == cudaSuccess) {
+                        cudaLaunchConfig_t lc = {};
+                        cudaLaunchAttribute attr[1];
+                        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                        attr[0].val.programmaticStreamSerializationAllowed = 1;
+                        lc.gridDim = dim3((unsigned)std::min<size_t>((size_t)m * H, (size_t)sms));
+                        lc.blockDim = dim3(ssm::kGtThreads);
+                        lc.dynamicSmemBytes = tsm;
+                        lc.stream = s;
+                        lc.attrs = attr;
+                        lc.numAttrs = 1;
+                        e = cudaLaunchKernelEx(&lc, kt, a, p.tm_state, nring);
+                    }
+                } else {
+                    ks<<<dim3((unsigned)H, m), ssm::kGdnThreads, ssm_, s>>>(a);
+                }
+                if (e == cudaSuccess) e = cudaGetLastError();
             }
         });
         return e;
     });
-    if (st == SSM_OK)
+    if (st == SSM_OK) {
         for (int i = 0; i < batch; ++i) pool->pending_ntok[(size_t)slots[i]] = n_tok;
+        pool->last_path = nring ? "gdn_verify_tc" : "gdn_verify";
+    }
     return st;
 }
 
@@ -959,6 +1269,8 @@ ssm_status ssm_gdn_slot_info(ssm_gdn_pool pool, int32_t slot, int64_t *position,
     if (flags) *flags = fl;
     return SSM_OK;
 }
+
+const char *ssm_gdn_last_path(ssm_gdn_pool pool) { return pool ? pool->last_path : "none"; }
 
 ssm_status ssm_gdn_status(ssm_gdn_pool pool, uint32_t *flags_out, int32_t clear, ssm_stream_t stream) {
     if (!pool || !flags_out) return SSM_ERR_INVALID_ARG;

@@ -77,7 +77,10 @@ ssm_status ssm_gdn_decode_step(ssm_gdn_pool pool, int32_t batch, const int32_t *
  * i = m .. 1, taking the weight beta_i (k_i . u) of v_i and then
  * u <- exp(g_i) (u - beta_i k_i (k_i . u)); the output is S_ckpt u plus the
  * weighted v_i.  The step's k, v, g and beta are staged after the log for
- * the commit.  Shapes as decode with [batch][n_tok] tokens. */
+ * the commit.  Shapes as decode with [batch][n_tok] tokens.  bf16 pools with
+ * dk = dv = 128 and 4 <= n_tok <= 32 take the checkpoint product S u on the tensor
+ * cores (fp32 operands read as tf32: at most 2^-10 of each product, below
+ * the bf16 rounding of y); other pools the exact fp32 CUDA-core kernel. */
 ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok, const int32_t *slots,
                                  const void *q, const void *k, const void *v, const float *g, const float *beta,
                                  void *y, ssm_stream_t stream);
@@ -98,6 +101,10 @@ ssm_status ssm_gdn_slot_info(ssm_gdn_pool pool, int32_t slot, int64_t *position,
 
 /* Read (and if clear != 0, clear) the pool's sticky device flags.  Synchronous. */
 ssm_status ssm_gdn_status(ssm_gdn_pool pool, uint32_t *flags_out, int32_t clear, ssm_stream_t stream);
+
+/* Kernel path of the pool's last verify: "gdn_verify_tc" (tensor cores),
+ * "gdn_verify" (CUDA cores) or "none".  The string is static. */
+const char *ssm_gdn_last_path(ssm_gdn_pool pool);
 
 #ifdef __cplusplus
 }

@@ -88,6 +88,9 @@ def _run_verify(m, dt_in, H, G, dk, dv, W, T1, p, steps, slots, n_slots=8, force
         parts = synth.gdn_batch_tokens(SEED, 100 + s, len(slots), T1, H, G, dk, dv, dt_in)
         y = _out((len(slots), T1, H, dv), dt_in)
         assert m.ssm_gdn_verify_replay(pool, slots, T1, *_dev(parts, dt_in), y) == m.SSM_OK
+        # bf16 pools with 128 x 128 heads take the checkpoint product on the tensor cores
+        tc = dt_in == synth.BF16 and dk == 128 and dv == 128 and 4 <= T1 <= 32
+        assert m.ssm_gdn_last_path(pool) == ("gdn_verify_tc" if tc else "gdn_verify")
         yo = opool.verify(slots, *_wide(parts, dt_in))
         check_close(to_host(y), yo, dt_in, f"y step {s}", positions_axis=1, cond=opool.last_cond)
         a = torch.from_numpy(np.ascontiguousarray(acc[s], dtype=np.int32)).cuda()
@@ -152,11 +155,13 @@ def test_replay_pool_used_for_decode_agrees_with_decode():
         m.ssm_gdn_destroy(dp)
 
 
-@pytest.mark.parametrize("which", ["q", "k", "v", "g", "beta"])
-def test_nonfinite_input_poisons_only_its_request(which):
+@pytest.mark.parametrize("which,dk,dv", [(w, 64, 64) for w in ("q", "k", "v", "g", "beta")] +
+                         [("k", 128, 128), ("beta", 128, 128)])
+def test_nonfinite_input_poisons_only_its_request(which, dk, dv):
+    """dk = dv = 128 (bf16) runs the tensor-core streaming kernel, whose gate drops the poisoned request."""
     import torch
     m = _mod()
-    H, G, dk, dv, dt_in, T1 = 4, 2, 64, 64, synth.BF16, 3
+    H, G, dt_in, T1 = 4, 2, synth.BF16, (4 if dk == 128 else 3)
     slots = [0, 1, 2]
     pool, opool = _pools(m, H, G, dk, dv, dt_in, 4, 8, T1)
     try:
@@ -167,6 +172,7 @@ def test_nonfinite_input_poisons_only_its_request(which):
         parts[idx] = bad
         y = _out((3, T1, H, dv), dt_in)
         assert m.ssm_gdn_verify_replay(pool, slots, T1, *_dev(tuple(parts), dt_in), y) == m.SSM_OK
+        assert m.ssm_gdn_last_path(pool) == ("gdn_verify_tc" if dk == 128 else "gdn_verify")
         st, flags = m.ssm_gdn_status(pool, clear=True)
         assert flags & m.SSM_FLAG_NONFINITE_INPUT
         assert m.ssm_gdn_slot_info(pool, 1)[3] & 1 and m.ssm_gdn_slot_info(pool, 0)[3] == 0
@@ -204,13 +210,14 @@ def test_bad_accept_and_misuse():
 
 
 def test_full_size_sampled_requests():
-    """Replay verify + commit at the benchmark's shape (32 value heads, 16 key
-    heads, 128 x 128, bf16, window 16, 8 drafts), 64 requests; sampled
-    requests checked against the oracle step by step."""
+    """Replay verify + commit at the benchmark's shape (256 requests, 32 value
+    heads, 16 key heads, 128 x 128, bf16, window 16, 8 drafts) on the
+    tensor-core streaming kernel; sampled requests checked against the oracle
+    step by step."""
     import torch
     m = _mod()
-    H, G, dk, dv, dt_in, W, T1, R = 32, 16, 128, 128, synth.BF16, 16, 9, 64
-    sample = [0, 17, 42, 63]
+    H, G, dk, dv, dt_in, W, T1, R = 32, 16, 128, 128, synth.BF16, 16, 9, 256
+    sample = [0, 17, 142, 255]
     init = np.stack([synth.gdn_init_state(SEED, s, H, dv, dk) for s in range(R)])
     pool = m.ssm_gdn_init(m.make_gdn_config(H, G, dk, dv, dt_in, W, T1), R, torch.from_numpy(init).cuda())
     opool = og.GdnOraclePool(H, G, dk, dv, len(sample), W=W, max_tokens=T1, init_state=init[sample].astype(np.float64))
@@ -221,6 +228,7 @@ def test_full_size_sampled_requests():
             parts = synth.gdn_batch_tokens(SEED, 600 + s, R, T1, H, G, dk, dv, dt_in)
             y = _out((R, T1, H, dv), dt_in)
             assert m.ssm_gdn_verify_replay(pool, slots, T1, *_dev(parts, dt_in), y) == m.SSM_OK
+            assert m.ssm_gdn_last_path(pool) == "gdn_verify_tc"
             yo = opool.verify(list(range(len(sample))), *(a[sample] for a in _wide(parts, dt_in)))
             check_close(to_host(y)[sample], yo, dt_in, f"sampled y step {s}", positions_axis=1, cond=opool.last_cond)
             assert m.ssm_gdn_commit(pool, slots, torch.from_numpy(acc[s]).cuda()) == m.SSM_OK
