@@ -36,7 +36,8 @@ EXPORTS = (
     "ssm_state_restore", "ssm_slot_info", "ssm_state_gather", "ssm_scan_chunk", "ssm_decode_step",
     "ssm_decode_steps_host",
     "ssm_verify_copy", "ssm_verify_replay", "ssm_state_commit", "ssm_pool_status", "ssm_last_path",
-    "ssm_status_string", "ssm_pool_bytes", "ssm_verify_replay_static", "ssm_receipt_bytes", "ssm_receipt_encode",
+    "ssm_status_string", "ssm_pool_bytes", "ssm_debug_stall_next_verify", "ssm_verify_replay_static",
+    "ssm_receipt_bytes", "ssm_receipt_encode",
     "ssm_receipt_decode", "ssm_state_checkpoint_receipt", "ssm_state_restore_receipt",
     "ssm_gdn_init", "ssm_gdn_destroy", "ssm_gdn_reset", "ssm_gdn_decode_step", "ssm_gdn_verify_replay",
     "ssm_gdn_commit", "ssm_gdn_gather", "ssm_gdn_slot_info", "ssm_gdn_status", "ssm_gdn_last_path",
@@ -109,6 +110,7 @@ def _load():
         "ssm_last_path": [V],
         "ssm_status_string": [ctypes.c_int],
         "ssm_pool_bytes": [V],
+        "ssm_debug_stall_next_verify": [V],
         "ssm_verify_replay_static": [I32, I32, I32, I32, I32, I32, I32, I32, I32, V, V, V, V, V,
                                      V, V, V, V, V, V, V, V, V],
         "ssm_receipt_encode": [ctypes.POINTER(ssm_receipt), V, V, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)],
@@ -543,6 +545,11 @@ def ssm_gdn_slot_info(pool: GdnPool, slot: int, stream=None):
     st = _lib.ssm_gdn_slot_info(pool.handle, int(slot), ctypes.byref(pos), ctypes.byref(ll), ctypes.byref(fl),
                                 _stream(stream))
     return st, int(pos.value), int(ll.value), int(fl.value)
+
+
+def ssm_debug_stall_next_verify(pool: Pool) -> int:
+    """Tests of the failure path: the pool's next tensor-core replay verify lets one CTA's waits run out."""
+    return _lib.ssm_debug_stall_next_verify(pool.handle)
 
 
 def ssm_gdn_last_path(pool) -> str:

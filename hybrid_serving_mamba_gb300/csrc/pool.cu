@@ -703,6 +703,8 @@ static ssm_status verify_common(ssm_pool pool, int32_t batch, int32_t n_tok, con
     DeviceGuard g(p.device);
     ssm::StepArgs a;
     fill_step(p, a, x, dt, B, C, A, D, y, n_tok);
+    a.test_stall = p.test_stall;
+    p.test_stall = 0;
     const char *path = mode == SSM_MODE_COPY ? "verify_copy" : "verify_replay";
     auto replay = [&path](const Pool &pl, const ssm::StepArgs &sa, cudaStream_t s) {
         return ssm::launch_verify_replay(pl, sa, s, &path);
@@ -777,5 +779,11 @@ ssm_status ssm_pool_status(ssm_pool pool, uint32_t *flags_out, int32_t clear, ss
 const char *ssm_last_path(ssm_pool pool) { return pool ? pool->p.last_path : ssm::static_last_path(); }
 
 size_t ssm_pool_bytes(ssm_pool pool) { return pool ? pool->p.bytes : 0; }
+
+ssm_status ssm_debug_stall_next_verify(ssm_pool pool) {
+    if (!pool) return SSM_ERR_INVALID_ARG;
+    pool->p.test_stall = 1;
+    return SSM_OK;
+}
 
 }  // extern "C"

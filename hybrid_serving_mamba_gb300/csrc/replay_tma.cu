@@ -743,7 +743,10 @@ __global__ void __launch_bounds__(TcShape<NM>::kThreads, 1)
                     int *hdr = reinterpret_cast<int *>(X + L.hdr);
                     hdr[0] = (int)gate;
                     hdr[1] = k;
-                    if (gate) {
+                    if (a.test_stall && blockIdx.x == 0 && u == 0) {
+                        // tests of the failure path: this item's loads are withheld, so the waits on them
+                        // run out and every role of this CTA leaves through its abort path
+                    } else if (gate) {
                         mbar_arrive(&xfull[xs_]);
                     } else {
                         mbar_arrive_expect_tx(&xfull[xs_], xbytes);

@@ -102,6 +102,7 @@ struct Pool {
     std::vector<uint8_t> released;
     std::vector<int32_t> pending_ntok;  // n_tok of the last uncommitted verify, 0 = none
     const char *last_path = "none";
+    int test_stall = 0;  // ssm_debug_stall_next_verify, one-shot
 };
 
 // ---------------------------------------------------------------- kernel args
@@ -140,6 +141,7 @@ struct StepArgs {  // decode, copy verify, replay verify
     int32_t *plain;
     int2 *fv_items;
     int32_t *counts;
+    int test_stall;   // tests of the failure path: withhold one per-item load (see ssm_debug_stall_next_verify)
     int batch;
     int32_t slots[kMaxSlotsPerLaunch];
 };

@@ -437,6 +437,17 @@ const char *ssm_status_string(ssm_status s);
 /* Bytes of device memory the pool holds. */
 size_t ssm_pool_bytes(ssm_pool pool);
 
+/*
+ * For tests of the failure path: the pool's next replay verify on the tensor
+ * cores withholds the per-item loads of one item in its first CTA, so that
+ * the waits on them run out (each bounded at about a second).  That CTA's
+ * roles then leave, the call's outputs for that item are not written, and
+ * the pool's flags report SSM_FLAG_TIMEOUT; nothing faults and the pool stays
+ * usable.  One-shot: the verify after it runs normally.  SSM_ERR_INVALID_ARG
+ * without a pool.
+ */
+ssm_status ssm_debug_stall_next_verify(ssm_pool pool);
+
 #ifdef __cplusplus
 }
 #endif

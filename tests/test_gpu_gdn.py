@@ -178,7 +178,7 @@ def test_nonfinite_input_poisons_only_its_request(which, dk, dv):
         assert m.ssm_gdn_slot_info(pool, 1)[3] & 1 and m.ssm_gdn_slot_info(pool, 0)[3] == 0
         good = [0, 2]
         yo = opool.verify(good, *(a[good] for a in _wide(tuple(parts), dt_in)))
-        check_close(to_host(y)[good], yo, dt_in, "the other requests", cond=opool.last_cond)
+        check_close(to_host(y[good]), yo, dt_in, "the other requests", cond=opool.last_cond)
         assert m.ssm_gdn_commit(pool, slots, torch.zeros(3, dtype=torch.int32, device="cuda")) == m.SSM_OK
         assert m.ssm_gdn_slot_info(pool, 1)[1] == 0 and m.ssm_gdn_slot_info(pool, 0)[1] == 1
         assert m.ssm_gdn_reset(pool, [1]) == m.SSM_OK

@@ -374,3 +374,54 @@ def test_nonfinite_verify_input_poisons_only_its_request(mode, where):
         check_close(to_host(got)[[0, 2]], opool.state[[0, 2]], synth.BF16, "healthy states")
     finally:
         m.ssm_state_destroy(pool)
+
+
+def test_bounded_wait_runs_out_and_the_pool_recovers():
+    """Failure path of the tensor-core replay verify, made on the host: the
+    next verify withholds one CTA's per-item loads
+    (ssm_debug_stall_next_verify), so the waits on them run out (each bounded,
+    about a second) and that CTA's roles leave through their abort paths.  The
+    call returns, SSM_FLAG_TIMEOUT is raised (and nothing else), and the same
+    step verified again, then committed, matches the oracle."""
+    import time
+
+    import torch
+    m = _mod()
+    H, P, N, G, R, T1, W = 4, 64, 128, 2, 4, 5, 8
+    A, D = synth.head_params(SEED + 5, H)
+    init = np.stack([synth.init_state(SEED + 5, s, H, P, N) for s in range(R)])
+    pool = m.ssm_state_init(m.make_config(H, P, N, G, synth.BF16, synth.F32, m.SSM_MODE_REPLAY, W, T1), R,
+                            torch.from_numpy(init).cuda())
+    opool = oracle.OraclePool(H, P, N, G, R, A, D, mode=oracle.REPLAY, W=W, max_tokens=T1,
+                              init_state=init.astype(np.float64))
+    Ad, Dd = torch.from_numpy(A).cuda(), torch.from_numpy(D).cuda()
+    slots = list(range(R))
+    try:
+        x, dt, B, C = synth.batch_tokens(SEED + 5, 0, R, T1, H, P, G, N, synth.BF16, synth.F32)
+        dev = _dev_inputs(x, dt, B, C, synth.BF16, synth.F32)
+        y = empty_like_out((R, T1, H, P), synth.BF16)
+        assert m.ssm_debug_stall_next_verify(pool) == m.SSM_OK
+        t0 = time.monotonic()
+        assert m.ssm_verify_replay(pool, slots, T1, *dev, Ad, Dd, y) == m.SSM_OK
+        assert m.ssm_last_path(pool) == "verify_replay_tc"
+        st, flags = m.ssm_pool_status(pool, clear=True)
+        assert st == m.SSM_OK and flags == m.SSM_FLAG_TIMEOUT, flags
+        assert time.monotonic() - t0 < 60
+        for sl in slots:  # a pool-wide flag: no slot is poisoned
+            assert m.ssm_slot_info(pool, sl)[1].flags == 0
+        # the same step again, then its commit, as if the failed call had not happened
+        y = empty_like_out((R, T1, H, P), synth.BF16)
+        assert m.ssm_verify_replay(pool, slots, T1, *dev, Ad, Dd, y) == m.SSM_OK
+        _, yo = opool.verify(slots, *_wide(x, dt, B, C, synth.BF16, synth.F32))
+        check_close(to_host(y), yo, synth.BF16, "y after the timeout", positions_axis=1, cond=opool.last_cond)
+        acc = np.array([2, 0, 4, 1], np.int32)
+        assert m.ssm_state_commit(pool, slots, torch.from_numpy(acc).cuda(), False, Ad) == m.SSM_OK
+        opool.commit(slots, acc)
+        x, dt, B, C = synth.batch_tokens(SEED + 5, 1, R, T1, H, P, G, N, synth.BF16, synth.F32)
+        assert m.ssm_verify_replay(pool, slots, T1, *_dev_inputs(x, dt, B, C, synth.BF16, synth.F32), Ad, Dd,
+                                   y) == m.SSM_OK
+        _, yo = opool.verify(slots, *_wide(x, dt, B, C, synth.BF16, synth.F32))
+        check_close(to_host(y), yo, synth.BF16, "the next step", positions_axis=1, cond=opool.last_cond)
+        assert m.ssm_pool_status(pool) == (m.SSM_OK, 0)
+    finally:
+        m.ssm_state_destroy(pool)
