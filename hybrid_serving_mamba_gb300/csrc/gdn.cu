@@ -286,9 +286,48 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_decode_kernel(const __grid
 
 // ---------------------------------------------------------------------------- replay verify
 
-__host__ __device__ inline size_t gdn_coef_smem(int DK, int dv, int wcap, int t1max, int hpg) {
-    return ((size_t)wcap * DK + (size_t)t1max * DK + 2 * (size_t)hpg * wcap + (size_t)hpg * t1max * wcap +
-            (size_t)wcap * dv) * sizeof(float);
+// The coefficient kernel's shared memory (bytes): fp32 keys [wcap][DK] (the log's, then the step's) and
+// queries [t1max][DK], exp(g) and beta [hpg][wcap] each, the log-term weights [hpg][t1max][wcap], the
+// values [wcap][hpg dv] as given (the log's, then the step's), and for bf16 inputs the keys and queries
+// as given [wcap + t1max][DK].
+struct CoefLayout {
+    size_t sq, sal, sbe, scw, svr, rkq, total;
+};
+__host__ __device__ inline CoefLayout coef_layout(int DK, int dv, int wcap, int t1max, int hpg, int in_b) {
+    CoefLayout L;
+    size_t o = (size_t)wcap * DK * 4;
+    L.sq = o;
+    o += (size_t)t1max * DK * 4;
+    L.sal = o;
+    o += (size_t)hpg * wcap * 4;
+    L.sbe = o;
+    o += (size_t)hpg * wcap * 4;
+    L.scw = o;
+    o += (size_t)hpg * t1max * wcap * 4;
+    o = (o + 15) & ~(size_t)15;
+    L.svr = o;
+    o += (size_t)wcap * hpg * dv * in_b;
+    o = (o + 15) & ~(size_t)15;
+    L.rkq = o;
+    if (in_b == 2) o += (size_t)(wcap + t1max) * DK * 2;
+    L.total = o;
+    return L;
+}
+__host__ __device__ inline size_t gdn_coef_smem(int DK, int dv, int wcap, int t1max, int hpg, int in_b) {
+    return coef_layout(DK, dv, wcap, t1max, hpg, in_b).total;
+}
+
+// 8-byte asynchronous global -> shared copy (both addresses 8-byte aligned)
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// Four values of the input type from shared memory, widened to fp32 (bf16: the bits moved up 16).
+__device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 lds4(const __nv_bfloat16 *p) {
+    const uint2 r = *reinterpret_cast<const uint2 *>(p);
+    return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u), __uint_as_float(r.y << 16),
+                       __uint_as_float(r.y & 0xFFFF0000u));
 }
 
 // Grid (G, batch): one CTA per request and key head, whose logged and step keys serve all its value
@@ -296,7 +335,7 @@ __host__ __device__ inline size_t gdn_coef_smem(int DK, int dv, int wcap, int t1
 // the eight lanes of a row group, u in the rows' layout, so that k_t . u takes three shuffles.  A
 // warp's four sweeps run the same number of steps (its longest), the shorter ones idle at the end.
 template <int DK, typename TI>
-__global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_constant__ GdnArgs a) {
+__global__ void __launch_bounds__(kGdnThreads, 4) gdn_coef_kernel(const __grid_constant__ GdnArgs a) {
     constexpr int NV = DK / 32;
     extern __shared__ __align__(16) float gsm[];
     const int kh = blockIdx.x, i = blockIdx.y, slot = a.slots[i], hpg = a.hpg, h0 = kh * hpg;
@@ -310,42 +349,100 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
         if (tid == 0) atomicOr(a.flags, SSM_FLAG_POISONED_SLOT);
         return;
     }
-    const int K = a.log_len[slot];
-    float *sk = gsm;                              // [K + T1][DK]: the log's keys, then the step's
-    float *sq = sk + (size_t)a.wcap * DK;         // [T1][DK]
-    float *sal = sq + (size_t)a.t1max * DK;       // [hpg][K + T1] exp(g)
-    float *sbe = sal + (size_t)hpg * a.wcap;      // [hpg][K + T1] beta
-    float *scw = sbe + (size_t)hpg * a.wcap;      // [hpg][T1][wcap] the weights of the logged values
-    const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK;
-    const TI *qs = static_cast<const TI *>(a.q), *ks = static_cast<const TI *>(a.k);
-    const TI *vs = static_cast<const TI *>(a.v);
+    const int K = a.log_len[slot], m = K + T1, hdv = hpg * a.dv;
+    const CoefLayout L = coef_layout(DK, a.dv, a.wcap, a.t1max, hpg, (int)sizeof(TI));
+    char *base = reinterpret_cast<char *>(gsm);
+    float *sk = gsm;                                       // [wcap][DK]: the log's keys, then the step's
+    float *sq = reinterpret_cast<float *>(base + L.sq);    // [t1max][DK]
+    float *sal = reinterpret_cast<float *>(base + L.sal);  // [hpg][wcap] exp(g)
+    float *sbe = reinterpret_cast<float *>(base + L.sbe);  // [hpg][wcap] beta
+    float *scw = reinterpret_cast<float *>(base + L.scw);  // [hpg][t1max][wcap] the weights of the logged values
+    TI *svr = reinterpret_cast<TI *>(base + L.svr);        // [wcap][hpg dv] values as given
+    // keys and queries as given: fp32 inputs land in place, bf16 ones beside and are widened below
+    constexpr bool kWide = sizeof(TI) == 2;
+    TI *rk = kWide ? reinterpret_cast<TI *>(base + L.rkq) : reinterpret_cast<TI *>(sk);
+    TI *rq = kWide ? rk + (size_t)a.wcap * DK : reinterpret_cast<TI *>(sq);
+    const TI *lk = static_cast<const TI *>(a.log_k) + (size_t)slot * a.wcap * a.G * DK + (size_t)kh * DK;
+    const TI *lv = static_cast<const TI *>(a.log_v) + ((size_t)slot * a.wcap * a.H + h0) * a.dv;
     const size_t kstep = ((size_t)i * T1 * a.G + kh) * DK;  // step token 0's key (and query) of this key head
-    stage_rows(sk, lk + (size_t)kh * DK, (size_t)a.G * DK, K, DK, tid, nthr);  // checked when it was logged
-    bool bad = stage_rows(sk + (size_t)K * DK, ks + kstep, (size_t)a.G * DK, T1, DK, tid, nthr);
-    bad |= stage_rows(sq, qs + kstep, (size_t)a.G * DK, T1, DK, tid, nthr);
-    for (int e = tid; e < hpg * K; e += nthr) {
-        const int hl = e / K, t = e - hl * K;
-        sal[(size_t)hl * a.wcap + t] = expf(a.log_g[((size_t)slot * a.wcap + t) * a.H + h0 + hl]);
-        sbe[(size_t)hl * a.wcap + t] = a.log_b[((size_t)slot * a.wcap + t) * a.H + h0 + hl];
+    const TI *ks = static_cast<const TI *>(a.k) + kstep, *qs = static_cast<const TI *>(a.q) + kstep;
+    const TI *vs = static_cast<const TI *>(a.v) + ((size_t)i * T1 * a.H + h0) * a.dv;
+    const size_t krow = (size_t)a.G * DK, vrow = (size_t)a.H * a.dv;
+    // every load of the CTA in flight at once: the keys (the log's, then the step's) and the step's
+    // queries in 16-byte pieces, the values of the hpg value heads (one contiguous run a token), then the
+    // gates with plain loads while the copies land
+    {
+        constexpr int KCH = DK * (int)sizeof(TI) / 16;  // pieces of a key row
+        for (int c = tid; c < (m + T1) * KCH; c += nthr) {
+            const int row = c / KCH, off = (c % KCH) * (16 / (int)sizeof(TI));
+            const TI *src = row < K ? lk + (size_t)row * krow
+                          : row < m ? ks + (size_t)(row - K) * krow
+                                    : qs + (size_t)(row - m) * krow;
+            TI *dst = row < m ? rk + (size_t)row * DK : rq + (size_t)(row - m) * DK;
+            cp_async16(dst + off, src + off);
+        }
+        if ((a.dv * (int)sizeof(TI)) % 16 == 0) {  // every head's run starts on a 16-byte boundary
+            const int vch = hdv * (int)sizeof(TI) / 16;
+            for (int c = tid; c < m * vch; c += nthr) {
+                const int row = c / vch, off = (c - row * vch) * (16 / (int)sizeof(TI));
+                const TI *src = row < K ? lv + (size_t)row * vrow : vs + (size_t)(row - K) * vrow;
+                cp_async16(svr + (size_t)row * hdv + off, src + off);
+            }
+        } else {  // bf16 with dv = 4 (mod 8): 8-byte pieces
+            const int vch = hdv * (int)sizeof(TI) / 8;
+            for (int c = tid; c < m * vch; c += nthr) {
+                const int row = c / vch, off = (c - row * vch) * (8 / (int)sizeof(TI));
+                const TI *src = row < K ? lv + (size_t)row * vrow : vs + (size_t)(row - K) * vrow;
+                cp_async8(svr + (size_t)row * hdv + off, src + off);
+            }
+        }
+        cp_async_commit();
     }
-    for (int e = tid; e < hpg * T1; e += nthr) {
-        const int hl = e / T1, j = e - hl * T1;
-        const size_t src = ((size_t)i * T1 + j) * a.H + h0 + hl, dst = ((size_t)slot * a.wcap + K + j) * a.H + h0 + hl;
-        const float gv = a.g[src], bv = a.beta[src];
-        bad |= !(isfinite(gv) && isfinite(bv));
-        sal[(size_t)hl * a.wcap + K + j] = expf(gv);
-        sbe[(size_t)hl * a.wcap + K + j] = bv;
-        a.log_g[dst] = gv;
-        a.log_b[dst] = bv;
+    bool bad = false;
+    for (int e = tid; e < hpg * m; e += nthr) {
+        const int hl = e / m, t = e - hl * m;
+        float gv, bv;
+        if (t < K) {
+            gv = a.log_g[((size_t)slot * a.wcap + t) * a.H + h0 + hl];
+            bv = a.log_b[((size_t)slot * a.wcap + t) * a.H + h0 + hl];
+        } else {  // the step's, checked and logged after the log (for the commit)
+            const size_t src = ((size_t)i * T1 + t - K) * a.H + h0 + hl, dst = ((size_t)slot * a.wcap + t) * a.H + h0 + hl;
+            gv = a.g[src];
+            bv = a.beta[src];
+            bad |= !(isfinite(gv) && isfinite(bv));
+            a.log_g[dst] = gv;
+            a.log_b[dst] = bv;
+        }
+        sal[(size_t)hl * a.wcap + t] = expf(gv);
+        sbe[(size_t)hl * a.wcap + t] = bv;
     }
-    // the step after the log, for the commit (the positions past log_len: a rejected request leaves
-    // nothing behind that a later commit reads): the value heads' v and the key head's k
-    TI *lv = static_cast<TI *>(a.log_v);
-    TI *lkw = static_cast<TI *>(a.log_k);
-    bad |= copy_rows(lv + (((size_t)slot * a.wcap + K) * a.H + h0) * a.dv, (size_t)a.H * a.dv,
-                     vs + ((size_t)i * T1 * a.H + h0) * a.dv, (size_t)a.H * a.dv, T1, hpg * a.dv, tid, nthr);
-    copy_rows(lkw + (((size_t)slot * a.wcap + K) * a.G + kh) * DK, (size_t)a.G * DK, ks + kstep, (size_t)a.G * DK, T1,
-              DK, tid, nthr);
+    cp_async_wait<0>();
+    __syncthreads();
+    // widen the keys and queries (bf16), check the step's rows, and copy the step after the log (the
+    // positions past log_len: a rejected request leaves nothing behind that a later commit reads)
+    using V4 = typename Vec4<TI>::T;
+    for (int c = tid; c < (m + T1) * (DK / 4); c += nthr) {
+        const int row = c / (DK / 4), off = 4 * (c % (DK / 4));
+        const TI *src = row < m ? rk + (size_t)row * DK + off : rq + (size_t)(row - m) * DK + off;
+        if (row >= K) {
+            const V4 raw = *reinterpret_cast<const V4 *>(src);
+            bad |= Vec4<TI>::bad(raw);
+            if (row < m)
+                *reinterpret_cast<V4 *>(static_cast<TI *>(a.log_k) +
+                                        ((size_t)slot * a.wcap + row) * krow + (size_t)kh * DK + off) = raw;
+        }
+        if (kWide) {
+            float *dst = row < m ? sk + (size_t)row * DK + off : sq + (size_t)(row - m) * DK + off;
+            *reinterpret_cast<float4 *>(dst) = lds4(src);
+        }
+    }
+    for (int c = tid; c < T1 * (hdv / 4); c += nthr) {
+        const int j = c / (hdv / 4), off = 4 * (c - j * (hdv / 4));
+        const V4 raw = *reinterpret_cast<const V4 *>(svr + (size_t)(K + j) * hdv + off);
+        bad |= Vec4<TI>::bad(raw);
+        *reinterpret_cast<V4 *>(static_cast<TI *>(a.log_v) + ((size_t)slot * a.wcap * a.H + h0) * a.dv +
+                                (size_t)(K + j) * vrow + off) = raw;
+    }
     if (__syncthreads_or(bad)) {
         if (tid == 0) poison(a, slot, SSM_FLAG_NONFINITE_INPUT);
         return;
@@ -367,22 +464,35 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
         for (int e = 0; e < NV; ++e) u[e] = *reinterpret_cast<const float4 *>(sq + (size_t)j * DK + 4 * (s + 8 * e));
         const float *al = sal + (size_t)hl * a.wcap, *be = sbe + (size_t)hl * a.wcap;
         float *csj = scw + ((size_t)hl * a.t1max + j) * a.wcap;
+        // the weight just past the sweep is zero: the log terms below take step tokens in pairs over the
+        // longer one's span (mj < wcap whenever a later step token exists)
+        if (act && s == 0 && mj < a.wcap) csj[mj] = 0.f;
+        // the next step's key is loaded while this step's dot product is reduced
+        float4 kn[NV];
+        {
+            const float *kt = sk + (size_t)(mmax - 1 < mj ? mmax - 1 : 0) * DK;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) kn[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
+        }
         for (int t = mmax - 1; t >= 0; --t) {
             const bool live = t < mj;
-            const float *kt = sk + (size_t)(live ? t : 0) * DK;
             float4 k4[NV];
-            float d = 0.f;
 #pragma unroll
-            for (int e = 0; e < NV; ++e) {
-                k4[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
-                d += dot4(k4[e], u[e]);
+            for (int e = 0; e < NV; ++e) k4[e] = kn[e];
+            if (t > 0) {
+                const float *kt = sk + (size_t)(t - 1 < mj ? t - 1 : 0) * DK;
+#pragma unroll
+                for (int e = 0; e < NV; ++e) kn[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
             }
-            d = red8(d);
+            float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < NV; ++e) acc2 = dot4x2(k4[e], u[e], acc2);
+            const float d = red8(acc2.x + acc2.y);
             if (live) {
                 const float bd = be[t] * d, at = al[t];
                 if (s == 0) csj[t] = bd;
 #pragma unroll
-                for (int e = 0; e < NV; ++e) u[e] = axpy4(at, u[e], -at * bd, k4[e]);
+                for (int e = 0; e < NV; ++e) u[e] = add_ck4(scale4(at, u[e]), -at * bd, k4[e]);
             }
         }
         if (act && a.uq_nm == 0) {
@@ -396,28 +506,30 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_coef_kernel(const __grid_cons
                 *reinterpret_cast<float4 *>(ub + ((size_t)e * a.uq_nm + j) * 32 + ((s ^ (j & 7)) << 2)) = u[e];
         }
     }
-    __syncthreads();  // the weights, and this CTA's staged step values in the log
-    // the log terms lt_j[p] = sum_{t < K + j + 1} w_j[t] v_t[p], a value head at a time: its values
-    // staged in shared memory, one thread per (token, column)
-    const int m = K + T1;
-    float *svl = scw + (size_t)hpg * a.t1max * a.wcap;  // [m][dv]
-    const TI *lvr = static_cast<const TI *>(a.log_v) + (size_t)slot * a.wcap * a.H * a.dv;
-    for (int hl = 0; hl < hpg; ++hl) {
-        stage_rows(svl, lvr + (size_t)(h0 + hl) * a.dv, (size_t)a.H * a.dv, m, a.dv, tid, nthr);
-        __syncthreads();
-        for (int e = tid; e < T1 * a.dv; e += nthr) {
-            const int j = e / a.dv, p = e - j * a.dv;
-            const float *w = scw + ((size_t)hl * a.t1max + j) * a.wcap;
-            const int mj = K + j + 1;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains, so the loads overlap
-            int t = 0;
-            for (; t + 4 <= mj; t += 4)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) acc[u] = fmaf(w[t + u], svl[(size_t)(t + u) * a.dv + p], acc[u]);
-            for (; t < mj; ++t) acc[0] = fmaf(w[t], svl[(size_t)t * a.dv + p], acc[0]);
-            a.lt[(((size_t)i * a.H + h0 + hl) * a.t1max + j) * a.dv + p] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    __syncthreads();  // the weights
+    // the log terms lt_j[p] = sum_{t < K + j + 1} w_j[t] v_t[p] from the staged values; a thread takes
+    // four columns of a pair of step tokens (j0, j0 + 1) of one value head, so that one staged load serves
+    // eight products (j0's weight past its sweep is the zero written above)
+    const int nq = a.dv >> 2, npair = (T1 + 1) >> 1;
+    for (int e = tid; e < hpg * npair * nq; e += nthr) {
+        const int hl = e / (npair * nq), r2 = e - hl * (npair * nq), jp = r2 / nq, c = r2 - jp * nq;
+        const int j0 = 2 * jp, j1 = min(j0 + 1, T1 - 1);
+        const float *w0 = scw + ((size_t)hl * a.t1max + j0) * a.wcap;
+        const float *w1 = scw + ((size_t)hl * a.t1max + j1) * a.wcap;
+        float2 lo0 = make_float2(0.f, 0.f), hi0 = lo0, lo1 = lo0, hi1 = lo0;
+        const TI *vc = svr + (size_t)hl * a.dv + 4 * c;
+#pragma unroll 4
+        for (int t = 0; t < K + j1 + 1; ++t) {
+            const float4 v4 = lds4(vc + (size_t)t * hdv);
+            const float x0 = w0[t], x1 = w1[t];
+            lo0 = ffma2(make_float2(x0, x0), make_float2(v4.x, v4.y), lo0);
+            hi0 = ffma2(make_float2(x0, x0), make_float2(v4.z, v4.w), hi0);
+            lo1 = ffma2(make_float2(x1, x1), make_float2(v4.x, v4.y), lo1);
+            hi1 = ffma2(make_float2(x1, x1), make_float2(v4.z, v4.w), hi1);
         }
-        __syncthreads();
+        float *lt0 = a.lt + (((size_t)i * a.H + h0 + hl) * a.t1max + j0) * a.dv + 4 * c;
+        *reinterpret_cast<float4 *>(lt0) = make_float4(lo0.x, lo0.y, hi0.x, hi0.y);
+        if (j1 != j0) *reinterpret_cast<float4 *>(lt0 + a.dv) = make_float4(lo1.x, lo1.y, hi1.x, hi1.y);
     }
 }
 
@@ -1002,7 +1114,8 @@ ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float 
         if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             max_smem = 0;
         const int wcap = c.window - 1 + c.max_tokens, hpg = c.nheads / c.nkheads;
-        const size_t need = std::max({ssm::gdn_coef_smem(c.dk, c.dv, wcap, c.max_tokens, hpg),
+        const size_t need = std::max({ssm::gdn_coef_smem(c.dk, c.dv, wcap, c.max_tokens, hpg,
+                                                         c.input_dtype == SSM_DTYPE_BF16 ? 2 : 4),
                                       ssm::gdn_stream_smem(c.dk, c.dv, c.max_tokens),
                                       ssm::gdn_fold_smem(c.dk, c.dv, wcap)});
         if (max_smem > 0 && need + 1024 > (size_t)max_smem) return SSM_ERR_INVALID_ARG;
@@ -1142,7 +1255,8 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
     const ssm_gdn_pool_s &p = *pool;
     const size_t G = (size_t)p.cfg.nkheads, H = (size_t)p.cfg.nheads, dk = (size_t)p.cfg.dk, dv = (size_t)p.cfg.dv;
     const size_t ib = (size_t)p.in_b, T = (size_t)n_tok;
-    const size_t csm = ssm::gdn_coef_smem(p.cfg.dk, p.cfg.dv, p.wcap, p.cfg.max_tokens, p.cfg.nheads / p.cfg.nkheads);
+    const size_t csm =
+        ssm::gdn_coef_smem(p.cfg.dk, p.cfg.dv, p.wcap, p.cfg.max_tokens, p.cfg.nheads / p.cfg.nkheads, p.in_b);
     // the coefficient kernel's block: four sweeps a warp, at least four warps for the staging and the
     // log terms
     const int nsw = (p.cfg.nheads / p.cfg.nkheads) * n_tok;

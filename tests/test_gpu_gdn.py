@@ -109,6 +109,8 @@ def _run_verify(m, dt_in, H, G, dk, dv, W, T1, p, steps, slots, n_slots=8, force
     (synth.BF16, 8, 4, 128, 128, 16, 9, 0.8),
     (synth.BF16, 4, 2, 128, 128, 8, 5, 0.6),
     (synth.BF16, 4, 1, 64, 128, 32, 17, 0.9),
+    (synth.F32, 4, 2, 128, 128, 8, 5, 0.7),
+    (synth.BF16, 2, 1, 128, 128, 32, 17, 0.9),
 ])
 def test_replay_verify_and_commit_match_oracle(dt_in, H, G, dk, dv, W, T1, p):
     m = _mod()
