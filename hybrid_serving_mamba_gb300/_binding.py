@@ -41,6 +41,7 @@ EXPORTS = (
     "ssm_receipt_decode", "ssm_state_checkpoint_receipt", "ssm_state_restore_receipt",
     "ssm_gdn_init", "ssm_gdn_destroy", "ssm_gdn_reset", "ssm_gdn_decode_step", "ssm_gdn_verify_replay",
     "ssm_gdn_commit", "ssm_gdn_gather", "ssm_gdn_slot_info", "ssm_gdn_status", "ssm_gdn_last_path",
+    "ssm_gdn_last_commit_path",
 )
 
 
@@ -127,6 +128,7 @@ def _load():
         "ssm_gdn_gather": [V, I32, P_I32, V, V],
         "ssm_gdn_slot_info": [V, I32, P_I64, P_I32, ctypes.POINTER(U32), V],
         "ssm_gdn_last_path": [V],
+        "ssm_gdn_last_commit_path": [V],
         "ssm_gdn_status": [V, ctypes.POINTER(U32), I32, V],
     }
     for name, args in sig.items():
@@ -135,6 +137,7 @@ def _load():
         f.restype = ctypes.c_int
     lib.ssm_last_path.restype = ctypes.c_char_p
     lib.ssm_gdn_last_path.restype = ctypes.c_char_p
+    lib.ssm_gdn_last_commit_path.restype = ctypes.c_char_p
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_pool_bytes.restype = ctypes.c_size_t
     lib.ssm_receipt_bytes.argtypes = [I32, I32, I32]
@@ -555,6 +558,11 @@ def ssm_debug_stall_next_verify(pool: Pool) -> int:
 def ssm_gdn_last_path(pool) -> str:
     """Kernel path of the gated-delta-rule pool's last verify."""
     return _lib.ssm_gdn_last_path(pool.handle if pool is not None else None).decode()
+
+
+def ssm_gdn_last_commit_path(pool) -> str:
+    """Fold path of the gated-delta-rule pool's last commit."""
+    return _lib.ssm_gdn_last_commit_path(pool.handle if pool is not None else None).decode()
 
 
 def ssm_gdn_status(pool: GdnPool, clear: bool = False, stream=None):

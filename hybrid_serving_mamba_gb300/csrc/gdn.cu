@@ -36,6 +36,7 @@ namespace ssm {
 namespace {
 
 constexpr int kGdnMaxBatch = 1024;  // requests per launch: slot lists travel in kernel parameters
+constexpr int kGdnListCount = 4 * kGdnMaxBatch;  // the fold list's count, after its {request, slot, M, 0} entries
 constexpr int kGdnWarps = 8;
 constexpr int kGdnThreads = 32 * kGdnWarps;
 constexpr int kGdnMaxWindow = 32, kGdnMaxTokens = 32;
@@ -52,6 +53,7 @@ struct GdnArgs {
     int uq_rows;          // kernel's operand layout: [4 blocks of 32 columns][uq_nm rows][32], 16-byte chunk c
                           // of row j at c ^ (j % 8)
     int32_t *fold_m;      // commit: tokens to fold per request of the launch (0: none)
+    int32_t *fold_list;   // commit: the launch's folding requests {i, slot, M, 0}, their count at [kGdnListCount]
     const void *q, *k, *v;
     const float *g, *beta;
     void *y;
@@ -853,6 +855,7 @@ __global__ void gdn_commit_kernel(const __grid_constant__ GdnArgs a) {
         } else {
             a.fold_m[i] = K + c;
             a.log_len[slot] = 0;
+            reinterpret_cast<int4 *>(a.fold_list)[atomicAdd(&a.fold_list[kGdnListCount], 1)] = make_int4(i, slot, K + c, 0);
         }
     }
 }
@@ -944,6 +947,445 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_fold_kernel(const __grid_c
     }
 }
 
+// ---------------------------------------------------------------------------- fold, tensor cores
+//
+// gdn_fold_tc_kernel: the fold of bf16 pools with dk = dv = 128 and logs of at most 32 tokens, in the
+// chunked (WY) form of the delta rule instead of token after token.  With G_t = g_0 + ... + g_t, unrolling
+// S_t = e^{g_t} S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T from the checkpoint S gives
+//   S_t = e^{G_t} S + sum_{s <= t} e^{G_t - G_s} u_s k_s^T,   u_t = b_t v_t - b_t e^{g_t} S_{t-1} k_t,
+// and substituting S_{t-1} into u_t gives U (I + A) = Y over the M logged tokens, where
+//   Y[p][t] = b_t v_t[p] - b_t e^{G_t} (S k_t)[p],   A[s][t] = b_t e^{G_t - G_s} (k_s . k_t) for s < t, else 0,
+// so that
+//   S_M = e^{G_{M-1}} S + Y P,   P = (I + A)^{-1} D K,   D = diag(e^{G_{M-1} - G_s}),
+// K the M x dk keys.  I + A is unit upper triangular: P[s] = D_s k_s - sum_{t > s} A[s][t] P[t], from the
+// last token back.  The products run on the tensor cores (kind::tf32): the keys' Gram matrix K K^T (the
+// keys widened into the operand layout serve as both operands; A spans 128 rows, of which the 32 read
+// back are the keys), X = S K^T with the checkpoint boxes read in place as A (N = 32), then Y P with Y as
+// A (written over the keys once X is out) and P^T as B (K = the tokens, 8 an MMA).  e^{G_{M-1}} S is
+// added in fp32 by the epilogue, so only the update passes through tf32 (2^-10 of each product, as in
+// the verify's product); fp32 pools and longer logs keep the CUDA-core fold above.
+//
+// An item is one (folding request, value head) of the commit's list; a CTA an SM takes items in turn.
+// Warps: 0-3 epilogue (thread = row p, TMEM lane quarter w): Y from X; then S_M = e^{G_{M-1}} S + Y P in
+//          place in the staged boxes;
+//        4-7 coefficients, into a two-stage ring: the gates' running sums (base 2), the keys widened into
+//          the operand layout, the values; the Gram matrix (issued by warp 4's lane 0 as soon as the keys
+//          are in, into TMEM columns 256 b + 160 .. + 191, and read back by warp 4 from lanes 0-31); A
+//          and P^T.  The next item's loads are issued while an item is worked on;
+//        8 checkpoint producer (lane 0): an item's four 32-column boxes into a two-stage ring; it stores
+//          each item's new rows back by TMA once the epilogue has written them, and refills the stage
+//          once the store has read it;
+//        9 MMA issuer (lane 0) and TMEM owner: X into columns 256 b, Y P into 256 b + 32 .. + 159
+//          (b = item % 2).
+constexpr int kGfCoef = 4, kGfProd = 8, kGfMma = 9, kGfThreads = 10 * 32;
+constexpr int kGfMaxTok = 32;
+constexpr uint32_t kGfCols = 512;
+constexpr uint32_t kGfState = 65536;  // four 16 KiB boxes: 128 rows x 32 fp32 each
+
+// Per-item stage: keys [4 blocks][32 rows][32 fp32] in the B layout of S K^T (then Y [128 rows][32 fp32]),
+// P^T [128 rows][32 fp32], the values [32][128] bf16 as logged, A^T [32][32], and the scalars b_t,
+// b_t e^{G_t}, e^{G_{M-1} - G_t}, G_t ([4][32]) and e^{G_{M-1}}.
+struct GfLayout {
+    uint32_t keys, pt, vals, am, sc, aux, aux_base, bars, total;
+};
+__host__ __device__ constexpr GfLayout gf_layout() {
+    return GfLayout{0u,
+                    16384u,
+                    32768u,
+                    32768u + kGfMaxTok * 128u * 2u,
+                    32768u + kGfMaxTok * 128u * 2u + kGfMaxTok * kGfMaxTok * 4u,
+                    32768u + kGfMaxTok * 128u * 2u + kGfMaxTok * kGfMaxTok * 4u + 1024u,
+                    2u * kGfState,
+                    2u * kGfState + 2u * (32768u + kGfMaxTok * 128u * 2u + kGfMaxTok * kGfMaxTok * 4u + 1024u),
+                    2u * kGfState + 2u * (32768u + kGfMaxTok * 128u * 2u + kGfMaxTok * kGfMaxTok * 4u + 1024u) +
+                        32u * 8u + 1024u};
+}
+
+// The descriptor of an operand `bytes` past the one d was made for: the start address field (bits 0-13)
+// holds the address >> 4, and shared memory addresses stay below 2^18, so the field takes the sum.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+// Named barrier id over 128 threads that ORs a predicate.
+template <int ID>
+__device__ __forceinline__ bool gf_bar_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(ID)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kGfThreads, 1)
+    gdn_fold_tc_kernel(const __grid_constant__ GdnArgs a, const __grid_constant__ CUtensorMap tm_state) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ uint32_t s_abort, s_tmem;
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    constexpr GfLayout L = gf_layout();
+    const int H = a.H, dv = 128;
+    const int n_items = *reinterpret_cast<volatile const int32_t *>(&a.fold_list[kGdnListCount]) * H;
+    const int4 *list = reinterpret_cast<const int4 *>(a.fold_list);  // {request, slot, M, 0} per folding request
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *sfull = bars, *sready = bars + 2;  // checkpoint stages: loaded; new rows written
+    uint64_t *cfull = bars + 4, *cempty = bars + 6;  // coefficient stages
+    uint64_t *xdone = bars + 8, *yfull = bars + 10, *ddone = bars + 12, *tfree = bars + 14;  // TMEM buffers
+    uint64_t *kfull = bars + 16;  // the keys, values and scalars of a coefficient stage (before A and P^T)
+    uint64_t *gdone = bars + 18;  // the Gram matrix of a TMEM buffer
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 20; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+        s_abort = 0u;
+    }
+    if (warp == kGfMma) tc::tmem_alloc(&s_tmem, kGfCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == kGfProd) {
+        // ------------------------------------------------------------ checkpoint producer
+        // It also stores each item's new rows back (once the epilogue has written them) and reuses the stage
+        // once the store has read it.
+        if (lane == 0) {
+            int last[2] = {-1, -1};
+            auto store = [&](int v) -> bool {
+                const int b = v & 1;
+                if (!gt_wait(&sready[b], (uint32_t)(v >> 1) & 1u, &s_abort, a.flags)) return false;
+                const int item = blockIdx.x + v * gridDim.x;
+                const int f = item / H, h = item - f * H, slot = list[f].y;
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_store_2d(&tm_state, kb * 32, (slot * H + h) * dv, smem + (size_t)b * kGfState + kb * 16384);
+                bulk_commit();
+                bulk_wait_read0();
+                return true;
+            };
+            int u = 0;
+            bool ok = true;
+            for (;; ++u) {
+                const int item = blockIdx.x + u * gridDim.x;
+                if (item >= n_items) break;
+                const int f = item / H, h = item - f * H, slot = list[f].y;
+                const int b = u & 1;
+                if (u >= 2 && !(ok = store(u - 2))) break;
+                mbar_arrive_expect_tx(&sfull[b], kGfState);
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_load_2d(smem + (size_t)b * kGfState + kb * 16384, &tm_state, kb * 32, (slot * H + h) * dv,
+                                &sfull[b]);
+                last[b] = u;
+            }
+            for (int v = u >= 2 ? u - 2 : 0; ok && v < u; ++v) ok = store(v);
+            bulk_wait0();  // every store has landed before the CTA exits
+            for (int b = 0; b < 2; ++b)  // and no load is still landing
+                if (last[b] >= 0 && !mbar_wait(&sfull[b], (uint32_t)(last[b] >> 1) & 1u))
+                    atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else if (warp >= kGfCoef && warp < kGfCoef + 4) {
+        // ------------------------------------------------------------ coefficients
+        // An item's loads are issued while the item before it is worked on: its values by async copies into
+        // its stage (once the stage is free), its keys (eight 4-value pieces a thread: token t = ct / 32 + 4 j,
+        // column 4 (ct % 32)) and gates (warp 4, a lane a token) into registers.
+        const int ct = threadIdx.x - 32 * kGfCoef, c4 = ct & 31;
+        uint2 kraw[8];
+        float gn = 0.f, bn = 0.f;
+        int mn = 0;
+        // the list entry of the item the next issue() takes, loaded one call ahead
+        auto entry = [&](int u) -> int4 {
+            const int item = blockIdx.x + u * gridDim.x;
+            return item < n_items ? list[item / H] : make_int4(0, 0, 0, 0);
+        };
+        int4 fq = entry(0);
+        int gissued = -1;  // the last item whose Gram matrix this role issued, and whether it was waited for
+        bool gwaited = true;
+        auto issue = [&](int u) -> bool {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) return true;
+            const int4 fe = fq;
+            const int h = item - (item / H) * H, slot = fe.y, kh = h / a.hpg;
+            const int M = fe.z, b = u & 1;
+            mn = M;
+            const bool ok = u < 2 || gt_wait(&cempty[b], (uint32_t)((u >> 1) - 1) & 1u, &s_abort, a.flags);
+            if (gf_bar_or<2>(!ok)) return false;
+            unsigned char *X = smem + L.aux_base + (size_t)b * L.aux;
+            const __nv_bfloat16 *lv =
+                static_cast<const __nv_bfloat16 *>(a.log_v) + ((size_t)slot * a.wcap * H + h) * dv;
+            for (int e = ct; e < M * 16; e += 128) {  // 16-byte pieces of the M value rows
+                const int t = e >> 4, c = e & 15;
+                cp_async16(X + L.vals + t * 256 + c * 16, lv + (size_t)t * H * dv + c * 8);
+            }
+            cp_async_commit();
+            const __nv_bfloat16 *lk =
+                static_cast<const __nv_bfloat16 *>(a.log_k) + ((size_t)slot * a.wcap * a.G + kh) * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = (ct >> 5) + 4 * j;
+                kraw[j] = t < M ? *reinterpret_cast<const uint2 *>(lk + (size_t)t * a.G * 128 + 4 * c4) : make_uint2(0u, 0u);
+            }
+            if (ct < 32) {
+                const size_t o = ((size_t)slot * a.wcap + ct) * H + h;
+                gn = ct < M ? a.log_g[o] : 0.f;
+                bn = ct < M ? a.log_b[o] : 0.f;
+            }
+            fq = entry(u + 1);
+            return true;
+        };
+        bool alive = issue(0);
+        for (int u = 0; alive; ++u) {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) break;
+            const int M = mn;
+            const int b = u & 1;
+            unsigned char *X = smem + L.aux_base + (size_t)b * L.aux;
+            float *sc = reinterpret_cast<float *>(X + L.sc);
+            float *amt = reinterpret_cast<float *>(X + L.am);  // A^T [t][s]
+            if (ct < 32) {  // the gates' running sums, a lane a token (zero past M)
+                const int t = ct;
+                float G = gn;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float n = __shfl_up_sync(0xffffffffu, G, off);
+                    if (t >= off) G += n;
+                }
+                G *= 1.4426950408889634f;  // base 2 from here on
+                const float GM = __shfl_sync(0xffffffffu, G, M - 1);
+                sc[t] = bn;
+                sc[32 + t] = t < M ? bn * exp2f(G) : 0.f;
+                sc[64 + t] = t < M ? exp2f(GM - G) : 0.f;
+                sc[96 + t] = G;
+                if (t == 0) sc[128] = exp2f(GM);
+            }
+            // the keys widened into the operand layout (block n / 32, row t, 16-byte chunk ((n % 32) / 4) ^ (t % 8))
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = (ct >> 5) + 4 * j;
+                const uint2 r = kraw[j];
+                *reinterpret_cast<float4 *>(X + L.keys + (c4 >> 3) * 4096 + t * 128 + (((c4 & 7) ^ (t & 7)) << 4)) =
+                    make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u),
+                                __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xFFFF0000u));
+            }
+            cp_async_wait<0>();            // this item's values
+            tc::fence_proxy_async_smem();  // the keys are read by the tensor cores
+            bar_sync_named(2, 128);
+            if (ct == 0) {
+                mbar_arrive(&kfull[b]);
+                // the Gram matrix K K^T, issued here so that it starts at once (rows past 32 of A are not read back)
+                tc::fence_after_sync();
+                const uint32_t dg = tmem + 256u * (uint32_t)b + 160u;
+                const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(X) + L.keys, 1024);
+                constexpr uint32_t idg = tc::idesc_tf32_f32(128, 32);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t d = desc_at(dk0, kb * 4096 + 32 * kk);
+                        tc::mma_tf32(dg, d, d, idg, (kb | kk) != 0);
+                    }
+                tc::mma_commit(&gdone[b]);
+            }
+            gissued = u;
+            gwaited = false;
+            if (!issue(u + 1)) break;  // the next item's loads land during this one's work
+            {  // -A^T[t][s] (zero unless s < t < M) from the Gram matrix: warp 4's lane s copies row s out of
+               // TMEM into the P^T region (rows 33 floats apart, so that the copy and the reads below take
+               // every bank once), then thread (t, q) forms the entries s = 8q .. 8q + 7 of row t
+                float *graw = reinterpret_cast<float *>(X + L.pt);
+                bool okg = true;
+                if (ct < 32) {
+                    okg = gt_wait(&gdone[b], (uint32_t)(u >> 1) & 1u, &s_abort, a.flags);
+                    if (__all_sync(0xffffffffu, okg)) {
+                        tc::fence_after_sync();
+                        float gr[32];
+                        tc::tmem_ld32(tmem + 256u * (uint32_t)b + 160u, gr);
+#pragma unroll
+                        for (int t = 0; t < kGfMaxTok; ++t) graw[ct * 33 + t] = gr[t];
+                        tc::fence_before_sync();
+                    } else {
+                        okg = false;
+                    }
+                }
+                if (ct == 0 && okg) gwaited = true;
+                if (gf_bar_or<2>(!okg)) break;
+                const int t = ct >> 2, s0 = (ct & 3) * 8;
+                const float nbt = -sc[t], Gt = sc[96 + t];
+                float av[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (t < M)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (s0 + j < t) av[j] = nbt * exp2f(Gt - sc[96 + s0 + j]) * graw[(s0 + j) * 33 + t];
+                *reinterpret_cast<float4 *>(amt + t * kGfMaxTok + s0) = make_float4(av[0], av[1], av[2], av[3]);
+                *reinterpret_cast<float4 *>(amt + t * kGfMaxTok + s0 + 4) = make_float4(av[4], av[5], av[6], av[7]);
+                bar_sync_named(2, 128);
+            }
+            {  // P by back substitution, right-looking: thread n holds column n, r[s] = D_s k_s[n] less the
+               // later rows' shares; r[t] is final once every row after t is applied (rows past M come out
+               // zero: their D, A and keys are)
+                const int n = ct, cn = (n & 31) >> 2;
+                const unsigned char *kn = X + L.keys + (n >> 5) * 4096 + (n & 3) * 4;
+                float r[kGfMaxTok];
+#pragma unroll
+                for (int s2 = 0; s2 < kGfMaxTok; ++s2)
+                    r[s2] = s2 < M ? sc[64 + s2] * *reinterpret_cast<const float *>(kn + s2 * 128 + ((cn ^ (s2 & 7)) << 4))
+                                   : 0.f;
+#pragma unroll
+                for (int t = kGfMaxTok - 1; t >= 1; --t) {  // pairs of rows with the two-wide FMA
+                    const float2 pt = make_float2(r[t], r[t]);
+#pragma unroll
+                    for (int s4 = 0; s4 < kGfMaxTok; s4 += 4) {
+                        if (s4 < t) {
+                            const float4 av = *reinterpret_cast<const float4 *>(amt + t * kGfMaxTok + s4);
+                            if (s4 + 1 < t) {
+                                const float2 v = ffma2(make_float2(av.x, av.y), pt, make_float2(r[s4], r[s4 + 1]));
+                                r[s4] = v.x;
+                                r[s4 + 1] = v.y;
+                            } else {
+                                r[s4] = fmaf(av.x, pt.x, r[s4]);
+                            }
+                            if (s4 + 3 < t) {
+                                const float2 v = ffma2(make_float2(av.z, av.w), pt, make_float2(r[s4 + 2], r[s4 + 3]));
+                                r[s4 + 2] = v.x;
+                                r[s4 + 3] = v.y;
+                            } else if (s4 + 2 < t) {
+                                r[s4 + 2] = fmaf(av.z, pt.x, r[s4 + 2]);
+                            }
+                        }
+                    }
+                }
+                // P^T row n in the B layout of Y P (K = the tokens): chunk c holds tokens 4c .. 4c + 3
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4 *>(X + L.pt + n * 128 + ((c ^ (n & 7)) << 4)) =
+                        make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+            }
+            tc::fence_proxy_async_smem();  // P^T is read by the tensor cores
+            bar_sync_named(2, 128);
+            if (ct == 0) mbar_arrive(&cfull[b]);
+        }
+        cp_async_wait<0>();  // no copy may still be landing when the CTA exits
+        // every MMA this role issued has completed before TMEM is released
+        if (ct == 0 && !gwaited && !mbar_wait(&gdone[gissued & 1], (uint32_t)(gissued >> 1) & 1u))
+            atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+    } else if (warp == kGfMma) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idx = tc::idesc_tf32_f32(128, 32), idd = tc::idesc_tf32_f32(128, 128);
+            uint64_t *lastb = nullptr;
+            uint32_t lastph = 0;
+            for (int u = 0;; ++u) {
+                const int item = blockIdx.x + u * gridDim.x;
+                if (item >= n_items) break;
+                const int M = list[item / H].z;
+                const int b = u & 1;
+                const uint32_t ph = (uint32_t)(u >> 1) & 1u;
+                if (u >= 2 && !gt_wait(&tfree[b], ph ^ 1u, &s_abort, a.flags)) break;
+                if (!gt_wait(&kfull[b], ph, &s_abort, a.flags)) break;
+                tc::fence_after_sync();
+                const uint32_t sb = smem_addr(smem + (size_t)b * kGfState);
+                const uint32_t xb = smem_addr(smem + L.aux_base + (size_t)b * L.aux);
+                const uint32_t dx = tmem + 256u * (uint32_t)b, dd = dx + 32u;
+                if (!gt_wait(&sfull[b], ph, &s_abort, a.flags)) break;
+                tc::fence_after_sync();
+                const uint64_t ds0 = tc::smem_desc_sw128(sb, 1024), dk0 = tc::smem_desc_sw128(xb + L.keys, 1024);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // K = 8 tf32 per MMA
+                        tc::mma_tf32(dx, desc_at(ds0, kb * 16384 + 32 * kk), desc_at(dk0, kb * 4096 + 32 * kk), idx,
+                                     (kb | kk) != 0);
+                tc::mma_commit(&xdone[b]);
+                lastb = &xdone[b];
+                lastph = ph;
+                if (!gt_wait(&cfull[b], ph, &s_abort, a.flags)) break;
+                if (!gt_wait(&yfull[b], ph, &s_abort, a.flags)) break;
+                tc::fence_after_sync();
+                const uint64_t dp0 = tc::smem_desc_sw128(xb + L.pt, 1024);
+                for (int kk = 0; kk < (M + 7) / 8; ++kk)
+                    tc::mma_tf32(dd, desc_at(dk0, 32 * kk), desc_at(dp0, 32 * kk), idd, kk != 0);
+                tc::mma_commit(&ddone[b]);
+                lastb = &ddone[b];
+            }
+            // every MMA issued has completed before TMEM is released
+            if (lastb && !mbar_wait(lastb, lastph)) atomicOr(a.flags, SSM_FLAG_TIMEOUT);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ epilogue
+        const int p = threadIdx.x;
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        for (int u = 0;; ++u) {
+            const int item = blockIdx.x + u * gridDim.x;
+            if (item >= n_items) break;
+            const int M = list[item / H].z;
+            const int b = u & 1;
+            const uint32_t ph = (uint32_t)(u >> 1) & 1u;
+            unsigned char *X = smem + L.aux_base + (size_t)b * L.aux;
+            unsigned char *S = smem + (size_t)b * kGfState;
+            bool ok = gt_wait(&kfull[b], ph, &s_abort, a.flags) && gt_wait(&sfull[b], ph, &s_abort, a.flags) &&
+                      gt_wait(&xdone[b], ph, &s_abort, a.flags);
+            if (gf_bar_or<1>(!ok)) break;
+            tc::fence_after_sync();
+            float x[32];
+            tc::tmem_ld32(tmem + lane_off + 256u * (uint32_t)b, x);
+            const float *sc = reinterpret_cast<const float *>(X + L.sc);
+            const __nv_bfloat16 *vals = reinterpret_cast<const __nv_bfloat16 *>(X + L.vals);
+            const float gam = sc[128];
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+                x[t] = t < M ? fmaf(sc[t], __bfloat162float(vals[t * 128 + p]), -sc[32 + t] * x[t]) : 0.f;
+            // Y row p over the keys, once the coefficient warps are done with them (and X is out): chunk c
+            // holds tokens 4c .. 4c + 3
+            ok = gt_wait(&cfull[b], ph, &s_abort, a.flags);
+            if (gf_bar_or<1>(!ok)) break;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4 *>(X + L.keys + p * 128 + ((c ^ (p & 7)) << 4)) =
+                    make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            bar_sync_named(1, 128);
+            if (p == 0) mbar_arrive(&yfull[b]);
+            ok = gt_wait(&ddone[b], ph, &s_abort, a.flags);
+            if (gf_bar_or<1>(!ok)) break;
+            tc::fence_after_sync();
+            if (p == 0) mbar_arrive(&cempty[b]);  // Y and P^T are read; the values and scalars were read above
+            // S_M = e^{G_{M-1}} S + Y P, row p, in place in the staged boxes
+#pragma unroll 1
+            for (int kb = 0; kb < 4; ++kb) {
+                float d[32];
+                tc::tmem_ld32(tmem + lane_off + 256u * (uint32_t)b + 32u + 32u * (uint32_t)kb, d);
+                unsigned char *row = S + kb * 16384 + p * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float4 *q = reinterpret_cast<float4 *>(row + ((c ^ (p & 7)) << 4));
+                    float4 s4 = *q;
+                    s4.x = fmaf(gam, s4.x, d[4 * c]);
+                    s4.y = fmaf(gam, s4.y, d[4 * c + 1]);
+                    s4.z = fmaf(gam, s4.z, d[4 * c + 2]);
+                    s4.w = fmaf(gam, s4.w, d[4 * c + 3]);
+                    *q = s4;
+                }
+            }
+            tc::fence_before_sync();
+            tc::fence_proxy_async_smem();  // the new rows are read by the producer's TMA store
+            bar_sync_named(1, 128);
+            if (p == 0) {
+                mbar_arrive(&tfree[b]);
+                mbar_arrive(&sready[b]);
+            }
+        }
+    }
+    __syncwarp();  // warps whose lane 0 ran a role alone arrive at the block barrier converged
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kGfMma) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kGfCols);
+    }
+}
+
 // ---------------------------------------------------------------------------- reset and gather
 
 __global__ void gdn_reset_kernel(const __grid_constant__ GdnArgs a, size_t per_slot) {
@@ -978,7 +1420,7 @@ struct ssm_gdn_pool_s {
     float *state = nullptr;
     void *log_k = nullptr, *log_v = nullptr;
     float *log_g = nullptr, *log_b = nullptr, *uq = nullptr, *lt = nullptr;
-    int32_t *log_len = nullptr, *fold_m = nullptr;
+    int32_t *log_len = nullptr, *fold_m = nullptr, *fold_list = nullptr;
     int64_t *position = nullptr;
     uint32_t *slot_flags = nullptr, *flags = nullptr;
     std::vector<int> pending_ntok;  // tokens of each slot's last verify (0: none since its commit)
@@ -988,6 +1430,9 @@ struct ssm_gdn_pool_s {
     bool tc_ok = false;
     int uq_rows = 0;
     const char *last_path = "none";
+    // the tensor-core fold (the same boxes; logs of at most 32 tokens)
+    bool fold_tc_ok = false;
+    const char *commit_path = "none";
 };
 
 namespace ssm {
@@ -1008,7 +1453,7 @@ ssm_status gdn_cuda(cudaError_t e) { return e == cudaSuccess ? SSM_OK : SSM_ERR_
 
 void gdn_free(ssm_gdn_pool_s *p) {
     void *bufs[] = {p->state, p->log_k, p->log_v, p->log_g, p->log_b, p->uq, p->lt,
-                    p->log_len, p->fold_m, p->position, p->slot_flags, p->flags};
+                    p->log_len, p->fold_m, p->fold_list, p->position, p->slot_flags, p->flags};
     for (void *b : bufs)
         if (b) cudaFree(b);
 }
@@ -1033,6 +1478,7 @@ GdnArgs gdn_args(const ssm_gdn_pool_s &p) {
     a.uq = p.uq;
     a.lt = p.lt;
     a.fold_m = p.fold_m;
+    a.fold_list = p.fold_list;
     a.H = p.cfg.nheads;
     a.G = p.cfg.nkheads;
     a.hpg = p.cfg.nheads / p.cfg.nkheads;
@@ -1143,6 +1589,7 @@ ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float 
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->lt, sr * H * T * (size_t)c.dv);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->log_len, ns);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->fold_m, (size_t)ssm::kGdnMaxBatch);
+    if (e == cudaSuccess) e = ssm::gdn_alloc(&p->fold_list, (size_t)ssm::kGdnListCount + 1);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->position, ns);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->slot_flags, ns);
     if (e == cudaSuccess) e = ssm::gdn_alloc(&p->flags, 1);
@@ -1171,6 +1618,9 @@ ssm_status ssm_gdn_init(const ssm_gdn_config *cfg, int32_t n_slots, const float 
         p->tc_ok = enc && enc(&p->tm_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p->state, dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        int max_smem = 0;
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device);
+        p->fold_tc_ok = p->tc_ok && p->wcap <= ssm::kGfMaxTok && ssm::gf_layout().total <= (uint32_t)max_smem;
     }
     *out = p;
     return SSM_OK;
@@ -1343,13 +1793,26 @@ ssm_status ssm_gdn_commit(ssm_gdn_pool pool, int32_t batch, const int32_t *slots
     const ssm_gdn_pool_s &p = *pool;
     const size_t fsm = ssm::gdn_fold_smem(p.cfg.dk, p.cfg.dv, p.wcap);
     const unsigned H = (unsigned)p.cfg.nheads;
+    int sms = 1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
     st = ssm::gdn_batches(p, slots, batch, [&](GdnArgs &a, int base, int m) {
         a.accept = accept + base;
         a.force_fold = force_fold ? 1 : 0;
         for (int i = 0; i < m; ++i) a.ntok[i] = pool->pending_ntok[(size_t)slots[base + i]];
-        ssm::gdn_commit_kernel<<<1, 1024, 0, s>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = cudaMemsetAsync(p.fold_list + ssm::kGdnListCount, 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return e;
+        ssm::gdn_commit_kernel<<<1, 1024, 0, s>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (p.fold_tc_ok) {  // persistent over the listed (request, value head) items, one CTA an SM
+            const uint32_t gsm = ssm::gf_layout().total;
+            e = ssm::gdn_smem(ssm::gdn_fold_tc_kernel, gsm);
+            if (e != cudaSuccess) return e;
+            ssm::gdn_fold_tc_kernel<<<(unsigned)sms, ssm::kGfThreads, gsm, s>>>(a, p.tm_state);
+            pool->commit_path = "gdn_fold_tc";
+            return cudaGetLastError();
+        }
+        pool->commit_path = "gdn_fold";
         GDN_DISPATCH(p, {
             auto kf = ssm::gdn_fold_kernel<DK, TI>;
             e = ssm::gdn_smem(kf, fsm);
@@ -1383,6 +1846,8 @@ ssm_status ssm_gdn_slot_info(ssm_gdn_pool pool, int32_t slot, int64_t *position,
     if (flags) *flags = fl;
     return SSM_OK;
 }
+
+const char *ssm_gdn_last_commit_path(ssm_gdn_pool pool) { return pool ? pool->commit_path : "none"; }
 
 const char *ssm_gdn_last_path(ssm_gdn_pool pool) { return pool ? pool->last_path : "none"; }
 

@@ -88,7 +88,13 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
 /* Commit the last verify of each slot: c = 1 + accept[i] (device int32, in
  * [0, n_tok - 1]) tokens.  If log_len + c < W and !force_fold they join the
  * log; otherwise the log and they are applied to the checkpoint in order
- * and the log empties.  Rejected drafts never enter the log.  position += c. */
+ * and the log empties.  Rejected drafts never enter the log.  position += c.
+ * bf16 pools with dk = dv = 128 and W - 1 + max_tokens <= 32 fold in the
+ * chunked form on the tensor cores (Gated DeltaNet's WY form: the checkpoint
+ * times the keys, then a rank-M update from a triangular solve; the
+ * checkpoint's own decay is applied in fp32 and only the update takes tf32
+ * operands, at most 2^-10 of each product); other pools fold token by token
+ * in fp32 on the CUDA cores. */
 ssm_status ssm_gdn_commit(ssm_gdn_pool pool, int32_t batch, const int32_t *slots, const int32_t *accept,
                           int32_t force_fold, ssm_stream_t stream);
 
@@ -105,6 +111,10 @@ ssm_status ssm_gdn_status(ssm_gdn_pool pool, uint32_t *flags_out, int32_t clear,
 /* Kernel path of the pool's last verify: "gdn_verify_tc" (tensor cores),
  * "gdn_verify" (CUDA cores) or "none".  The string is static. */
 const char *ssm_gdn_last_path(ssm_gdn_pool pool);
+
+/* Fold path of the pool's last commit: "gdn_fold_tc" (tensor cores),
+ * "gdn_fold" (CUDA cores) or "none".  The string is static. */
+const char *ssm_gdn_last_commit_path(ssm_gdn_pool pool);
 
 #ifdef __cplusplus
 }

@@ -96,6 +96,9 @@ def _run_verify(m, dt_in, H, G, dk, dv, W, T1, p, steps, slots, n_slots=8, force
         a = torch.from_numpy(np.ascontiguousarray(acc[s], dtype=np.int32)).cuda()
         ff = s in force_at
         assert m.ssm_gdn_commit(pool, slots, a, ff) == m.SSM_OK
+        # bf16 pools with 128 x 128 heads and logs of at most 32 tokens fold on the tensor cores
+        fold_tc = dt_in == synth.BF16 and dk == 128 and dv == 128 and W - 1 + T1 <= 32
+        assert m.ssm_gdn_last_commit_path(pool) == ("gdn_fold_tc" if fold_tc else "gdn_fold")
         folds += len(opool.commit(slots, acc[s], force_fold=ff))
         for sl in slots:
             st, pos, ll, fl = m.ssm_gdn_slot_info(pool, sl)
@@ -111,6 +114,7 @@ def _run_verify(m, dt_in, H, G, dk, dv, W, T1, p, steps, slots, n_slots=8, force
     (synth.BF16, 4, 1, 64, 128, 32, 17, 0.9),
     (synth.F32, 4, 2, 128, 128, 8, 5, 0.7),
     (synth.BF16, 2, 1, 128, 128, 32, 17, 0.9),
+    (synth.BF16, 4, 2, 128, 128, 16, 17, 0.95),
 ])
 def test_replay_verify_and_commit_match_oracle(dt_in, H, G, dk, dv, W, T1, p):
     m = _mod()
@@ -234,7 +238,9 @@ def test_full_size_sampled_requests():
             yo = opool.verify(list(range(len(sample))), *(a[sample] for a in _wide(parts, dt_in)))
             check_close(to_host(y)[sample], yo, dt_in, f"sampled y step {s}", positions_axis=1, cond=opool.last_cond)
             assert m.ssm_gdn_commit(pool, slots, torch.from_numpy(acc[s]).cuda()) == m.SSM_OK
+            assert m.ssm_gdn_last_commit_path(pool) == "gdn_fold_tc"
             opool.commit(list(range(len(sample))), acc[s][sample])
         assert m.ssm_gdn_status(pool)[1] == 0
+        check_close(_states(m, pool, sample), opool.state, dt_in, "sampled checkpoints")
     finally:
         m.ssm_gdn_destroy(pool)
