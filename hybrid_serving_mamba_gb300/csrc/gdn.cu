@@ -24,6 +24,7 @@
 // step after the log; a streaming kernel then reads each checkpoint row once
 // for all step tokens.
 #include <algorithm>
+#include <utility>
 #include <cstring>
 #include <vector>
 
@@ -345,8 +346,10 @@ __global__ void __launch_bounds__(kGdnThreads, 4) gdn_coef_kernel(const __grid_c
     const int nthr = blockDim.x, nwarps = nthr >> 5;  // sized by the host to the sweeps
     const int T1 = a.n_tok;
     // the tensor-core streaming kernel may start its checkpoint loads as this grid drains; it waits for
-    // this grid's completion before it reads anything written here
+    // this grid's completion before it reads anything written here.  This grid may itself start as the
+    // previous commit's fold drains: nothing is read before that grid has completed.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (a.slot_flags[slot] & kSlotPoisoned) {
         if (tid == 0) atomicOr(a.flags, SSM_FLAG_POISONED_SLOT);
         return;
@@ -834,8 +837,12 @@ __global__ void __launch_bounds__(kGtThreads, 1)
 
 // ---------------------------------------------------------------------------- commit and fold
 
-// One CTA: per request, append the kept tokens to the log or mark the request for a fold.
+// One CTA: per request, append the kept tokens to the log or mark the request for a fold (and list it).
 __global__ void gdn_commit_kernel(const __grid_constant__ GdnArgs a) {
+    // the fold may be scheduled now: it waits for this grid before it reads the list
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) a.fold_list[kGdnListCount] = 0;
+    __syncthreads();
     for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
         const int slot = a.slots[i];
         a.fold_m[i] = 0;
@@ -1027,7 +1034,6 @@ __global__ void __launch_bounds__(kGfThreads, 1)
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     constexpr GfLayout L = gf_layout();
     const int H = a.H, dv = 128;
-    const int n_items = *reinterpret_cast<volatile const int32_t *>(&a.fold_list[kGdnListCount]) * H;
     const int4 *list = reinterpret_cast<const int4 *>(a.fold_list);  // {request, slot, M, 0} per folding request
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *sfull = bars, *sready = bars + 2;  // checkpoint stages: loaded; new rows written
@@ -1047,6 +1053,12 @@ __global__ void __launch_bounds__(kGfThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = s_tmem;
+    // launched programmatically after the commit kernel: the set-up above ran under it; its list is read
+    // once it has completed.  The next verify's coefficient kernel may be scheduled meanwhile (it waits
+    // for this grid before reading anything).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int n_items = *reinterpret_cast<volatile const int32_t *>(&a.fold_list[kGdnListCount]) * H;
 
     if (warp == kGfProd) {
         // ------------------------------------------------------------ checkpoint producer
@@ -1511,6 +1523,24 @@ cudaError_t gdn_smem(Kernel k, size_t bytes) {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// A launch that may begin while the stream's previous kernel drains (programmatic dependent launch):
+// the kernel waits for that grid (griddepcontrol.wait) before it reads anything the grid writes.
+template <typename... KArgs, typename... Args>
+cudaError_t gdn_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                           Args &&...args) {
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
+
 // dk and the input type as template arguments
 #define GDN_DISPATCH(p, ...)                                                                   \
     do {                                                                                       \
@@ -1748,24 +1778,14 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
             auto ks = ssm::gdn_stream_kernel<DK, TI>;
             e = ssm::gdn_smem(kc, csm);
             if (e == cudaSuccess) e = ssm::gdn_smem(ks, ssm_);
+            if (e == cudaSuccess) e = ssm::gdn_launch_pdl(kc, dim3((unsigned)G, m), dim3(coef_threads), csm, s, a);
             if (e == cudaSuccess) {
-                kc<<<dim3((unsigned)G, m), coef_threads, csm, s>>>(a);
                 if (nring) {  // bf16, dk = dv = 128: the tensor-core streaming kernel
                     auto kt = NM == 16 ? ssm::gdn_stream_tc_kernel<16> : ssm::gdn_stream_tc_kernel<32>;
                     e = ssm::gdn_smem(kt, tsm);
-                    if (e == cudaSuccess) {
-                        cudaLaunchConfig_t lc = {};
-                        cudaLaunchAttribute attr[1];
-                        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-                        attr[0].val.programmaticStreamSerializationAllowed = 1;
-                        lc.gridDim = dim3((unsigned)std::min<size_t>((size_t)m * H, (size_t)sms));
-                        lc.blockDim = dim3(ssm::kGtThreads);
-                        lc.dynamicSmemBytes = tsm;
-                        lc.stream = s;
-                        lc.attrs = attr;
-                        lc.numAttrs = 1;
-                        e = cudaLaunchKernelEx(&lc, kt, a, p.tm_state, nring);
-                    }
+                    if (e == cudaSuccess)
+                        e = ssm::gdn_launch_pdl(kt, dim3((unsigned)std::min<size_t>((size_t)m * H, (size_t)sms)),
+                                                dim3(ssm::kGtThreads), tsm, s, a, p.tm_state, nring);
                 } else {
                     ks<<<dim3((unsigned)H, m), ssm::kGdnThreads, ssm_, s>>>(a);
                 }
@@ -1799,18 +1819,17 @@ ssm_status ssm_gdn_commit(ssm_gdn_pool pool, int32_t batch, const int32_t *slots
         a.accept = accept + base;
         a.force_fold = force_fold ? 1 : 0;
         for (int i = 0; i < m; ++i) a.ntok[i] = pool->pending_ntok[(size_t)slots[base + i]];
-        cudaError_t e = cudaMemsetAsync(p.fold_list + ssm::kGdnListCount, 0, sizeof(int32_t), s);
-        if (e != cudaSuccess) return e;
         ssm::gdn_commit_kernel<<<1, 1024, 0, s>>>(a);
-        e = cudaGetLastError();
+        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (p.fold_tc_ok) {  // persistent over the listed (request, value head) items, one CTA an SM
             const uint32_t gsm = ssm::gf_layout().total;
             e = ssm::gdn_smem(ssm::gdn_fold_tc_kernel, gsm);
             if (e != cudaSuccess) return e;
-            ssm::gdn_fold_tc_kernel<<<(unsigned)sms, ssm::kGfThreads, gsm, s>>>(a, p.tm_state);
+            e = ssm::gdn_launch_pdl(ssm::gdn_fold_tc_kernel, dim3((unsigned)sms), dim3(ssm::kGfThreads), gsm, s, a,
+                                    p.tm_state);
             pool->commit_path = "gdn_fold_tc";
-            return cudaGetLastError();
+            return e;
         }
         pool->commit_path = "gdn_fold";
         GDN_DISPATCH(p, {
