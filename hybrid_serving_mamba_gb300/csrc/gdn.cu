@@ -976,14 +976,13 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_fold_kernel(const __grid_c
 // Warps: 0-3 epilogue (thread = row p, TMEM lane quarter w): Y from X; then S_M = e^{G_{M-1}} S + Y P in
 //          place in the staged boxes;
 //        4-7 coefficients, into a two-stage ring: the gates' running sums (base 2), the keys widened into
-//          the operand layout, the values; the Gram matrix (issued by warp 4's lane 0 as soon as the keys
-//          are in, into TMEM columns 256 b + 160 .. + 191, and read back by warp 4 from lanes 0-31); A
-//          and P^T.  The next item's loads are issued while an item is worked on;
+//          the operand layout, the values; A from the Gram matrix (read back by warp 4 from TMEM lanes
+//          0-31) and P^T.  The next item's loads are issued while an item is worked on;
 //        8 checkpoint producer (lane 0): an item's four 32-column boxes into a two-stage ring; it stores
 //          each item's new rows back by TMA once the epilogue has written them, and refills the stage
 //          once the store has read it;
-//        9 MMA issuer (lane 0) and TMEM owner: X into columns 256 b, Y P into 256 b + 32 .. + 159
-//          (b = item % 2).
+//        9 MMA issuer (lane 0) and TMEM owner: the Gram matrix as soon as the keys are in, into columns
+//          256 b + 160 .. + 191; X into 256 b; Y P into 256 b + 32 .. + 159 (b = item % 2).
 constexpr int kGfCoef = 4, kGfProd = 8, kGfMma = 9, kGfThreads = 10 * 32;
 constexpr int kGfMaxTok = 32;
 constexpr uint32_t kGfCols = 512;
@@ -1025,6 +1024,49 @@ __device__ __forceinline__ bool gf_bar_or(bool pred) {
         : "r"((uint32_t)pred), "n"(ID)
         : "memory");
     return r != 0;
+}
+
+// P by back substitution, right-looking: thread n holds column n, r[s] = D_s k_s[n] less the later rows'
+// shares, r[t] final once every row after t is applied (the coefficient table holds -A^T); tokens from
+// B on are zero (M <= B), and P^T row n goes to the B layout of Y P (chunk c: tokens 4c .. 4c + 3).
+template <int B>
+__device__ __forceinline__ void gf_solve(unsigned char *X, const GfLayout &L, int n, int M) {
+    const float *sc = reinterpret_cast<const float *>(X + L.sc);
+    const float *amt = reinterpret_cast<const float *>(X + L.am);
+    const int cn = (n & 31) >> 2;
+    const unsigned char *kn = X + L.keys + (n >> 5) * 4096 + (n & 3) * 4;
+    float r[B];
+#pragma unroll
+    for (int s = 0; s < B; ++s)
+        r[s] = s < M ? sc[64 + s] * *reinterpret_cast<const float *>(kn + s * 128 + ((cn ^ (s & 7)) << 4)) : 0.f;
+#pragma unroll
+    for (int t = B - 1; t >= 1; --t) {  // pairs of rows with the two-wide FMA
+        const float2 pt = make_float2(r[t], r[t]);
+#pragma unroll
+        for (int s4 = 0; s4 < B; s4 += 4) {
+            if (s4 < t) {
+                const float4 av = *reinterpret_cast<const float4 *>(amt + t * kGfMaxTok + s4);
+                if (s4 + 1 < t) {
+                    const float2 v = ffma2(make_float2(av.x, av.y), pt, make_float2(r[s4], r[s4 + 1]));
+                    r[s4] = v.x;
+                    r[s4 + 1] = v.y;
+                } else {
+                    r[s4] = fmaf(av.x, pt.x, r[s4]);
+                }
+                if (s4 + 3 < t) {
+                    const float2 v = ffma2(make_float2(av.z, av.w), pt, make_float2(r[s4 + 2], r[s4 + 3]));
+                    r[s4 + 2] = v.x;
+                    r[s4 + 3] = v.y;
+                } else if (s4 + 2 < t) {
+                    r[s4 + 2] = fmaf(av.z, pt.x, r[s4 + 2]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4 *>(X + L.pt + n * 128 + ((c ^ (n & 7)) << 4)) =
+            4 * c < B ? make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void __launch_bounds__(kGfThreads, 1)
@@ -1112,8 +1154,6 @@ __global__ void __launch_bounds__(kGfThreads, 1)
             return item < n_items ? list[item / H] : make_int4(0, 0, 0, 0);
         };
         int4 fq = entry(0);
-        int gissued = -1;  // the last item whose Gram matrix this role issued, and whether it was waited for
-        bool gwaited = true;
         auto issue = [&](int u) -> bool {
             const int item = blockIdx.x + u * gridDim.x;
             if (item >= n_items) return true;
@@ -1183,24 +1223,7 @@ __global__ void __launch_bounds__(kGfThreads, 1)
             cp_async_wait<0>();            // this item's values
             tc::fence_proxy_async_smem();  // the keys are read by the tensor cores
             bar_sync_named(2, 128);
-            if (ct == 0) {
-                mbar_arrive(&kfull[b]);
-                // the Gram matrix K K^T, issued here so that it starts at once (rows past 32 of A are not read back)
-                tc::fence_after_sync();
-                const uint32_t dg = tmem + 256u * (uint32_t)b + 160u;
-                const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(X) + L.keys, 1024);
-                constexpr uint32_t idg = tc::idesc_tf32_f32(128, 32);
-#pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t d = desc_at(dk0, kb * 4096 + 32 * kk);
-                        tc::mma_tf32(dg, d, d, idg, (kb | kk) != 0);
-                    }
-                tc::mma_commit(&gdone[b]);
-            }
-            gissued = u;
-            gwaited = false;
+            if (ct == 0) mbar_arrive(&kfull[b]);  // the MMA warp starts the Gram matrix at once
             if (!issue(u + 1)) break;  // the next item's loads land during this one's work
             {  // -A^T[t][s] (zero unless s < t < M) from the Gram matrix: warp 4's lane s copies row s out of
                // TMEM into the P^T region (rows 33 floats apart, so that the copy and the reads below take
@@ -1220,7 +1243,6 @@ __global__ void __launch_bounds__(kGfThreads, 1)
                         okg = false;
                     }
                 }
-                if (ct == 0 && okg) gwaited = true;
                 if (gf_bar_or<2>(!okg)) break;
                 const int t = ct >> 2, s0 = (ct & 3) * 8;
                 const float nbt = -sc[t], Gt = sc[96 + t];
@@ -1233,54 +1255,18 @@ __global__ void __launch_bounds__(kGfThreads, 1)
                 *reinterpret_cast<float4 *>(amt + t * kGfMaxTok + s0 + 4) = make_float4(av[4], av[5], av[6], av[7]);
                 bar_sync_named(2, 128);
             }
-            {  // P by back substitution, right-looking: thread n holds column n, r[s] = D_s k_s[n] less the
-               // later rows' shares; r[t] is final once every row after t is applied (rows past M come out
-               // zero: their D, A and keys are)
-                const int n = ct, cn = (n & 31) >> 2;
-                const unsigned char *kn = X + L.keys + (n >> 5) * 4096 + (n & 3) * 4;
-                float r[kGfMaxTok];
-#pragma unroll
-                for (int s2 = 0; s2 < kGfMaxTok; ++s2)
-                    r[s2] = s2 < M ? sc[64 + s2] * *reinterpret_cast<const float *>(kn + s2 * 128 + ((cn ^ (s2 & 7)) << 4))
-                                   : 0.f;
-#pragma unroll
-                for (int t = kGfMaxTok - 1; t >= 1; --t) {  // pairs of rows with the two-wide FMA
-                    const float2 pt = make_float2(r[t], r[t]);
-#pragma unroll
-                    for (int s4 = 0; s4 < kGfMaxTok; s4 += 4) {
-                        if (s4 < t) {
-                            const float4 av = *reinterpret_cast<const float4 *>(amt + t * kGfMaxTok + s4);
-                            if (s4 + 1 < t) {
-                                const float2 v = ffma2(make_float2(av.x, av.y), pt, make_float2(r[s4], r[s4 + 1]));
-                                r[s4] = v.x;
-                                r[s4 + 1] = v.y;
-                            } else {
-                                r[s4] = fmaf(av.x, pt.x, r[s4]);
-                            }
-                            if (s4 + 3 < t) {
-                                const float2 v = ffma2(make_float2(av.z, av.w), pt, make_float2(r[s4 + 2], r[s4 + 3]));
-                                r[s4 + 2] = v.x;
-                                r[s4 + 3] = v.y;
-                            } else if (s4 + 2 < t) {
-                                r[s4 + 2] = fmaf(av.z, pt.x, r[s4 + 2]);
-                            }
-                        }
-                    }
-                }
-                // P^T row n in the B layout of Y P (K = the tokens): chunk c holds tokens 4c .. 4c + 3
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(X + L.pt + n * 128 + ((c ^ (n & 7)) << 4)) =
-                        make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+            // P by back substitution (rows past M come out zero), at the item's token bound
+            switch ((M + 7) >> 3) {
+            case 1: gf_solve<8>(X, L, ct, M); break;
+            case 2: gf_solve<16>(X, L, ct, M); break;
+            case 3: gf_solve<24>(X, L, ct, M); break;
+            default: gf_solve<32>(X, L, ct, M); break;
             }
             tc::fence_proxy_async_smem();  // P^T is read by the tensor cores
             bar_sync_named(2, 128);
             if (ct == 0) mbar_arrive(&cfull[b]);
         }
         cp_async_wait<0>();  // no copy may still be landing when the CTA exits
-        // every MMA this role issued has completed before TMEM is released
-        if (ct == 0 && !gwaited && !mbar_wait(&gdone[gissued & 1], (uint32_t)(gissued >> 1) & 1u))
-            atomicOr(a.flags, SSM_FLAG_TIMEOUT);
     } else if (warp == kGfMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -1298,10 +1284,21 @@ __global__ void __launch_bounds__(kGfThreads, 1)
                 tc::fence_after_sync();
                 const uint32_t sb = smem_addr(smem + (size_t)b * kGfState);
                 const uint32_t xb = smem_addr(smem + L.aux_base + (size_t)b * L.aux);
-                const uint32_t dx = tmem + 256u * (uint32_t)b, dd = dx + 32u;
+                const uint32_t dx = tmem + 256u * (uint32_t)b, dd = dx + 32u, dg = dx + 160u;
+                const uint64_t dk0 = tc::smem_desc_sw128(xb + L.keys, 1024);
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb)  // the Gram matrix: rows past 32 of A are not read back
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t d = desc_at(dk0, kb * 4096 + 32 * kk);
+                        tc::mma_tf32(dg, d, d, idx, (kb | kk) != 0);
+                    }
+                tc::mma_commit(&gdone[b]);
+                lastb = &gdone[b];
+                lastph = ph;
                 if (!gt_wait(&sfull[b], ph, &s_abort, a.flags)) break;
                 tc::fence_after_sync();
-                const uint64_t ds0 = tc::smem_desc_sw128(sb, 1024), dk0 = tc::smem_desc_sw128(xb + L.keys, 1024);
+                const uint64_t ds0 = tc::smem_desc_sw128(sb, 1024);
 #pragma unroll
                 for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
