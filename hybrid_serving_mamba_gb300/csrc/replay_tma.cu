@@ -94,8 +94,27 @@ __host__ __device__ inline size_t gcoef_x_offset(int T1, int mmax, int N, int nw
     f = (f + 1) & ~(size_t)1;
     return (f * 4 + (size_t)nwarps * mmax * 8 + 15) & ~(size_t)15;
 }
-__host__ __device__ inline size_t gcoef_smem_bytes(int T1, int mmax, int N, int nwarps, size_t xbytes) {
-    return gcoef_x_offset(T1, mmax, N, nwarps) + xbytes;
+// After the step's x: for bf16 inputs C [T1][N] and B [mmax][N] as given (fp32 inputs land in place), then
+// the dt of the window's positions for the group's heads [hpg][mmax].
+struct GcoefLayout {
+    size_t craw, braw, dta, total;
+};
+__host__ __device__ inline GcoefLayout gcoef_layout(int T1, int mmax, int N, int nwarps, size_t xbytes, int in_b,
+                                                    int hpg) {
+    GcoefLayout L;
+    size_t o = (gcoef_x_offset(T1, mmax, N, nwarps) + xbytes + 15) & ~(size_t)15;
+    L.craw = o;
+    if (in_b == 2) o += (size_t)T1 * N * 2;
+    L.braw = o;
+    if (in_b == 2) o += (size_t)mmax * N * 2;
+    L.dta = o;
+    o += (size_t)hpg * mmax * 4;
+    L.total = o;
+    return L;
+}
+__host__ __device__ inline size_t gcoef_smem_bytes(int T1, int mmax, int N, int nwarps, size_t xbytes, int in_b,
+                                                   int hpg) {
+    return gcoef_layout(T1, mmax, N, nwarps, xbytes, in_b, hpg).total;
 }
 
 // Rows of x, B, C are moved 16 bytes at a time: the launcher checks that
@@ -135,7 +154,6 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
     float *sC = reinterpret_cast<float *>(smem4);
     float *sB = sC + (size_t)T1 * N;
     float *sCB = sB + (size_t)mmax * N;
-    float *sDt = sCB + (size_t)T1 * mmax;
     size_t off = (size_t)T1 * N + (size_t)mmax * N + (size_t)T1 * mmax + (size_t)nwarps * mmax;
     off = (off + 1) & ~(size_t)1;
     Sum2 *sCum = reinterpret_cast<Sum2 *>(reinterpret_cast<float *>(smem4) + off);
@@ -174,12 +192,44 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
         const int kb = n >> 5, c = (n & 31) >> 2;
         return cf + ((size_t)kb * nm + j) * 32 + ((c ^ (j & 7)) << 2);
     };
+    // every load of the CTA in flight at once: C and B rows (the log's, then the step's) as 16-byte async
+    // copies into shared memory (fp32 inputs straight into place, bf16 beside and widened below), and the
+    // dt of the window's positions for the group's heads, the step's checked and staged after the log
+    const GcoefLayout GL = gcoef_layout(T1, mmax, N, nwarps, (size_t)T1 * xrow, (int)sizeof(TI), hpg);
+    unsigned char *sbytes = reinterpret_cast<unsigned char *>(smem4);
+    TI *rC = sizeof(TI) == 2 ? reinterpret_cast<TI *>(sbytes + GL.craw) : reinterpret_cast<TI *>(sC);
+    TI *rB = sizeof(TI) == 2 ? reinterpret_cast<TI *>(sbytes + GL.braw) : reinterpret_cast<TI *>(sB);
+    float *sDa = reinterpret_cast<float *>(sbytes + GL.dta);  // [hpg][mmax]
+    for (int e = threadIdx.x; e < T1 * NV; e += blockDim.x) {
+        const int j = e / NV, q = e - j * NV;
+        cp_async16(rC + (size_t)j * N + q * EV, stepC + (((size_t)i * T1 + j) * a.G + g) * N + q * EV);
+    }
+    for (int e = threadIdx.x; e < m * NV; e += blockDim.x) {
+        const int s = e / NV, q = e - s * NV;
+        cp_async16(rB + (size_t)s * N + q * EV, s < k ? lB + ((size_t)s * a.G + g) * N + q * EV
+                                                      : stepB + (((size_t)i * T1 + (s - k)) * a.G + g) * N + q * EV);
+    }
+    cp_async_commit();
+    for (int e = threadIdx.x; e < hpg * m; e += blockDim.x) {
+        const int hh = e / m, s = e - hh * m, h = g * hpg + hh;
+        float d;
+        if (s < k) {
+            d = a.log_dt[((size_t)slot * a.wcap + s) * H + h];
+        } else {
+            d = load_dt(a.dt, ((size_t)i * T1 + (s - k)) * H + h, a.dt_bf16);
+            bad |= !isfinite(d);
+            a.log_dt[((size_t)slot * a.wcap + kl + (s - k)) * H + h] = d;
+        }
+        sDa[(size_t)hh * mmax + s] = d;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
     for (int e = threadIdx.x; e < T1 * NV; e += blockDim.x) {  // C rows, also kept in fp32
         const int j = e / NV, q = e - j * NV;
-        const uint4 v = *reinterpret_cast<const uint4 *>(stepC + (((size_t)i * T1 + j) * a.G + g) * N + q * EV);
+        const uint4 v = *reinterpret_cast<const uint4 *>(rC + (size_t)j * N + q * EV);
         bad |= V::nonfinite(v);
         float *o = sC + (size_t)j * N + q * EV;
-        V::widen(v, o);
+        if (sizeof(TI) == 2) V::widen(v, o);
         if (bf_op) {
             *reinterpret_cast<uint4 *>(cfb_chunk(j, q * EV)) = v;
         } else {
@@ -201,21 +251,12 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
     }
     for (int e = threadIdx.x; e < m * NV; e += blockDim.x) {  // B rows: the log, then the step
         const int s = e / NV, q = e - s * NV;
-        uint4 v;
-        if (s < k) {
-            v = *reinterpret_cast<const uint4 *>(lB + ((size_t)s * a.G + g) * N + q * EV);
-        } else {
-            v = *reinterpret_cast<const uint4 *>(stepB + (((size_t)i * T1 + (s - k)) * a.G + g) * N + q * EV);
+        const uint4 v = *reinterpret_cast<const uint4 *>(rB + (size_t)s * N + q * EV);
+        if (s >= k) {
             bad |= V::nonfinite(v);
             *reinterpret_cast<uint4 *>(wB + ((size_t)lrow(s) * a.G + g) * N + q * EV) = v;  // staged after the log
         }
-        V::widen(v, sB + (size_t)s * N + q * EV);
-    }
-    for (int e = threadIdx.x; e < T1 * hpg; e += blockDim.x) {  // the step's dt, staged after the log
-        const int t = e / hpg, h = g * hpg + (e - t * hpg);
-        const float d = load_dt(a.dt, ((size_t)i * T1 + t) * H + h, a.dt_bf16);
-        bad |= !isfinite(d);
-        a.log_dt[((size_t)slot * a.wcap + kl + t) * H + h] = d;
+        if (sizeof(TI) == 2) V::widen(v, sB + (size_t)s * N + q * EV);
     }
     {  // the step's x, once landed: the non-finite check
         __syncthreads();  // the barrier's initialisation is visible to every thread
@@ -254,13 +295,11 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
         sCB[(size_t)j * mmax + s] = v;
     }
     __syncthreads();
-    float *dts = sDt + (size_t)warp * mmax;
     Sum2 *cum = sCum + (size_t)warp * mmax;
     for (int hh = warp; hh < hpg; hh += nwarps) {
         const int h = g * hpg + hh;
         const float A = a.A[h], D = a.D[h];
-        for (int s = lane; s < m; s += 32) dts[s] = a.log_dt[((size_t)slot * a.wcap + lrow(s)) * H + h];
-        __syncwarp();
+        const float *dts = sDa + (size_t)hh * mmax;
         warp_prefix_sum2(dts, cum, m, lane);  // differences of these are exact to fp32
         __syncwarp();
         // W rows over the whole stride: zero past k + j, so readers need no bound
@@ -1111,7 +1150,7 @@ bool replay_tma_encode(Pool &p) {
 
 size_t replay_coef_smem_bytes(const Pool &pool, int n_tok) {
     return gcoef_smem_bytes(n_tok, pool.wcap - pool.t1max + n_tok, pool.N, kCoefThreads / 32,
-                            (size_t)n_tok * pool.hpg * pool.P * pool.in_bytes);
+                            (size_t)n_tok * pool.hpg * pool.P * pool.in_bytes, pool.in_bytes, pool.hpg);
 }
 
 cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaStream_t s, const char **path) {
