@@ -24,6 +24,7 @@
 // step after the log; a streaming kernel then reads each checkpoint row once
 // for all step tokens.
 #include <algorithm>
+#include <type_traits>
 #include <utility>
 #include <cstring>
 #include <vector>
@@ -472,23 +473,33 @@ __global__ void __launch_bounds__(kGdnThreads, 4) gdn_coef_kernel(const __grid_c
         // the weight just past the sweep is zero: the log terms below take step tokens in pairs over the
         // longer one's span (mj < wcap whenever a later step token exists)
         if (act && s == 0 && mj < a.wcap) csj[mj] = 0.f;
-        // the next step's key is loaded while this step's dot product is reduced
-        float4 kn[NV];
-        {
-            const float *kt = sk + (size_t)(mmax - 1 < mj ? mmax - 1 : 0) * DK;
+        // the next step's key is loaded while this step's dot product is reduced; bf16 pools read the keys
+        // as given (8-byte pieces, half the shared-memory wavefronts of the fp32 rows) and widen them here
+        using KRaw = typename std::conditional<kWide, uint2, float4>::type;
+        auto kload = [&](int t, KRaw (&kr)[NV]) {
 #pragma unroll
-            for (int e = 0; e < NV; ++e) kn[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
-        }
+            for (int e = 0; e < NV; ++e) {
+                if constexpr (kWide)
+                    kr[e] = *reinterpret_cast<const uint2 *>(rk + (size_t)t * DK + 4 * (s + 8 * e));
+                else
+                    kr[e] = *reinterpret_cast<const float4 *>(sk + (size_t)t * DK + 4 * (s + 8 * e));
+            }
+        };
+        auto kwiden = [](KRaw r) -> float4 {
+            if constexpr (kWide)
+                return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u),
+                                   __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xFFFF0000u));
+            else
+                return r;
+        };
+        KRaw kn[NV];
+        kload(mmax - 1 < mj ? mmax - 1 : 0, kn);
         for (int t = mmax - 1; t >= 0; --t) {
             const bool live = t < mj;
             float4 k4[NV];
 #pragma unroll
-            for (int e = 0; e < NV; ++e) k4[e] = kn[e];
-            if (t > 0) {
-                const float *kt = sk + (size_t)(t - 1 < mj ? t - 1 : 0) * DK;
-#pragma unroll
-                for (int e = 0; e < NV; ++e) kn[e] = *reinterpret_cast<const float4 *>(kt + 4 * (s + 8 * e));
-            }
+            for (int e = 0; e < NV; ++e) k4[e] = kwiden(kn[e]);
+            if (t > 0) kload(t - 1 < mj ? t - 1 : 0, kn);
             float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int e = 0; e < NV; ++e) acc2 = dot4x2(k4[e], u[e], acc2);
