@@ -126,6 +126,37 @@ def test_replay_form_equals_the_recurrence():
         assert np.allclose(got, o[K:], rtol=1e-11, atol=1e-12), K
 
 
+def test_chunked_wy_fold_equals_the_recurrence():
+    """The fold in the chunked (WY) form the tensor-core kernel evaluates,
+    restated here on its own in fp64: with G_t the running sum of the gates,
+    S_M = e^{G_{M-1}} S + Y P, Y[:, t] = b_t v_t - b_t e^{G_t} S k_t,
+    P = (I + A)^{-1} D K, A[s][t] = b_t e^{G_t - G_s} (k_s . k_t) for s < t,
+    D = diag(e^{G_{M-1} - G_s}).  It must equal the oracle's token-by-token
+    recurrence for any window length, including one token, 32 and a gate
+    near zero; a transposed A or a D taken from the start fails it."""
+    for seed, M in ((21, 1), (22, 2), (23, 7), (24, 24), (25, 32)):
+        S0, _, k, v, g, b = _rand(seed, M, 9, 6)
+        if M >= 7:
+            g[3] = -40.0  # a gate near zero
+        want, _ = gdn.run_head(S0, None, k, v, g, b)
+        G = np.cumsum(g)
+        A = np.zeros((M, M))
+        for s_ in range(M):
+            for t in range(s_ + 1, M):
+                A[s_, t] = b[t] * np.exp(G[t] - G[s_]) * (k[s_] @ k[t])
+        D = np.exp(G[-1] - G)
+        P = np.linalg.solve(np.eye(M) + A, D[:, None] * k)
+        Y = v.T * b - (S0 @ k.T) * (b * np.exp(G))
+        got = np.exp(G[-1]) * S0 + Y @ P
+        assert np.allclose(got, want, rtol=1e-11, atol=1e-11), (seed, M)
+        # the pins above are sharp: A transposed, or D measured from the first token, give another state
+        if M >= 2:
+            bad = np.exp(G[-1]) * S0 + Y @ np.linalg.solve(np.eye(M) + A.T, D[:, None] * k)
+            assert not np.allclose(bad, want, rtol=1e-6, atol=1e-6)
+            bad = np.exp(G[-1]) * S0 + Y @ np.linalg.solve(np.eye(M) + A, np.exp(G - G[0])[:, None] * k)
+            assert not np.allclose(bad, want, rtol=1e-6, atol=1e-6)
+
+
 def test_pool_commit_keeps_only_accepted_tokens():
     """Through verify / commit with folds at different points, every output and
     the final state equal one sequential run over the accepted tokens alone
