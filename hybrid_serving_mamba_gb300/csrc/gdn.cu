@@ -427,19 +427,31 @@ __global__ void __launch_bounds__(kGdnThreads, 4) gdn_coef_kernel(const __grid_c
     // widen the keys and queries (bf16), check the step's rows, and copy the step after the log (the
     // positions past log_len: a rejected request leaves nothing behind that a later commit reads)
     using V4 = typename Vec4<TI>::T;
-    for (int c = tid; c < (m + T1) * (DK / 4); c += nthr) {
-        const int row = c / (DK / 4), off = 4 * (c % (DK / 4));
-        const TI *src = row < m ? rk + (size_t)row * DK + off : rq + (size_t)(row - m) * DK + off;
-        if (row >= K) {
+    if constexpr (kWide) {
+        // the log's keys were checked when they were logged: the pass starts at the step's keys; the
+        // sweeps read bf16 keys as staged, so only the queries are widened
+        for (int c = tid; c < (m + T1 - K) * (DK / 4); c += nthr) {
+            const int row = K + c / (DK / 4), off = 4 * (c % (DK / 4));
+            const TI *src = row < m ? rk + (size_t)row * DK + off : rq + (size_t)(row - m) * DK + off;
             const V4 raw = *reinterpret_cast<const V4 *>(src);
             bad |= Vec4<TI>::bad(raw);
             if (row < m)
-                *reinterpret_cast<V4 *>(static_cast<TI *>(a.log_k) +
-                                        ((size_t)slot * a.wcap + row) * krow + (size_t)kh * DK + off) = raw;
+                *reinterpret_cast<V4 *>(static_cast<TI *>(a.log_k) + ((size_t)slot * a.wcap + row) * krow +
+                                        (size_t)kh * DK + off) = raw;
+            else
+                *reinterpret_cast<float4 *>(sq + (size_t)(row - m) * DK + off) = lds4(src);
         }
-        if (kWide) {
-            float *dst = row < m ? sk + (size_t)row * DK + off : sq + (size_t)(row - m) * DK + off;
-            *reinterpret_cast<float4 *>(dst) = lds4(src);
+    } else {
+        for (int c = tid; c < (m + T1) * (DK / 4); c += nthr) {
+            const int row = c / (DK / 4), off = 4 * (c % (DK / 4));
+            const TI *src = row < m ? rk + (size_t)row * DK + off : rq + (size_t)(row - m) * DK + off;
+            if (row >= K) {
+                const V4 raw = *reinterpret_cast<const V4 *>(src);
+                bad |= Vec4<TI>::bad(raw);
+                if (row < m)
+                    *reinterpret_cast<V4 *>(static_cast<TI *>(a.log_k) +
+                                            ((size_t)slot * a.wcap + row) * krow + (size_t)kh * DK + off) = raw;
+            }
         }
     }
     for (int c = tid; c < T1 * (hdv / 4); c += nthr) {
