@@ -290,16 +290,16 @@ __global__ void __launch_bounds__(kGdnThreads, 2) gdn_decode_kernel(const __grid
 
 // ---------------------------------------------------------------------------- replay verify
 
-// The coefficient kernel's shared memory (bytes): fp32 keys [wcap][DK] (the log's, then the step's) and
-// queries [t1max][DK], exp(g) and beta [hpg][wcap] each, the log-term weights [hpg][t1max][wcap], the
-// values [wcap][hpg dv] as given (the log's, then the step's), and for bf16 inputs the keys and queries
-// as given [wcap + t1max][DK].
+// The coefficient kernel's shared memory (bytes): for fp32 inputs the keys [wcap][DK] (the log's, then
+// the step's), fp32 queries [t1max][DK], exp(g) and beta [hpg][wcap] each, the log-term weights
+// [hpg][t1max][wcap], the values [wcap][hpg dv] as given (the log's, then the step's), and for bf16
+// inputs the keys and queries as given [wcap + t1max][DK] (the sweeps read those keys directly).
 struct CoefLayout {
     size_t sq, sal, sbe, scw, svr, rkq, total;
 };
 __host__ __device__ inline CoefLayout coef_layout(int DK, int dv, int wcap, int t1max, int hpg, int in_b) {
     CoefLayout L;
-    size_t o = (size_t)wcap * DK * 4;
+    size_t o = in_b == 2 ? 0 : (size_t)wcap * DK * 4;
     L.sq = o;
     o += (size_t)t1max * DK * 4;
     L.sal = o;
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kGdnThreads, 4) gdn_coef_kernel(const __grid_c
     const int K = a.log_len[slot], m = K + T1, hdv = hpg * a.dv;
     const CoefLayout L = coef_layout(DK, a.dv, a.wcap, a.t1max, hpg, (int)sizeof(TI));
     char *base = reinterpret_cast<char *>(gsm);
-    float *sk = gsm;                                       // [wcap][DK]: the log's keys, then the step's
+    float *sk = gsm;                                       // fp32 inputs: [wcap][DK] the log's keys, then the step's
     float *sq = reinterpret_cast<float *>(base + L.sq);    // [t1max][DK]
     float *sal = reinterpret_cast<float *>(base + L.sal);  // [hpg][wcap] exp(g)
     float *sbe = reinterpret_cast<float *>(base + L.sbe);  // [hpg][wcap] beta
