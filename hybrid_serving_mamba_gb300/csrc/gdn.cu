@@ -1757,10 +1757,10 @@ ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok
     const size_t ib = (size_t)p.in_b, T = (size_t)n_tok;
     const size_t csm =
         ssm::gdn_coef_smem(p.cfg.dk, p.cfg.dv, p.wcap, p.cfg.max_tokens, p.cfg.nheads / p.cfg.nkheads, p.in_b);
-    // the coefficient kernel's block: four sweeps a warp, at least four warps for the staging and the
-    // log terms
+    // the coefficient kernel's block: four sweeps a warp; at least three warps, for the staging and the
+    // log terms (few sweeps, as in a one-token step, run best at three: more CTAs an SM)
     const int nsw = (p.cfg.nheads / p.cfg.nkheads) * n_tok;
-    const unsigned coef_threads = (unsigned)(32 * std::min(ssm::kGdnWarps, std::max(4, (nsw + 3) / 4)));
+    const unsigned coef_threads = (unsigned)(32 * std::min(ssm::kGdnWarps, std::max(3, (nsw + 3) / 4)));
     const size_t ssm_ = ssm::gdn_stream_smem(p.cfg.dk, p.cfg.dv, p.cfg.max_tokens);
     // the tensor-core streaming kernel: as many 16 KiB checkpoint slots as fit beside its per-item ring
     const int NM = n_tok <= 16 ? 16 : 32;
