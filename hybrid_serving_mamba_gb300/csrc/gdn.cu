@@ -326,6 +326,12 @@ __device__ __forceinline__ void cp_async8(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
+// Two fp32 values rounded to bf16 (round to nearest even) and packed, the first in the low half.
+__device__ __forceinline__ uint32_t bf2_pack(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 // Four values of the input type from shared memory, widened to fp32 (bf16: the bits moved up 16).
 __device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ float4 lds4(const __nv_bfloat16 *p) {
@@ -555,9 +561,17 @@ __global__ void __launch_bounds__(kGdnThreads, 4) gdn_coef_kernel(const __grid_c
             lo1 = ffma2(make_float2(x1, x1), make_float2(v4.x, v4.y), lo1);
             hi1 = ffma2(make_float2(x1, x1), make_float2(v4.z, v4.w), hi1);
         }
-        float *lt0 = a.lt + (((size_t)i * a.H + h0 + hl) * a.t1max + j0) * a.dv + 4 * c;
-        *reinterpret_cast<float4 *>(lt0) = make_float4(lo0.x, lo0.y, hi0.x, hi0.y);
-        if (j1 != j0) *reinterpret_cast<float4 *>(lt0 + a.dv) = make_float4(lo1.x, lo1.y, hi1.x, hi1.y);
+        const size_t lo = (((size_t)i * a.H + h0 + hl) * a.t1max + j0) * a.dv + 4 * c;
+        if (a.uq_nm) {  // the tensor-core stream, whose outputs are bf16, takes the log terms in bf16
+            __nv_bfloat16 *lt0 = reinterpret_cast<__nv_bfloat16 *>(a.lt) + lo;
+            *reinterpret_cast<uint2 *>(lt0) = make_uint2(bf2_pack(lo0.x, lo0.y), bf2_pack(hi0.x, hi0.y));
+            if (j1 != j0)
+                *reinterpret_cast<uint2 *>(lt0 + a.dv) = make_uint2(bf2_pack(lo1.x, lo1.y), bf2_pack(hi1.x, hi1.y));
+        } else {
+            float *lt0 = a.lt + lo;
+            *reinterpret_cast<float4 *>(lt0) = make_float4(lo0.x, lo0.y, hi0.x, hi0.y);
+            if (j1 != j0) *reinterpret_cast<float4 *>(lt0 + a.dv) = make_float4(lo1.x, lo1.y, hi1.x, hi1.y);
+        }
     }
 }
 
@@ -643,12 +657,12 @@ struct GtLayout {
     uint32_t u, lt, hdr, aux, aux_base, bars;
 };
 
-// Per-item stage: U [4 column blocks][NM rows][32 fp32], the log terms [t1max][dv], a header (the gate).
+// Per-item stage: U [4 column blocks][NM rows][32 fp32], the log terms [t1max][dv] bf16, a header (the gate).
 __host__ __device__ inline GtLayout gt_layout(int NM, int t1max, int dv, int nring) {
     GtLayout L;
     L.u = 0;
     L.lt = 4u * (uint32_t)NM * 128u;
-    L.hdr = L.lt + (uint32_t)t1max * (uint32_t)dv * 4u;
+    L.hdr = L.lt + (uint32_t)t1max * (uint32_t)dv * 2u;
     L.aux = (L.hdr + 16u + 1023u) & ~1023u;
     L.aux_base = (uint32_t)nring * 16384u;
     L.bars = L.aux_base + kGtAux * L.aux;
@@ -722,7 +736,7 @@ __global__ void __launch_bounds__(kGtThreads, 1)
             asm volatile("griddepcontrol.wait;" ::: "memory");  // U, the log terms and the flags are written
             int xlast[kGtAux];
             for (int s = 0; s < kGtAux; ++s) xlast[s] = -1;
-            const uint32_t ubytes = 4u * NM * 128u, lbytes = (uint32_t)T1 * dv * 4u;
+            const uint32_t ubytes = 4u * NM * 128u, lbytes = (uint32_t)T1 * dv * 2u;
             for (int u = 0;; ++u) {
                 const int item = blockIdx.x + u * gridDim.x;
                 if (item >= n_items) break;
@@ -737,7 +751,9 @@ __global__ void __launch_bounds__(kGtThreads, 1)
                 } else {
                     mbar_arrive_expect_tx(&xfull[xs], ubytes + lbytes);
                     bulk_g2s(X + L.u, a.uq + ((size_t)i * H + h) * a.uq_rows * 128, ubytes, &xfull[xs]);
-                    bulk_g2s(X + L.lt, a.lt + ((size_t)i * H + h) * a.t1max * dv, lbytes, &xfull[xs]);
+                    bulk_g2s(X + L.lt,
+                             reinterpret_cast<const __nv_bfloat16 *>(a.lt) + ((size_t)i * H + h) * a.t1max * dv,
+                             lbytes, &xfull[xs]);
                     xlast[xs] = u;
                 }
             }
@@ -839,11 +855,12 @@ __global__ void __launch_bounds__(kGtThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&dempty[db]);
             if (!gate) {
-                const float *lt = reinterpret_cast<const float *>(X + L.lt);
+                const __nv_bfloat16 *lt = reinterpret_cast<const __nv_bfloat16 *>(X + L.lt);
                 __nv_bfloat16 *yr = y + ((size_t)i * T1 * H + h) * dv + p;
 #pragma unroll
                 for (int j = 0; j < NM; ++j)
-                    if (j < T1) yr[(size_t)j * H * dv] = __float2bfloat16_rn(d[j] + lt[(size_t)j * dv + p]);
+                    if (j < T1)
+                        yr[(size_t)j * H * dv] = __float2bfloat16_rn(d[j] + __bfloat162float(lt[(size_t)j * dv + p]));
             }
             __syncwarp();  // the stage is read (U by the MMAs, done above; the log terms here)
             if (lane == 0) mbar_arrive(&xempty[xs]);
