@@ -79,8 +79,9 @@ ssm_status ssm_gdn_decode_step(ssm_gdn_pool pool, int32_t batch, const int32_t *
  * weighted v_i.  The step's k, v, g and beta are staged after the log for
  * the commit.  Shapes as decode with [batch][n_tok] tokens.  bf16 pools with
  * dk = dv = 128 and 4 <= n_tok <= 32 take the checkpoint product S u on the tensor
- * cores (fp32 operands read as tf32: at most 2^-10 of each product, below
- * the bf16 rounding of y); other pools the exact fp32 CUDA-core kernel. */
+ * cores (fp32 operands read as tf32: at most 2^-10 of each product) and add
+ * the weighted logged values rounded to bf16 (2^-9 of that term), both below
+ * the bf16 rounding of y; other pools the exact fp32 CUDA-core kernels. */
 ssm_status ssm_gdn_verify_replay(ssm_gdn_pool pool, int32_t batch, int32_t n_tok, const int32_t *slots,
                                  const void *q, const void *k, const void *v, const float *g, const float *beta,
                                  void *y, ssm_stream_t stream);
