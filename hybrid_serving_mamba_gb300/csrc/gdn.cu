@@ -148,36 +148,6 @@ template <> struct Vec4<__nv_bfloat16> {
     }
 };
 
-// The same between global matrices in the input type (staging the step into the log), with the check.
-template <typename TI>
-__device__ __forceinline__ bool copy_rows(TI *dst, size_t dstride, const TI *src, size_t sstride, int rows, int cols,
-                                          int tid, int nthr) {
-    using V = typename Vec4<TI>::T;
-    const int cq = cols >> 2, total = rows * cq;
-    bool bad = false;
-    for (int base = tid; base < total; base += 4 * nthr) {
-        V v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = base + u * nthr;
-            if (e < total) {
-                const int r = e / cq, c = e - r * cq;
-                v[u] = *reinterpret_cast<const V *>(src + (size_t)r * sstride + 4 * c);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = base + u * nthr;
-            if (e < total) {
-                const int r = e / cq, c = e - r * cq;
-                bad |= Vec4<TI>::bad(v[u]);
-                *reinterpret_cast<V *>(dst + (size_t)r * dstride + 4 * c) = v[u];
-            }
-        }
-    }
-    return bad;
-}
-
 __device__ __forceinline__ void poison(const GdnArgs &a, int slot, uint32_t flag) {
     atomicOr(a.flags, flag);
     atomicOr(a.slot_flags + slot, kSlotPoisoned);
