@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(kFtThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     __shared__ uint32_t s_abort, s_tmem;
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    // the next verify's coefficient kernel may be scheduled as this grid drains (it waits for it)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int P = a.P, H = a.H;
     const FtLayout L = ft_layout(a.wwin, P, KP);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);  // tiles landed

@@ -27,6 +27,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "pdl.cuh"
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -314,8 +315,12 @@ __device__ void move_range(char *base, size_t row_bytes, int from, int to, int c
     }
 }
 
-// CTA (listed move, slice).
+// CTA (listed move, slice).  Launched programmatically after the commit's index kernel: the next verify's
+// coefficient kernel may be scheduled as this grid drains (it waits for it); the list is read once the
+// index kernel has completed.
 __global__ void __launch_bounds__(kMoveThreads) log_move_kernel(const __grid_constant__ CommitArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if ((int)blockIdx.x >= a.counts[2]) return;
     const int4 mv = a.moves[blockIdx.x];
     const int slot = a.slots[mv.x], from = mv.y, to = mv.z, c = mv.w;
@@ -329,8 +334,19 @@ __global__ void __launch_bounds__(kMoveThreads) log_move_kernel(const __grid_con
 
 // One thread per request: the index side of the commit (bit exact).  kMoves:
 // a commit of a pool that folds in its verify (appends, moving staged tokens).
+// reset: one CTA covers the batch and clears the fold and move counts itself
+// (else the host clears them before the launch).
 template <bool kMoves>
-__global__ void commit_meta_kernel(const __grid_constant__ CommitArgs a, int replay) {
+__global__ void commit_meta_kernel(const __grid_constant__ CommitArgs a, int replay, int reset) {
+    // the log move (or the fold) may be scheduled now: it waits for this grid before it reads the lists
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (reset) {
+        if (threadIdx.x == 0 && replay) {
+            *a.fold_count = 0;
+            if (kMoves) a.counts[2] = 0;
+        }
+        __syncthreads();
+    }
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.batch) return;
     const int slot = a.slots[i];
@@ -542,20 +558,24 @@ cudaError_t launch_verify_replay(const Pool &pool, const StepArgs &a, cudaStream
 cudaError_t launch_commit(const Pool &pool, const CommitArgs &a, cudaStream_t s, const char **path) {
     const bool replay = pool.cfg.mode == SSM_MODE_REPLAY;
     const bool moves = a.fold_w && !a.flush;
-    if (replay) {
+    // up to 1024 requests one CTA clears the counts in the kernel; else the host clears them first
+    const bool one = a.batch <= 1024;
+    if (replay && !one) {
         cudaError_t e = cudaMemsetAsync(a.fold_count, 0, sizeof(int32_t), s);
         if (e == cudaSuccess && moves) e = cudaMemsetAsync(&a.counts[2], 0, sizeof(int32_t), s);
         if (e != cudaSuccess) return e;
     }
-    if (moves) commit_meta_kernel<true><<<(a.batch + 127) / 128, 128, 0, s>>>(a, 1);
-    else commit_meta_kernel<false><<<(a.batch + 127) / 128, 128, 0, s>>>(a, replay ? 1 : 0);
+    const dim3 mgrid(one ? 1u : (unsigned)((a.batch + 127) / 128));
+    const dim3 mblock(one ? (unsigned)((a.batch + 31) / 32 * 32) : 128u);
+    if (moves) commit_meta_kernel<true><<<mgrid, mblock, 0, s>>>(a, 1, one ? 1 : 0);
+    else commit_meta_kernel<false><<<mgrid, mblock, 0, s>>>(a, replay ? 1 : 0, one ? 1 : 0);
     if (path) *path = "commit_copy";
     if (replay) {
         cudaError_t ep = cudaGetLastError();
         if (ep != cudaSuccess) return ep;
         if (moves) {
-            log_move_kernel<<<dim3(a.batch, kMoveParts), kMoveThreads, 0, s>>>(a);
-            ep = cudaGetLastError();
+            ep = launch_pdl(log_move_kernel, dim3(a.batch, kMoveParts), dim3(kMoveThreads), 0, s, a);
+            if (ep == cudaSuccess) ep = cudaGetLastError();
             if (ep != cudaSuccess) return ep;
             if (path) *path = "commit_replay_append";
             if (!a.force_fold) return cudaSuccess;  // nothing folds here

@@ -34,6 +34,7 @@
 
 #include <algorithm>
 
+#include "pdl.cuh"
 #include "ssm_internal.cuh"
 #include "tc.cuh"
 #include "tma.cuh"
@@ -126,8 +127,10 @@ __global__ void __launch_bounds__(kCoefThreads, 5) replay_group_coef_kernel(cons
     constexpr int NV = N / EV;        // 16-byte vectors per B or C row
     extern __shared__ float4 smem4[];
     // the streaming kernel may be scheduled as CTAs of this one drain; it waits for this grid's
-    // completion before it reads anything this kernel writes
+    // completion before it reads anything this kernel writes.  This grid may itself start as the
+    // previous commit's last kernel drains: nothing is read before that grid has completed.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g = blockIdx.x, i = blockIdx.y;
     const int slot = a.slots[i];
     const int T1 = a.n_tok, H = a.H, P = a.P, hpg = a.hpg;
@@ -1220,13 +1223,14 @@ cudaError_t launch_verify_replay_tma(const Pool &pool, const StepArgs &a, cudaSt
                                          : replay_group_coef_kernel<NN, __nv_bfloat16, false>;
             e = set_smem(k, csmem);
             if (e != cudaSuccess) return e;
-            k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(ac);
+            e = launch_pdl(k, dim3(a.G, a.batch), dim3(kCoefThreads), csmem, s, ac);
         } else {
             auto k = replay_group_coef_kernel<NN, float, false>;
             e = set_smem(k, csmem);
             if (e != cudaSuccess) return e;
-            k<<<dim3(a.G, a.batch), kCoefThreads, csmem, s>>>(ac);
+            e = launch_pdl(k, dim3(a.G, a.batch), dim3(kCoefThreads), csmem, s, ac);
         }
+        if (e != cudaSuccess) return e;
     });
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
